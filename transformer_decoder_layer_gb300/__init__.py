@@ -1,0 +1,285 @@
+"""Python binding of libqwenlayer.so: a GB300 (sm_103a) Qwen-style decoder layer.
+
+This module only marshals arguments (torch tensors -> device pointers, the
+current CUDA stream) into the C ABI declared in ``include/qwen_layer.h``.
+Every step of the layer runs in the library's CUDA kernels; there is no CPU
+fallback, and every call raises if the shared library is not built or a call
+returns an error.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB as _LIB_PATH
+
+__all__ = [
+    "QwenError", "lib", "LayerConfig", "Layer", "rmsnorm", "linear", "head_last_token",
+    "poll_error", "STATUS",
+]
+
+STATUS = {
+    0: "QWEN_OK", 1: "QWEN_ERR_INVALID_ARG", 2: "QWEN_ERR_UNSUPPORTED",
+    3: "QWEN_ERR_CAPACITY", 4: "QWEN_ERR_CUDA", 5: "QWEN_ERR_TIMEOUT", 6: "QWEN_ERR_RANGE",
+}
+
+
+class QwenError(RuntimeError):
+    def __init__(self, code, where=""):
+        self.code = int(code)
+        super().__init__(f"{where}: {STATUS.get(self.code, self.code)}")
+
+
+class _Config(ctypes.Structure):
+    _fields_ = [
+        ("d", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("ffn", ctypes.c_int32), ("qkv_bias", ctypes.c_int32),
+        ("qk_norm", ctypes.c_int32), ("rope_theta", ctypes.c_double),
+        ("rms_eps", ctypes.c_float), ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
+        ("norm_topk_prob", ctypes.c_int32), ("router_bias", ctypes.c_int32),
+        ("max_tokens", ctypes.c_int32), ("max_batch", ctypes.c_int32),
+        ("max_seq", ctypes.c_int32), ("max_position", ctypes.c_int32),
+    ]
+
+
+_WEIGHT_FIELDS = ["gamma_attn", "gamma_mlp", "gamma_q", "gamma_k", "w_q", "w_k", "w_v", "b_q",
+                  "b_k", "b_v", "w_o", "w_gate", "w_up", "w_down", "w_router", "b_router"]
+
+
+class _Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _WEIGHT_FIELDS]
+
+
+_VP, _I32, _SZ, _F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+_SIGS = {
+    "qwen_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "qwen_layer_packed_bytes": (_SZ, [ctypes.POINTER(_Config)]),
+    "qwen_layer_workspace_bytes": (_SZ, [ctypes.POINTER(_Config), _I32, _I32]),
+    "qwen_layer_create": (ctypes.c_int, [ctypes.POINTER(_Config), ctypes.POINTER(_Weights), _VP,
+                                         _SZ, _VP, ctypes.POINTER(_VP)]),
+    "qwen_layer_destroy": (None, [_VP]),
+    "qwen_layer_prefill": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, _VP, _VP, _VP, _VP, _VP,
+                                          _SZ, _VP]),
+    "qwen_layer_decode": (ctypes.c_int, [_VP, _VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _SZ,
+                                         _VP]),
+    "qwen_moe_ffn": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "qwen_head_workspace_bytes": (_SZ, [_I32, _I32, _I32]),
+    "qwen_head_last_token": (ctypes.c_int, [_VP, _I32, _I32, _I32, _VP, _VP, _I32, _F32, _VP,
+                                            _VP, _SZ, _VP]),
+    "qwen_rmsnorm": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _I32, _F32, _VP]),
+    "qwen_linear": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, _I32, _VP]),
+    "qwen_layer_poll_error": (ctypes.c_int, [_VP, _VP]),
+    "qwen_poll_error": (ctypes.c_int, [_VP]),
+    "qwen_device_sm_count": (_I32, []),
+}
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """Load libqwenlayer.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            if not hasattr(L, name):
+                continue  # the ABI test insists every declared symbol exists
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(rc, where):
+    if rc != 0:
+        raise QwenError(rc, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, dtype, name):
+    import torch
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+# ---------------------------------------------------------------- handle-less calls
+
+def rmsnorm(x, gamma, eps, out=None, out_fp32=None, stream=None):
+    """y = gamma * x / sqrt(mean(x^2) + eps) row-wise (BF16 in/out)."""
+    import torch
+    _need(x, torch.bfloat16, "x")
+    _need(gamma, torch.bfloat16, "gamma")
+    d = x.shape[-1]
+    rows = x.numel() // d
+    out = torch.empty_like(x) if out is None else out
+    _check(lib().qwen_rmsnorm(_ptr(x), _ptr(gamma), _ptr(out), _ptr(out_fp32), rows, d,
+                              float(eps), _stream(stream)), "qwen_rmsnorm")
+    return out
+
+
+def linear(x, w, out=None, stream=None):
+    """y = x W^T on the tensor cores: x [M,K], w [N,K] BF16 -> y [M,N] BF16."""
+    import torch
+    _need(x, torch.bfloat16, "x")
+    _need(w, torch.bfloat16, "w")
+    K = x.shape[-1]
+    M = x.numel() // K
+    N = w.shape[0]
+    out = torch.empty((*x.shape[:-1], N), dtype=torch.bfloat16, device=x.device) if out is None else out
+    _check(lib().qwen_linear(_ptr(x), _ptr(w), _ptr(out), M, N, K, _stream(stream)), "qwen_linear")
+    return out
+
+
+def poll_error(stream=None):
+    """Synchronise and return (then clear) the library-wide device status."""
+    return lib().qwen_poll_error(_stream(stream))
+
+
+def head_workspace_bytes(B, d, V):
+    return lib().qwen_head_workspace_bytes(B, d, V)
+
+
+def head_last_token(y, gamma_final, w_lm, eps, logits=None, workspace=None, stream=None):
+    """logits[b] = RMSNorm(y[b, -1]) W_lm^T (FP32 logits)."""
+    import torch
+    _need(y, torch.bfloat16, "y")
+    B, T, d = y.shape
+    V = w_lm.shape[0]
+    logits = torch.empty((B, V), dtype=torch.float32, device=y.device) if logits is None else logits
+    nbytes = head_workspace_bytes(B, d, V)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=y.device)
+    _check(lib().qwen_head_last_token(_ptr(y), B, T, d, _ptr(gamma_final), _ptr(w_lm), V,
+                                      float(eps), _ptr(logits), _ptr(workspace),
+                                      workspace.numel(), _stream(stream)),
+           "qwen_head_last_token")
+    return logits
+
+
+# ---------------------------------------------------------------- layer handle
+
+class LayerConfig:
+    """Build the C ``qwen_layer_config`` from a shape object (any object or dict
+    with the shape fields) plus capacities."""
+
+    def __init__(self, shape, max_tokens, max_batch, max_seq, max_position):
+        get = (lambda k, dflt=0: shape.get(k, dflt)) if isinstance(shape, dict) else \
+            (lambda k, dflt=0: getattr(shape, k, dflt))
+        self.c = _Config(
+            d=get("d"), n_q_heads=get("n_q_heads"), n_kv_heads=get("n_kv_heads"),
+            head_dim=get("head_dim"), ffn=get("ffn"), qkv_bias=get("qkv_bias"),
+            qk_norm=get("qk_norm"), rope_theta=float(get("rope_theta", 1.0e6)),
+            rms_eps=float(get("rms_eps", 1.0e-6)), n_experts=get("n_experts"),
+            top_k=get("top_k"), norm_topk_prob=get("norm_topk_prob", 1),
+            router_bias=get("router_bias"), max_tokens=int(max_tokens),
+            max_batch=int(max_batch), max_seq=int(max_seq), max_position=int(max_position))
+
+    def __getattr__(self, k):
+        return getattr(self.__dict__["c"], k)
+
+
+class Layer:
+    """One decoder layer: packed weights (device) + a library handle."""
+
+    def __init__(self, cfg: LayerConfig, weights: dict, device="cuda", stream=None):
+        import torch
+        self.cfg = cfg
+        L = lib()
+        nbytes = L.qwen_layer_packed_bytes(ctypes.byref(cfg.c))
+        if nbytes == 0:
+            raise QwenError(1, "qwen_layer_packed_bytes (invalid config)")
+        self.packed = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        w = _Weights()
+        for n in _WEIGHT_FIELDS:
+            t = weights.get(n)
+            if t is not None:
+                if not t.is_cuda or not t.is_contiguous():
+                    raise ValueError(f"weight {n} must be a contiguous CUDA tensor")
+                setattr(w, n, t.data_ptr())
+        h = ctypes.c_void_p()
+        _check(L.qwen_layer_create(ctypes.byref(cfg.c), ctypes.byref(w), _ptr(self.packed),
+                                   nbytes, _stream(stream), ctypes.byref(h)), "qwen_layer_create")
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            lib().qwen_layer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def workspace_bytes(self, B, T):
+        return lib().qwen_layer_workspace_bytes(ctypes.byref(self.cfg.c), B, T)
+
+    def workspace(self, B, T, device="cuda"):
+        import torch
+        return torch.empty(max(self.workspace_bytes(B, T), 256), dtype=torch.uint8, device=device)
+
+    def prefill(self, x, positions, cache_start, k_cache, v_cache, out=None, workspace=None,
+                stream=None):
+        import torch
+        _need(x, torch.bfloat16, "x")
+        B, T, _ = x.shape
+        out = torch.empty_like(x) if out is None else out
+        ws = self.workspace(B, T, x.device) if workspace is None else workspace
+        _check(lib().qwen_layer_prefill(self.handle, _ptr(x), _ptr(out), B, T, _ptr(positions),
+                                        _ptr(cache_start), _ptr(k_cache), _ptr(v_cache),
+                                        _ptr(ws), ws.numel(), _stream(stream)),
+               "qwen_layer_prefill")
+        return out
+
+    def decode(self, x, positions, cache_len, k_cache, v_cache, out=None, workspace=None,
+               stream=None):
+        import torch
+        _need(x, torch.bfloat16, "x")
+        B = x.shape[0]
+        out = torch.empty_like(x) if out is None else out
+        ws = self.workspace(B, 1, x.device) if workspace is None else workspace
+        _check(lib().qwen_layer_decode(self.handle, _ptr(x), _ptr(out), B, _ptr(positions),
+                                       _ptr(cache_len), _ptr(k_cache), _ptr(v_cache), _ptr(ws),
+                                       ws.numel(), _stream(stream)), "qwen_layer_decode")
+        return out
+
+    def moe_ffn(self, r, r_fp32=None, out=None, topk_idx=None, topk_w=None, logits=None,
+                workspace=None, stream=None):
+        import torch
+        _need(r, torch.bfloat16, "r")
+        T = r.shape[0]
+        out = torch.empty_like(r) if out is None else out
+        ws = self.workspace(1, T, r.device) if workspace is None else workspace
+        _check(lib().qwen_moe_ffn(self.handle, _ptr(r), _ptr(r_fp32), _ptr(out), T,
+                                  _ptr(topk_idx), _ptr(topk_w), _ptr(logits), _ptr(ws),
+                                  ws.numel(), _stream(stream)), "qwen_moe_ffn")
+        return out
+
+    def poll_error(self, stream=None):
+        return lib().qwen_layer_poll_error(self.handle, _stream(stream))

@@ -1,0 +1,98 @@
+// C ABI: status strings, device queries and the handle-less entry points
+// (qwen_rmsnorm, qwen_linear).
+#include <cstdio>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace qwen {
+
+// Status word for entry points that have no layer handle (qwen_linear, ...).
+// A module-scope device variable: no allocation is needed to use it.
+static __device__ int g_lib_status;
+
+int* lib_status_ptr() {
+  static int* p = nullptr;
+  if (!p) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_lib_status) == cudaSuccess) p = static_cast<int*>(a);
+  }
+  return p;
+}
+
+int device_sm_count() {
+  static int cached = 0;
+  if (!cached) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      cached = n;
+    else
+      cached = 1;
+  }
+  return cached;
+}
+
+}  // namespace qwen
+
+using namespace qwen;
+
+extern "C" {
+
+const char* qwen_status_string(qwen_status s) {
+  switch (s) {
+    case QWEN_OK: return "ok";
+    case QWEN_ERR_INVALID_ARG: return "invalid argument";
+    case QWEN_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case QWEN_ERR_CAPACITY: return "capacity exceeded";
+    case QWEN_ERR_CUDA: return "CUDA error";
+    case QWEN_ERR_TIMEOUT: return "device wait timed out";
+    case QWEN_ERR_RANGE: return "cache slot or position out of range";
+  }
+  return "unknown status";
+}
+
+int32_t qwen_device_sm_count(void) { return device_sm_count(); }
+
+qwen_status qwen_rmsnorm(const void* x, const void* gamma, void* y, float* y_fp32, int32_t rows,
+                         int32_t d, float eps, void* stream) {
+  if (rows < 0 || d <= 0) return QWEN_ERR_INVALID_ARG;
+  if (rows == 0) return QWEN_OK;
+  if (!x || !gamma || !y) return QWEN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y) |
+       reinterpret_cast<uintptr_t>(gamma)) & 15)
+    return QWEN_ERR_INVALID_ARG;
+  return rmsnorm_launch(static_cast<const bf16*>(x), static_cast<const bf16*>(gamma),
+                        static_cast<bf16*>(y), y_fp32, nullptr, rows, d, eps,
+                        static_cast<cudaStream_t>(stream));
+}
+
+qwen_status qwen_linear(const void* x, const void* w, void* y, int32_t M, int32_t N, int32_t K,
+                        void* stream) {
+  if (M < 0 || N <= 0 || K <= 0) return QWEN_ERR_INVALID_ARG;
+  if (M == 0) return QWEN_OK;
+  if (!x || !w || !y) return QWEN_ERR_INVALID_ARG;
+  if ((K & 7) || (N & 7)) return QWEN_ERR_UNSUPPORTED;
+  GemmEpilogue epi{};
+  epi.mode = EPI_STORE;
+  epi.out = static_cast<bf16*>(y);
+  epi.ldo = N;
+  return gemm_tc(static_cast<const bf16*>(x), K, static_cast<const bf16*>(w), K, M, N, K, epi,
+                 lib_status_ptr(), static_cast<cudaStream_t>(stream));
+}
+
+qwen_status qwen_poll_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return QWEN_ERR_CUDA;
+  int* p = lib_status_ptr();
+  if (!p) return QWEN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return QWEN_ERR_CUDA;
+  if (v) {
+    const int zero = 0;
+    cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice);
+  }
+  return static_cast<qwen_status>(v);
+}
+
+}  // extern "C"

@@ -1,0 +1,454 @@
+// Persistent tcgen05 GEMM for sm_103a: D[M,N] = A[M,K] * B[N,K]^T in BF16 with
+// FP32 accumulation in tensor memory, fed by TMA through an mbarrier ring, with
+// fused epilogues for the decoder layer's projections.
+//
+// Every projection of the layer is a "token rows x weight rows" product of this
+// shape ("Qwen2.5-7B 结构拆解" §03.2: [B,S,d] is flattened to [B*S,d] and each
+// projection is one GEMM against the [out,in] weight, §03.1).
+//
+// CTA layout (192 threads, one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer: A tile [128 x 64] and B tile [BN x 64] per stage
+//   warp 1      TMEM allocator + MMA issuer (one elected lane)
+//   warps 2..5  epilogue: tcgen05.ld of the 128 x BN FP32 accumulator, fused
+//               math, global stores.  Warp w reads TMEM lanes 32*(w%4)..+31.
+// Two accumulators in TMEM (2 x BN columns) let the epilogue of tile i overlap
+// the main loop of tile i+1.
+#include "common.cuh"
+#include "internal.h"
+#include "qkv_epilogue.cuh"
+
+#include <cudaTypedefs.h>
+
+namespace qwen {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;  // 64 bf16 = 128 bytes = one swizzle row
+constexpr int kGemmThreads = 192;
+constexpr int kGroupM = 16;  // raster: 16 m-blocks share a sweep over n
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int A_BYTES = kBM * kBK * 2;
+  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
+  static constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 + 1024;
+};
+
+struct TileInfo {
+  int m0, n0, row_end, b_row0;
+};
+
+// Map a linear tile id to output coordinates.  Dense mode: groups of kGroupM
+// m-blocks are swept across all n-blocks so the active B tiles and A rows both
+// stay in L2.  Grouped mode: (group, m-block within group, n-block).
+__device__ __forceinline__ bool get_tile(int tile, int M, int N, int BN, int n_nblk,
+                                         const GemmEpilogue& epi, const int* s_tile_prefix,
+                                         TileInfo& ti) {
+  if (epi.group_offsets == nullptr) {
+    const int n_mblk = (M + kBM - 1) / kBM;
+    if (tile >= n_mblk * n_nblk) return false;
+    const int per_group = kGroupM * n_nblk;
+    const int g = tile / per_group;
+    const int first_m = g * kGroupM;
+    const int gm = min(kGroupM, n_mblk - first_m);
+    const int r = tile - g * per_group;
+    const int mb = first_m + r % gm;
+    const int nb = r / gm;
+    ti.m0 = mb * kBM;
+    ti.n0 = nb * BN;
+    ti.row_end = M;
+    ti.b_row0 = ti.n0;
+    return true;
+  }
+  // grouped: s_tile_prefix[g] = m-tiles of groups < g (n_groups+1 entries)
+  const int total_m = s_tile_prefix[epi.n_groups];
+  if (tile >= total_m * n_nblk) return false;
+  const int mt = tile / n_nblk;
+  const int nb = tile - mt * n_nblk;
+  int lo = 0, hi = epi.n_groups - 1;  // last g with prefix[g] <= mt
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_tile_prefix[mid] <= mt) lo = mid; else hi = mid - 1;
+  }
+  const int g = lo;
+  const int row_begin = epi.group_offsets[g];
+  ti.m0 = row_begin + (mt - s_tile_prefix[g]) * kBM;
+  ti.row_end = epi.group_offsets[g + 1];
+  ti.n0 = nb * BN;
+  ti.b_row0 = g * N + ti.n0;
+  return true;
+}
+
+template <int BN, int EPI>
+__device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, bool row_ok, int n0,
+                                              int N, const GemmEpilogue& epi, int* err) {
+  if constexpr (EPI == EPI_QKV) {
+    const int dh = epi.qkv.dh;
+    if (dh == 128) {
+#pragma unroll 1
+      for (int h0 = 0; h0 < BN; h0 += 128) {
+        float v[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(taddr + h0 + 32 * c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[32 * c + i] = __uint_as_float(r[i]);
+        }
+        if (row_ok && n0 + h0 < N) qkv_head_finish<128>(v, row, (n0 + h0) / 128, epi.qkv, err);
+      }
+    } else {
+#pragma unroll 1
+      for (int h0 = 0; h0 < BN; h0 += 64) {
+        float v[64];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[32];
+          tmem_ld32(taddr + h0 + 32 * c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[32 * c + i] = __uint_as_float(r[i]);
+        }
+        if (row_ok && n0 + h0 < N) qkv_head_finish<64>(v, row, (n0 + h0) / 64, epi.qkv, err);
+      }
+    }
+  } else if constexpr (EPI == EPI_SWIGLU) {
+    // columns [128j, 128j+64) are gate rows, [128j+64, 128j+128) the matching up rows
+#pragma unroll 1
+    for (int j = 0; j < BN; j += 128) {
+#pragma unroll 1
+      for (int h = 0; h < 64; h += 32) {
+        uint32_t g[32], u[32];
+        tmem_ld32(taddr + j + h, g);
+        tmem_ld32(taddr + j + 64 + h, u);
+        tmem_ld_wait();
+        const int col = (n0 + j) / 2 + h;  // output feature
+        if (row_ok && n0 + j < N) {
+          uint4* dst = reinterpret_cast<uint4*>(epi.out + (size_t)row * epi.ldo + col);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float gv = __uint_as_float(g[8 * q + e]);
+              o[e] = silu_f(gv) * __uint_as_float(u[8 * q + e]);
+            }
+            uint4 w;
+            w.x = pack_bf16x2(o[0], o[1]);
+            w.y = pack_bf16x2(o[2], o[3]);
+            w.z = pack_bf16x2(o[4], o[5]);
+            w.w = pack_bf16x2(o[6], o[7]);
+            dst[q] = w;
+          }
+        }
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t r[32];
+      tmem_ld32(taddr + c, r);
+      tmem_ld_wait();
+      const int col = n0 + c;
+      if (!row_ok || col >= N) continue;
+      const bool full = col + 32 <= N;
+      if constexpr (EPI == EPI_F32) {
+        float* dst = epi.out32 + (size_t)row * epi.ldo32 + col;
+        if (full) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<float4*>(dst)[q] =
+                make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                            __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < N - col) dst[i] = __uint_as_float(r[i]);
+        }
+      } else {
+        float o[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
+        if constexpr (EPI == EPI_RESID) {
+          const bf16* rs = epi.resid + (size_t)row * epi.ldr + col;
+          if (full) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint4 u = reinterpret_cast<const uint4*>(rs)[q];
+              const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f = unpack_bf16x2(w[e]);
+                o[8 * q + 2 * e] += f.x;
+                o[8 * q + 2 * e + 1] += f.y;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < N - col) o[i] += bf2f(rs[i]);
+          }
+          if (epi.out32) {
+            float* d32 = epi.out32 + (size_t)row * epi.ldo32 + col;
+            if (full) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                reinterpret_cast<float4*>(d32)[q] =
+                    make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < N - col) d32[i] = o[i];
+            }
+          }
+        }
+        bf16* dst = epi.out + (size_t)row * epi.ldo + col;
+        if (full) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack_bf16x2(o[8 * q], o[8 * q + 1]);
+            w.y = pack_bf16x2(o[8 * q + 2], o[8 * q + 3]);
+            w.z = pack_bf16x2(o[8 * q + 4], o[8 * q + 5]);
+            w.w = pack_bf16x2(o[8 * q + 6], o[8 * q + 7]);
+            reinterpret_cast<uint4*>(dst)[q] = w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i < N - col) dst[i] = f2bf(o[i]);
+        }
+      }
+    }
+  }
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   int M, int N, int K, GemmEpilogue epi, int* err) {
+  using C = GemmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_tile_prefix = reinterpret_cast<int*>(tmem_slot + 4);  // up to 256 groups
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_nblk = (N + BN - 1) / BN;
+  const int n_kblk = (K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    *abort_flag = 0;
+    if (epi.group_offsets) {
+      int acc = 0;
+      for (int g = 0; g < epi.n_groups; ++g) {
+        s_tile_prefix[g] = acc;
+        const int rows = epi.group_offsets[g + 1] - epi.group_offsets[g];
+        acc += (rows + kBM - 1) / kBM;
+      }
+      s_tile_prefix[epi.n_groups] = acc;
+    }
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      TileInfo ti;
+      for (int tile = blockIdx.x; get_tile(tile, M, N, BN, n_nblk, epi, s_tile_prefix, ti);
+           tile += gridDim.x) {
+        for (int kb = 0; kb < n_kblk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) goto producer_done;
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * kBK, ti.m0);
+          tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * kBK, ti.b_row0);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // drain: wait until the MMA warp has consumed every stage we filled, so
+      // no TMA write is still in flight when the CTA exits
+      for (int s = 0; s < C::STAGES; ++s) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) break;
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    producer_done:;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      TileInfo ti;
+      for (int tile = blockIdx.x; get_tile(tile, M, N, BN, n_nblk, epi, s_tile_prefix, ti);
+           tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < n_kblk; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = smem_desc_sw128(a0 + 32 * k, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(b0 + 32 * k, 16, 1024);
+            umma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+      }
+    }
+  } else {
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int local = 0;
+    TileInfo ti;
+    for (int tile = blockIdx.x; get_tile(tile, M, N, BN, n_nblk, epi, s_tile_prefix, ti);
+         tile += gridDim.x, ++local) {
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, err)) break;
+      tc_fence_after();
+      const int row = ti.m0 + q * 32 + lane;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      epilogue_tile<BN, EPI>(taddr, row, row < ti.row_end, ti.n0, N, epi, err);
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D BF16 tensor [rows][cols] with row stride `ld` elements; box [box_rows][64]
+// with the 128-byte swizzle.
+static bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint64_t ld, uint32_t box_rows) {
+  auto enc = get_encode_fn();
+  if (!enc) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || ((ld * 2) & 15)) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int EPI>
+static qwen_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
+                             const GemmEpilogue& epi, int* err, int grid, cudaStream_t st) {
+  auto kern = gemm_tc_kernel<BN, EPI>;
+  static bool attr_done = false;  // per template instance
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             GemmCfg<BN>::SMEM_BYTES) != cudaSuccess)
+      return QWEN_ERR_CUDA;
+    attr_done = true;
+  }
+  kern<<<grid, kGemmThreads, GemmCfg<BN>::SMEM_BYTES, st>>>(ta, tb, M, N, K, epi, err);
+  return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
+}
+
+qwen_status gemm_tc(const bf16* A, int lda, const bf16* B, int ldb, int M, int N, int K,
+                    const GemmEpilogue& epi, int* err, cudaStream_t st) {
+  if (M == 0 || N == 0) return QWEN_OK;
+  if (K <= 0 || (K & 7) || (N & 7)) return QWEN_ERR_UNSUPPORTED;
+  if (epi.group_offsets && (epi.n_groups <= 0 || epi.n_groups > 250)) return QWEN_ERR_UNSUPPORTED;
+  constexpr int BN = 256;
+  const uint64_t b_rows = epi.group_offsets ? (uint64_t)N * epi.n_groups : (uint64_t)N;
+  CUtensorMap ta, tb;
+  if (!make_tmap_bf16(&ta, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, kBM)) return QWEN_ERR_CUDA;
+  if (!make_tmap_bf16(&tb, B, b_rows, (uint64_t)K, (uint64_t)ldb, BN)) return QWEN_ERR_CUDA;
+  const int sms = device_sm_count();
+  int tiles;
+  if (epi.group_offsets) {
+    tiles = sms;  // the number of tiles is only known on the device
+  } else {
+    tiles = ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
+  }
+  const int grid = tiles < sms ? tiles : sms;
+  switch (epi.mode) {
+    case EPI_STORE: return launch_bn<BN, EPI_STORE>(ta, tb, M, N, K, epi, err, grid, st);
+    case EPI_RESID: return launch_bn<BN, EPI_RESID>(ta, tb, M, N, K, epi, err, grid, st);
+    case EPI_SWIGLU: return launch_bn<BN, EPI_SWIGLU>(ta, tb, M, N, K, epi, err, grid, st);
+    case EPI_QKV: return launch_bn<BN, EPI_QKV>(ta, tb, M, N, K, epi, err, grid, st);
+    case EPI_F32: return launch_bn<BN, EPI_F32>(ta, tb, M, N, K, epi, err, grid, st);
+    default: return QWEN_ERR_INVALID_ARG;
+  }
+}
+
+}  // namespace qwen

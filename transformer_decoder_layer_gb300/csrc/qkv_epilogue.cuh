@@ -1,0 +1,93 @@
+// Per-(token, head) finish of the fused QKV projection: bias, Qwen3 QK-norm,
+// rotate_half RoPE, then Q store or K/V cache append.  Used by the prefill GEMM
+// epilogue and by the decode split-K reduction, so both paths share one
+// definition of the step.
+//
+// Qwen3 layer page ("推理系统 03"): §4 projections, §5 per-head RMSNorm over dh
+// with one shared gamma for Q and one for K (V untouched), §6 RoPE pairing
+// (i, i + dh/2) by angle p * theta^(-2i/dh) (cos/sin read from a table built in
+// FP64 on the host), §12 the cache keeps K after QK-norm and RoPE.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace qwen {
+
+template <int DH>
+__device__ __forceinline__ void qkv_head_finish(float (&v)[DH], int m, int head,
+                                                const QkvParams& p, int* err) {
+  const int kind = head < p.Hq ? 0 : (head < p.Hq + p.Hkv ? 1 : 2);  // q, k, v
+  if (p.bias) {
+    const float4* bb = reinterpret_cast<const float4*>(p.bias + (size_t)head * DH);
+#pragma unroll
+    for (int i = 0; i < DH / 4; ++i) {
+      const float4 b4 = __ldg(bb + i);
+      v[4 * i] += b4.x;
+      v[4 * i + 1] += b4.y;
+      v[4 * i + 2] += b4.z;
+      v[4 * i + 3] += b4.w;
+    }
+  }
+  if (kind < 2) {
+    if (p.gamma_q) {
+      float ss = 0.f;
+#pragma unroll
+      for (int i = 0; i < DH; ++i) ss = fmaf(v[i], v[i], ss);
+      const float rstd = rsqrtf(ss / (float)DH + p.eps);
+      const uint4* g4 = reinterpret_cast<const uint4*>(kind == 0 ? p.gamma_q : p.gamma_k);
+#pragma unroll
+      for (int i = 0; i < DH / 8; ++i) {
+        const uint4 gu = __ldg(g4 + i);
+        const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 g = unpack_bf16x2(gw[j]);
+          v[8 * i + 2 * j] = g.x * (v[8 * i + 2 * j] * rstd);
+          v[8 * i + 2 * j + 1] = g.y * (v[8 * i + 2 * j + 1] * rstd);
+        }
+      }
+    }
+    const int pos = p.positions[m];
+    if (pos < 0 || pos >= p.max_position) {
+      record_error(err, QWEN_ERR_RANGE);
+      return;
+    }
+    const float4* tab = reinterpret_cast<const float4*>(p.rope + (size_t)pos * (DH / 2));
+#pragma unroll
+    for (int i = 0; i < DH / 4; ++i) {
+      const float4 cs = __ldg(tab + i);  // (cos, sin) of pairs 2i and 2i+1
+      const float a0 = v[2 * i], b0 = v[2 * i + DH / 2];
+      const float a1 = v[2 * i + 1], b1 = v[2 * i + 1 + DH / 2];
+      v[2 * i] = a0 * cs.x - b0 * cs.y;
+      v[2 * i + DH / 2] = b0 * cs.x + a0 * cs.y;
+      v[2 * i + 1] = a1 * cs.z - b1 * cs.w;
+      v[2 * i + 1 + DH / 2] = b1 * cs.z + a1 * cs.w;
+    }
+  }
+  const int b = m / p.T, t = m - (m / p.T) * p.T;
+  bf16* dst;
+  if (kind == 0) {
+    dst = p.q_out + (((size_t)b * p.Hq + head) * p.T + t) * DH;
+  } else {
+    const int slot = p.slot0[b] + t;
+    if (slot < 0 || slot >= p.max_seq) {
+      record_error(err, QWEN_ERR_RANGE);
+      return;
+    }
+    const int g = kind == 1 ? head - p.Hq : head - p.Hq - p.Hkv;
+    dst = (kind == 1 ? p.k_cache : p.v_cache) + (((size_t)b * p.Hkv + g) * p.max_seq + slot) * DH;
+  }
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < DH / 8; ++i) {
+    uint4 o;
+    o.x = pack_bf16x2(v[8 * i], v[8 * i + 1]);
+    o.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+    o.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+    o.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+    d4[i] = o;
+  }
+}
+
+}  // namespace qwen

@@ -1,0 +1,103 @@
+// RMSNorm over the feature axis, one warp per row, 128-bit loads/stores.
+//
+// Qwen3 layer page ("推理系统 03"), §3: y_j = gamma_j x_j / sqrt(mean_k x_k^2 + eps),
+// with the mean square accumulated in FP32.  The whole row stays in registers
+// between the reduction and the scaling, so each element is read once.
+#include "common.cuh"
+#include "internal.h"
+
+namespace qwen {
+
+template <int MAXC>
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x,
+                                                      const float* __restrict__ x32,
+                                                      const bf16* __restrict__ gamma,
+                                                      bf16* __restrict__ y,
+                                                      float* __restrict__ y32, int rows, int d,
+                                                      float eps) {
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int nch = d >> 3;  // 8-element chunks
+  float v[MAXC][8];
+  float ss = 0.f;
+  if (x32) {
+    const float4* xr = reinterpret_cast<const float4*>(x32 + (size_t)row * d);
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nch) {
+        const float4 a = xr[2 * c], b = xr[2 * c + 1];
+        v[i][0] = a.x; v[i][1] = a.y; v[i][2] = a.z; v[i][3] = a.w;
+        v[i][4] = b.x; v[i][5] = b.y; v[i][6] = b.z; v[i][7] = b.w;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ss = fmaf(v[i][j], v[i][j], ss);
+      }
+    }
+  } else {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * d);
+#pragma unroll
+    for (int i = 0; i < MAXC; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nch) {
+        const uint4 u = xr[c];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = unpack_bf16x2(w[j]);
+          v[i][2 * j] = f.x;
+          v[i][2 * j + 1] = f.y;
+          ss = fmaf(f.x, f.x, ss);
+          ss = fmaf(f.y, f.y, ss);
+        }
+      }
+    }
+  }
+  ss = warp_sum(ss);
+  const float rstd = rsqrtf(ss / (float)d + eps);
+  const uint4* gr = reinterpret_cast<const uint4*>(gamma);
+  uint4* yr = reinterpret_cast<uint4*>(y + (size_t)row * d);
+#pragma unroll
+  for (int i = 0; i < MAXC; ++i) {
+    const int c = lane + 32 * i;
+    if (c < nch) {
+      const uint4 gu = gr[c];
+      const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w};
+      float o[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 g = unpack_bf16x2(gw[j]);
+        o[2 * j] = g.x * (v[i][2 * j] * rstd);
+        o[2 * j + 1] = g.y * (v[i][2 * j + 1] * rstd);
+      }
+      uint4 out;
+      out.x = pack_bf16x2(o[0], o[1]);
+      out.y = pack_bf16x2(o[2], o[3]);
+      out.z = pack_bf16x2(o[4], o[5]);
+      out.w = pack_bf16x2(o[6], o[7]);
+      yr[c] = out;
+      if (y32) {
+        float4* y4 = reinterpret_cast<float4*>(y32 + (size_t)row * d);
+        y4[2 * c] = make_float4(o[0], o[1], o[2], o[3]);
+        y4[2 * c + 1] = make_float4(o[4], o[5], o[6], o[7]);
+      }
+    }
+  }
+}
+
+qwen_status rmsnorm_launch(const bf16* x, const bf16* gamma, bf16* y, float* y32,
+                           const float* x32, int rows, int d, float eps, cudaStream_t st) {
+  if (rows == 0) return QWEN_OK;
+  if (d <= 0 || (d & 7) || d > 8192) return QWEN_ERR_UNSUPPORTED;
+  const int threads = 256;
+  const int blocks = (rows * 32 + threads - 1) / threads;
+  if (d <= 2048)
+    rmsnorm_kernel<8><<<blocks, threads, 0, st>>>(x, x32, gamma, y, y32, rows, d, eps);
+  else if (d <= 4096)
+    rmsnorm_kernel<16><<<blocks, threads, 0, st>>>(x, x32, gamma, y, y32, rows, d, eps);
+  else
+    rmsnorm_kernel<32><<<blocks, threads, 0, st>>>(x, x32, gamma, y, y32, rows, d, eps);
+  return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
+}
+
+}  // namespace qwen
