@@ -62,8 +62,8 @@ qwen_status qwen_rmsnorm(const void* x, const void* gamma, void* y, float* y_fp3
   if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y) |
        reinterpret_cast<uintptr_t>(gamma)) & 15)
     return QWEN_ERR_INVALID_ARG;
-  return rmsnorm_launch(static_cast<const bf16*>(x), static_cast<const bf16*>(gamma),
-                        static_cast<bf16*>(y), y_fp32, nullptr, rows, d, eps,
+  return rmsnorm_launch(static_cast<const bf16*>(x), static_cast<const bf16*>(gamma), y,
+                        /*y_f16=*/false, y_fp32, nullptr, rows, d, eps,
                         static_cast<cudaStream_t>(stream));
 }
 
@@ -75,10 +75,10 @@ qwen_status qwen_linear(const void* x, const void* w, void* y, int32_t M, int32_
   if ((K & 7) || (N & 7)) return QWEN_ERR_UNSUPPORTED;
   GemmEpilogue epi{};
   epi.mode = EPI_STORE;
-  epi.out = static_cast<bf16*>(y);
+  epi.out = y;
   epi.ldo = N;
-  return gemm_tc(static_cast<const bf16*>(x), K, static_cast<const bf16*>(w), K, M, N, K, epi,
-                 lib_status_ptr(), static_cast<cudaStream_t>(stream));
+  return gemm_tc(x, K, w, K, M, N, K, /*op_f16=*/false, epi, lib_status_ptr(),
+                 static_cast<cudaStream_t>(stream));
 }
 
 qwen_status qwen_poll_error(void* stream) {

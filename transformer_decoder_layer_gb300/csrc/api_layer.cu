@@ -1,0 +1,561 @@
+// C ABI of the layer handle: validation, weight packing, workspace layout and
+// the orchestration of prefill / decode / MoE on the caller's stream.
+//
+// Layer structure, Qwen3 layer page ("推理系统 03"), §2:
+//   R = X + Attention(RMSNorm_1(X)),  Y = R + MLP(RMSNorm_2(R)).
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+#include "layer.h"
+
+namespace qwen {
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool config_valid(const qwen_layer_config& c) {
+  if (c.d <= 0 || c.d % 64 || c.d > 8192) return false;
+  if (c.n_q_heads <= 0 || c.n_kv_heads <= 0 || c.n_q_heads % c.n_kv_heads) return false;
+  if (c.n_q_heads / c.n_kv_heads > 16) return false;
+  if (c.head_dim != 64 && c.head_dim != 128) return false;
+  if (c.ffn <= 0 || c.ffn % 64) return false;
+  if (!(c.rope_theta > 0.0) || !(c.rms_eps >= 0.f)) return false;
+  if (c.qkv_bias != 0 && c.qkv_bias != 1) return false;
+  if (c.qk_norm != 0 && c.qk_norm != 1) return false;
+  if (c.n_experts < 0 || c.n_experts > 256) return false;
+  if (c.n_experts > 0) {
+    if (c.top_k < 1 || c.top_k > 8 || c.top_k > c.n_experts) return false;
+    if (c.norm_topk_prob != 1) return false;
+  }
+  if (c.max_tokens <= 0 || c.max_batch <= 0 || c.max_seq <= 0 || c.max_position <= 0) return false;
+  return true;
+}
+
+PackedLayout packed_layout(const qwen_layer_config& c) {
+  PackedLayout L{};
+  const size_t d = c.d, dh = c.head_dim, nq = (size_t)c.n_q_heads * dh,
+               nkv = (size_t)c.n_kv_heads * dh, nqkv = nq + 2 * nkv, f = c.ffn;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  L.status = take(256);
+  L.rope = take((size_t)c.max_position * (dh / 2) * sizeof(float2));
+  L.gamma_attn = take(d * 2);
+  L.gamma_mlp = take(d * 2);
+  L.gamma_q = take(dh * 2);
+  L.gamma_k = take(dh * 2);
+  L.w_qkv = take(nqkv * d * 2);
+  L.b_qkv = take(nqkv * 4);
+  L.w_o = take(d * nq * 2);
+  if (c.n_experts == 0) {
+    L.w_gu = take(2 * f * d * 2);
+    L.w_down = take(d * f * 2);
+  } else {
+    const size_t e = c.n_experts;
+    L.w_router = take(e * d * 2);
+    L.b_router = take(e * 4);
+    L.w_gu = take(e * 2 * f * d * 2);
+    L.w_down = take(e * d * f * 2);
+  }
+  L.total = o;
+  return L;
+}
+
+WorkspaceLayout workspace_layout(const qwen_layer_config& c, int B, int T) {
+  WorkspaceLayout W{};
+  const size_t M = (size_t)B * T, d = c.d, dh = c.head_dim, nq = (size_t)c.n_q_heads * dh,
+               f = c.ffn;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  W.xh = take(M * d * 2);
+  W.q = take(M * nq * 2);
+  W.attn = take(M * nq * 2);
+  W.r32 = take(M * d * 4);  // residual stream R kept in FP32
+  W.z = take(M * d * 2);
+  if (c.n_experts == 0) {
+    W.h = take(M * f * 2);
+  } else {
+    const size_t e = c.n_experts, k = c.top_k, mk = M * k;
+    W.z32 = take(M * d * 4);
+    W.logits = take(M * e * 4);
+    W.topk_idx = take(mk * 4);
+    W.topk_w = take(mk * 4);
+    W.offsets = take((e + 1) * 4);
+    W.perm = take(mk * 4);
+    W.inv = take(mk * 4);
+    W.zp = take(mk * d * 2);
+    W.hp = take(mk * f * 2);
+    W.yp = take(mk * d * 2);
+  }
+  if (T == 1) {
+    int chunk = 0, splits = 0;
+    decode_attn_plan(c, B, &chunk, &splits);
+    W.part = take(decode_part_bytes(c, B));
+    W.attn_o = take((size_t)B * c.n_q_heads * splits * dh * 4);
+    W.attn_ml = take((size_t)B * c.n_q_heads * splits * 2 * 4);
+  }
+  W.total = o;
+  return W;
+}
+
+// ------------------------------------------------------------- packing
+
+__global__ void bf16_to_f32_kernel(const bf16* __restrict__ src, float* __restrict__ dst, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) dst[i] = __bfloat162float(src[i]);
+}
+
+static bool copy_d2d(void* dst, const void* src, size_t bytes, cudaStream_t st) {
+  return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st) == cudaSuccess;
+}
+
+// Copy BF16 weight rows into the packed FP16 buffer.  BF16 -> FP16 is exact
+// for magnitudes in [2^-14, 65504] (FP16 keeps more mantissa bits); smaller
+// magnitudes land on the FP16 subnormal grid (absolute error <= 2^-25) and
+// larger ones saturate.  Row placement: mode 0 keeps the row order; modes 1
+// and 2 interleave gate (1) and up (2) rows in 64-row blocks, block 2i = gate
+// block i and block 2i+1 = up block i, so one GEMM tile holds both halves of
+// every SwiGLU output feature.
+__global__ void pack_rows_f16_kernel(f16* __restrict__ dst, const bf16* __restrict__ src,
+                                     size_t rows, int d, int mode) {
+  const int cpr = d / 8;  // 16-byte chunks per row
+  const size_t nch = rows * (size_t)cpr;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nch;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = i / cpr;
+    const int c = (int)(i - r * cpr);
+    const size_t dr = mode == 0 ? r : (r / 64) * 128 + (r % 64) + (mode == 2 ? 64 : 0);
+    const uint4 u = reinterpret_cast<const uint4*>(src)[i];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = unpack_bf16x2(w[j]);
+      o[j] = pack_f16x2(fminf(fmaxf(f.x, -65504.f), 65504.f), fminf(fmaxf(f.y, -65504.f), 65504.f));
+    }
+    reinterpret_cast<uint4*>(dst)[dr * cpr + c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+static bool pack_rows(f16* dst, const void* src, size_t rows, size_t d, int mode,
+                      cudaStream_t st) {
+  if (rows == 0) return true;
+  const size_t nch = rows * (d / 8);
+  const int blocks = (int)((nch + 255) / 256 < 65535 ? (nch + 255) / 256 : 65535);
+  pack_rows_f16_kernel<<<blocks, 256, 0, st>>>(dst, static_cast<const bf16*>(src), rows, (int)d,
+                                               mode);
+  return cudaGetLastError() == cudaSuccess;
+}
+
+}  // namespace qwen
+
+using namespace qwen;
+
+extern "C" {
+
+size_t qwen_layer_packed_bytes(const qwen_layer_config* cfg) {
+  if (!cfg || !config_valid(*cfg)) return 0;
+  return packed_layout(*cfg).total;
+}
+
+size_t qwen_layer_workspace_bytes(const qwen_layer_config* cfg, int32_t B, int32_t T) {
+  if (!cfg || !config_valid(*cfg) || B <= 0 || T <= 0) return 0;
+  return workspace_layout(*cfg, B, T).total;
+}
+
+qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_weights* w,
+                              void* packed, size_t packed_bytes, void* stream,
+                              qwen_layer_t* out) {
+  if (!cfg || !w || !packed || !out) return QWEN_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!config_valid(*cfg)) {
+    if (cfg->head_dim != 64 && cfg->head_dim != 128 && cfg->head_dim > 0)
+      return QWEN_ERR_UNSUPPORTED;
+    return QWEN_ERR_INVALID_ARG;
+  }
+  const qwen_layer_config& c = *cfg;
+  const PackedLayout L = packed_layout(c);
+  if (packed_bytes < L.total) return QWEN_ERR_CAPACITY;
+  if (reinterpret_cast<uintptr_t>(packed) & 255) return QWEN_ERR_INVALID_ARG;
+  const bool moe = c.n_experts > 0;
+  if (!w->gamma_attn || !w->gamma_mlp || !w->w_q || !w->w_k || !w->w_v || !w->w_o ||
+      !w->w_gate || !w->w_up || !w->w_down)
+    return QWEN_ERR_INVALID_ARG;
+  if (c.qk_norm && (!w->gamma_q || !w->gamma_k)) return QWEN_ERR_INVALID_ARG;
+  if (c.qkv_bias && (!w->b_q || !w->b_k || !w->b_v)) return QWEN_ERR_INVALID_ARG;
+  if (moe && (!w->w_router || (c.router_bias && !w->b_router))) return QWEN_ERR_INVALID_ARG;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* P = static_cast<uint8_t*>(packed);
+  const size_t d = c.d, dh = c.head_dim, nq = (size_t)c.n_q_heads * dh,
+               nkv = (size_t)c.n_kv_heads * dh, f = c.ffn;
+
+  qwen_layer_s* h = new (std::nothrow) qwen_layer_s();
+  if (!h) return QWEN_ERR_CAPACITY;
+  h->cfg = c;
+  h->packed = P;
+  h->L = L;
+  h->status = reinterpret_cast<int*>(P + L.status);
+  h->rope = reinterpret_cast<float2*>(P + L.rope);
+  h->gamma_attn = reinterpret_cast<bf16*>(P + L.gamma_attn);
+  h->gamma_mlp = reinterpret_cast<bf16*>(P + L.gamma_mlp);
+  h->gamma_q = c.qk_norm ? reinterpret_cast<bf16*>(P + L.gamma_q) : nullptr;
+  h->gamma_k = c.qk_norm ? reinterpret_cast<bf16*>(P + L.gamma_k) : nullptr;
+  h->w_qkv = reinterpret_cast<f16*>(P + L.w_qkv);
+  h->b_qkv = c.qkv_bias ? reinterpret_cast<float*>(P + L.b_qkv) : nullptr;
+  h->w_o = reinterpret_cast<f16*>(P + L.w_o);
+  h->w_gu = reinterpret_cast<f16*>(P + L.w_gu);
+  h->w_down = reinterpret_cast<f16*>(P + L.w_down);
+  h->w_router = moe ? reinterpret_cast<bf16*>(P + L.w_router) : nullptr;
+  h->b_router = (moe && c.router_bias) ? reinterpret_cast<float*>(P + L.b_router) : nullptr;
+
+  bool ok = cudaMemsetAsync(h->status, 0, 256, st) == cudaSuccess;
+  ok = ok && copy_d2d(h->gamma_attn, w->gamma_attn, d * 2, st);
+  ok = ok && copy_d2d(h->gamma_mlp, w->gamma_mlp, d * 2, st);
+  if (c.qk_norm) {
+    ok = ok && copy_d2d(h->gamma_q, w->gamma_q, dh * 2, st);
+    ok = ok && copy_d2d(h->gamma_k, w->gamma_k, dh * 2, st);
+  }
+  ok = ok && pack_rows(h->w_qkv, w->w_q, nq, d, 0, st);
+  ok = ok && pack_rows(h->w_qkv + nq * d, w->w_k, nkv, d, 0, st);
+  ok = ok && pack_rows(h->w_qkv + (nq + nkv) * d, w->w_v, nkv, d, 0, st);
+  if (c.qkv_bias && ok) {
+    bf16_to_f32_kernel<<<(int)((nq + 255) / 256), 256, 0, st>>>(
+        static_cast<const bf16*>(w->b_q), h->b_qkv, (int)nq);
+    bf16_to_f32_kernel<<<(int)((nkv + 255) / 256), 256, 0, st>>>(
+        static_cast<const bf16*>(w->b_k), h->b_qkv + nq, (int)nkv);
+    bf16_to_f32_kernel<<<(int)((nkv + 255) / 256), 256, 0, st>>>(
+        static_cast<const bf16*>(w->b_v), h->b_qkv + nq + nkv, (int)nkv);
+    ok = cudaGetLastError() == cudaSuccess;
+  }
+  ok = ok && pack_rows(h->w_o, w->w_o, d, nq, 0, st);
+  const size_t n_exp = moe ? (size_t)c.n_experts : 1;
+  ok = ok && pack_rows(h->w_gu, w->w_gate, n_exp * f, d, 1, st);
+  ok = ok && pack_rows(h->w_gu, w->w_up, n_exp * f, d, 2, st);
+  ok = ok && pack_rows(h->w_down, w->w_down, n_exp * d, f, 0, st);
+  if (moe) {
+    ok = ok && copy_d2d(h->w_router, w->w_router, n_exp * d * 2, st);
+    if (c.router_bias) ok = ok && copy_d2d(h->b_router, w->b_router, n_exp * 4, st);
+  }
+  // RoPE table: (cos, sin) of p * theta^(-2i/dh), angles and trig in FP64.
+  // Qwen3 layer page, §6 (frequency equation).
+  if (ok) {
+    const int half = c.head_dim / 2;
+    std::vector<float2> tab((size_t)c.max_position * half);
+    for (int i = 0; i < half; ++i) {
+      const double omega = std::pow(c.rope_theta, -2.0 * i / (double)c.head_dim);
+      for (int p = 0; p < c.max_position; ++p) {
+        const double ang = (double)p * omega;
+        tab[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      }
+    }
+    ok = cudaMemcpyAsync(h->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice,
+                         st) == cudaSuccess;
+    ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
+  }
+  if (!ok) {
+    delete h;
+    return QWEN_ERR_CUDA;
+  }
+  *out = h;
+  return QWEN_OK;
+}
+
+void qwen_layer_destroy(qwen_layer_t layer) { delete layer; }
+
+qwen_status qwen_layer_poll_error(qwen_layer_t layer, void* stream) {
+  if (!layer) return QWEN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return QWEN_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, layer->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return QWEN_ERR_CUDA;
+  if (v) {
+    if (cudaMemset(layer->status, 0, sizeof(int)) != cudaSuccess) return QWEN_ERR_CUDA;
+  }
+  return static_cast<qwen_status>(v);
+}
+
+qwen_status qwen_layer_prefill(qwen_layer_t layer, const void* x, void* y, int32_t B, int32_t T,
+                               const int32_t* positions, const int32_t* cache_start,
+                               void* k_cache, void* v_cache, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (!layer) return QWEN_ERR_INVALID_ARG;
+  const qwen_layer_config& c = layer->cfg;
+  if (B < 0 || T < 0) return QWEN_ERR_INVALID_ARG;
+  if (B == 0 || T == 0) return QWEN_OK;
+  if (!x || !y || !positions || !cache_start || !k_cache || !v_cache || !workspace)
+    return QWEN_ERR_INVALID_ARG;
+  if (x == y) return QWEN_ERR_INVALID_ARG;
+  if (B > c.max_batch || (int64_t)B * T > c.max_tokens || T > c.max_seq) return QWEN_ERR_CAPACITY;
+  const WorkspaceLayout W = workspace_layout(c, B, T);
+  if (workspace_bytes < W.total) return QWEN_ERR_CAPACITY;
+  if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(x) |
+       reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(k_cache) |
+       reinterpret_cast<uintptr_t>(v_cache)) & 15)
+    return QWEN_ERR_INVALID_ARG;
+  return layer_prefill(layer, static_cast<const bf16*>(x), static_cast<bf16*>(y), B, T,
+                       positions, cache_start, static_cast<bf16*>(k_cache),
+                       static_cast<bf16*>(v_cache), static_cast<uint8_t*>(workspace), W,
+                       static_cast<cudaStream_t>(stream));
+}
+
+qwen_status qwen_layer_decode(qwen_layer_t layer, const void* x, void* y, int32_t B,
+                              const int32_t* positions, const int32_t* cache_len, void* k_cache,
+                              void* v_cache, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  if (!layer) return QWEN_ERR_INVALID_ARG;
+  const qwen_layer_config& c = layer->cfg;
+  if (B < 0) return QWEN_ERR_INVALID_ARG;
+  if (B == 0) return QWEN_OK;
+  if (!x || !y || !positions || !cache_len || !k_cache || !v_cache || !workspace)
+    return QWEN_ERR_INVALID_ARG;
+  if (x == y) return QWEN_ERR_INVALID_ARG;
+  if (B > c.max_batch || B > c.max_tokens) return QWEN_ERR_CAPACITY;
+  const WorkspaceLayout W = workspace_layout(c, B, 1);
+  if (workspace_bytes < W.total) return QWEN_ERR_CAPACITY;
+  if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(x) |
+       reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(k_cache) |
+       reinterpret_cast<uintptr_t>(v_cache)) & 15)
+    return QWEN_ERR_INVALID_ARG;
+  return layer_decode(layer, static_cast<const bf16*>(x), static_cast<bf16*>(y), B, positions,
+                      cache_len, static_cast<bf16*>(k_cache), static_cast<bf16*>(v_cache),
+                      static_cast<uint8_t*>(workspace), W, static_cast<cudaStream_t>(stream));
+}
+
+qwen_status qwen_moe_ffn(qwen_layer_t layer, const void* r, const float* r_fp32, void* y,
+                         int32_t T, int32_t* topk_idx, float* topk_w, float* logits,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  if (!layer) return QWEN_ERR_INVALID_ARG;
+  const qwen_layer_config& c = layer->cfg;
+  if (c.n_experts == 0) return QWEN_ERR_UNSUPPORTED;
+  if (T < 0) return QWEN_ERR_INVALID_ARG;
+  if (T == 0) return QWEN_OK;
+  if (!r || !y || !workspace || r == y) return QWEN_ERR_INVALID_ARG;
+  if (T > c.max_tokens) return QWEN_ERR_CAPACITY;
+  const WorkspaceLayout W = workspace_layout(c, 1, T);
+  if (workspace_bytes < W.total) return QWEN_ERR_CAPACITY;
+  if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(r) |
+       reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(r_fp32)) & 15)
+    return QWEN_ERR_INVALID_ARG;
+  return moe_forward(layer, static_cast<const bf16*>(r), r_fp32, static_cast<bf16*>(y), T,
+                     topk_idx, topk_w, logits, static_cast<uint8_t*>(workspace), W,
+                     static_cast<cudaStream_t>(stream));
+}
+
+size_t qwen_head_workspace_bytes(int32_t B, int32_t d, int32_t V) {
+  if (B <= 0 || d <= 0 || V <= 0) return 0;
+  const size_t xn = align256((size_t)B * d * 2);
+  if (B > 256) return xn;
+  const size_t ldp = (B + 3) & ~3;
+  return xn + align256((size_t)decode_splits(V, d) * V * ldp * 4);
+}
+
+qwen_status qwen_head_last_token(const void* y, int32_t B, int32_t T, int32_t d,
+                                 const void* gamma_final, const void* w_lm, int32_t V, float eps,
+                                 float* logits, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  if (B < 0 || T <= 0 || d <= 0 || V <= 0) return QWEN_ERR_INVALID_ARG;
+  if (B == 0) return QWEN_OK;
+  if (!y || !gamma_final || !w_lm || !logits || !workspace) return QWEN_ERR_INVALID_ARG;
+  if ((d & 63) || d > 8192 || (V & 7)) return QWEN_ERR_UNSUPPORTED;
+  if (workspace_bytes < qwen_head_workspace_bytes(B, d, V)) return QWEN_ERR_CAPACITY;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  bf16* xn = static_cast<bf16*>(workspace);
+  const bf16* last = static_cast<const bf16*>(y) + (size_t)(T - 1) * d;
+  qwen_status s = rmsnorm_launch(last, static_cast<const bf16*>(gamma_final), xn, false, nullptr,
+                                 nullptr, B, d, eps, st, (size_t)T * d);
+  if (s) return s;
+  int* err = lib_status_ptr();
+  if (B > 256) {
+    GemmEpilogue e{};
+    e.mode = EPI_F32;
+    e.out32 = logits;
+    e.ldo32 = V;
+    return gemm_tc(xn, d, w_lm, d, B, V, d, /*op_f16=*/false, e, err, st);
+  }
+  float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                         align256((size_t)B * d * 2));
+  const int S = decode_splits(V, d);
+  if ((s = gemm_decode_splitk(w_lm, xn, d, B, V, d, S, /*op_f16=*/false, part, err, st)))
+    return s;
+  return reduce_f32(part, S, B, V, logits, V, st);
+}
+
+}  // extern "C"
+
+namespace qwen {
+
+// One projection of a decode step: swap-AB split-K on the tensor cores, then
+// the reduction that applies the step's epilogue.
+enum DecEpi { DEC_QKV, DEC_RESID, DEC_SWIGLU };
+
+static qwen_status decode_proj(const f16* Wt, const f16* X, int B, int N, int K, float* part,
+                               int* err, cudaStream_t st, int& splits) {
+  splits = decode_splits(N, K);
+  return gemm_decode_splitk(Wt, X, K, B, N, K, splits, /*op_f16=*/true, part, err, st);
+}
+
+qwen_status layer_decode(qwen_layer_s* L, const bf16* x, bf16* y, int B, const int32_t* positions,
+                         const int32_t* cache_len, bf16* kc, bf16* vc, uint8_t* ws,
+                         const WorkspaceLayout& W, cudaStream_t st) {
+  const qwen_layer_config& c = L->cfg;
+  const int d = c.d, dh = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
+  const int nq = Hq * dh, nqkv = nq + 2 * Hkv * dh, f = c.ffn;
+  f16* xh = reinterpret_cast<f16*>(ws + W.xh);
+  bf16* q = reinterpret_cast<bf16*>(ws + W.q);
+  f16* attn = reinterpret_cast<f16*>(ws + W.attn);
+  float* r32 = reinterpret_cast<float*>(ws + W.r32);
+  float* part = reinterpret_cast<float*>(ws + W.part);
+  int* err = L->status;
+  qwen_status s;
+  int S = 1;
+  const bool swap = B <= 256;
+
+  if ((s = rmsnorm_launch(x, L->gamma_attn, xh, true, nullptr, nullptr, B, d, c.rms_eps, st)))
+    return s;
+  const QkvParams qp = make_qkv_params(L, positions, cache_len, q, kc, vc, 1);
+  if (swap) {
+    if ((s = decode_proj(L->w_qkv, xh, B, nqkv, d, part, err, st, S))) return s;
+    if ((s = reduce_qkv(part, S, B, nqkv, qp, err, st))) return s;
+  } else {
+    GemmEpilogue e{};
+    e.mode = EPI_QKV;
+    e.qkv = qp;
+    if ((s = gemm_tc(xh, d, L->w_qkv, d, B, nqkv, d, true, e, err, st))) return s;
+  }
+  int chunk = 0, splits = 0;
+  decode_attn_plan(c, B, &chunk, &splits);
+  if ((s = attention_decode(q, kc, vc, cache_len, B, Hq, Hkv, dh, c.max_seq, chunk, splits,
+                            reinterpret_cast<float*>(ws + W.attn_o),
+                            reinterpret_cast<float*>(ws + W.attn_ml), attn, err, st)))
+    return s;
+  if (swap) {
+    if ((s = decode_proj(L->w_o, attn, B, d, nq, part, err, st, S))) return s;
+    if ((s = reduce_resid(part, S, B, d, x, nullptr, nullptr, r32, st))) return s;
+  } else {
+    GemmEpilogue e{};
+    e.mode = EPI_RESID;
+    e.out = nullptr;
+    e.resid = x;
+    e.ldr = d;
+    e.out32 = r32;
+    e.ldo32 = d;
+    if ((s = gemm_tc(attn, nq, L->w_o, nq, B, d, nq, true, e, err, st))) return s;
+  }
+  if (c.n_experts)
+    return moe_forward(L, nullptr, r32, y, B, nullptr, nullptr, nullptr, ws, W, st);
+  f16* z = reinterpret_cast<f16*>(ws + W.z);
+  f16* hbuf = reinterpret_cast<f16*>(ws + W.h);
+  if ((s = rmsnorm_launch(nullptr, L->gamma_mlp, z, true, nullptr, r32, B, d, c.rms_eps, st)))
+    return s;
+  if (swap) {
+    if ((s = decode_proj(L->w_gu, z, B, 2 * f, d, part, err, st, S))) return s;
+    if ((s = reduce_swiglu(part, S, B, f, hbuf, st))) return s;
+    if ((s = decode_proj(L->w_down, hbuf, B, d, f, part, err, st, S))) return s;
+    return reduce_resid(part, S, B, d, nullptr, r32, y, nullptr, st);
+  }
+  GemmEpilogue eg{};
+  eg.mode = EPI_SWIGLU;
+  eg.out = hbuf;
+  eg.out_f16 = 1;
+  eg.ldo = f;
+  if ((s = gemm_tc(z, d, L->w_gu, d, B, 2 * f, d, true, eg, err, st))) return s;
+  GemmEpilogue ed{};
+  ed.mode = EPI_RESID;
+  ed.out = y;
+  ed.ldo = d;
+  ed.resid32 = r32;
+  ed.ldr = d;
+  return gemm_tc(hbuf, f, L->w_down, f, B, d, f, true, ed, err, st);
+}
+
+qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, bf16* y, int B, int T,
+                          const int32_t* positions, const int32_t* slot0, bf16* kc, bf16* vc,
+                          uint8_t* ws, const WorkspaceLayout& W, cudaStream_t st) {
+  const qwen_layer_config& c = L->cfg;
+  const int M = B * T, d = c.d, dh = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
+  const int nq = Hq * dh, nqkv = nq + 2 * Hkv * dh, f = c.ffn;
+  f16* xh = reinterpret_cast<f16*>(ws + W.xh);
+  bf16* q = reinterpret_cast<bf16*>(ws + W.q);
+  f16* attn = reinterpret_cast<f16*>(ws + W.attn);
+  float* r32 = reinterpret_cast<float*>(ws + W.r32);
+  int* err = L->status;
+  qwen_status s;
+
+  // RMSNorm_1
+  if ((s = rmsnorm_launch(x, L->gamma_attn, xh, true, nullptr, nullptr, M, d, c.rms_eps, st)))
+    return s;
+  // fused QKV: bias, QK-norm, RoPE, Q store, K/V cache append
+  GemmEpilogue e{};
+  e.mode = EPI_QKV;
+  e.qkv = make_qkv_params(L, positions, slot0, q, kc, vc, T);
+  if ((s = gemm_tc(xh, d, L->w_qkv, d, M, nqkv, d, true, e, err, st))) return s;
+  // causal GQA attention over the cache
+  if ((s = attention_prefill(q, kc, vc, slot0, attn, B, T, Hq, Hkv, dh, c.max_seq, err, st)))
+    return s;
+  // O projection + residual; R stays in FP32 (it reaches Y unchanged through
+  // the second residual, so rounding it to BF16 would put that rounding on Y)
+  GemmEpilogue eo{};
+  eo.mode = EPI_RESID;
+  eo.out = nullptr;
+  eo.resid = x;
+  eo.ldr = d;
+  eo.out32 = r32;
+  eo.ldo32 = d;
+  if ((s = gemm_tc(attn, nq, L->w_o, nq, M, d, nq, true, eo, err, st))) return s;
+  if (c.n_experts) return moe_forward(L, nullptr, r32, y, M, nullptr, nullptr, nullptr, ws, W, st);
+  // RMSNorm_2, gate/up + SiLU*mul, down + residual
+  f16* z = reinterpret_cast<f16*>(ws + W.z);
+  f16* hbuf = reinterpret_cast<f16*>(ws + W.h);
+  if ((s = rmsnorm_launch(nullptr, L->gamma_mlp, z, true, nullptr, r32, M, d, c.rms_eps, st)))
+    return s;
+  GemmEpilogue eg{};
+  eg.mode = EPI_SWIGLU;
+  eg.out = hbuf;
+  eg.out_f16 = 1;
+  eg.ldo = f;
+  if ((s = gemm_tc(z, d, L->w_gu, d, M, 2 * f, d, true, eg, err, st))) return s;
+  GemmEpilogue ed{};
+  ed.mode = EPI_RESID;
+  ed.out = y;
+  ed.ldo = d;
+  ed.resid32 = r32;
+  ed.ldr = d;
+  return gemm_tc(hbuf, f, L->w_down, f, M, d, f, true, ed, err, st);
+}
+
+QkvParams make_qkv_params(const qwen_layer_s* L, const int32_t* positions, const int32_t* slot0,
+                          bf16* q, bf16* kc, bf16* vc, int T) {
+  const qwen_layer_config& c = L->cfg;
+  QkvParams p{};
+  p.bias = L->b_qkv;
+  p.gamma_q = L->gamma_q;
+  p.gamma_k = L->gamma_k;
+  p.rope = L->rope;
+  p.positions = positions;
+  p.slot0 = slot0;
+  p.q_out = q;
+  p.k_cache = kc;
+  p.v_cache = vc;
+  p.T = T;
+  p.Hq = c.n_q_heads;
+  p.Hkv = c.n_kv_heads;
+  p.dh = c.head_dim;
+  p.max_seq = c.max_seq;
+  p.max_position = c.max_position;
+  p.eps = c.rms_eps;
+  return p;
+}
+
+}  // namespace qwen

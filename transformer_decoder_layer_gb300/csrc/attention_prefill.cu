@@ -54,7 +54,7 @@ struct AttnCfg {
 struct AttnArgs {
   int B, T, Hq, Hkv, max_seq;
   const int32_t* slot0;  // [B] cache slot of the first new token
-  bf16* out;             // [B*T][Hq*DH]
+  f16* out;              // [B*T][Hq*DH], FP16 operand of the O projection
   float scale_log2;      // log2(e) / sqrt(dh)
   int* err;
 };
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc_fence_after();
       const float inv_l = 1.f / l_sum;
       const bool row_ok = t < a.T;
-      bf16* dst = a.out + ((size_t)b * a.T + t) * (size_t)(a.Hq * DH) + (size_t)h * DH;
+      f16* dst = a.out + ((size_t)b * a.T + t) * (size_t)(a.Hq * DH) + (size_t)h * DH;
 #pragma unroll
       for (int c = 0; c < DH / 32; ++c) {
         uint32_t oo[32];
@@ -320,10 +320,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(oo[8 * q]) * inv_l, __uint_as_float(oo[8 * q + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(oo[8 * q + 2]) * inv_l, __uint_as_float(oo[8 * q + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(oo[8 * q + 4]) * inv_l, __uint_as_float(oo[8 * q + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(oo[8 * q + 6]) * inv_l, __uint_as_float(oo[8 * q + 7]) * inv_l);
+            w.x = pack_f16x2(__uint_as_float(oo[8 * q]) * inv_l, __uint_as_float(oo[8 * q + 1]) * inv_l);
+            w.y = pack_f16x2(__uint_as_float(oo[8 * q + 2]) * inv_l, __uint_as_float(oo[8 * q + 3]) * inv_l);
+            w.z = pack_f16x2(__uint_as_float(oo[8 * q + 4]) * inv_l, __uint_as_float(oo[8 * q + 5]) * inv_l);
+            w.w = pack_f16x2(__uint_as_float(oo[8 * q + 6]) * inv_l, __uint_as_float(oo[8 * q + 7]) * inv_l);
             reinterpret_cast<uint4*>(dst + 32 * c)[q] = w;
           }
         }
@@ -385,7 +385,7 @@ static qwen_status launch_dh(const CUtensorMap& q, const CUtensorMap& k, const C
 
 // q [B][Hq][T][dh], caches [B][Hkv][max_seq][dh], out [B*T][Hq*dh].
 qwen_status attention_prefill(const bf16* q, const bf16* k_cache, const bf16* v_cache,
-                              const int32_t* slot0, bf16* out, int B, int T, int Hq, int Hkv,
+                              const int32_t* slot0, f16* out, int B, int T, int Hq, int Hkv,
                               int dh, int max_seq, int* err, cudaStream_t st) {
   if (B == 0 || T == 0) return QWEN_OK;
   CUtensorMap tq, tk, tv;

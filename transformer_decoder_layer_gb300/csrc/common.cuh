@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/qwen_layer.h"
@@ -13,6 +14,7 @@
 namespace qwen {
 
 typedef __nv_bfloat16 bf16;
+typedef __half f16;
 
 // Upper bound on any single wait inside a kernel (ns of %globaltimer).  A wait
 // that runs out records QWEN_ERR_TIMEOUT in the device status word and makes
@@ -153,14 +155,21 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// Instruction descriptor for kind::f16: D = F32, A = B = BF16, both K-major.
-//   bits 4-5 D format (1 = F32), 7-9 A format (1 = BF16), 10-12 B format,
-//   15/16 A/B major (0 = K), 17-22 N >> 3, 24-28 M >> 4.
+// Instruction descriptor for kind::f16 with an FP32 accumulator.
+//   bits 4-5 D format (1 = F32), 7-9 A format and 10-12 B format (0 = F16,
+//   1 = BF16; A and B always share one type), 15/16 A/B major (0 = K-major,
+//   1 = MN-major), 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool f16_operands,
+                                                    bool a_mn_major = false,
+                                                    bool b_mn_major = false) {
+  return (1u << 4) | ((f16_operands ? 0u : 1u) << 7) | ((f16_operands ? 0u : 1u) << 10) |
+         ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major = false,
                                                       bool b_mn_major = false) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
-         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+  return idesc_f32acc(M, N, false, a_mn_major, b_mn_major);
 }
 
 // Shared-memory matrix descriptor with the 128-byte swizzle (layout type 2),
@@ -223,6 +232,21 @@ __device__ __forceinline__ bf16 f2bf(float x) { return __float2bfloat16_rn(x); }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Round a pair to the 16-bit operand type of the next tensor-core step.
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool to_f16) {
+  return to_f16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
+  __half2 v = *reinterpret_cast<__half2*>(&u);
+  return __half22float2(v);
 }
 
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {

@@ -1,0 +1,402 @@
+// Decode-step projections: one token per sequence, so every projection is a
+// skinny product [B x K] x [N x K]^T that is bound by streaming the weight
+// from HBM ("Qwen2.5-7B 结构拆解" §11: single-stream decode speed is bandwidth
+// divided by weight bytes).
+//
+// Swap-AB: the weight is the MMA's A operand (128 weight rows fill the M=128
+// tensor-core tile), the B tokens are its N operand (padded to 16..256).  The
+// K dimension is split so that (n-tile, k-split) units cover every SM; a
+// persistent CTA walks its units with a deep TMA ring so enough weight bytes
+// are in flight.  Each unit writes FP32 partials part[s][n][b]; a reduction
+// kernel sums the splits in a fixed order (deterministic) and applies the
+// step's epilogue (residual add, SiLU*up, or the fused QKV finish).
+#include "common.cuh"
+#include "internal.h"
+#include "layer.h"
+#include "qkv_epilogue.cuh"
+
+#include <cudaTypedefs.h>
+
+namespace qwen {
+
+namespace {
+
+constexpr int kDBM = 128;
+constexpr int kDBK = 64;
+constexpr int kDThreads = 192;
+
+template <int BP>
+struct DecCfg {
+  static constexpr int A_BYTES = kDBM * kDBK * 2;  // 16 KB of weight per stage
+  static constexpr int B_BYTES = BP * kDBK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 12 ? 12 : (200 * 1024) / STAGE_BYTES;
+  static constexpr int TMEM_COLS = 2 * BP < 32 ? 32 : 2 * BP;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+};
+
+}  // namespace
+
+template <int BP>
+__global__ void __launch_bounds__(kDThreads, 1)
+    gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       int B, int N, int K, int splits, int ldp, uint32_t idesc,
+                       float* __restrict__ part, int* err) {
+  using C = DecCfg<BP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles = (N + kDBM - 1) / kDBM;
+  const int n_kblk = (K + kDBK - 1) / kDBK;
+  const int units = n_tiles * splits;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto unit_range = [&](int u, int& n0, int& kb0, int& kb1, int& s) {
+    const int tile = u / splits;
+    s = u - tile * splits;
+    n0 = tile * kDBM;
+    kb0 = (int)(((long long)s * n_kblk) / splits);
+    kb1 = (int)(((long long)(s + 1) * n_kblk) / splits);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmW);
+      tma_prefetch_desc(&tmX);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        int n0, kb0, kb1, s;
+        unit_range(u, n0, kb0, kb1, s);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) goto prod_done;
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          tma_load_2d(sA + stage * C::A_BYTES, &tmW, &full[stage], kb * kDBK, n0);
+          tma_load_2d(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * kDBK, 0);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int i = 0; i < C::STAGES; ++i) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) break;
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    prod_done:;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
+        int n0, kb0, kb1, s;
+        unit_range(u, n0, kb0, kb1, s);
+        const int acc = local & 1;
+        if (!mbar_wait(&tempty[acc], ((local >> 1) & 1) ^ 1u, abort_flag, err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * BP;
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < kDBK / 16; ++k)
+            umma_f16(d, smem_desc_sw128(a0 + 32 * k, 16, 1024), smem_desc_sw128(b0 + 32 * k, 16, 1024),
+                     idesc, (kb != kb0) || k);
+          umma_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+      }
+    }
+  } else {
+    const int q = warp & 3;
+    int local = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
+      int n0, kb0, kb1, s;
+      unit_range(u, n0, kb0, kb1, s);
+      const int acc = local & 1;
+      if (!mbar_wait(&tfull[acc], (local >> 1) & 1, abort_flag, err)) break;
+      tc_fence_after();
+      const int n = n0 + q * 32 + lane;
+      float* dst = part + ((size_t)s * N + n) * ldp;
+#pragma unroll 1
+      for (int c = 0; c < BP; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BP + c, r);
+        tmem_ld_wait();
+        if (n < N && c < B) {
+          if (c + 32 <= B && (ldp & 3) == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              reinterpret_cast<float4*>(dst + c)[i] =
+                  make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                              __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c + i < B) dst[c + i] = __uint_as_float(r[i]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ reductions
+
+__global__ void reduce_resid_kernel(const float* __restrict__ part, int splits, int B, int N,
+                                    int ldp, const bf16* __restrict__ resid,
+                                    const float* __restrict__ resid32, bf16* __restrict__ out,
+                                    float* __restrict__ out32) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // over N * B, b fastest
+  if (i >= N * B) return;
+  const int n = i / B, b = i - n * B;
+  float acc = 0.f;
+  for (int s = 0; s < splits; ++s) acc += part[((size_t)s * N + n) * ldp + b];
+  acc += resid32 ? resid32[(size_t)b * N + n] : __bfloat162float(resid[(size_t)b * N + n]);
+  if (out) out[(size_t)b * N + n] = __float2bfloat16_rn(acc);
+  if (out32) out32[(size_t)b * N + n] = acc;
+}
+
+// h[b][j] = SiLU(gate_j) * up_j with gate row (j/64)*128 + j%64 and up row +64.
+__global__ void reduce_swiglu_kernel(const float* __restrict__ part, int splits, int B, int f,
+                                     int ldp, f16* __restrict__ h) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= f * B) return;
+  const int j = i / B, b = i - j * B;
+  const int n_gate = (j >> 6) * 128 + (j & 63);
+  const int N = 2 * f;
+  float g = 0.f, u = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    g += part[((size_t)s * N + n_gate) * ldp + b];
+    u += part[((size_t)s * N + n_gate + 64) * ldp + b];
+  }
+  h[(size_t)b * f + j] = __float2half_rn(silu_f(g) * u);
+}
+
+template <int DH>
+__global__ void reduce_qkv_kernel(const float* __restrict__ part, int splits, int B, int Nqkv,
+                                  int ldp, QkvParams p, int* err) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // over (b, head)
+  const int heads = p.Hq + 2 * p.Hkv;
+  if (i >= B * heads) return;
+  const int b = i / heads, head = i - b * heads;
+  float v[DH];
+#pragma unroll
+  for (int e = 0; e < DH; ++e) v[e] = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const float* src = part + ((size_t)s * Nqkv + (size_t)head * DH) * ldp + b;
+#pragma unroll
+    for (int e = 0; e < DH; ++e) v[e] += src[(size_t)e * ldp];
+  }
+  qkv_head_finish<DH>(v, b, head, p, err);
+}
+
+__global__ void reduce_f32_kernel(const float* __restrict__ part, int splits, int B, int N, int ldp,
+                                  float* __restrict__ out, int ldo) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= N * B) return;
+  const int n = i / B, b = i - n * B;
+  float acc = 0.f;
+  for (int s = 0; s < splits; ++s) acc += part[((size_t)s * N + n) * ldp + b];
+  out[(size_t)b * ldo + n] = acc;
+}
+
+// ------------------------------------------------------------------ host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 enc_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+static bool tmap2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                   uint32_t box_rows, bool f16) {
+  auto enc = enc_fn();
+  if (!enc || (reinterpret_cast<uintptr_t>(base) & 15) || ((ld * 2) & 15)) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kDBK, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int pad_batch(int B) {
+  if (B <= 16) return 16;
+  if (B <= 32) return 32;
+  if (B <= 64) return 64;
+  if (B <= 128) return 128;
+  return 256;
+}
+
+int decode_splits(int N, int K) {
+  const int sms = device_sm_count();
+  const int tiles = (N + kDBM - 1) / kDBM;
+  const int kblk = (K + kDBK - 1) / kDBK;
+  int best = 1;
+  double best_score = -1.0;
+  for (int s = 1; s <= 32 && s <= kblk / 2; ++s) {
+    const int units = tiles * s;
+    const int waves = (units + sms - 1) / sms;
+    const double eff = (double)units / ((double)waves * sms);
+    const double score = eff - 0.004 * s;  // small preference for fewer partials
+    if (score > best_score + 1e-9) {
+      best_score = score;
+      best = s;
+    }
+  }
+  return best;
+}
+
+static inline int ldp_of(int B) { return (B + 3) & ~3; }
+
+size_t decode_part_bytes(const qwen_layer_config& c, int B) {
+  const size_t d = c.d, nq = (size_t)c.n_q_heads * c.head_dim,
+               nqkv = nq + 2 * (size_t)c.n_kv_heads * c.head_dim, f = c.ffn;
+  const size_t ldp = ldp_of(B);
+  size_t m = 0;
+  auto upd = [&](size_t N, size_t K) {
+    const size_t s = decode_splits((int)N, (int)K);
+    const size_t need = s * N * ldp * 4;
+    if (need > m) m = need;
+  };
+  upd(nqkv, d);
+  upd(d, nq);
+  if (c.n_experts == 0) {
+    upd(2 * f, d);
+    upd(d, f);
+  }
+  return m;
+}
+
+template <int BP>
+static qwen_status launch_dec(const CUtensorMap& tw, const CUtensorMap& tx, int B, int N, int K,
+                              int splits, bool op_f16, float* part, int* err, cudaStream_t st) {
+  auto kern = gemm_decode_kernel<BP>;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DecCfg<BP>::SMEM_BYTES) != cudaSuccess)
+      return QWEN_ERR_CUDA;
+    attr = true;
+  }
+  const int units = ((N + kDBM - 1) / kDBM) * splits;
+  const int sms = device_sm_count();
+  const int grid = units < sms ? units : sms;
+  kern<<<grid, kDThreads, DecCfg<BP>::SMEM_BYTES, st>>>(tw, tx, B, N, K, splits, ldp_of(B),
+                                                        idesc_f32acc(kDBM, BP, op_f16), part, err);
+  return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
+}
+
+qwen_status gemm_decode_splitk(const void* W, const void* X, int ldx, int B, int N, int K,
+                               int splits, bool op_f16, float* part, int* err, cudaStream_t st) {
+  if (B <= 0 || B > 256) return QWEN_ERR_UNSUPPORTED;
+  if ((K & 7) || splits < 1) return QWEN_ERR_UNSUPPORTED;
+  const int bp = pad_batch(B);
+  CUtensorMap tw, tx;
+  if (!tmap2d(&tw, W, (uint64_t)N, (uint64_t)K, (uint64_t)K, kDBM, op_f16)) return QWEN_ERR_CUDA;
+  if (!tmap2d(&tx, X, (uint64_t)B, (uint64_t)K, (uint64_t)ldx, bp, op_f16)) return QWEN_ERR_CUDA;
+  switch (bp) {
+    case 16: return launch_dec<16>(tw, tx, B, N, K, splits, op_f16, part, err, st);
+    case 32: return launch_dec<32>(tw, tx, B, N, K, splits, op_f16, part, err, st);
+    case 64: return launch_dec<64>(tw, tx, B, N, K, splits, op_f16, part, err, st);
+    case 128: return launch_dec<128>(tw, tx, B, N, K, splits, op_f16, part, err, st);
+    default: return launch_dec<256>(tw, tx, B, N, K, splits, op_f16, part, err, st);
+  }
+}
+
+static inline int blocks_for(long long n, int t) { return (int)((n + t - 1) / t); }
+
+qwen_status reduce_resid(const float* part, int splits, int B, int N, const bf16* resid,
+                         const float* resid32, bf16* out, float* out32, cudaStream_t st) {
+  reduce_resid_kernel<<<blocks_for((long long)N * B, 256), 256, 0, st>>>(
+      part, splits, B, N, ldp_of(B), resid, resid32, out, out32);
+  return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
+}
+
+qwen_status reduce_swiglu(const float* part, int splits, int B, int f, f16* h, cudaStream_t st) {
+  reduce_swiglu_kernel<<<blocks_for((long long)f * B, 256), 256, 0, st>>>(part, splits, B, f,
+                                                                            ldp_of(B), h);
+  return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
+}
+
+qwen_status reduce_qkv(const float* part, int splits, int B, int Nqkv, const QkvParams& p, int* err,
+                       cudaStream_t st) {
+  const int n = B * (p.Hq + 2 * p.Hkv);
+  if (p.dh == 128)
+    reduce_qkv_kernel<128><<<blocks_for(n, 64), 64, 0, st>>>(part, splits, B, Nqkv, ldp_of(B), p, err);
+  else
+    reduce_qkv_kernel<64><<<blocks_for(n, 64), 64, 0, st>>>(part, splits, B, Nqkv, ldp_of(B), p, err);
+  return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
+}
+
+qwen_status reduce_f32(const float* part, int splits, int B, int N, float* out, int ldo,
+                       cudaStream_t st) {
+  reduce_f32_kernel<<<blocks_for((long long)N * B, 256), 256, 0, st>>>(part, splits, B, N,
+                                                                         ldp_of(B), out, ldo);
+  return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
+}
+
+}  // namespace qwen

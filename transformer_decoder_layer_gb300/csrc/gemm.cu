@@ -127,7 +127,8 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, bool row_
         tmem_ld_wait();
         const int col = (n0 + j) / 2 + h;  // output feature
         if (row_ok && n0 + j < N) {
-          uint4* dst = reinterpret_cast<uint4*>(epi.out + (size_t)row * epi.ldo + col);
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(epi.out) +
+                                                (size_t)row * epi.ldo + col);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             float o[8];
@@ -137,10 +138,10 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, bool row_
               o[e] = silu_f(gv) * __uint_as_float(u[8 * q + e]);
             }
             uint4 w;
-            w.x = pack_bf16x2(o[0], o[1]);
-            w.y = pack_bf16x2(o[2], o[3]);
-            w.z = pack_bf16x2(o[4], o[5]);
-            w.w = pack_bf16x2(o[6], o[7]);
+            w.x = pack2(o[0], o[1], epi.out_f16);
+            w.y = pack2(o[2], o[3], epi.out_f16);
+            w.z = pack2(o[4], o[5], epi.out_f16);
+            w.w = pack2(o[6], o[7], epi.out_f16);
             dst[q] = w;
           }
         }
@@ -173,23 +174,41 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, bool row_
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(r[i]);
         if constexpr (EPI == EPI_RESID) {
-          const bf16* rs = epi.resid + (size_t)row * epi.ldr + col;
-          if (full) {
+          if (epi.resid32) {
+            const float* rs = epi.resid32 + (size_t)row * epi.ldr + col;
+            if (full) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint4 u = reinterpret_cast<const uint4*>(rs)[q];
-              const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 f = unpack_bf16x2(w[e]);
-                o[8 * q + 2 * e] += f.x;
-                o[8 * q + 2 * e + 1] += f.y;
+              for (int q = 0; q < 8; ++q) {
+                const float4 f = reinterpret_cast<const float4*>(rs)[q];
+                o[4 * q] += f.x;
+                o[4 * q + 1] += f.y;
+                o[4 * q + 2] += f.z;
+                o[4 * q + 3] += f.w;
               }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < N - col) o[i] += rs[i];
             }
           } else {
+            const bf16* rs = epi.resid + (size_t)row * epi.ldr + col;
+            if (full) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < N - col) o[i] += bf2f(rs[i]);
+              for (int q = 0; q < 4; ++q) {
+                const uint4 u = reinterpret_cast<const uint4*>(rs)[q];
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 f = unpack_bf16x2(w[e]);
+                  o[8 * q + 2 * e] += f.x;
+                  o[8 * q + 2 * e + 1] += f.y;
+                }
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < N - col) o[i] += bf2f(rs[i]);
+            }
           }
           if (epi.out32) {
             float* d32 = epi.out32 + (size_t)row * epi.ldo32 + col;
@@ -204,22 +223,27 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, bool row_
                 if (i < N - col) d32[i] = o[i];
             }
           }
+          if (epi.out == nullptr) continue;
         }
-        bf16* dst = epi.out + (size_t)row * epi.ldo + col;
+        uint16_t* dst = static_cast<uint16_t*>(epi.out) + (size_t)row * epi.ldo + col;
         if (full) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 w;
-            w.x = pack_bf16x2(o[8 * q], o[8 * q + 1]);
-            w.y = pack_bf16x2(o[8 * q + 2], o[8 * q + 3]);
-            w.z = pack_bf16x2(o[8 * q + 4], o[8 * q + 5]);
-            w.w = pack_bf16x2(o[8 * q + 6], o[8 * q + 7]);
+            w.x = pack2(o[8 * q], o[8 * q + 1], epi.out_f16);
+            w.y = pack2(o[8 * q + 2], o[8 * q + 3], epi.out_f16);
+            w.z = pack2(o[8 * q + 4], o[8 * q + 5], epi.out_f16);
+            w.w = pack2(o[8 * q + 6], o[8 * q + 7], epi.out_f16);
             reinterpret_cast<uint4*>(dst)[q] = w;
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (i < N - col) dst[i] = f2bf(o[i]);
+          for (int i = 0; i < 32; i += 2)
+            if (i < N - col) {
+              const uint32_t p = pack2(o[i], o[i + 1], epi.out_f16);
+              dst[i] = static_cast<uint16_t>(p & 0xFFFFu);
+              if (i + 1 < N - col) dst[i + 1] = static_cast<uint16_t>(p >> 16);
+            }
         }
       }
     }
@@ -229,7 +253,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, bool row_
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   int M, int N, int K, GemmEpilogue epi, int* err) {
+                   int M, int N, int K, uint32_t idesc, GemmEpilogue epi, int* err) {
   using C = GemmCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -314,7 +338,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -394,8 +417,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 
 // 2-D BF16 tensor [rows][cols] with row stride `ld` elements; box [box_rows][64]
 // with the 128-byte swizzle.
-static bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                           uint64_t ld, uint32_t box_rows) {
+static bool make_tmap_16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                         uint64_t ld, uint32_t box_rows, bool f16) {
   auto enc = get_encode_fn();
   if (!enc) return false;
   if ((reinterpret_cast<uintptr_t>(base) & 15) || ((ld * 2) & 15)) return false;
@@ -403,14 +426,16 @@ static bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, ui
   cuuint64_t strides[1] = {ld * 2};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  return enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(base), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int BN, int EPI>
 static qwen_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
-                             const GemmEpilogue& epi, int* err, int grid, cudaStream_t st) {
+                             uint32_t idesc, const GemmEpilogue& epi, int* err, int grid,
+                             cudaStream_t st) {
   auto kern = gemm_tc_kernel<BN, EPI>;
   static bool attr_done = false;  // per template instance
   if (!attr_done) {
@@ -419,20 +444,22 @@ static qwen_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M
       return QWEN_ERR_CUDA;
     attr_done = true;
   }
-  kern<<<grid, kGemmThreads, GemmCfg<BN>::SMEM_BYTES, st>>>(ta, tb, M, N, K, epi, err);
+  kern<<<grid, kGemmThreads, GemmCfg<BN>::SMEM_BYTES, st>>>(ta, tb, M, N, K, idesc, epi, err);
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
-qwen_status gemm_tc(const bf16* A, int lda, const bf16* B, int ldb, int M, int N, int K,
-                    const GemmEpilogue& epi, int* err, cudaStream_t st) {
+qwen_status gemm_tc(const void* A, int lda, const void* B, int ldb, int M, int N, int K,
+                    bool op_f16, const GemmEpilogue& epi, int* err, cudaStream_t st) {
   if (M == 0 || N == 0) return QWEN_OK;
   if (K <= 0 || (K & 7) || (N & 7)) return QWEN_ERR_UNSUPPORTED;
   if (epi.group_offsets && (epi.n_groups <= 0 || epi.n_groups > 250)) return QWEN_ERR_UNSUPPORTED;
   constexpr int BN = 256;
   const uint64_t b_rows = epi.group_offsets ? (uint64_t)N * epi.n_groups : (uint64_t)N;
   CUtensorMap ta, tb;
-  if (!make_tmap_bf16(&ta, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, kBM)) return QWEN_ERR_CUDA;
-  if (!make_tmap_bf16(&tb, B, b_rows, (uint64_t)K, (uint64_t)ldb, BN)) return QWEN_ERR_CUDA;
+  if (!make_tmap_16(&ta, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, kBM, op_f16))
+    return QWEN_ERR_CUDA;
+  if (!make_tmap_16(&tb, B, b_rows, (uint64_t)K, (uint64_t)ldb, BN, op_f16)) return QWEN_ERR_CUDA;
+  const uint32_t idesc = idesc_f32acc(kBM, BN, op_f16);
   const int sms = device_sm_count();
   int tiles;
   if (epi.group_offsets) {
@@ -442,11 +469,11 @@ qwen_status gemm_tc(const bf16* A, int lda, const bf16* B, int ldb, int M, int N
   }
   const int grid = tiles < sms ? tiles : sms;
   switch (epi.mode) {
-    case EPI_STORE: return launch_bn<BN, EPI_STORE>(ta, tb, M, N, K, epi, err, grid, st);
-    case EPI_RESID: return launch_bn<BN, EPI_RESID>(ta, tb, M, N, K, epi, err, grid, st);
-    case EPI_SWIGLU: return launch_bn<BN, EPI_SWIGLU>(ta, tb, M, N, K, epi, err, grid, st);
-    case EPI_QKV: return launch_bn<BN, EPI_QKV>(ta, tb, M, N, K, epi, err, grid, st);
-    case EPI_F32: return launch_bn<BN, EPI_F32>(ta, tb, M, N, K, epi, err, grid, st);
+    case EPI_STORE: return launch_bn<BN, EPI_STORE>(ta, tb, M, N, K, idesc, epi, err, grid, st);
+    case EPI_RESID: return launch_bn<BN, EPI_RESID>(ta, tb, M, N, K, idesc, epi, err, grid, st);
+    case EPI_SWIGLU: return launch_bn<BN, EPI_SWIGLU>(ta, tb, M, N, K, idesc, epi, err, grid, st);
+    case EPI_QKV: return launch_bn<BN, EPI_QKV>(ta, tb, M, N, K, idesc, epi, err, grid, st);
+    case EPI_F32: return launch_bn<BN, EPI_F32>(ta, tb, M, N, K, idesc, epi, err, grid, st);
     default: return QWEN_ERR_INVALID_ARG;
   }
 }

@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/qwen_layer.h"
@@ -13,7 +14,7 @@ namespace qwen {
 // Epilogues of the tensor-core GEMM D = A B^T (A [M,K], B [N,K], K-major).
 enum EpiMode : int {
   EPI_STORE = 0,   // out[M,N] bf16 = D
-  EPI_RESID = 1,   // out = D + resid (bf16), optional fp32 copy
+  EPI_RESID = 1,   // D + residual (bf16 or fp32): bf16 out and/or fp32 out32
   EPI_SWIGLU = 2,  // B rows interleaved gate/up in 64-row blocks: out[M,N/2] = SiLU(g)*u
   EPI_QKV = 3,     // bias, QK-norm, RoPE, Q store + K/V cache append
   EPI_F32 = 4,     // out32[M,N] fp32 = D
@@ -37,9 +38,11 @@ struct QkvParams {
 
 struct GemmEpilogue {
   int mode;
-  __nv_bfloat16* out;  // bf16 output
+  void* out;    // 16-bit output (BF16, or FP16 when out_f16)
+  int out_f16;
   int ldo;
-  const __nv_bfloat16* resid;  // residual input (EPI_RESID)
+  const __nv_bfloat16* resid;  // residual input (EPI_RESID), BF16 ...
+  const float* resid32;        // ... or FP32 (takes precedence when set)
   int ldr;
   float* out32;  // fp32 output (EPI_F32, or optional copy in EPI_RESID)
   int ldo32;
@@ -54,14 +57,26 @@ struct GemmEpilogue {
 int device_sm_count();
 int* lib_status_ptr();  // device status word used by handle-less entry points
 
-// The tensor-core GEMM.  A [M,K] (row stride lda elements), B [N,K] (ldb).
-// For grouped mode, B holds n_groups stacked [N,K] matrices and A rows of
-// group g live in [group_offsets[g], group_offsets[g+1]).
-qwen_status gemm_tc(const __nv_bfloat16* A, int lda, const __nv_bfloat16* B, int ldb, int M,
-                    int N, int K, const GemmEpilogue& epi, int* err, cudaStream_t st);
+// The tensor-core GEMM.  A [M,K] (row stride lda elements), B [N,K] (ldb),
+// both BF16 or both FP16 (op_f16).  For grouped mode, B holds n_groups stacked
+// [N,K] matrices and A rows of group g live in [group_offsets[g],
+// group_offsets[g+1]).
+qwen_status gemm_tc(const void* A, int lda, const void* B, int ldb, int M, int N, int K,
+                    bool op_f16, const GemmEpilogue& epi, int* err, cudaStream_t st);
 
-qwen_status rmsnorm_launch(const __nv_bfloat16* x, const __nv_bfloat16* gamma,
-                           __nv_bfloat16* y, float* y32, const float* x32, int rows, int d,
-                           float eps, cudaStream_t st);
+// Causal GQA flash attention for prefill: q [B][Hq][T][dh], caches
+// [B][Hkv][max_seq][dh], out [B*T][Hq*dh]; query t of sequence b sits in cache
+// slot slot0[b] + t and sees slots <= its own.
+qwen_status attention_prefill(const __nv_bfloat16* q, const __nv_bfloat16* k_cache,
+                              const __nv_bfloat16* v_cache, const int32_t* slot0,
+                              __half* out, int B, int T, int Hq, int Hkv, int dh,
+                              int max_seq, int* err, cudaStream_t st);
+
+// y[r] = gamma * x[r] / sqrt(mean(x[r]^2) + eps); input rows `x_stride`
+// elements apart (0 = d), read from x32 (FP32) when given, else x (BF16);
+// y is BF16, or FP16 when y_f16.
+qwen_status rmsnorm_launch(const __nv_bfloat16* x, const __nv_bfloat16* gamma, void* y,
+                           bool y_f16, float* y32, const float* x32, int rows, int d, float eps,
+                           cudaStream_t st, size_t x_stride = 0);
 
 }  // namespace qwen

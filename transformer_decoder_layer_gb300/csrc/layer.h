@@ -1,0 +1,99 @@
+// The layer handle, the packed-weight and workspace layouts, and the internal
+// entry points of the prefill / decode / MoE orchestration.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace qwen {
+
+struct PackedLayout {
+  size_t status, rope, gamma_attn, gamma_mlp, gamma_q, gamma_k, w_qkv, b_qkv, w_o, w_gu, w_down,
+      w_router, b_router, total;
+};
+
+struct WorkspaceLayout {
+  size_t xh, q, attn, r32, z, h;
+  // MoE
+  size_t z32, logits, topk_idx, topk_w, offsets, perm, inv, zp, hp, yp;
+  // decode (T == 1)
+  size_t part, attn_o, attn_ml;
+  size_t total;
+};
+
+}  // namespace qwen
+
+struct qwen_layer_s {
+  qwen_layer_config cfg;
+  uint8_t* packed;
+  qwen::PackedLayout L;
+  int* status;
+  float2* rope;
+  __nv_bfloat16 *gamma_attn, *gamma_mlp, *gamma_q, *gamma_k;
+  // projection weights are held as FP16 (converted exactly from BF16 at create)
+  __half* w_qkv;
+  float* b_qkv;
+  __half* w_o;
+  __half *w_gu, *w_down;  // gate/up rows interleaved in 64-row blocks
+  __nv_bfloat16* w_router;
+  float* b_router;
+};
+
+namespace qwen {
+
+bool config_valid(const qwen_layer_config& c);
+PackedLayout packed_layout(const qwen_layer_config& c);
+WorkspaceLayout workspace_layout(const qwen_layer_config& c, int B, int T);
+
+QkvParams make_qkv_params(const qwen_layer_s* L, const int32_t* positions, const int32_t* slot0,
+                          __nv_bfloat16* q, __nv_bfloat16* kc, __nv_bfloat16* vc, int T);
+
+qwen_status layer_prefill(qwen_layer_s* L, const __nv_bfloat16* x, __nv_bfloat16* y, int B, int T,
+                          const int32_t* positions, const int32_t* slot0, __nv_bfloat16* kc,
+                          __nv_bfloat16* vc, uint8_t* ws, const WorkspaceLayout& W,
+                          cudaStream_t st);
+
+qwen_status layer_decode(qwen_layer_s* L, const __nv_bfloat16* x, __nv_bfloat16* y, int B,
+                         const int32_t* positions, const int32_t* cache_len, __nv_bfloat16* kc,
+                         __nv_bfloat16* vc, uint8_t* ws, const WorkspaceLayout& W,
+                         cudaStream_t st);
+
+qwen_status moe_forward(qwen_layer_s* L, const __nv_bfloat16* r, const float* r32,
+                        __nv_bfloat16* y, int T, int32_t* topk_idx_out, float* topk_w_out,
+                        float* logits_out, uint8_t* ws, const WorkspaceLayout& W,
+                        cudaStream_t st);
+
+// ---- decode building blocks (decode_gemm.cu, attention_decode.cu)
+
+// Number of K splits the swap-AB decode GEMM uses for an [N, K] weight.
+int decode_splits(int N, int K);
+// Bytes of FP32 partials the decode GEMM of the layer needs for batch B.
+size_t decode_part_bytes(const qwen_layer_config& c, int B);
+// Attention split-KV plan: keys per split and number of splits for batch B.
+void decode_attn_plan(const qwen_layer_config& c, int B, int* chunk, int* splits);
+
+// part[s][n][b] (row stride ldp = round_up(B, 4)) = sum over split s's k-range
+// of W[n, k] X[b, k].  W [N, K], X [B, K] (row stride ldx).
+qwen_status gemm_decode_splitk(const void* W, const void* X, int ldx, int B, int N, int K,
+                               int splits, bool op_f16, float* part, int* err, cudaStream_t st);
+
+// Reductions over the splits followed by the step's epilogue.
+qwen_status reduce_resid(const float* part, int splits, int B, int N, const __nv_bfloat16* resid,
+                         const float* resid32, __nv_bfloat16* out, float* out32, cudaStream_t st);
+qwen_status reduce_swiglu(const float* part, int splits, int B, int f, __half* h,
+                          cudaStream_t st);
+qwen_status reduce_qkv(const float* part, int splits, int B, int Nqkv, const QkvParams& p,
+                       int* err, cudaStream_t st);
+qwen_status reduce_f32(const float* part, int splits, int B, int N, float* out, int ldo,
+                       cudaStream_t st);
+
+// Split-KV decode attention and its merge: q [B][Hq][dh]; query b sits in cache
+// slot cache_len[b] and attends slots 0..cache_len[b].  out [B][Hq*dh].
+qwen_status attention_decode(const __nv_bfloat16* q, const __nv_bfloat16* kc,
+                             const __nv_bfloat16* vc, const int32_t* cache_len, int B, int Hq,
+                             int Hkv, int dh, int max_seq, int chunk, int splits, float* part_o,
+                             float* part_ml, __half* out, int* err, cudaStream_t st);
+
+}  // namespace qwen

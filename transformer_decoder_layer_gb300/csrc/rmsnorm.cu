@@ -12,9 +12,9 @@ template <int MAXC>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x,
                                                       const float* __restrict__ x32,
                                                       const bf16* __restrict__ gamma,
-                                                      bf16* __restrict__ y,
+                                                      void* __restrict__ y, bool y_f16,
                                                       float* __restrict__ y32, int rows, int d,
-                                                      float eps) {
+                                                      float eps, size_t xs) {
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -22,7 +22,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
   float v[MAXC][8];
   float ss = 0.f;
   if (x32) {
-    const float4* xr = reinterpret_cast<const float4*>(x32 + (size_t)row * d);
+    const float4* xr = reinterpret_cast<const float4*>(x32 + (size_t)row * xs);
 #pragma unroll
     for (int i = 0; i < MAXC; ++i) {
       const int c = lane + 32 * i;
@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
       }
     }
   } else {
-    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * d);
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * xs);
 #pragma unroll
     for (int i = 0; i < MAXC; ++i) {
       const int c = lane + 32 * i;
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
   ss = warp_sum(ss);
   const float rstd = rsqrtf(ss / (float)d + eps);
   const uint4* gr = reinterpret_cast<const uint4*>(gamma);
-  uint4* yr = reinterpret_cast<uint4*>(y + (size_t)row * d);
+  uint4* yr = reinterpret_cast<uint4*>(static_cast<uint16_t*>(y) + (size_t)row * d);
 #pragma unroll
   for (int i = 0; i < MAXC; ++i) {
     const int c = lane + 32 * i;
@@ -71,10 +71,10 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
         o[2 * j + 1] = g.y * (v[i][2 * j + 1] * rstd);
       }
       uint4 out;
-      out.x = pack_bf16x2(o[0], o[1]);
-      out.y = pack_bf16x2(o[2], o[3]);
-      out.z = pack_bf16x2(o[4], o[5]);
-      out.w = pack_bf16x2(o[6], o[7]);
+      out.x = pack2(o[0], o[1], y_f16);
+      out.y = pack2(o[2], o[3], y_f16);
+      out.z = pack2(o[4], o[5], y_f16);
+      out.w = pack2(o[6], o[7], y_f16);
       yr[c] = out;
       if (y32) {
         float4* y4 = reinterpret_cast<float4*>(y32 + (size_t)row * d);
@@ -85,18 +85,20 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
   }
 }
 
-qwen_status rmsnorm_launch(const bf16* x, const bf16* gamma, bf16* y, float* y32,
-                           const float* x32, int rows, int d, float eps, cudaStream_t st) {
+qwen_status rmsnorm_launch(const bf16* x, const bf16* gamma, void* y, bool y_f16, float* y32,
+                           const float* x32, int rows, int d, float eps, cudaStream_t st,
+                           size_t x_stride) {
   if (rows == 0) return QWEN_OK;
   if (d <= 0 || (d & 7) || d > 8192) return QWEN_ERR_UNSUPPORTED;
+  const size_t xs = x_stride ? x_stride : (size_t)d;
   const int threads = 256;
   const int blocks = (rows * 32 + threads - 1) / threads;
   if (d <= 2048)
-    rmsnorm_kernel<8><<<blocks, threads, 0, st>>>(x, x32, gamma, y, y32, rows, d, eps);
+    rmsnorm_kernel<8><<<blocks, threads, 0, st>>>(x, x32, gamma, y, y_f16, y32, rows, d, eps, xs);
   else if (d <= 4096)
-    rmsnorm_kernel<16><<<blocks, threads, 0, st>>>(x, x32, gamma, y, y32, rows, d, eps);
+    rmsnorm_kernel<16><<<blocks, threads, 0, st>>>(x, x32, gamma, y, y_f16, y32, rows, d, eps, xs);
   else
-    rmsnorm_kernel<32><<<blocks, threads, 0, st>>>(x, x32, gamma, y, y32, rows, d, eps);
+    rmsnorm_kernel<32><<<blocks, threads, 0, st>>>(x, x32, gamma, y, y_f16, y32, rows, d, eps, xs);
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
