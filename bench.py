@@ -1,0 +1,476 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 Qwen-style decoder layer (one JSON line on rank 0).
+
+Headline: one decode step of a Qwen2.5-7B-shaped layer (d=3584, Hq=28, Hkv=4,
+dh=128, f=18944, qkv bias) for B sequences against a BF16 KV cache holding 4096
+tokens (the new token is position/slot 4096), in microseconds per step per
+layer (lower is better).  A step is the whole layer: RMSNorm, fused QKV (+bias,
+RoPE, cache append), split-KV attention, O projection + residual, RMSNorm,
+gate/up + SiLU*up, down + residual.  Inputs are resident in HBM; weights
+(466 MB) plus the KV cache exceed the 126 MB L2, so no flush is needed.
+
+The same line carries: the B sweep (1, 8, 32, 64); prefill of a Qwen3-8B-shaped
+layer (tokens/s, TFLOP/s, per-kernel tensor roofline); `roofline` for the
+dominant decode kernel from CUDA events recorded around it inside the timed
+region; `e2e` through the C ABI with pinned host buffers copied in and out every
+step; `cpu_baseline` (the FP64 oracle on the host cores, a bounded sample);
+`clocks` sampled with nvidia-smi during the timed region; `gpu_launches`
+counted by the library.
+
+`--impl reference` times the FP64 oracle on the same workload instead (rank 0
+only) and prints the same line with "impl": "reference".
+Multi-GPU runs are independent replicas (the layer has no exchange step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill tokens/s & decode µs/step per layer; % of BF16 tensor / HBM roofline"
+CACHE_FILLED = 4096
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return (float(j["hbm_gbs"]), float(j["bf16_tflops"]),
+                float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), "measured")
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (background)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        t0, t1 = self.window or (0, 1e30)
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        near = inside or [s for t, s in self.samples if t0 - 0.2 <= t <= t1 + 0.2]
+        sm, mx, reasons = [], None, set()
+        for s in near:
+            parts = [p.strip() for p in s.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                    "samples_in_window": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples_in_window": len(inside)}
+
+
+# ------------------------------------------------------------------ workload
+
+def decode_bytes(shape, B):
+    """Algorithmic bytes of one decode step: weights + KV read + KV write + X/Y."""
+    d, hq, hkv, dh, f = shape.d, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn
+    nq, nkv = hq * dh, hkv * dh
+    weights = 2 * (d * (nq + 2 * nkv) + d * nq + 3 * d * f) + 4 * (nq + 2 * nkv) * shape.qkv_bias
+    kv_read = B * 2 * hkv * CACHE_FILLED * dh * 2
+    kv_write = B * 2 * nkv * 2
+    xy = B * d * 2 * 2
+    return weights + kv_read + kv_write + xy
+
+
+def linear_params(shape):
+    d, hq, hkv, dh, f = shape.d, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn
+    return d * hq * dh + 2 * d * hkv * dh + hq * dh * d + 3 * d * f
+
+
+class DecodeBench:
+    def __init__(self, q, torch, shape, B, layer, max_seq, tag="bench"):
+        import synth
+        self.q, self.torch, self.shape, self.B = q, torch, shape, B
+        self.layer = layer
+        dev = torch.device("cuda")
+        self.x_cpu = synth.activations([B, shape.d], tag, f"x{B}")
+        kc, vc = synth.kv_cache(B, shape.n_kv_heads, max_seq, shape.head_dim, CACHE_FILLED, tag)
+        self.kc_cpu, self.vc_cpu = kc, vc
+        self.x = self.x_cpu.to(dev)
+        self.kc, self.vc = kc.to(dev), vc.to(dev)
+        self.pos = torch.full((B,), CACHE_FILLED, dtype=torch.int32, device=dev)
+        self.clen = torch.full((B,), CACHE_FILLED, dtype=torch.int32, device=dev)
+        self.y = torch.empty_like(self.x)
+        self.ws = layer.workspace(B, 1)
+
+    def step(self):
+        self.layer.decode(self.x, self.pos, self.clen, self.kc, self.vc, out=self.y,
+                          workspace=self.ws)
+
+    def timed(self, steps, warmup, trace_stage=None, clocks=None):
+        torch = self.torch
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        evs = []
+        if trace_stage:
+            for _ in range(steps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                b.record()  # creates the events before the library records them
+                evs.append((a, b))
+            torch.cuda.synchronize()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        n0 = self.q.launch_count()
+        torch.cuda.synchronize()
+        w0 = time.time()
+        t_start.record()
+        for i in range(steps):
+            if trace_stage:
+                self.layer.set_trace({trace_stage: evs[i]})
+            self.step()
+        t_end.record()
+        torch.cuda.synchronize()
+        w1 = time.time()
+        if trace_stage:
+            self.layer.set_trace(None)
+        if clocks:
+            clocks.mark(w0, w1)
+        n_launch = self.q.launch_count() - n0
+        total_ms = t_start.elapsed_time(t_end)
+        kern_ms = [a.elapsed_time(b) for a, b in evs] if evs else []
+        assert self.layer.poll_error() == 0, "device status set during the benchmark"
+        return total_ms, kern_ms, n_launch
+
+    def e2e(self, steps, warmup):
+        """Through the C ABI with pinned host buffers copied in/out every step."""
+        torch = self.torch
+        xh = self.x_cpu.pin_memory()
+        ph = torch.full((self.B,), CACHE_FILLED, dtype=torch.int32).pin_memory()
+        ch = torch.full((self.B,), CACHE_FILLED, dtype=torch.int32).pin_memory()
+        yh = torch.empty((self.B, self.shape.d), dtype=torch.bfloat16).pin_memory()
+
+        def one():
+            self.x.copy_(xh, non_blocking=True)
+            self.pos.copy_(ph, non_blocking=True)
+            self.clen.copy_(ch, non_blocking=True)
+            self.step()
+            yh.copy_(self.y, non_blocking=True)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            one()
+        b.record()
+        torch.cuda.synchronize()
+        h2d = xh.numel() * 2 + ph.numel() * 4 + ch.numel() * 4
+        d2h = yh.numel() * 2
+        return a.elapsed_time(b), h2d, d2h
+
+
+def prefill_bench(q, torch, shape, B, T, steps, warmup, peak_tflops, tag="bench_prefill"):
+    import synth
+    dev = torch.device("cuda")
+    w = {k: v.to(dev) for k, v in synth.layer_weights(shape, tag).items()}
+    cfg = q.LayerConfig(shape, max_tokens=B * T, max_batch=B, max_seq=T, max_position=T)
+    layer = q.Layer(cfg, w)
+    x = synth.activations([B, T, shape.d], tag, f"x{B}_{T}").to(dev)
+    kc = torch.zeros((B, shape.n_kv_heads, T, shape.head_dim), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    pos = torch.arange(T, dtype=torch.int32, device=dev).repeat(B)
+    start = torch.zeros(B, dtype=torch.int32, device=dev)
+    y = torch.empty_like(x)
+    ws = layer.workspace(B, T)
+    for _ in range(warmup):
+        layer.prefill(x, pos, start, kc, vc, out=y, workspace=ws)
+    torch.cuda.synchronize()
+    stages = ["qkv", "attn", "o", "gate_up", "down"]
+    per = {s: [] for s in stages}
+    tot = []
+    for _ in range(steps):
+        evs = {}
+        for s in stages:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            b.record()
+            evs[s] = (a, b)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        layer.set_trace(evs)
+        t0.record()
+        layer.prefill(x, pos, start, kc, vc, out=y, workspace=ws)
+        t1.record()
+        torch.cuda.synchronize()
+        tot.append(t0.elapsed_time(t1))
+        for s in stages:
+            per[s].append(evs[s][0].elapsed_time(evs[s][1]))
+    layer.set_trace(None)
+    assert layer.poll_error() == 0
+    ms = statistics.median(tot)
+    M = B * T
+    P = linear_params(shape)
+    hq, dh, f, d = shape.n_q_heads, shape.head_dim, shape.ffn, shape.d
+    attn_metric = 4 * B * T * T * hq * dh
+    attn_exec = 2 * B * hq * dh * T * (T + 1)
+    flops = {"qkv": 2 * M * d * (hq * dh + 2 * shape.n_kv_heads * dh), "attn": attn_exec,
+             "o": 2 * M * hq * dh * d, "gate_up": 2 * M * d * 2 * f, "down": 2 * M * f * d}
+    kern = {}
+    for s in stages:
+        t = statistics.median(per[s])
+        tf = flops[s] / (t * 1e-3) / 1e12
+        kern[s] = {"ms": round(t, 4), "tflops": round(tf, 1), "frac": round(tf / peak_tflops, 3)}
+    del layer
+    return {
+        "workload": f"qwen3-8b-shaped layer prefill B={B} T={T}",
+        "ms": round(ms, 4),
+        "tokens_per_s": round(M / (ms * 1e-3), 1),
+        "tflops_metric": round((2 * P * M + attn_metric) / (ms * 1e-3) / 1e12, 1),
+        "tflops_executed": round((2 * P * M + attn_exec) / (ms * 1e-3) / 1e12, 1),
+        "frac_of_peak_executed": round((2 * P * M + attn_exec) / (ms * 1e-3) / 1e12 / peak_tflops, 3),
+        "kernels": kern,
+    }
+
+
+# ------------------------------------------------------------------ oracle timing
+
+class OracleDecode:
+    """The FP64 oracle on single sequences of the decode workload (host cores)."""
+
+    def __init__(self, shape, B, tag="bench"):
+        import synth
+        self.shape, self.B = shape, B
+        self.w64 = synth.weights_f64(synth.layer_weights(shape, tag))
+        self.x = synth.to_f64(synth.activations([B, shape.d], tag, f"x{B}"))
+        kc, vc = synth.kv_cache(1, shape.n_kv_heads, CACHE_FILLED + 1, shape.head_dim,
+                                CACHE_FILLED, tag)
+        self.k64, self.v64 = synth.to_f64(kc)[0], synth.to_f64(vc)[0]
+        self.i = 0
+
+    def one(self):
+        import numpy as np
+
+        import oracle
+        kk, vv = self.k64.copy(), self.v64.copy()
+        t0 = time.perf_counter()
+        oracle.layer_forward(self.x[self.i % self.B][None], self.w64, self.shape.as_dict(),
+                             np.array([CACHE_FILLED]), kk, vv, np.array([CACHE_FILLED]))
+        self.i += 1
+        return time.perf_counter() - t0
+
+
+def oracle_decode_seconds_per_seq(shape, B, budget_s):
+    o = OracleDecode(shape, B)
+    o.one()  # warm-up
+    times, t_begin = [], time.time()
+    while time.time() - t_begin < budget_s and len(times) < 256:
+        times.append(o.one())
+    return statistics.median(times), len(times)
+
+
+def oracle_decode_steps(shape, B, warmup, steps):
+    o = OracleDecode(shape, B)
+    for _ in range(warmup):
+        o.one()
+    times = [o.one() for _ in range(steps)]
+    return statistics.median(times), len(times)
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batch", type=int, default=32)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    import synth
+    shape = synth.QWEN25_7B
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    B = args.batch
+    workload = (f"qwen2.5-7b-shaped layer decode: d=3584 Hq=28 Hkv=4 dh=128 f=18944 qkv-bias, "
+                f"B={B}, {CACHE_FILLED} cached tokens, new token at position {CACHE_FILLED}")
+    config = {"workload": workload, "batch": B, "cache_tokens": CACHE_FILLED,
+              "l2": "inputs larger than L2 (466 MB weights + B x 8.4 MB KV per step; no flush)",
+              "parallelism": f"{world} independent replica(s)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # each step is a bounded sample of the workload: one of the B sequences'
+        # decode step through the FP64 oracle, scaled by B
+        per_seq, n = oracle_decode_steps(shape, B, args.warmup, args.steps)
+        us = per_seq * B * 1e6
+        line = {"metric": METRIC, "value": round(us, 1), "unit": "us/step", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3),
+                "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic", "config": config, "impl": "reference",
+                "cpu_baseline": {"value": round(us, 1), "unit": "us/step", "cores": host_cores(),
+                                 "kind": "oracle",
+                                 "sample": f"{n} single-sequence decode steps (median) x B={B}"},
+                "e2e": {"value": round(us, 1), "unit": "us/step", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    import transformer_decoder_layer_gb300 as q
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    hbm_gbs, bf16_tf, bf16_tf_sus, peak_kind = load_peaks()
+
+    dev = torch.device("cuda")
+    w = {k: v.to(dev) for k, v in synth.layer_weights(shape, "bench").items()}
+    max_b = max(64, B)
+    cfg = q.LayerConfig(shape, max_tokens=max_b, max_batch=max_b, max_seq=CACHE_FILLED + 1,
+                        max_position=CACHE_FILLED + 1)
+    layer = q.Layer(cfg, w)
+
+    bench = DecodeBench(q, torch, shape, B, layer, CACHE_FILLED + 1)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    total_ms, kern_ms, n_launch = bench.timed(args.steps, args.warmup, trace_stage="gate_up",
+                                              clocks=clocks)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    # whole job: world * steps decode steps in the slowest rank's time
+    us_per_step = total_ms * 1e3 / (args.steps * world)
+    step_bytes = decode_bytes(shape, B)
+
+    # roofline of the dominant kernel: the gate/up projection (weights dominate)
+    d, f = shape.d, shape.ffn
+    gu_bytes = 2 * f * d * 2 + B * d * 2
+    gu_ms = statistics.mean(kern_ms)
+    achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "gemm_decode_kernel (gate/up, swap-AB split-K)",
+                "achieved": round(achieved, 1), "peak": hbm_gbs, "unit": "GB/s",
+                "frac": round(achieved / hbm_gbs, 3), "traffic": None,
+                "peak_kind": f"{peak_kind} hbm_gbs",
+                "algorithmic_bytes": gu_bytes, "avg_ms": round(gu_ms, 4),
+                "step_achieved_gbs": round(step_bytes / (us_per_step * 1e-6) / 1e9, 1),
+                "step_frac": round(step_bytes / (us_per_step * 1e-6) / 1e9 / hbm_gbs, 3)}
+
+    e2e_ms, h2d, d2h = bench.e2e(max(args.steps // 2, 10), args.warmup)
+    e2e_us = e2e_ms * 1e3 / max(args.steps // 2, 10)
+
+    line = {"metric": METRIC, "value": round(us_per_step, 2), "unit": "us/step",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(us_per_step / 1e3, 5), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 I/O and KV cache; fp16/bf16 tensor-core operands; fp32 accumulate",
+            "data": "synthetic (seeded N(0,1) activations and cache, N(0,0.02) weights)",
+            "config": config, "roofline": roofline,
+            "e2e": {"value": round(e2e_us, 2), "unit": "us/step", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": int(n_launch), "clocks": clk}
+
+    if rank == 0 and not args.no_sweep:
+        sweep = {}
+        for bb in (1, 8, 32, 64):
+            db = DecodeBench(q, torch, shape, bb, layer, CACHE_FILLED + 1, tag="bench")
+            tms, _, _ = db.timed(max(args.steps // 2, 20), args.warmup)
+            us = tms * 1e3 / max(args.steps // 2, 20)
+            gbs = decode_bytes(shape, bb) / (us * 1e-6) / 1e9
+            sweep[f"B={bb}"] = {"us_per_step": round(us, 2), "GB_per_s": round(gbs, 1),
+                                "frac_hbm": round(gbs / hbm_gbs, 3),
+                                "bytes_per_step": decode_bytes(shape, bb)}
+            del db
+        line["decode_sweep"] = sweep
+    del bench
+    if rank == 0 and not args.no_prefill:
+        pf = []
+        for (pb, pt) in ((1, 4096), (1, 1024), (8, 1024), (1, 16384)):
+            pf.append(prefill_bench(q, torch, synth.QWEN3_8B, pb, pt, 5, 3, bf16_tf))
+        line["prefill"] = pf
+    if rank == 0 and world == 1:
+        per_seq, n = oracle_decode_seconds_per_seq(shape, B, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(per_seq * B * 1e6, 1), "unit": "us/step",
+                                "cores": host_cores(), "kind": "oracle",
+                                "sample": f"{n} single-sequence decode steps of the same layer "
+                                          f"and cache, median time x B={B}"}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -188,6 +188,38 @@ QWEN_API qwen_status qwen_rmsnorm(const void* x, const void* gamma, void* y, flo
 QWEN_API qwen_status qwen_linear(const void* x, const void* w, void* y, int32_t M, int32_t N,
                         int32_t K, void* stream);
 
+/* Stages of one prefill / decode call, in launch order (a call runs the
+ * stages its path needs; the *_FINISH stages are the decode path's split-K
+ * reductions, ATTN_MERGE its split-KV merge). */
+typedef enum {
+  QWEN_STAGE_NORM1 = 0,
+  QWEN_STAGE_QKV = 1,
+  QWEN_STAGE_QKV_FINISH = 2,
+  QWEN_STAGE_ATTN = 3,
+  QWEN_STAGE_ATTN_MERGE = 4,
+  QWEN_STAGE_O = 5,
+  QWEN_STAGE_O_FINISH = 6,
+  QWEN_STAGE_NORM2 = 7,
+  QWEN_STAGE_GATE_UP = 8,
+  QWEN_STAGE_GATE_UP_FINISH = 9,
+  QWEN_STAGE_DOWN = 10,
+  QWEN_STAGE_DOWN_FINISH = 11,
+  QWEN_STAGE_MOE = 12, /* the whole MoE block of a MoE layer */
+  QWEN_STAGE_COUNT = 13
+} qwen_stage;
+
+/* Optional per-stage timing.  `events` (host array of 2 * QWEN_STAGE_COUNT
+ * cudaEvent_t handles, entries may be NULL) is remembered by the handle; every
+ * later prefill/decode call records events[2*s] on its stream right before
+ * stage s and events[2*s+1] right after it, for each stage it runs and each
+ * non-NULL entry.  Pass events = NULL to stop.  The array must stay valid
+ * until tracing is switched off. */
+QWEN_API qwen_status qwen_layer_set_trace(qwen_layer_t layer, void* const* events);
+
+/* Number of kernel launches this library has issued in this process (all
+ * handles, all entry points); a host-side counter. */
+QWEN_API uint64_t qwen_launch_count(void);
+
 /* Synchronise `stream`, then read and clear the handle's device status word.
  * Returns QWEN_OK, QWEN_ERR_TIMEOUT or QWEN_ERR_RANGE (or QWEN_ERR_CUDA). */
 QWEN_API qwen_status qwen_layer_poll_error(qwen_layer_t layer, void* stream);

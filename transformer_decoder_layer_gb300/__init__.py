@@ -72,7 +72,12 @@ _SIGS = {
     "qwen_layer_poll_error": (ctypes.c_int, [_VP, _VP]),
     "qwen_poll_error": (ctypes.c_int, [_VP]),
     "qwen_device_sm_count": (_I32, []),
+    "qwen_layer_set_trace": (ctypes.c_int, [_VP, _VP]),
+    "qwen_launch_count": (ctypes.c_uint64, []),
 }
+
+STAGES = ["norm1", "qkv", "qkv_finish", "attn", "attn_merge", "o", "o_finish", "norm2",
+          "gate_up", "gate_up_finish", "down", "down_finish", "moe"]
 
 _lib = None
 
@@ -283,3 +288,24 @@ class Layer:
 
     def poll_error(self, stream=None):
         return lib().qwen_layer_poll_error(self.handle, _stream(stream))
+
+    def set_trace(self, events):
+        """events: dict stage-name -> (start, end) torch.cuda.Event (or None to stop).
+
+        Later prefill/decode calls record the given events around those stages."""
+        if events is None:
+            self._trace = None
+            _check(lib().qwen_layer_set_trace(self.handle, None), "qwen_layer_set_trace")
+            return
+        arr = (ctypes.c_void_p * (2 * len(STAGES)))()
+        for name, (ev0, ev1) in events.items():
+            i = STAGES.index(name)
+            arr[2 * i] = ev0.cuda_event
+            arr[2 * i + 1] = ev1.cuda_event
+        self._trace = (arr, events)  # keep alive while tracing
+        _check(lib().qwen_layer_set_trace(self.handle, arr), "qwen_layer_set_trace")
+
+
+def launch_count():
+    """Kernel launches issued by the library so far in this process."""
+    return int(lib().qwen_launch_count())

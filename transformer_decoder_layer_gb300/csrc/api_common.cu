@@ -1,11 +1,16 @@
 // C ABI: status strings, device queries and the handle-less entry points
 // (qwen_rmsnorm, qwen_linear).
+#include <atomic>
 #include <cstdio>
 
 #include "common.cuh"
 #include "internal.h"
 
 namespace qwen {
+
+static std::atomic<unsigned long long> g_launches{0};
+
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 
 // Status word for entry points that have no layer handle (qwen_linear, ...).
 // A module-scope device variable: no allocation is needed to use it.
@@ -53,6 +58,8 @@ const char* qwen_status_string(qwen_status s) {
 }
 
 int32_t qwen_device_sm_count(void) { return device_sm_count(); }
+
+uint64_t qwen_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 qwen_status qwen_rmsnorm(const void* x, const void* gamma, void* y, float* y_fp32, int32_t rows,
                          int32_t d, float eps, void* stream) {

@@ -154,6 +154,7 @@ static bool pack_rows(f16* dst, const void* src, size_t rows, size_t d, int mode
   const int blocks = (int)((nch + 255) / 256 < 65535 ? (nch + 255) / 256 : 65535);
   pack_rows_f16_kernel<<<blocks, 256, 0, st>>>(dst, static_cast<const bf16*>(src), rows, (int)d,
                                                mode);
+  count_launches();
   return cudaGetLastError() == cudaSuccess;
 }
 
@@ -236,6 +237,7 @@ qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_wei
         static_cast<const bf16*>(w->b_k), h->b_qkv + nq, (int)nkv);
     bf16_to_f32_kernel<<<(int)((nkv + 255) / 256), 256, 0, st>>>(
         static_cast<const bf16*>(w->b_v), h->b_qkv + nq + nkv, (int)nkv);
+    count_launches(3);
     ok = cudaGetLastError() == cudaSuccess;
   }
   ok = ok && pack_rows(h->w_o, w->w_o, d, nq, 0, st);
@@ -272,6 +274,17 @@ qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_wei
 }
 
 void qwen_layer_destroy(qwen_layer_t layer) { delete layer; }
+
+qwen_status qwen_layer_set_trace(qwen_layer_t layer, void* const* events) {
+  if (!layer) return QWEN_ERR_INVALID_ARG;
+  if (!events) {
+    layer->tracing = false;
+    return QWEN_OK;
+  }
+  for (int i = 0; i < 2 * QWEN_STAGE_COUNT; ++i) layer->trace[i] = events[i];
+  layer->tracing = true;
+  return QWEN_OK;
+}
 
 qwen_status qwen_layer_poll_error(qwen_layer_t layer, void* stream) {
   if (!layer) return QWEN_ERR_INVALID_ARG;
@@ -396,10 +409,23 @@ qwen_status qwen_head_last_token(const void* y, int32_t B, int32_t T, int32_t d,
 
 namespace qwen {
 
-// One projection of a decode step: swap-AB split-K on the tensor cores, then
-// the reduction that applies the step's epilogue.
-enum DecEpi { DEC_QKV, DEC_RESID, DEC_SWIGLU };
+// Record the trace event of `stage` (begin = 0, end = 1) when tracing is on.
+static inline void mark(const qwen_layer_s* L, int stage, int end, cudaStream_t st) {
+  if (!L->tracing) return;
+  void* e = L->trace[2 * stage + end];
+  if (e) cudaEventRecord(static_cast<cudaEvent_t>(e), st);
+}
 
+#define QWEN_STAGE_RUN(stage, expr)            \
+  do {                                         \
+    mark(L, (stage), 0, st);                   \
+    const qwen_status s_ = (expr);             \
+    if (s_ != QWEN_OK) return s_;              \
+    mark(L, (stage), 1, st);                   \
+  } while (0)
+
+// One projection of a decode step: swap-AB split-K on the tensor cores; the
+// reduction that follows applies the step's epilogue.
 static qwen_status decode_proj(const f16* Wt, const f16* X, int B, int N, int K, float* part,
                                int* err, cudaStream_t st, int& splits) {
   splits = decode_splits(N, K);
@@ -417,67 +443,78 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, bf16* y, int B, const i
   f16* attn = reinterpret_cast<f16*>(ws + W.attn);
   float* r32 = reinterpret_cast<float*>(ws + W.r32);
   float* part = reinterpret_cast<float*>(ws + W.part);
+  f16* z = reinterpret_cast<f16*>(ws + W.z);
+  f16* hbuf = reinterpret_cast<f16*>(ws + W.h);
   int* err = L->status;
-  qwen_status s;
   int S = 1;
+  // swap-AB needs the batch on the MMA's N (<= 256); larger batches take the
+  // prefill-shaped GEMMs with the same fused epilogues
   const bool swap = B <= 256;
 
-  if ((s = rmsnorm_launch(x, L->gamma_attn, xh, true, nullptr, nullptr, B, d, c.rms_eps, st)))
-    return s;
+  // RMSNorm_1 -> X-hat (FP16 operand)
+  QWEN_STAGE_RUN(QWEN_STAGE_NORM1, rmsnorm_launch(x, L->gamma_attn, xh, true, nullptr, nullptr,
+                                                  B, d, c.rms_eps, st));
+  // Q/K/V, then bias, QK-norm, RoPE, Q store and K/V append at slot cache_len[b]
   const QkvParams qp = make_qkv_params(L, positions, cache_len, q, kc, vc, 1);
   if (swap) {
-    if ((s = decode_proj(L->w_qkv, xh, B, nqkv, d, part, err, st, S))) return s;
-    if ((s = reduce_qkv(part, S, B, nqkv, qp, err, st))) return s;
+    QWEN_STAGE_RUN(QWEN_STAGE_QKV, decode_proj(L->w_qkv, xh, B, nqkv, d, part, err, st, S));
+    QWEN_STAGE_RUN(QWEN_STAGE_QKV_FINISH, reduce_qkv(part, S, B, nqkv, qp, err, st));
   } else {
     GemmEpilogue e{};
     e.mode = EPI_QKV;
     e.qkv = qp;
-    if ((s = gemm_tc(xh, d, L->w_qkv, d, B, nqkv, d, true, e, err, st))) return s;
+    QWEN_STAGE_RUN(QWEN_STAGE_QKV, gemm_tc(xh, d, L->w_qkv, d, B, nqkv, d, true, e, err, st));
   }
+  // split-KV attention over slots 0..cache_len[b], then the merge
   int chunk = 0, splits = 0;
   decode_attn_plan(c, B, &chunk, &splits);
-  if ((s = attention_decode(q, kc, vc, cache_len, B, Hq, Hkv, dh, c.max_seq, chunk, splits,
-                            reinterpret_cast<float*>(ws + W.attn_o),
-                            reinterpret_cast<float*>(ws + W.attn_ml), attn, err, st)))
-    return s;
+  QWEN_STAGE_RUN(QWEN_STAGE_ATTN,
+                 attention_decode(q, kc, vc, cache_len, B, Hq, Hkv, dh, c.max_seq, chunk, splits,
+                                  reinterpret_cast<float*>(ws + W.attn_o),
+                                  reinterpret_cast<float*>(ws + W.attn_ml), attn, err, st));
+  // O projection + residual -> R (FP32)
   if (swap) {
-    if ((s = decode_proj(L->w_o, attn, B, d, nq, part, err, st, S))) return s;
-    if ((s = reduce_resid(part, S, B, d, x, nullptr, nullptr, r32, st))) return s;
+    QWEN_STAGE_RUN(QWEN_STAGE_O, decode_proj(L->w_o, attn, B, d, nq, part, err, st, S));
+    QWEN_STAGE_RUN(QWEN_STAGE_O_FINISH, reduce_resid(part, S, B, d, x, nullptr, nullptr, r32, st));
   } else {
     GemmEpilogue e{};
     e.mode = EPI_RESID;
-    e.out = nullptr;
     e.resid = x;
     e.ldr = d;
     e.out32 = r32;
     e.ldo32 = d;
-    if ((s = gemm_tc(attn, nq, L->w_o, nq, B, d, nq, true, e, err, st))) return s;
+    QWEN_STAGE_RUN(QWEN_STAGE_O, gemm_tc(attn, nq, L->w_o, nq, B, d, nq, true, e, err, st));
   }
-  if (c.n_experts)
-    return moe_forward(L, nullptr, r32, y, B, nullptr, nullptr, nullptr, ws, W, st);
-  f16* z = reinterpret_cast<f16*>(ws + W.z);
-  f16* hbuf = reinterpret_cast<f16*>(ws + W.h);
-  if ((s = rmsnorm_launch(nullptr, L->gamma_mlp, z, true, nullptr, r32, B, d, c.rms_eps, st)))
-    return s;
+  if (c.n_experts) {
+    QWEN_STAGE_RUN(QWEN_STAGE_MOE,
+                   moe_forward(L, nullptr, r32, y, B, nullptr, nullptr, nullptr, ws, W, st));
+    return QWEN_OK;
+  }
+  // RMSNorm_2 -> Z, gate/up + SiLU*up -> H, down + residual -> Y
+  QWEN_STAGE_RUN(QWEN_STAGE_NORM2, rmsnorm_launch(nullptr, L->gamma_mlp, z, true, nullptr, r32, B,
+                                                  d, c.rms_eps, st));
   if (swap) {
-    if ((s = decode_proj(L->w_gu, z, B, 2 * f, d, part, err, st, S))) return s;
-    if ((s = reduce_swiglu(part, S, B, f, hbuf, st))) return s;
-    if ((s = decode_proj(L->w_down, hbuf, B, d, f, part, err, st, S))) return s;
-    return reduce_resid(part, S, B, d, nullptr, r32, y, nullptr, st);
+    QWEN_STAGE_RUN(QWEN_STAGE_GATE_UP, decode_proj(L->w_gu, z, B, 2 * f, d, part, err, st, S));
+    QWEN_STAGE_RUN(QWEN_STAGE_GATE_UP_FINISH, reduce_swiglu(part, S, B, f, hbuf, st));
+    QWEN_STAGE_RUN(QWEN_STAGE_DOWN, decode_proj(L->w_down, hbuf, B, d, f, part, err, st, S));
+    QWEN_STAGE_RUN(QWEN_STAGE_DOWN_FINISH,
+                   reduce_resid(part, S, B, d, nullptr, r32, y, nullptr, st));
+    return QWEN_OK;
   }
   GemmEpilogue eg{};
   eg.mode = EPI_SWIGLU;
   eg.out = hbuf;
   eg.out_f16 = 1;
   eg.ldo = f;
-  if ((s = gemm_tc(z, d, L->w_gu, d, B, 2 * f, d, true, eg, err, st))) return s;
+  QWEN_STAGE_RUN(QWEN_STAGE_GATE_UP, gemm_tc(z, d, L->w_gu, d, B, 2 * f, d, true, eg, err, st));
   GemmEpilogue ed{};
   ed.mode = EPI_RESID;
   ed.out = y;
   ed.ldo = d;
   ed.resid32 = r32;
   ed.ldr = d;
-  return gemm_tc(hbuf, f, L->w_down, f, B, d, f, true, ed, err, st);
+  QWEN_STAGE_RUN(QWEN_STAGE_DOWN, gemm_tc(hbuf, f, L->w_down, f, B, d, f, true, ed, err, st));
+  return QWEN_OK;
 }
 
 qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, bf16* y, int B, int T,
@@ -490,49 +527,52 @@ qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, bf16* y, int B, int T,
   bf16* q = reinterpret_cast<bf16*>(ws + W.q);
   f16* attn = reinterpret_cast<f16*>(ws + W.attn);
   float* r32 = reinterpret_cast<float*>(ws + W.r32);
+  f16* z = reinterpret_cast<f16*>(ws + W.z);
+  f16* hbuf = reinterpret_cast<f16*>(ws + W.h);
   int* err = L->status;
-  qwen_status s;
 
-  // RMSNorm_1
-  if ((s = rmsnorm_launch(x, L->gamma_attn, xh, true, nullptr, nullptr, M, d, c.rms_eps, st)))
-    return s;
+  // RMSNorm_1 -> X-hat (FP16 operand)
+  QWEN_STAGE_RUN(QWEN_STAGE_NORM1, rmsnorm_launch(x, L->gamma_attn, xh, true, nullptr, nullptr,
+                                                  M, d, c.rms_eps, st));
   // fused QKV: bias, QK-norm, RoPE, Q store, K/V cache append
   GemmEpilogue e{};
   e.mode = EPI_QKV;
   e.qkv = make_qkv_params(L, positions, slot0, q, kc, vc, T);
-  if ((s = gemm_tc(xh, d, L->w_qkv, d, M, nqkv, d, true, e, err, st))) return s;
+  QWEN_STAGE_RUN(QWEN_STAGE_QKV, gemm_tc(xh, d, L->w_qkv, d, M, nqkv, d, true, e, err, st));
   // causal GQA attention over the cache
-  if ((s = attention_prefill(q, kc, vc, slot0, attn, B, T, Hq, Hkv, dh, c.max_seq, err, st)))
-    return s;
+  QWEN_STAGE_RUN(QWEN_STAGE_ATTN, attention_prefill(q, kc, vc, slot0, attn, B, T, Hq, Hkv, dh,
+                                                    c.max_seq, err, st));
   // O projection + residual; R stays in FP32 (it reaches Y unchanged through
   // the second residual, so rounding it to BF16 would put that rounding on Y)
   GemmEpilogue eo{};
   eo.mode = EPI_RESID;
-  eo.out = nullptr;
   eo.resid = x;
   eo.ldr = d;
   eo.out32 = r32;
   eo.ldo32 = d;
-  if ((s = gemm_tc(attn, nq, L->w_o, nq, M, d, nq, true, eo, err, st))) return s;
-  if (c.n_experts) return moe_forward(L, nullptr, r32, y, M, nullptr, nullptr, nullptr, ws, W, st);
+  QWEN_STAGE_RUN(QWEN_STAGE_O, gemm_tc(attn, nq, L->w_o, nq, M, d, nq, true, eo, err, st));
+  if (c.n_experts) {
+    QWEN_STAGE_RUN(QWEN_STAGE_MOE,
+                   moe_forward(L, nullptr, r32, y, M, nullptr, nullptr, nullptr, ws, W, st));
+    return QWEN_OK;
+  }
   // RMSNorm_2, gate/up + SiLU*mul, down + residual
-  f16* z = reinterpret_cast<f16*>(ws + W.z);
-  f16* hbuf = reinterpret_cast<f16*>(ws + W.h);
-  if ((s = rmsnorm_launch(nullptr, L->gamma_mlp, z, true, nullptr, r32, M, d, c.rms_eps, st)))
-    return s;
+  QWEN_STAGE_RUN(QWEN_STAGE_NORM2, rmsnorm_launch(nullptr, L->gamma_mlp, z, true, nullptr, r32, M,
+                                                  d, c.rms_eps, st));
   GemmEpilogue eg{};
   eg.mode = EPI_SWIGLU;
   eg.out = hbuf;
   eg.out_f16 = 1;
   eg.ldo = f;
-  if ((s = gemm_tc(z, d, L->w_gu, d, M, 2 * f, d, true, eg, err, st))) return s;
+  QWEN_STAGE_RUN(QWEN_STAGE_GATE_UP, gemm_tc(z, d, L->w_gu, d, M, 2 * f, d, true, eg, err, st));
   GemmEpilogue ed{};
   ed.mode = EPI_RESID;
   ed.out = y;
   ed.ldo = d;
   ed.resid32 = r32;
   ed.ldr = d;
-  return gemm_tc(hbuf, f, L->w_down, f, M, d, f, true, ed, err, st);
+  QWEN_STAGE_RUN(QWEN_STAGE_DOWN, gemm_tc(hbuf, f, L->w_down, f, M, d, f, true, ed, err, st));
+  return QWEN_OK;
 }
 
 QkvParams make_qkv_params(const qwen_layer_s* L, const int32_t* positions, const int32_t* slot0,

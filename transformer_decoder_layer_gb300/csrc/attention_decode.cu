@@ -414,10 +414,12 @@ static qwen_status launch_attn_dec(const CUtensorMap& tk, const CUtensorMap& tv,
   const int sms = device_sm_count();
   const int grid = units < sms ? units : sms;
   kern<<<grid, kDecAttnThreads, DecAttnCfg<DH>::SMEM_BYTES, st>>>(tk, tv, a);
+  count_launches();
   if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;
   const int BH = a.B * a.Hq;
   attn_decode_merge_kernel<DH><<<(BH * 32 + 255) / 256, 256, 0, st>>>(a.part_o, a.part_ml, BH,
                                                                        a.splits, out);
+  count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 

@@ -380,6 +380,7 @@ static qwen_status launch_dh(const CUtensorMap& q, const CUtensorMap& k, const C
   const int n_qt = (a.T + kQT - 1) / kQT;
   const int grid = n_qt * a.B * a.Hq;
   kern<<<grid, kAttnThreads, AttnCfg<DH>::SMEM_BYTES, st>>>(q, k, v, a);
+  count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 

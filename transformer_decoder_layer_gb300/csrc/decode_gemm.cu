@@ -347,6 +347,7 @@ static qwen_status launch_dec(const CUtensorMap& tw, const CUtensorMap& tx, int 
   const int grid = units < sms ? units : sms;
   kern<<<grid, kDThreads, DecCfg<BP>::SMEM_BYTES, st>>>(tw, tx, B, N, K, splits, ldp_of(B),
                                                         idesc_f32acc(kDBM, BP, op_f16), part, err);
+  count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
@@ -373,12 +374,14 @@ qwen_status reduce_resid(const float* part, int splits, int B, int N, const bf16
                          const float* resid32, bf16* out, float* out32, cudaStream_t st) {
   reduce_resid_kernel<<<blocks_for((long long)N * B, 256), 256, 0, st>>>(
       part, splits, B, N, ldp_of(B), resid, resid32, out, out32);
+  count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
 qwen_status reduce_swiglu(const float* part, int splits, int B, int f, f16* h, cudaStream_t st) {
   reduce_swiglu_kernel<<<blocks_for((long long)f * B, 256), 256, 0, st>>>(part, splits, B, f,
                                                                             ldp_of(B), h);
+  count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
@@ -389,6 +392,7 @@ qwen_status reduce_qkv(const float* part, int splits, int B, int Nqkv, const Qkv
     reduce_qkv_kernel<128><<<blocks_for(n, 64), 64, 0, st>>>(part, splits, B, Nqkv, ldp_of(B), p, err);
   else
     reduce_qkv_kernel<64><<<blocks_for(n, 64), 64, 0, st>>>(part, splits, B, Nqkv, ldp_of(B), p, err);
+  count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
@@ -396,6 +400,7 @@ qwen_status reduce_f32(const float* part, int splits, int B, int N, float* out, 
                        cudaStream_t st) {
   reduce_f32_kernel<<<blocks_for((long long)N * B, 256), 256, 0, st>>>(part, splits, B, N,
                                                                          ldp_of(B), out, ldo);
+  count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 

@@ -445,6 +445,7 @@ static qwen_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M
     attr_done = true;
   }
   kern<<<grid, kGemmThreads, GemmCfg<BN>::SMEM_BYTES, st>>>(ta, tb, M, N, K, idesc, epi, err);
+  count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 

@@ -55,6 +55,8 @@ struct GemmEpilogue {
 };
 
 int device_sm_count();
+// Host-side count of kernel launches issued by the library (qwen_launch_count).
+void count_launches(int n = 1);
 int* lib_status_ptr();  // device status word used by handle-less entry points
 
 // The tensor-core GEMM.  A [M,K] (row stride lda elements), B [N,K] (ldb),

@@ -39,6 +39,9 @@ struct qwen_layer_s {
   __half *w_gu, *w_down;  // gate/up rows interleaved in 64-row blocks
   __nv_bfloat16* w_router;
   float* b_router;
+  // optional per-stage events (qwen_layer_set_trace)
+  bool tracing = false;
+  void* trace[2 * QWEN_STAGE_COUNT] = {};
 };
 
 namespace qwen {

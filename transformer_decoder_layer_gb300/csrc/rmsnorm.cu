@@ -99,6 +99,7 @@ qwen_status rmsnorm_launch(const bf16* x, const bf16* gamma, void* y, bool y_f16
     rmsnorm_kernel<16><<<blocks, threads, 0, st>>>(x, x32, gamma, y, y_f16, y32, rows, d, eps, xs);
   else
     rmsnorm_kernel<32><<<blocks, threads, 0, st>>>(x, x32, gamma, y, y_f16, y32, rows, d, eps, xs);
+  count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
