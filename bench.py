@@ -158,6 +158,9 @@ class DecodeBench:
                           workspace=self.ws)
 
     def timed(self, steps, warmup, trace_stage=None, clocks=None):
+        """K decode steps captured once as a CUDA graph and replayed in the timed
+        region (the captured kernels are exactly the eager ones).  With
+        trace_stage, that stage of every step is bracketed by its own events."""
         torch = self.torch
         for _ in range(warmup):
             self.step()
@@ -165,32 +168,41 @@ class DecodeBench:
         evs = []
         if trace_stage:
             for _ in range(steps):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
                 a.record()
                 b.record()  # creates the events before the library records them
                 evs.append((a, b))
             torch.cuda.synchronize()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        n0 = self.q.launch_count()
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(steps):
+                if trace_stage:
+                    self.layer.set_trace({trace_stage: evs[i]})
+                self.step()
+        n_launch = self.q.launch_count() - n0  # kernels per replay
+        if trace_stage:
+            self.layer.set_trace(None)
+        for _ in range(max(1, warmup // steps)):
+            graph.replay()
+        torch.cuda.synchronize()
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
-        n0 = self.q.launch_count()
-        torch.cuda.synchronize()
         w0 = time.time()
         t_start.record()
-        for i in range(steps):
-            if trace_stage:
-                self.layer.set_trace({trace_stage: evs[i]})
-            self.step()
+        graph.replay()
         t_end.record()
         torch.cuda.synchronize()
         w1 = time.time()
-        if trace_stage:
-            self.layer.set_trace(None)
         if clocks:
             clocks.mark(w0, w1)
-        n_launch = self.q.launch_count() - n0
         total_ms = t_start.elapsed_time(t_end)
         kern_ms = [a.elapsed_time(b) for a, b in evs] if evs else []
         assert self.layer.poll_error() == 0, "device status set during the benchmark"
+        del graph
         return total_ms, kern_ms, n_launch
 
     def e2e(self, steps, warmup):

@@ -370,8 +370,7 @@ size_t qwen_head_workspace_bytes(int32_t B, int32_t d, int32_t V) {
   if (B <= 0 || d <= 0 || V <= 0) return 0;
   const size_t xn = align256((size_t)B * d * 2);
   if (B > 256) return xn;
-  const size_t ldp = (B + 3) & ~3;
-  return xn + align256((size_t)decode_splits(V, d) * V * ldp * 4);
+  return xn + align256((size_t)decode_splits(V, d) * V * (size_t)B * 4);
 }
 
 qwen_status qwen_head_last_token(const void* y, int32_t B, int32_t T, int32_t d,
@@ -410,10 +409,18 @@ qwen_status qwen_head_last_token(const void* y, int32_t B, int32_t T, int32_t d,
 namespace qwen {
 
 // Record the trace event of `stage` (begin = 0, end = 1) when tracing is on.
+// Inside a CUDA-graph capture the event becomes an external event-record node,
+// so it is recorded (and timed) on every replay.
 static inline void mark(const qwen_layer_s* L, int stage, int end, cudaStream_t st) {
   if (!L->tracing) return;
   void* e = L->trace[2 * stage + end];
-  if (e) cudaEventRecord(static_cast<cudaEvent_t>(e), st);
+  if (!e) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(st, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(static_cast<cudaEvent_t>(e), st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(static_cast<cudaEvent_t>(e), st);
 }
 
 #define QWEN_STAGE_RUN(stage, expr)            \

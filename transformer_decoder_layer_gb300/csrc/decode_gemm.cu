@@ -40,8 +40,8 @@ struct DecCfg {
 template <int BP>
 __global__ void __launch_bounds__(kDThreads, 1)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                       int B, int N, int K, int splits, int ldp, uint32_t idesc,
-                       float* __restrict__ part, int* err) {
+                       int B, int N, int K, int splits, uint32_t idesc, float* __restrict__ part,
+                       int* err) {
   using C = DecCfg<BP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -162,25 +162,19 @@ __global__ void __launch_bounds__(kDThreads, 1)
       const int acc = local & 1;
       if (!mbar_wait(&tfull[acc], (local >> 1) & 1, abort_flag, err)) break;
       tc_fence_after();
+      // part[s][b][n]: for each batch column the 32 lanes (consecutive weight
+      // rows n) write 128 contiguous bytes
       const int n = n0 + q * 32 + lane;
-      float* dst = part + ((size_t)s * N + n) * ldp;
+      float* dst = part + (size_t)s * B * N + n;
 #pragma unroll 1
       for (int c = 0; c < BP; c += 32) {
         uint32_t r[32];
         tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BP + c, r);
         tmem_ld_wait();
-        if (n < N && c < B) {
-          if (c + 32 <= B && (ldp & 3) == 0) {
+        if (n < N) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              reinterpret_cast<float4*>(dst + c)[i] =
-                  make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                              __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c + i < B) dst[c + i] = __uint_as_float(r[i]);
-          }
+          for (int i = 0; i < 32; ++i)
+            if (c + i < B) dst[(size_t)(c + i) * N] = __uint_as_float(r[i]);
         }
       }
       tc_fence_before();
@@ -196,62 +190,116 @@ __global__ void __launch_bounds__(kDThreads, 1)
 }
 
 // ------------------------------------------------------------------ reductions
+// Partials are part[s][b][n]; the splits are summed in order s = 0, 1, ...
 
 __global__ void reduce_resid_kernel(const float* __restrict__ part, int splits, int B, int N,
-                                    int ldp, const bf16* __restrict__ resid,
+                                    const bf16* __restrict__ resid,
                                     const float* __restrict__ resid32, bf16* __restrict__ out,
                                     float* __restrict__ out32) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // over N * B, b fastest
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // over B * N, n fastest
   if (i >= N * B) return;
-  const int n = i / B, b = i - n * B;
+  const size_t plane = (size_t)B * N;
   float acc = 0.f;
-  for (int s = 0; s < splits; ++s) acc += part[((size_t)s * N + n) * ldp + b];
-  acc += resid32 ? resid32[(size_t)b * N + n] : __bfloat162float(resid[(size_t)b * N + n]);
-  if (out) out[(size_t)b * N + n] = __float2bfloat16_rn(acc);
-  if (out32) out32[(size_t)b * N + n] = acc;
+  for (int s = 0; s < splits; ++s) acc += part[s * plane + i];
+  acc += resid32 ? resid32[i] : __bfloat162float(resid[i]);
+  if (out) out[i] = __float2bfloat16_rn(acc);
+  if (out32) out32[i] = acc;
 }
 
 // h[b][j] = SiLU(gate_j) * up_j with gate row (j/64)*128 + j%64 and up row +64.
 __global__ void reduce_swiglu_kernel(const float* __restrict__ part, int splits, int B, int f,
-                                     int ldp, f16* __restrict__ h) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+                                     f16* __restrict__ h) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // over B * f, j fastest
   if (i >= f * B) return;
-  const int j = i / B, b = i - j * B;
-  const int n_gate = (j >> 6) * 128 + (j & 63);
+  const int b = i / f, j = i - b * f;
   const int N = 2 * f;
+  const int n_gate = (j >> 6) * 128 + (j & 63);
+  const size_t plane = (size_t)B * N;
+  const float* src = part + (size_t)b * N + n_gate;
   float g = 0.f, u = 0.f;
   for (int s = 0; s < splits; ++s) {
-    g += part[((size_t)s * N + n_gate) * ldp + b];
-    u += part[((size_t)s * N + n_gate + 64) * ldp + b];
+    g += src[s * plane];
+    u += src[s * plane + 64];
   }
-  h[(size_t)b * f + j] = __float2half_rn(silu_f(g) * u);
+  h[i] = __float2half_rn(silu_f(g) * u);
 }
 
+// One warp per (b, head): lane e holds channels e, e+32, e+64, e+96 (dh = 128)
+// or e, e+32 (dh = 64), so the rotate_half pairs (i, i + dh/2) stay in a lane.
+// The same step as qkv_head_finish: bias, QK-norm (warp reduction over dh),
+// RoPE from the FP64-built table, then Q store or K/V cache append.
 template <int DH>
 __global__ void reduce_qkv_kernel(const float* __restrict__ part, int splits, int B, int Nqkv,
-                                  int ldp, QkvParams p, int* err) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;  // over (b, head)
+                                  QkvParams p, int* err) {
+  constexpr int PER = DH / 32;
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
   const int heads = p.Hq + 2 * p.Hkv;
-  if (i >= B * heads) return;
-  const int b = i / heads, head = i - b * heads;
-  float v[DH];
+  if (wid >= B * heads) return;
+  const int b = wid / heads, head = wid - b * heads;
+  const size_t plane = (size_t)B * Nqkv;
+  const float* src = part + (size_t)b * Nqkv + (size_t)head * DH + lane;
+  float v[PER];
 #pragma unroll
-  for (int e = 0; e < DH; ++e) v[e] = 0.f;
+  for (int e = 0; e < PER; ++e) v[e] = 0.f;
   for (int s = 0; s < splits; ++s) {
-    const float* src = part + ((size_t)s * Nqkv + (size_t)head * DH) * ldp + b;
 #pragma unroll
-    for (int e = 0; e < DH; ++e) v[e] += src[(size_t)e * ldp];
+    for (int e = 0; e < PER; ++e) v[e] += src[s * plane + 32 * e];
   }
-  qkv_head_finish<DH>(v, b, head, p, err);
+  const int kind = head < p.Hq ? 0 : (head < p.Hq + p.Hkv ? 1 : 2);
+  if (p.bias) {
+#pragma unroll
+    for (int e = 0; e < PER; ++e) v[e] += p.bias[(size_t)head * DH + lane + 32 * e];
+  }
+  if (kind < 2) {
+    if (p.gamma_q) {
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) ss = fmaf(v[e], v[e], ss);
+      ss = warp_sum(ss);
+      const float rstd = rsqrtf(ss / (float)DH + p.eps);
+      const bf16* gm = kind == 0 ? p.gamma_q : p.gamma_k;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) v[e] = __bfloat162float(gm[lane + 32 * e]) * (v[e] * rstd);
+    }
+    const int pos = p.positions[b];
+    if (pos < 0 || pos >= p.max_position) {
+      if (lane == 0) record_error(err, QWEN_ERR_RANGE);
+      return;
+    }
+    const float2* tab = p.rope + (size_t)pos * (DH / 2);
+#pragma unroll
+    for (int e = 0; e < PER / 2; ++e) {
+      const float2 cs = tab[lane + 32 * e];
+      const float lo = v[e], hi = v[e + PER / 2];
+      v[e] = lo * cs.x - hi * cs.y;
+      v[e + PER / 2] = hi * cs.x + lo * cs.y;
+    }
+  }
+  bf16* dst;
+  if (kind == 0) {
+    dst = p.q_out + ((size_t)b * p.Hq + head) * DH;  // T == 1
+  } else {
+    const int slot = p.slot0[b];
+    if (slot < 0 || slot >= p.max_seq) {
+      if (lane == 0) record_error(err, QWEN_ERR_RANGE);
+      return;
+    }
+    const int g = kind == 1 ? head - p.Hq : head - p.Hq - p.Hkv;
+    dst = (kind == 1 ? p.k_cache : p.v_cache) + (((size_t)b * p.Hkv + g) * p.max_seq + slot) * DH;
+  }
+#pragma unroll
+  for (int e = 0; e < PER; ++e) dst[lane + 32 * e] = __float2bfloat16_rn(v[e]);
 }
 
-__global__ void reduce_f32_kernel(const float* __restrict__ part, int splits, int B, int N, int ldp,
+__global__ void reduce_f32_kernel(const float* __restrict__ part, int splits, int B, int N,
                                   float* __restrict__ out, int ldo) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= N * B) return;
-  const int n = i / B, b = i - n * B;
+  const int b = i / N, n = i - b * N;
+  const size_t plane = (size_t)B * N;
   float acc = 0.f;
-  for (int s = 0; s < splits; ++s) acc += part[((size_t)s * N + n) * ldp + b];
+  for (int s = 0; s < splits; ++s) acc += part[s * plane + i];
   out[(size_t)b * ldo + n] = acc;
 }
 
@@ -310,16 +358,13 @@ int decode_splits(int N, int K) {
   return best;
 }
 
-static inline int ldp_of(int B) { return (B + 3) & ~3; }
-
 size_t decode_part_bytes(const qwen_layer_config& c, int B) {
   const size_t d = c.d, nq = (size_t)c.n_q_heads * c.head_dim,
                nqkv = nq + 2 * (size_t)c.n_kv_heads * c.head_dim, f = c.ffn;
-  const size_t ldp = ldp_of(B);
   size_t m = 0;
   auto upd = [&](size_t N, size_t K) {
     const size_t s = decode_splits((int)N, (int)K);
-    const size_t need = s * N * ldp * 4;
+    const size_t need = s * N * (size_t)B * 4;
     if (need > m) m = need;
   };
   upd(nqkv, d);
@@ -345,7 +390,7 @@ static qwen_status launch_dec(const CUtensorMap& tw, const CUtensorMap& tx, int 
   const int units = ((N + kDBM - 1) / kDBM) * splits;
   const int sms = device_sm_count();
   const int grid = units < sms ? units : sms;
-  kern<<<grid, kDThreads, DecCfg<BP>::SMEM_BYTES, st>>>(tw, tx, B, N, K, splits, ldp_of(B),
+  kern<<<grid, kDThreads, DecCfg<BP>::SMEM_BYTES, st>>>(tw, tx, B, N, K, splits,
                                                         idesc_f32acc(kDBM, BP, op_f16), part, err);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
@@ -373,33 +418,32 @@ static inline int blocks_for(long long n, int t) { return (int)((n + t - 1) / t)
 qwen_status reduce_resid(const float* part, int splits, int B, int N, const bf16* resid,
                          const float* resid32, bf16* out, float* out32, cudaStream_t st) {
   reduce_resid_kernel<<<blocks_for((long long)N * B, 256), 256, 0, st>>>(
-      part, splits, B, N, ldp_of(B), resid, resid32, out, out32);
+      part, splits, B, N, resid, resid32, out, out32);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
 qwen_status reduce_swiglu(const float* part, int splits, int B, int f, f16* h, cudaStream_t st) {
-  reduce_swiglu_kernel<<<blocks_for((long long)f * B, 256), 256, 0, st>>>(part, splits, B, f,
-                                                                            ldp_of(B), h);
+  reduce_swiglu_kernel<<<blocks_for((long long)f * B, 256), 256, 0, st>>>(part, splits, B, f, h);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
 qwen_status reduce_qkv(const float* part, int splits, int B, int Nqkv, const QkvParams& p, int* err,
                        cudaStream_t st) {
-  const int n = B * (p.Hq + 2 * p.Hkv);
+  const long long threads = 32LL * B * (p.Hq + 2 * p.Hkv);
   if (p.dh == 128)
-    reduce_qkv_kernel<128><<<blocks_for(n, 64), 64, 0, st>>>(part, splits, B, Nqkv, ldp_of(B), p, err);
+    reduce_qkv_kernel<128><<<blocks_for(threads, 128), 128, 0, st>>>(part, splits, B, Nqkv, p, err);
   else
-    reduce_qkv_kernel<64><<<blocks_for(n, 64), 64, 0, st>>>(part, splits, B, Nqkv, ldp_of(B), p, err);
+    reduce_qkv_kernel<64><<<blocks_for(threads, 128), 128, 0, st>>>(part, splits, B, Nqkv, p, err);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
 qwen_status reduce_f32(const float* part, int splits, int B, int N, float* out, int ldo,
                        cudaStream_t st) {
-  reduce_f32_kernel<<<blocks_for((long long)N * B, 256), 256, 0, st>>>(part, splits, B, N,
-                                                                         ldp_of(B), out, ldo);
+  reduce_f32_kernel<<<blocks_for((long long)N * B, 256), 256, 0, st>>>(part, splits, B, N, out,
+                                                                         ldo);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }

@@ -77,8 +77,8 @@ size_t decode_part_bytes(const qwen_layer_config& c, int B);
 // Attention split-KV plan: keys per split and number of splits for batch B.
 void decode_attn_plan(const qwen_layer_config& c, int B, int* chunk, int* splits);
 
-// part[s][n][b] (row stride ldp = round_up(B, 4)) = sum over split s's k-range
-// of W[n, k] X[b, k].  W [N, K], X [B, K] (row stride ldx).
+// part[s][b][n] = sum over split s's k-range of W[n, k] X[b, k].
+// W [N, K], X [B, K] (row stride ldx).
 qwen_status gemm_decode_splitk(const void* W, const void* X, int ldx, int B, int N, int K,
                                int splits, bool op_f16, float* part, int* err, cudaStream_t st);
 
