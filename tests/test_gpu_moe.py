@@ -1,0 +1,160 @@
+"""MoE parity of the CUDA path (through the C ABI) against the FP64 oracle.
+
+Top-k indices must match the oracle exactly wherever the oracle's k-th minus
+(k+1)-th logit gap exceeds 1e-3; where it does not, both selections are
+correct, and the GPU output is compared with the oracle evaluated under the
+GPU's selection (weights = softmax of the oracle logits at those experts)."""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from layer_harness import GpuLayer, f64
+from parity import assert_parity
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+GAP = 1e-3
+
+SMALL_MOE = synth.LayerConfig(d=512, n_q_heads=8, n_kv_heads=2, head_dim=64, ffn=256, qk_norm=1,
+                              n_experts=16, top_k=4, router_bias=1)
+
+
+def _moe_reference(r64, w64, cfg, gpu_idx):
+    """Oracle MoE; ambiguous tokens re-evaluated under the GPU's selection."""
+    y, logits, idx, wts, gap, z = oracle.moe_block(r64, w64, cfg)
+    amb = gap <= GAP
+    if amb.any():
+        sel = np.take_along_axis(logits, gpu_idx.astype(np.int64), axis=1)
+        p = np.exp(sel - sel.max(1, keepdims=True))
+        p /= p.sum(1, keepdims=True)
+        idx2 = np.where(amb[:, None], gpu_idx, idx)
+        wts2 = np.where(amb[:, None], p, wts)
+        y = oracle.moe_block(r64, w64, cfg, routing=(idx2, wts2))[0]
+    return y, logits, idx, wts, gap
+
+
+def _run_moe_ffn(shape, tag, T, fp32_input=False):
+    w_cpu = synth.layer_weights(shape, tag)
+    r = synth.activations([T, shape.d], tag, "r")
+    g = GpuLayer(shape, w_cpu, max_tokens=T, max_batch=1, max_seq=8, max_position=8)
+    k, E = shape.top_k, shape.n_experts
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    wts = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    lg = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    r_dev = r.cuda()
+    r32 = r_dev.float() if fp32_input else None
+    y = g.layer.moe_ffn(r_dev, r_fp32=r32, topk_idx=idx, topk_w=wts, logits=lg)
+    assert g.layer.poll_error() == 0
+    w64 = synth.weights_f64(w_cpu)
+    gi = idx.cpu().numpy()
+    ref, logits, oidx, owts, gap = _moe_reference(f64(r), w64, shape.as_dict(), gi)
+    return f64(y.float()), ref, gi, wts.cpu().numpy(), lg.cpu().numpy(), logits, oidx, owts, gap
+
+
+def _check_routing(gi, gw, glog, logits, oidx, owts, gap):
+    clear = gap > GAP
+    assert clear.mean() > 0.8, "too few unambiguous tokens for a meaningful check"
+    assert np.array_equal(gi[clear], oidx[clear]), (
+        f"top-k mismatch on {np.sum(np.any(gi[clear] != oidx[clear], axis=1))} unambiguous tokens")
+    assert np.allclose(gw[clear], owts[clear], atol=1e-5)
+    assert np.allclose(glog, logits, atol=2e-5, rtol=1e-5)
+    # every selection is a valid top-k: distinct experts, weights sum to one
+    assert all(len(set(row)) == len(row) for row in gi)
+    assert np.allclose(gw.sum(1), 1.0, atol=1e-5)
+
+
+def test_moe_ffn_small_ragged():
+    """E=16, k=4, T=300 (ragged tiles per expert), biased router."""
+    y, ref, gi, gw, glog, logits, oidx, owts, gap = _run_moe_ffn(SMALL_MOE, "moe_s", 300)
+    _check_routing(gi, gw, glog, logits, oidx, owts, gap)
+    assert_parity(y, ref, what="MoE Y")
+
+
+def test_moe_ffn_fp32_residual_input():
+    y, ref, gi, gw, glog, logits, oidx, owts, gap = _run_moe_ffn(SMALL_MOE, "moe_s32", 77,
+                                                                 fp32_input=True)
+    _check_routing(gi, gw, glog, logits, oidx, owts, gap)
+    assert_parity(y, ref, what="MoE Y (fp32 R)")
+
+
+@pytest.fixture(scope="module")
+def a3b_weights():
+    return synth.layer_weights(synth.QWEN3_30B_A3B, "a3b")
+
+
+def test_moe_ffn_qwen3_30b_a3b_full(a3b_weights):
+    """Qwen3-30B-A3B-shaped MoE block at T=4096, E=128, k=8, mf=768."""
+    shape = synth.QWEN3_30B_A3B
+    T = 4096
+    r = synth.activations([T, shape.d], "a3b", "r")
+    g = GpuLayer(shape, a3b_weights, max_tokens=T, max_batch=1, max_seq=8, max_position=8)
+    idx = torch.empty((T, 8), dtype=torch.int32, device="cuda")
+    wts = torch.empty((T, 8), dtype=torch.float32, device="cuda")
+    lg = torch.empty((T, 128), dtype=torch.float32, device="cuda")
+    y = g.layer.moe_ffn(r.cuda(), topk_idx=idx, topk_w=wts, logits=lg)
+    assert g.layer.poll_error() == 0
+    gi = idx.cpu().numpy()
+    w64 = synth.weights_f64(a3b_weights)
+    ref, logits, oidx, owts, gap = _moe_reference(f64(r), w64, shape.as_dict(), gi)
+    _check_routing(gi, wts.cpu().numpy(), lg.cpu().numpy(), logits, oidx, owts, gap)
+    assert_parity(f64(y.float()), ref, what="MoE Y")
+    # the router bias skews expert loads, as the workload intends
+    loads = np.bincount(gi.reshape(-1), minlength=128)
+    assert loads.max() > 2 * loads.mean()
+
+
+def _moe_layer_case(shape, w_cpu, tag, B, T, rows):
+    x = synth.activations([B, T, shape.d], tag)
+    g = GpuLayer(shape, w_cpu, max_tokens=B * T, max_batch=B, max_seq=T, max_position=T)
+    kc = torch.zeros((B, shape.n_kv_heads, T, shape.head_dim), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    y = g.prefill(x, np.tile(np.arange(T), (B, 1)), [0] * B, kc, vc)
+    w64 = synth.weights_f64(w_cpu)
+    cfg = shape.as_dict()
+    yg = f64(y.float())
+    for b in range(B):
+        kk = np.zeros((shape.n_kv_heads, T, shape.head_dim))
+        vv = np.zeros_like(kk)
+        yo, r, (logits, idx, wts, gap) = oracle.moe_layer_forward(
+            f64(x)[b], w64, cfg, np.arange(T), kk, vv, np.arange(T), rows=rows)
+        clear = gap > 10 * GAP  # R differs from the oracle by attention rounding
+        assert clear.mean() > 0.7
+        assert_parity(yg[b, rows][clear], yo[clear], what=f"MoE layer Y (b={b})")
+
+
+def test_moe_layer_prefill_small():
+    shape = SMALL_MOE
+    rows = np.array([0, 1, 63, 64, 65, 127, 128, 200, 255])
+    _moe_layer_case(shape, synth.layer_weights(shape, "moel"), "moel", 2, 256, rows)
+
+
+def test_moe_layer_prefill_qwen3_30b_a3b(a3b_weights):
+    """Full Qwen3-30B-A3B-shaped MoE layer, T=4096, sampled rows."""
+    T = 4096
+    rows = np.unique(np.r_[0, 1, 127, 128, 2048, 4095,
+                           np.random.default_rng(1).integers(0, T, 40)])
+    _moe_layer_case(synth.QWEN3_30B_A3B, a3b_weights, "a3bl", 1, T, rows)
+
+
+def test_moe_layer_decode():
+    """MoE layer decode (tiny per-expert groups), B=8 against 100 cached slots."""
+    shape = SMALL_MOE
+    B, L = 8, 100
+    w_cpu = synth.layer_weights(shape, "moed")
+    x = synth.activations([B, shape.d], "moed")
+    kc, vc = synth.kv_cache(B, shape.n_kv_heads, L + 1, shape.head_dim, L, "moed")
+    g = GpuLayer(shape, w_cpu, max_tokens=B, max_batch=B, max_seq=L + 1, max_position=L + 1)
+    kd, vd = kc.cuda(), vc.cuda()
+    y = g.decode(x, np.full(B, L), [L] * B, kd, vd)
+    w64 = synth.weights_f64(w_cpu)
+    cfg = shape.as_dict()
+    yg = f64(y.float())
+    for b in range(B):
+        kk, vv = f64(kc)[b].copy(), f64(vc)[b].copy()
+        yo, r, (logits, idx, wts, gap) = oracle.moe_layer_forward(
+            f64(x)[b][None], w64, cfg, np.array([L]), kk, vv, np.array([L]))
+        if gap[0] > 10 * GAP:
+            assert_parity(yg[b][None], yo, what=f"decode Y b={b}")

@@ -90,6 +90,7 @@ WorkspaceLayout workspace_layout(const qwen_layer_config& c, int B, int T) {
     W.logits = take(M * e * 4);
     W.topk_idx = take(mk * 4);
     W.topk_w = take(mk * 4);
+    W.counts = take(e * 4);
     W.offsets = take((e + 1) * 4);
     W.perm = take(mk * 4);
     W.inv = take(mk * 4);

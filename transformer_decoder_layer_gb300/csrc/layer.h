@@ -17,7 +17,7 @@ struct PackedLayout {
 struct WorkspaceLayout {
   size_t xh, q, attn, r32, z, h;
   // MoE
-  size_t z32, logits, topk_idx, topk_w, offsets, perm, inv, zp, hp, yp;
+  size_t z32, logits, topk_idx, topk_w, counts, offsets, perm, inv, zp, hp, yp;
   // decode (T == 1)
   size_t part, attn_o, attn_ml;
   size_t total;
