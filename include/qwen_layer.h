@@ -176,6 +176,23 @@ QWEN_API qwen_status qwen_head_last_token(const void* y, int32_t B, int32_t T, i
                                  float eps, float* logits, void* workspace,
                                  size_t workspace_bytes, void* stream);
 
+/* qwen_head_last_token without a workspace, for callers that cannot allocate
+ * device memory at call time (for example a server that has committed all of
+ * its HBM to a fixed arena, or a loop where an allocation would synchronise
+ * the device).  The pages have no counterpart: this is a library convenience.
+ * Same arguments and result as qwen_head_last_token minus the workspace.  The
+ * normalised last rows (B * d BF16 values) live in a 2 MiB device array inside
+ * the library, held on every GPU that loads it until the process exits:
+ * B * d * 2 must be <= 2 MiB (e.g. B = 256 at d = 4096, B = 128 at d = 8192)
+ * and B <= 256, else QWEN_ERR_CAPACITY.  The array's device address is looked
+ * up on the first call made on each device (make that first call before any
+ * stream capture).  All calls share the array: calls that overlap on the GPU
+ * race on it.  Nothing is allocated or freed. */
+QWEN_API qwen_status qwen_head_last_token_noalloc(const void* y, int32_t B, int32_t T, int32_t d,
+                                                  const void* gamma_final, const void* w_lm,
+                                                  int32_t V, float eps, float* logits,
+                                                  void* stream);
+
 /* One RMSNorm pass (the layer's norm step on its own, Qwen3 layer page §3):
  *   y[r] = gamma * x[r] / sqrt(mean(x[r]^2) + eps), rows x d, BF16 in/out,
  *   optional FP32 copy of y (y_fp32 may be NULL).  d % 8 == 0.            */

@@ -67,6 +67,8 @@ _SIGS = {
     "qwen_head_workspace_bytes": (_SZ, [_I32, _I32, _I32]),
     "qwen_head_last_token": (ctypes.c_int, [_VP, _I32, _I32, _I32, _VP, _VP, _I32, _F32, _VP,
                                             _VP, _SZ, _VP]),
+    "qwen_head_last_token_noalloc": (ctypes.c_int, [_VP, _I32, _I32, _I32, _VP, _VP, _I32, _F32,
+                                                    _VP, _VP]),
     "qwen_rmsnorm": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _I32, _F32, _VP]),
     "qwen_linear": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, _I32, _VP]),
     "qwen_layer_poll_error": (ctypes.c_int, [_VP, _VP]),
@@ -183,6 +185,22 @@ def head_last_token(y, gamma_final, w_lm, eps, logits=None, workspace=None, stre
                                       float(eps), _ptr(logits), _ptr(workspace),
                                       workspace.numel(), _stream(stream)),
            "qwen_head_last_token")
+    return logits
+
+
+def head_last_token_noalloc(y, gamma_final, w_lm, eps, logits=None, stream=None):
+    """Same result as head_last_token, with no workspace: for callers that
+    cannot allocate device memory at call time (the library keeps the
+    normalised rows in its own fixed device array; B * d * 2 <= 2 MiB).
+    Calls that overlap on the GPU race on that array."""
+    import torch
+    _need(y, torch.bfloat16, "y")
+    B, T, d = y.shape
+    V = w_lm.shape[0]
+    logits = torch.empty((B, V), dtype=torch.float32, device=y.device) if logits is None else logits
+    _check(lib().qwen_head_last_token_noalloc(_ptr(y), B, T, d, _ptr(gamma_final), _ptr(w_lm), V,
+                                              float(eps), _ptr(logits), _stream(stream)),
+           "qwen_head_last_token_noalloc")
     return logits
 
 
