@@ -154,6 +154,23 @@ QWEN_API qwen_status qwen_layer_decode(qwen_layer_t layer, const void* x, void* 
                               void* k_cache, void* v_cache, void* workspace,
                               size_t workspace_bytes, void* stream);
 
+/* The same two calls with the residual stream in FP32 across calls (the
+ * hidden state a stack of layers passes from layer to layer): exactly one of
+ * x (BF16) / x_fp32 (FP32, [B, T, d] resp. [B, d]) is the input, and y (BF16)
+ * and/or y_fp32 (FP32) receive the output (at least one non-NULL; y_fp32 may
+ * not alias x_fp32).  Rounding the hidden state to BF16 between layers is the
+ * dominant error of a deep stack; keeping it in FP32 removes it. */
+QWEN_API qwen_status qwen_layer_prefill_ex(qwen_layer_t layer, const void* x, const float* x_fp32,
+                                           void* y, float* y_fp32, int32_t B, int32_t T,
+                                           const int32_t* positions, const int32_t* cache_start,
+                                           void* k_cache, void* v_cache, void* workspace,
+                                           size_t workspace_bytes, void* stream);
+QWEN_API qwen_status qwen_layer_decode_ex(qwen_layer_t layer, const void* x, const float* x_fp32,
+                                          void* y, float* y_fp32, int32_t B,
+                                          const int32_t* positions, const int32_t* cache_len,
+                                          void* k_cache, void* v_cache, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
 /* MoE block alone on T tokens: Y = R + sum_j w_j Expert_{idx_j}(RMSNorm_2(R)).
  *   r        [T, d] BF16 residual-stream input; y [T, d] BF16 output.
  *   r_fp32   optional [T, d] FP32 copy of r used for the norm and router

@@ -40,6 +40,21 @@ import numpy as np
 # Elementary steps
 # --------------------------------------------------------------------------
 
+def round_to_bf16(x):
+    """Round float64 values to the nearest bfloat16 (ties to even), returned as
+    float64.  Used only when a caller asks the oracle to model BF16 storage.
+
+    bfloat16 keeps the top 16 bits of an IEEE float32; the value is first
+    rounded to float32 (exact for every value this oracle stores), then the
+    low 16 bits are rounded to nearest even on the bit pattern.
+    """
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> 16) & 1
+    u = ((u + 0x7FFF + lsb) >> 16) << 16
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
 def rmsnorm(x, gamma, eps):
     """RMSNorm over the last axis.
 
@@ -178,13 +193,15 @@ def _qkv(xh, w, cfg):
 
 
 def attention_block(x, w, cfg, positions, k_cache, v_cache, slots,
-                    causal=True, rows=None):
+                    causal=True, rows=None, cache_bf16=False):
     """R = X + Attention(RMSNorm_1(X)) for one sequence ([P3] §2, §4-§9).
 
     x: [T, d]; positions, slots: [T] ints; k_cache, v_cache: [Hkv, S_max, dh]
     float64 arrays updated in place with the new post-QK-norm, post-RoPE K and
     V rows ([P1] §09.1; [P3] §12).  ``rows`` restricts the returned rows (the
     K/V of every row is still computed and written, since later rows read it).
+    ``cache_bf16`` models a cache held in BF16 storage: appended K/V rows are
+    rounded to BF16, so attention reads what such a cache holds.
     Returns R for the requested rows.
     """
     x = np.asarray(x, dtype=np.float64)
@@ -195,6 +212,8 @@ def attention_block(x, w, cfg, positions, k_cache, v_cache, slots,
     q, k, v = _qkv(xh, w, cfg)
     q = apply_rope_rotate_half(q, positions, theta)
     k = apply_rope_rotate_half(k, positions, theta)
+    if cache_bf16:
+        k, v = round_to_bf16(k), round_to_bf16(v)
     k_cache[:, slots, :] = k.transpose(1, 0, 2)
     v_cache[:, slots, :] = v.transpose(1, 0, 2)
     if rows is None:
@@ -221,7 +240,7 @@ def mlp_block(r, w, cfg):
 
 
 def layer_forward(x, w, cfg, positions, k_cache, v_cache, slots,
-                  causal=True, rows=None):
+                  causal=True, rows=None, cache_bf16=False):
     """Dense layer forward for one sequence: attention block then MLP block.
 
     [P3] §2: R = X + Attention(RMSNorm_1(X)), Y = R + MLP(RMSNorm_2(R)); the
@@ -229,7 +248,7 @@ def layer_forward(x, w, cfg, positions, k_cache, v_cache, slots,
     same call with T = 1 in slot ``cache_len`` ([P1] §09.1).
     """
     r = attention_block(x, w, cfg, positions, k_cache, v_cache, slots,
-                        causal=causal, rows=rows)
+                        causal=causal, rows=rows, cache_bf16=cache_bf16)
     return mlp_block(r, w, cfg)
 
 

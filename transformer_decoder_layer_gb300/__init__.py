@@ -15,8 +15,8 @@ import os
 from ._build import LIB as _LIB_PATH
 
 __all__ = [
-    "QwenError", "lib", "LayerConfig", "Layer", "rmsnorm", "linear", "head_last_token",
-    "poll_error", "STATUS",
+    "QwenError", "lib", "LayerConfig", "Layer", "Stack", "rmsnorm", "linear", "head_last_token",
+    "head_last_token_noalloc", "poll_error", "launch_count", "STATUS",
 ]
 
 STATUS = {
@@ -63,6 +63,10 @@ _SIGS = {
                                           _SZ, _VP]),
     "qwen_layer_decode": (ctypes.c_int, [_VP, _VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP, _SZ,
                                          _VP]),
+    "qwen_layer_prefill_ex": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _I32, _I32, _VP, _VP, _VP,
+                                             _VP, _VP, _SZ, _VP]),
+    "qwen_layer_decode_ex": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _VP,
+                                            _VP, _SZ, _VP]),
     "qwen_moe_ffn": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "qwen_head_workspace_bytes": (_SZ, [_I32, _I32, _I32]),
     "qwen_head_last_token": (ctypes.c_int, [_VP, _I32, _I32, _I32, _VP, _VP, _I32, _F32, _VP,
@@ -267,30 +271,51 @@ class Layer:
         import torch
         return torch.empty(max(self.workspace_bytes(B, T), 256), dtype=torch.uint8, device=device)
 
-    def prefill(self, x, positions, cache_start, k_cache, v_cache, out=None, workspace=None,
-                stream=None):
+    @staticmethod
+    def _io(x, out, out32):
+        """Split x into (bf16, fp32) inputs and default the output: BF16 in ->
+        BF16 out; FP32 in -> FP32 out (the residual interface across layers)."""
         import torch
-        _need(x, torch.bfloat16, "x")
+        if not x.is_cuda or not x.is_contiguous():
+            raise ValueError("x must be a contiguous CUDA tensor")
+        if x.dtype == torch.bfloat16:
+            xb, x32 = x, None
+        elif x.dtype == torch.float32:
+            xb, x32 = None, x
+        else:
+            raise ValueError(f"x must be bfloat16 or float32, got {x.dtype}")
+        if out is None and out32 is None:
+            if x32 is None:
+                out = torch.empty_like(x)
+            else:
+                out32 = torch.empty_like(x)
+        return xb, x32, out, out32
+
+    def prefill(self, x, positions, cache_start, k_cache, v_cache, out=None, workspace=None,
+                stream=None, out32=None):
+        """x [B, T, d] BF16 (or FP32: the FP32 residual interface).  Returns the
+        BF16 output if `out` is used, else the FP32 one."""
         B, T, _ = x.shape
-        out = torch.empty_like(x) if out is None else out
+        xb, x32, out, out32 = self._io(x, out, out32)
         ws = self.workspace(B, T, x.device) if workspace is None else workspace
-        _check(lib().qwen_layer_prefill(self.handle, _ptr(x), _ptr(out), B, T, _ptr(positions),
-                                        _ptr(cache_start), _ptr(k_cache), _ptr(v_cache),
-                                        _ptr(ws), ws.numel(), _stream(stream)),
-               "qwen_layer_prefill")
-        return out
+        _check(lib().qwen_layer_prefill_ex(self.handle, _ptr(xb), _ptr(x32), _ptr(out),
+                                           _ptr(out32), B, T, _ptr(positions), _ptr(cache_start),
+                                           _ptr(k_cache), _ptr(v_cache), _ptr(ws), ws.numel(),
+                                           _stream(stream)), "qwen_layer_prefill")
+        return out if out is not None else out32
 
     def decode(self, x, positions, cache_len, k_cache, v_cache, out=None, workspace=None,
-               stream=None):
-        import torch
-        _need(x, torch.bfloat16, "x")
+               stream=None, out32=None):
+        """x [B, d] BF16 (or FP32).  Returns the BF16 output if `out` is used,
+        else the FP32 one."""
         B = x.shape[0]
-        out = torch.empty_like(x) if out is None else out
+        xb, x32, out, out32 = self._io(x, out, out32)
         ws = self.workspace(B, 1, x.device) if workspace is None else workspace
-        _check(lib().qwen_layer_decode(self.handle, _ptr(x), _ptr(out), B, _ptr(positions),
-                                       _ptr(cache_len), _ptr(k_cache), _ptr(v_cache), _ptr(ws),
-                                       ws.numel(), _stream(stream)), "qwen_layer_decode")
-        return out
+        _check(lib().qwen_layer_decode_ex(self.handle, _ptr(xb), _ptr(x32), _ptr(out),
+                                          _ptr(out32), B, _ptr(positions), _ptr(cache_len),
+                                          _ptr(k_cache), _ptr(v_cache), _ptr(ws), ws.numel(),
+                                          _stream(stream)), "qwen_layer_decode")
+        return out if out is not None else out32
 
     def moe_ffn(self, r, r_fp32=None, out=None, topk_idx=None, topk_w=None, logits=None,
                 workspace=None, stream=None):
@@ -327,3 +352,98 @@ class Layer:
 def launch_count():
     """Kernel launches issued by the library so far in this process."""
     return int(lib().qwen_launch_count())
+
+
+class Stack:
+    """A stack of decoder layers followed by the final RMSNorm and the lm_head
+    applied to the last position of each sequence ("Qwen2.5-7B 结构拆解" §01,
+    §03.8).  Holds one layer handle and one KV cache pair per layer; every call
+    is a sequence of C-ABI calls on the current stream (capturable as a CUDA
+    graph: nothing here allocates inside prefill/decode after the first call
+    of a given shape).  The hidden state passes between layers in FP32 (the
+    FP32 residual interface); only the last layer's output is BF16."""
+
+    def __init__(self, shape, layer_weights, gamma_final, w_lm, max_batch, max_seq,
+                 max_tokens=None, device="cuda"):
+        import torch
+        self.shape = shape
+        get = (lambda k: shape[k]) if isinstance(shape, dict) else (lambda k: getattr(shape, k))
+        self.d, self.hkv, self.dh = get("d"), get("n_kv_heads"), get("head_dim")
+        self.eps = float(get("rms_eps"))
+        self.max_batch, self.max_seq = max_batch, max_seq
+        self.max_tokens = max_tokens or max_batch * max_seq
+        cfg = LayerConfig(shape, max_tokens=self.max_tokens, max_batch=max_batch,
+                          max_seq=max_seq, max_position=max_seq)
+        self.layers = []
+        for w in layer_weights:  # an iterable: weights may be produced one layer at a time
+            self.layers.append(Layer(cfg, w))
+        self.gamma_final, self.w_lm = gamma_final, w_lm
+        self.V = w_lm.shape[0]
+        n = len(self.layers)
+        shp = (max_batch, self.hkv, max_seq, self.dh)
+        self.k = [torch.zeros(shp, dtype=torch.bfloat16, device=device) for _ in range(n)]
+        self.v = [torch.zeros(shp, dtype=torch.bfloat16, device=device) for _ in range(n)]
+        self._ws = {}
+        self._bufs = {}
+
+    def workspace(self, B, T):
+        import torch
+        key = (B, T)
+        if key not in self._ws:
+            nbytes = max(self.layers[0].workspace_bytes(B, T), head_workspace_bytes(B, self.d, self.V))
+            self._ws[key] = torch.empty(nbytes, dtype=torch.uint8, device=self.k[0].device)
+        return self._ws[key]
+
+    def _pingpong(self, shape):
+        """Two FP32 buffers for the hidden state between layers plus the BF16
+        output of the last layer."""
+        import torch
+        if shape not in self._bufs:
+            dev = self.k[0].device
+            self._bufs[shape] = ([torch.empty(shape, dtype=torch.float32, device=dev)
+                                  for _ in range(2)],
+                                 torch.empty(shape, dtype=torch.bfloat16, device=dev))
+        return self._bufs[shape]
+
+    def caches(self, B):
+        """Per-layer cache views for the first B sequences."""
+        return [(k[:B], v[:B]) for k, v in zip(self.k, self.v)]
+
+    def decode(self, x, positions, cache_len, logits=None):
+        """One decode step through every layer, then the head: x [B, d] BF16."""
+        B = x.shape[0]
+        ws = self.workspace(B, 1)
+        f32, last = self._pingpong(tuple(x.shape))
+        h = x
+        n = len(self.layers)
+        for i, layer in enumerate(self.layers):
+            if i == n - 1:
+                layer.decode(h, positions, cache_len, self.k[i][:B], self.v[i][:B], out=last,
+                             workspace=ws)
+                h = last
+            else:
+                h = layer.decode(h, positions, cache_len, self.k[i][:B], self.v[i][:B],
+                                 out32=f32[i % 2], workspace=ws)
+        return head_last_token(h.view(B, 1, self.d), self.gamma_final, self.w_lm, self.eps,
+                               logits=logits, workspace=ws)
+
+    def prefill(self, x, positions, cache_start, logits=None):
+        """Prefill of x [B, T, d] through every layer; logits of the last position."""
+        B, T, _ = x.shape
+        ws = self.workspace(B, T)
+        f32, last = self._pingpong(tuple(x.shape))
+        h = x
+        n = len(self.layers)
+        for i, layer in enumerate(self.layers):
+            if i == n - 1:
+                layer.prefill(h, positions, cache_start, self.k[i][:B], self.v[i][:B], out=last,
+                              workspace=ws)
+                h = last
+            else:
+                h = layer.prefill(h, positions, cache_start, self.k[i][:B], self.v[i][:B],
+                                  out32=f32[i % 2], workspace=ws)
+        return head_last_token(h, self.gamma_final, self.w_lm, self.eps, logits=logits,
+                               workspace=ws), h
+
+    def poll_error(self):
+        return max(layer.poll_error() for layer in self.layers)

@@ -2,6 +2,7 @@
 // (qwen_rmsnorm, qwen_linear).
 #include <atomic>
 #include <cstdio>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "internal.h"
@@ -23,6 +24,15 @@ int* lib_status_ptr() {
     if (cudaGetSymbolAddress(&a, g_lib_status) == cudaSuccess) p = static_cast<int*>(a);
   }
   return p;
+}
+
+bool pdl_enabled() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("QWEN_PDL");
+    v = (e && e[0] == '0') ? 0 : 1;
+  }
+  return v == 1;
 }
 
 int device_sm_count() {

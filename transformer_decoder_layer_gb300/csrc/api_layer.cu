@@ -300,51 +300,75 @@ qwen_status qwen_layer_poll_error(qwen_layer_t layer, void* stream) {
   return static_cast<qwen_status>(v);
 }
 
-qwen_status qwen_layer_prefill(qwen_layer_t layer, const void* x, void* y, int32_t B, int32_t T,
-                               const int32_t* positions, const int32_t* cache_start,
-                               void* k_cache, void* v_cache, void* workspace,
-                               size_t workspace_bytes, void* stream) {
+// Shared argument checks of the prefill/decode entry points.
+static qwen_status check_io(const void* x, const float* x32, const void* y, const float* y32,
+                            const void* workspace, const void* kc, const void* vc) {
+  if ((x == nullptr) == (x32 == nullptr)) return QWEN_ERR_INVALID_ARG;
+  if (!y && !y32) return QWEN_ERR_INVALID_ARG;
+  if (!workspace || !kc || !vc) return QWEN_ERR_INVALID_ARG;
+  const void* in = x ? x : static_cast<const void*>(x32);
+  if (in == y || in == static_cast<const void*>(y32)) return QWEN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(in) |
+       reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(y32) |
+       reinterpret_cast<uintptr_t>(kc) | reinterpret_cast<uintptr_t>(vc)) & 15)
+    return QWEN_ERR_INVALID_ARG;
+  return QWEN_OK;
+}
+
+qwen_status qwen_layer_prefill_ex(qwen_layer_t layer, const void* x, const float* x_fp32, void* y,
+                                  float* y_fp32, int32_t B, int32_t T, const int32_t* positions,
+                                  const int32_t* cache_start, void* k_cache, void* v_cache,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
   if (!layer) return QWEN_ERR_INVALID_ARG;
   const qwen_layer_config& c = layer->cfg;
   if (B < 0 || T < 0) return QWEN_ERR_INVALID_ARG;
   if (B == 0 || T == 0) return QWEN_OK;
-  if (!x || !y || !positions || !cache_start || !k_cache || !v_cache || !workspace)
-    return QWEN_ERR_INVALID_ARG;
-  if (x == y) return QWEN_ERR_INVALID_ARG;
+  if (!positions || !cache_start) return QWEN_ERR_INVALID_ARG;
+  if (qwen_status s = check_io(x, x_fp32, y, y_fp32, workspace, k_cache, v_cache)) return s;
   if (B > c.max_batch || (int64_t)B * T > c.max_tokens || T > c.max_seq) return QWEN_ERR_CAPACITY;
   const WorkspaceLayout W = workspace_layout(c, B, T);
   if (workspace_bytes < W.total) return QWEN_ERR_CAPACITY;
-  if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(x) |
-       reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(k_cache) |
-       reinterpret_cast<uintptr_t>(v_cache)) & 15)
-    return QWEN_ERR_INVALID_ARG;
-  return layer_prefill(layer, static_cast<const bf16*>(x), static_cast<bf16*>(y), B, T,
-                       positions, cache_start, static_cast<bf16*>(k_cache),
+  return layer_prefill(layer, static_cast<const bf16*>(x), x_fp32, static_cast<bf16*>(y), y_fp32,
+                       B, T, positions, cache_start, static_cast<bf16*>(k_cache),
                        static_cast<bf16*>(v_cache), static_cast<uint8_t*>(workspace), W,
                        static_cast<cudaStream_t>(stream));
+}
+
+qwen_status qwen_layer_prefill(qwen_layer_t layer, const void* x, void* y, int32_t B, int32_t T,
+                               const int32_t* positions, const int32_t* cache_start,
+                               void* k_cache, void* v_cache, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (!x || !y) return QWEN_ERR_INVALID_ARG;
+  return qwen_layer_prefill_ex(layer, x, nullptr, y, nullptr, B, T, positions, cache_start,
+                               k_cache, v_cache, workspace, workspace_bytes, stream);
+}
+
+qwen_status qwen_layer_decode_ex(qwen_layer_t layer, const void* x, const float* x_fp32, void* y,
+                                 float* y_fp32, int32_t B, const int32_t* positions,
+                                 const int32_t* cache_len, void* k_cache, void* v_cache,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (!layer) return QWEN_ERR_INVALID_ARG;
+  const qwen_layer_config& c = layer->cfg;
+  if (B < 0) return QWEN_ERR_INVALID_ARG;
+  if (B == 0) return QWEN_OK;
+  if (!positions || !cache_len) return QWEN_ERR_INVALID_ARG;
+  if (qwen_status s = check_io(x, x_fp32, y, y_fp32, workspace, k_cache, v_cache)) return s;
+  if (B > c.max_batch || B > c.max_tokens) return QWEN_ERR_CAPACITY;
+  const WorkspaceLayout W = workspace_layout(c, B, 1);
+  if (workspace_bytes < W.total) return QWEN_ERR_CAPACITY;
+  return layer_decode(layer, static_cast<const bf16*>(x), x_fp32, static_cast<bf16*>(y), y_fp32, B,
+                      positions, cache_len, static_cast<bf16*>(k_cache),
+                      static_cast<bf16*>(v_cache), static_cast<uint8_t*>(workspace), W,
+                      static_cast<cudaStream_t>(stream));
 }
 
 qwen_status qwen_layer_decode(qwen_layer_t layer, const void* x, void* y, int32_t B,
                               const int32_t* positions, const int32_t* cache_len, void* k_cache,
                               void* v_cache, void* workspace, size_t workspace_bytes,
                               void* stream) {
-  if (!layer) return QWEN_ERR_INVALID_ARG;
-  const qwen_layer_config& c = layer->cfg;
-  if (B < 0) return QWEN_ERR_INVALID_ARG;
-  if (B == 0) return QWEN_OK;
-  if (!x || !y || !positions || !cache_len || !k_cache || !v_cache || !workspace)
-    return QWEN_ERR_INVALID_ARG;
-  if (x == y) return QWEN_ERR_INVALID_ARG;
-  if (B > c.max_batch || B > c.max_tokens) return QWEN_ERR_CAPACITY;
-  const WorkspaceLayout W = workspace_layout(c, B, 1);
-  if (workspace_bytes < W.total) return QWEN_ERR_CAPACITY;
-  if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(x) |
-       reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(k_cache) |
-       reinterpret_cast<uintptr_t>(v_cache)) & 15)
-    return QWEN_ERR_INVALID_ARG;
-  return layer_decode(layer, static_cast<const bf16*>(x), static_cast<bf16*>(y), B, positions,
-                      cache_len, static_cast<bf16*>(k_cache), static_cast<bf16*>(v_cache),
-                      static_cast<uint8_t*>(workspace), W, static_cast<cudaStream_t>(stream));
+  if (!x || !y) return QWEN_ERR_INVALID_ARG;
+  return qwen_layer_decode_ex(layer, x, nullptr, y, nullptr, B, positions, cache_len, k_cache,
+                              v_cache, workspace, workspace_bytes, stream);
 }
 
 qwen_status qwen_moe_ffn(qwen_layer_t layer, const void* r, const float* r_fp32, void* y,
@@ -362,7 +386,7 @@ qwen_status qwen_moe_ffn(qwen_layer_t layer, const void* r, const float* r_fp32,
   if ((reinterpret_cast<uintptr_t>(workspace) | reinterpret_cast<uintptr_t>(r) |
        reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(r_fp32)) & 15)
     return QWEN_ERR_INVALID_ARG;
-  return moe_forward(layer, static_cast<const bf16*>(r), r_fp32, static_cast<bf16*>(y), T,
+  return moe_forward(layer, static_cast<const bf16*>(r), r_fp32, static_cast<bf16*>(y), nullptr, T,
                      topk_idx, topk_w, logits, static_cast<uint8_t*>(workspace), W,
                      static_cast<cudaStream_t>(stream));
 }
@@ -437,12 +461,13 @@ static inline void mark(const qwen_layer_s* L, int stage, int end, cudaStream_t 
 static qwen_status decode_proj(const f16* Wt, const f16* X, int B, int N, int K, float* part,
                                int* err, cudaStream_t st, int& splits) {
   splits = decode_splits(N, K);
-  return gemm_decode_splitk(Wt, X, K, B, N, K, splits, /*op_f16=*/true, part, err, st);
+  return gemm_decode_splitk(Wt, X, K, B, N, K, splits, /*op_f16=*/true, part, err, st,
+                            /*w_static=*/true);
 }
 
-qwen_status layer_decode(qwen_layer_s* L, const bf16* x, bf16* y, int B, const int32_t* positions,
-                         const int32_t* cache_len, bf16* kc, bf16* vc, uint8_t* ws,
-                         const WorkspaceLayout& W, cudaStream_t st) {
+qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16* y, float* y32,
+                         int B, const int32_t* positions, const int32_t* cache_len, bf16* kc,
+                         bf16* vc, uint8_t* ws, const WorkspaceLayout& W, cudaStream_t st) {
   const qwen_layer_config& c = L->cfg;
   const int d = c.d, dh = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
   const int nq = Hq * dh, nqkv = nq + 2 * Hkv * dh, f = c.ffn;
@@ -460,8 +485,8 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, bf16* y, int B, const i
   const bool swap = B <= 256;
 
   // RMSNorm_1 -> X-hat (FP16 operand)
-  QWEN_STAGE_RUN(QWEN_STAGE_NORM1, rmsnorm_launch(x, L->gamma_attn, xh, true, nullptr, nullptr,
-                                                  B, d, c.rms_eps, st));
+  QWEN_STAGE_RUN(QWEN_STAGE_NORM1, rmsnorm_launch(x, L->gamma_attn, xh, true, nullptr, x32, B,
+                                                  d, c.rms_eps, st));
   // Q/K/V, then bias, QK-norm, RoPE, Q store and K/V append at slot cache_len[b]
   const QkvParams qp = make_qkv_params(L, positions, cache_len, q, kc, vc, 1);
   if (swap) {
@@ -470,6 +495,8 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, bf16* y, int B, const i
   } else {
     GemmEpilogue e{};
     e.mode = EPI_QKV;
+    e.b_static = 1;
+  e.b_static = 1;
     e.qkv = qp;
     QWEN_STAGE_RUN(QWEN_STAGE_QKV, gemm_tc(xh, d, L->w_qkv, d, B, nqkv, d, true, e, err, st));
   }
@@ -483,11 +510,13 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, bf16* y, int B, const i
   // O projection + residual -> R (FP32)
   if (swap) {
     QWEN_STAGE_RUN(QWEN_STAGE_O, decode_proj(L->w_o, attn, B, d, nq, part, err, st, S));
-    QWEN_STAGE_RUN(QWEN_STAGE_O_FINISH, reduce_resid(part, S, B, d, x, nullptr, nullptr, r32, st));
+    QWEN_STAGE_RUN(QWEN_STAGE_O_FINISH, reduce_resid(part, S, B, d, x, x32, nullptr, r32, st));
   } else {
     GemmEpilogue e{};
     e.mode = EPI_RESID;
+    e.b_static = 1;
     e.resid = x;
+    e.resid32 = x32;
     e.ldr = d;
     e.out32 = r32;
     e.ldo32 = d;
@@ -495,7 +524,7 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, bf16* y, int B, const i
   }
   if (c.n_experts) {
     QWEN_STAGE_RUN(QWEN_STAGE_MOE,
-                   moe_forward(L, nullptr, r32, y, B, nullptr, nullptr, nullptr, ws, W, st));
+                   moe_forward(L, nullptr, r32, y, y32, B, nullptr, nullptr, nullptr, ws, W, st));
     return QWEN_OK;
   }
   // RMSNorm_2 -> Z, gate/up + SiLU*up -> H, down + residual -> Y
@@ -506,28 +535,32 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, bf16* y, int B, const i
     QWEN_STAGE_RUN(QWEN_STAGE_GATE_UP_FINISH, reduce_swiglu(part, S, B, f, hbuf, st));
     QWEN_STAGE_RUN(QWEN_STAGE_DOWN, decode_proj(L->w_down, hbuf, B, d, f, part, err, st, S));
     QWEN_STAGE_RUN(QWEN_STAGE_DOWN_FINISH,
-                   reduce_resid(part, S, B, d, nullptr, r32, y, nullptr, st));
+                   reduce_resid(part, S, B, d, nullptr, r32, y, y32, st));
     return QWEN_OK;
   }
   GemmEpilogue eg{};
   eg.mode = EPI_SWIGLU;
+  eg.b_static = 1;
   eg.out = hbuf;
   eg.out_f16 = 1;
   eg.ldo = f;
   QWEN_STAGE_RUN(QWEN_STAGE_GATE_UP, gemm_tc(z, d, L->w_gu, d, B, 2 * f, d, true, eg, err, st));
   GemmEpilogue ed{};
   ed.mode = EPI_RESID;
+  ed.b_static = 1;
   ed.out = y;
   ed.ldo = d;
   ed.resid32 = r32;
   ed.ldr = d;
+  ed.out32 = y32;
+  ed.ldo32 = d;
   QWEN_STAGE_RUN(QWEN_STAGE_DOWN, gemm_tc(hbuf, f, L->w_down, f, B, d, f, true, ed, err, st));
   return QWEN_OK;
 }
 
-qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, bf16* y, int B, int T,
-                          const int32_t* positions, const int32_t* slot0, bf16* kc, bf16* vc,
-                          uint8_t* ws, const WorkspaceLayout& W, cudaStream_t st) {
+qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, const float* x32, bf16* y, float* y32,
+                          int B, int T, const int32_t* positions, const int32_t* slot0, bf16* kc,
+                          bf16* vc, uint8_t* ws, const WorkspaceLayout& W, cudaStream_t st) {
   const qwen_layer_config& c = L->cfg;
   const int M = B * T, d = c.d, dh = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
   const int nq = Hq * dh, nqkv = nq + 2 * Hkv * dh, f = c.ffn;
@@ -540,11 +573,12 @@ qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, bf16* y, int B, int T,
   int* err = L->status;
 
   // RMSNorm_1 -> X-hat (FP16 operand)
-  QWEN_STAGE_RUN(QWEN_STAGE_NORM1, rmsnorm_launch(x, L->gamma_attn, xh, true, nullptr, nullptr,
-                                                  M, d, c.rms_eps, st));
+  QWEN_STAGE_RUN(QWEN_STAGE_NORM1, rmsnorm_launch(x, L->gamma_attn, xh, true, nullptr, x32, M,
+                                                  d, c.rms_eps, st));
   // fused QKV: bias, QK-norm, RoPE, Q store, K/V cache append
   GemmEpilogue e{};
   e.mode = EPI_QKV;
+  e.b_static = 1;
   e.qkv = make_qkv_params(L, positions, slot0, q, kc, vc, T);
   QWEN_STAGE_RUN(QWEN_STAGE_QKV, gemm_tc(xh, d, L->w_qkv, d, M, nqkv, d, true, e, err, st));
   // causal GQA attention over the cache
@@ -554,14 +588,16 @@ qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, bf16* y, int B, int T,
   // the second residual, so rounding it to BF16 would put that rounding on Y)
   GemmEpilogue eo{};
   eo.mode = EPI_RESID;
+  eo.b_static = 1;
   eo.resid = x;
+  eo.resid32 = x32;
   eo.ldr = d;
   eo.out32 = r32;
   eo.ldo32 = d;
   QWEN_STAGE_RUN(QWEN_STAGE_O, gemm_tc(attn, nq, L->w_o, nq, M, d, nq, true, eo, err, st));
   if (c.n_experts) {
     QWEN_STAGE_RUN(QWEN_STAGE_MOE,
-                   moe_forward(L, nullptr, r32, y, M, nullptr, nullptr, nullptr, ws, W, st));
+                   moe_forward(L, nullptr, r32, y, y32, M, nullptr, nullptr, nullptr, ws, W, st));
     return QWEN_OK;
   }
   // RMSNorm_2, gate/up + SiLU*mul, down + residual
@@ -569,16 +605,20 @@ qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, bf16* y, int B, int T,
                                                   d, c.rms_eps, st));
   GemmEpilogue eg{};
   eg.mode = EPI_SWIGLU;
+  eg.b_static = 1;
   eg.out = hbuf;
   eg.out_f16 = 1;
   eg.ldo = f;
   QWEN_STAGE_RUN(QWEN_STAGE_GATE_UP, gemm_tc(z, d, L->w_gu, d, M, 2 * f, d, true, eg, err, st));
   GemmEpilogue ed{};
   ed.mode = EPI_RESID;
+  ed.b_static = 1;
   ed.out = y;
   ed.ldo = d;
   ed.resid32 = r32;
   ed.ldr = d;
+  ed.out32 = y32;
+  ed.ldo32 = d;
   QWEN_STAGE_RUN(QWEN_STAGE_DOWN, gemm_tc(hbuf, f, L->w_down, f, M, d, f, true, ed, err, st));
   return QWEN_OK;
 }

@@ -86,6 +86,8 @@ template <int DH>
 __global__ void __launch_bounds__(kDecAttnThreads, 1)
     attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        DecAttnArgs a) {
+  pdl_trigger();
+  pdl_wait();
   using C = DecAttnCfg<DH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -335,6 +337,8 @@ template <int DH>
 __global__ void attn_decode_merge_kernel(const float* __restrict__ part_o,
                                          const float* __restrict__ part_ml, int BH, int splits,
                                          f16* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= BH) return;
@@ -413,12 +417,12 @@ static qwen_status launch_attn_dec(const CUtensorMap& tk, const CUtensorMap& tv,
   const int units = a.B * a.Hkv * a.splits;
   const int sms = device_sm_count();
   const int grid = units < sms ? units : sms;
-  kern<<<grid, kDecAttnThreads, DecAttnCfg<DH>::SMEM_BYTES, st>>>(tk, tv, a);
+  launch_k(kern, dim3(grid), dim3(kDecAttnThreads), DecAttnCfg<DH>::SMEM_BYTES, st, tk, tv, a);
   count_launches();
   if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;
   const int BH = a.B * a.Hq;
-  attn_decode_merge_kernel<DH><<<(BH * 32 + 255) / 256, 256, 0, st>>>(a.part_o, a.part_ml, BH,
-                                                                       a.splits, out);
+  launch_k(attn_decode_merge_kernel<DH>, dim3((BH * 32 + 255) / 256), dim3(256), 0, st,
+           (const float*)a.part_o, (const float*)a.part_ml, BH, a.splits, out);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }

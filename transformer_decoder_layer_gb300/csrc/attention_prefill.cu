@@ -66,6 +66,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, AttnArgs a) {
+  pdl_trigger();
+  pdl_wait();
   using C = AttnCfg<DH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -379,7 +381,7 @@ static qwen_status launch_dh(const CUtensorMap& q, const CUtensorMap& k, const C
   }
   const int n_qt = (a.T + kQT - 1) / kQT;
   const int grid = n_qt * a.B * a.Hq;
-  kern<<<grid, kAttnThreads, AttnCfg<DH>::SMEM_BYTES, st>>>(q, k, v, a);
+  launch_k(kern, dim3(grid), dim3(kAttnThreads), AttnCfg<DH>::SMEM_BYTES, st, q, k, v, a);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }

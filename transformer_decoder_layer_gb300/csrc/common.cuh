@@ -35,6 +35,20 @@ __device__ __forceinline__ void record_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// ----------------------------------------------------------------- PDL
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start before its predecessor on the stream finishes.
+// pdl_wait() blocks the calling thread until every predecessor grid has
+// completed and its memory is visible (a no-op when launched normally);
+// every thread calls it before touching memory an earlier kernel writes or
+// reads.  pdl_trigger() lets the next kernel begin launching.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -40,8 +40,8 @@ struct DecCfg {
 template <int BP>
 __global__ void __launch_bounds__(kDThreads, 1)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                       int B, int N, int K, int splits, uint32_t idesc, float* __restrict__ part,
-                       int* err) {
+                       int B, int N, int K, int splits, uint32_t idesc, int w_static,
+                       float* __restrict__ part, int* err) {
   using C = DecCfg<BP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = (N + kDBM - 1) / kDBM;
   const int n_kblk = (K + kDBK - 1) / kDBK;
@@ -93,16 +94,34 @@ __global__ void __launch_bounds__(kDThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmW);
       tma_prefetch_desc(&tmX);
+      // weights are never written by the kernels before this one: stream the
+      // first stages of weight tiles while the previous kernel finishes
+      int pre = 0;
+      if (w_static && blockIdx.x < units) {
+        int n0, kb0, kb1, s;
+        unit_range(blockIdx.x, n0, kb0, kb1, s);
+        pre = min(C::STAGES, kb1 - kb0);
+        for (int i = 0; i < pre; ++i) {
+          mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+          tma_load_2d(sA + i * C::A_BYTES, &tmW, &full[i], (kb0 + i) * kDBK, n0);
+        }
+      }
+      pdl_wait();
       int stage = 0;
       uint32_t phase = 0;
+      int g = 0;
       for (int u = blockIdx.x; u < units; u += gridDim.x) {
         int n0, kb0, kb1, s;
         unit_range(u, n0, kb0, kb1, s);
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) goto prod_done;
-          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_2d(sA + stage * C::A_BYTES, &tmW, &full[stage], kb * kDBK, n0);
-          tma_load_2d(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * kDBK, 0);
+        for (int kb = kb0; kb < kb1; ++kb, ++g) {
+          if (g < pre) {
+            tma_load_2d(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * kDBK, 0);
+          } else {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) goto prod_done;
+            mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+            tma_load_2d(sA + stage * C::A_BYTES, &tmW, &full[stage], kb * kDBK, n0);
+            tma_load_2d(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * kDBK, 0);
+          }
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -154,6 +173,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
       }
     }
   } else {
+    pdl_wait();  // the partials may still be read by the previous kernel
     const int q = warp & 3;
     int local = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
@@ -196,6 +216,8 @@ __global__ void reduce_resid_kernel(const float* __restrict__ part, int splits, 
                                     const bf16* __restrict__ resid,
                                     const float* __restrict__ resid32, bf16* __restrict__ out,
                                     float* __restrict__ out32) {
+  pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;  // over B * N, n fastest
   if (i >= N * B) return;
   const size_t plane = (size_t)B * N;
@@ -209,6 +231,8 @@ __global__ void reduce_resid_kernel(const float* __restrict__ part, int splits, 
 // h[b][j] = SiLU(gate_j) * up_j with gate row (j/64)*128 + j%64 and up row +64.
 __global__ void reduce_swiglu_kernel(const float* __restrict__ part, int splits, int B, int f,
                                      f16* __restrict__ h) {
+  pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;  // over B * f, j fastest
   if (i >= f * B) return;
   const int b = i / f, j = i - b * f;
@@ -231,6 +255,8 @@ __global__ void reduce_swiglu_kernel(const float* __restrict__ part, int splits,
 template <int DH>
 __global__ void reduce_qkv_kernel(const float* __restrict__ part, int splits, int B, int Nqkv,
                                   QkvParams p, int* err) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int PER = DH / 32;
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -294,6 +320,8 @@ __global__ void reduce_qkv_kernel(const float* __restrict__ part, int splits, in
 
 __global__ void reduce_f32_kernel(const float* __restrict__ part, int splits, int B, int N,
                                   float* __restrict__ out, int ldo) {
+  pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= N * B) return;
   const int b = i / N, n = i - b * N;
@@ -378,7 +406,8 @@ size_t decode_part_bytes(const qwen_layer_config& c, int B) {
 
 template <int BP>
 static qwen_status launch_dec(const CUtensorMap& tw, const CUtensorMap& tx, int B, int N, int K,
-                              int splits, bool op_f16, float* part, int* err, cudaStream_t st) {
+                              int splits, bool op_f16, bool w_static, float* part, int* err,
+                              cudaStream_t st) {
   auto kern = gemm_decode_kernel<BP>;
   static bool attr = false;
   if (!attr) {
@@ -390,14 +419,15 @@ static qwen_status launch_dec(const CUtensorMap& tw, const CUtensorMap& tx, int 
   const int units = ((N + kDBM - 1) / kDBM) * splits;
   const int sms = device_sm_count();
   const int grid = units < sms ? units : sms;
-  kern<<<grid, kDThreads, DecCfg<BP>::SMEM_BYTES, st>>>(tw, tx, B, N, K, splits,
-                                                        idesc_f32acc(kDBM, BP, op_f16), part, err);
+  launch_k(kern, dim3(grid), dim3(kDThreads), DecCfg<BP>::SMEM_BYTES, st, tw, tx, B, N, K, splits,
+           idesc_f32acc(kDBM, BP, op_f16), w_static ? 1 : 0, part, err);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
 qwen_status gemm_decode_splitk(const void* W, const void* X, int ldx, int B, int N, int K,
-                               int splits, bool op_f16, float* part, int* err, cudaStream_t st) {
+                               int splits, bool op_f16, float* part, int* err, cudaStream_t st,
+                               bool w_static) {
   if (B <= 0 || B > 256) return QWEN_ERR_UNSUPPORTED;
   if ((K & 7) || splits < 1) return QWEN_ERR_UNSUPPORTED;
   const int bp = pad_batch(B);
@@ -405,11 +435,11 @@ qwen_status gemm_decode_splitk(const void* W, const void* X, int ldx, int B, int
   if (!tmap2d(&tw, W, (uint64_t)N, (uint64_t)K, (uint64_t)K, kDBM, op_f16)) return QWEN_ERR_CUDA;
   if (!tmap2d(&tx, X, (uint64_t)B, (uint64_t)K, (uint64_t)ldx, bp, op_f16)) return QWEN_ERR_CUDA;
   switch (bp) {
-    case 16: return launch_dec<16>(tw, tx, B, N, K, splits, op_f16, part, err, st);
-    case 32: return launch_dec<32>(tw, tx, B, N, K, splits, op_f16, part, err, st);
-    case 64: return launch_dec<64>(tw, tx, B, N, K, splits, op_f16, part, err, st);
-    case 128: return launch_dec<128>(tw, tx, B, N, K, splits, op_f16, part, err, st);
-    default: return launch_dec<256>(tw, tx, B, N, K, splits, op_f16, part, err, st);
+    case 16: return launch_dec<16>(tw, tx, B, N, K, splits, op_f16, w_static, part, err, st);
+    case 32: return launch_dec<32>(tw, tx, B, N, K, splits, op_f16, w_static, part, err, st);
+    case 64: return launch_dec<64>(tw, tx, B, N, K, splits, op_f16, w_static, part, err, st);
+    case 128: return launch_dec<128>(tw, tx, B, N, K, splits, op_f16, w_static, part, err, st);
+    default: return launch_dec<256>(tw, tx, B, N, K, splits, op_f16, w_static, part, err, st);
   }
 }
 
@@ -417,14 +447,15 @@ static inline int blocks_for(long long n, int t) { return (int)((n + t - 1) / t)
 
 qwen_status reduce_resid(const float* part, int splits, int B, int N, const bf16* resid,
                          const float* resid32, bf16* out, float* out32, cudaStream_t st) {
-  reduce_resid_kernel<<<blocks_for((long long)N * B, 256), 256, 0, st>>>(
-      part, splits, B, N, resid, resid32, out, out32);
+  launch_k(reduce_resid_kernel, dim3(blocks_for((long long)N * B, 256)), dim3(256), 0, st, part,
+           splits, B, N, resid, resid32, out, out32);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
 qwen_status reduce_swiglu(const float* part, int splits, int B, int f, f16* h, cudaStream_t st) {
-  reduce_swiglu_kernel<<<blocks_for((long long)f * B, 256), 256, 0, st>>>(part, splits, B, f, h);
+  launch_k(reduce_swiglu_kernel, dim3(blocks_for((long long)f * B, 256)), dim3(256), 0, st, part,
+           splits, B, f, h);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
@@ -433,17 +464,19 @@ qwen_status reduce_qkv(const float* part, int splits, int B, int Nqkv, const Qkv
                        cudaStream_t st) {
   const long long threads = 32LL * B * (p.Hq + 2 * p.Hkv);
   if (p.dh == 128)
-    reduce_qkv_kernel<128><<<blocks_for(threads, 128), 128, 0, st>>>(part, splits, B, Nqkv, p, err);
+    launch_k(reduce_qkv_kernel<128>, dim3(blocks_for(threads, 128)), dim3(128), 0, st, part, splits,
+             B, Nqkv, p, err);
   else
-    reduce_qkv_kernel<64><<<blocks_for(threads, 128), 128, 0, st>>>(part, splits, B, Nqkv, p, err);
+    launch_k(reduce_qkv_kernel<64>, dim3(blocks_for(threads, 128)), dim3(128), 0, st, part, splits,
+             B, Nqkv, p, err);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
 qwen_status reduce_f32(const float* part, int splits, int B, int N, float* out, int ldo,
                        cudaStream_t st) {
-  reduce_f32_kernel<<<blocks_for((long long)N * B, 256), 256, 0, st>>>(part, splits, B, N, out,
-                                                                         ldo);
+  launch_k(reduce_f32_kernel, dim3(blocks_for((long long)N * B, 256)), dim3(256), 0, st, part,
+           splits, B, N, out, ldo);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }

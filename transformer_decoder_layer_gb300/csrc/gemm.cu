@@ -268,12 +268,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_tile_prefix = reinterpret_cast<int*>(tmem_slot + 4);  // up to 256 groups
 
+  pdl_trigger();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_nblk = (N + BN - 1) / BN;
   const int n_kblk = (K + kBK - 1) / kBK;
 
   if (threadIdx.x == 0) {
+    if (epi.group_offsets) pdl_wait();  // the group offsets come from the previous kernel
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
@@ -309,16 +311,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      // stream the first B (weight) tiles while the previous kernel finishes
+      int pre = 0;
+      TileInfo ti;
+      if (epi.b_static && !epi.group_offsets &&
+          get_tile(blockIdx.x, M, N, BN, n_nblk, epi, s_tile_prefix, ti)) {
+        pre = min(C::STAGES, n_kblk);
+        for (int i = 0; i < pre; ++i) {
+          mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+          tma_load_2d(sB + i * C::B_BYTES, &tmB, &full[i], i * kBK, ti.b_row0);
+        }
+      }
+      pdl_wait();
       int stage = 0;
       uint32_t phase = 0;
-      TileInfo ti;
+      int g = 0;
       for (int tile = blockIdx.x; get_tile(tile, M, N, BN, n_nblk, epi, s_tile_prefix, ti);
            tile += gridDim.x) {
-        for (int kb = 0; kb < n_kblk; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) goto producer_done;
-          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-          tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * kBK, ti.m0);
-          tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * kBK, ti.b_row0);
+        for (int kb = 0; kb < n_kblk; ++kb, ++g) {
+          if (g < pre) {
+            tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * kBK, ti.m0);
+          } else {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) goto producer_done;
+            mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+            tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * kBK, ti.m0);
+            tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * kBK, ti.b_row0);
+          }
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -375,6 +393,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else {
+    pdl_wait();  // residuals and outputs are shared with earlier kernels
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int local = 0;
     TileInfo ti;
@@ -444,7 +463,8 @@ static qwen_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M
       return QWEN_ERR_CUDA;
     attr_done = true;
   }
-  kern<<<grid, kGemmThreads, GemmCfg<BN>::SMEM_BYTES, st>>>(ta, tb, M, N, K, idesc, epi, err);
+  launch_k(kern, dim3(grid), dim3(kGemmThreads), GemmCfg<BN>::SMEM_BYTES, st, ta, tb, M, N, K,
+           idesc, epi, err);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }

@@ -52,9 +52,35 @@ struct GemmEpilogue {
   // matrices; output rows are A rows.
   const int32_t* group_offsets;  // [n_groups+1] (device)
   int n_groups;
+  // B is never written by the kernel launched just before this one (packed
+  // layer weights): its first tiles may be fetched before waiting on it.
+  int b_static;
 };
 
 int device_sm_count();
+
+// Whether kernels are launched with programmatic dependent launch (default on;
+// QWEN_PDL=0 in the environment turns it off).
+bool pdl_enabled();
+
+// Launch `kern` on `st`, with programmatic stream serialisation when enabled.
+// Every kernel launched this way calls pdl_wait() before using memory that
+// earlier kernels touch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 // Host-side count of kernel launches issued by the library (qwen_launch_count).
 void count_launches(int n = 1);
 int* lib_status_ptr();  // device status word used by handle-less entry points

@@ -53,20 +53,22 @@ WorkspaceLayout workspace_layout(const qwen_layer_config& c, int B, int T);
 QkvParams make_qkv_params(const qwen_layer_s* L, const int32_t* positions, const int32_t* slot0,
                           __nv_bfloat16* q, __nv_bfloat16* kc, __nv_bfloat16* vc, int T);
 
-qwen_status layer_prefill(qwen_layer_s* L, const __nv_bfloat16* x, __nv_bfloat16* y, int B, int T,
-                          const int32_t* positions, const int32_t* slot0, __nv_bfloat16* kc,
-                          __nv_bfloat16* vc, uint8_t* ws, const WorkspaceLayout& W,
-                          cudaStream_t st);
+// x (BF16) or x32 (FP32) is the input; y (BF16) and/or y32 (FP32) the output.
+qwen_status layer_prefill(qwen_layer_s* L, const __nv_bfloat16* x, const float* x32,
+                          __nv_bfloat16* y, float* y32, int B, int T, const int32_t* positions,
+                          const int32_t* slot0, __nv_bfloat16* kc, __nv_bfloat16* vc,
+                          uint8_t* ws, const WorkspaceLayout& W, cudaStream_t st);
 
-qwen_status layer_decode(qwen_layer_s* L, const __nv_bfloat16* x, __nv_bfloat16* y, int B,
-                         const int32_t* positions, const int32_t* cache_len, __nv_bfloat16* kc,
-                         __nv_bfloat16* vc, uint8_t* ws, const WorkspaceLayout& W,
-                         cudaStream_t st);
+qwen_status layer_decode(qwen_layer_s* L, const __nv_bfloat16* x, const float* x32,
+                         __nv_bfloat16* y, float* y32, int B, const int32_t* positions,
+                         const int32_t* cache_len, __nv_bfloat16* kc, __nv_bfloat16* vc,
+                         uint8_t* ws, const WorkspaceLayout& W, cudaStream_t st);
 
+// MoE block: residual input r (BF16) or r32 (FP32); output y (BF16) and/or y32.
 qwen_status moe_forward(qwen_layer_s* L, const __nv_bfloat16* r, const float* r32,
-                        __nv_bfloat16* y, int T, int32_t* topk_idx_out, float* topk_w_out,
-                        float* logits_out, uint8_t* ws, const WorkspaceLayout& W,
-                        cudaStream_t st);
+                        __nv_bfloat16* y, float* y32, int T, int32_t* topk_idx_out,
+                        float* topk_w_out, float* logits_out, uint8_t* ws,
+                        const WorkspaceLayout& W, cudaStream_t st);
 
 // ---- decode building blocks (decode_gemm.cu, attention_decode.cu)
 
@@ -79,8 +81,11 @@ void decode_attn_plan(const qwen_layer_config& c, int B, int* chunk, int* splits
 
 // part[s][b][n] = sum over split s's k-range of W[n, k] X[b, k].
 // W [N, K], X [B, K] (row stride ldx).
+// w_static: W is never written by the kernel launched just before (the packed
+// layer weights), so its first tiles may be fetched before waiting on it.
 qwen_status gemm_decode_splitk(const void* W, const void* X, int ldx, int B, int N, int K,
-                               int splits, bool op_f16, float* part, int* err, cudaStream_t st);
+                               int splits, bool op_f16, float* part, int* err, cudaStream_t st,
+                               bool w_static = false);
 
 // Reductions over the splits followed by the step's epilogue.
 qwen_status reduce_resid(const float* part, int splits, int B, int N, const __nv_bfloat16* resid,

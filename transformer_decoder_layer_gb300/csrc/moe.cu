@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ z
                                                      const float* __restrict__ br,
                                                      float* __restrict__ logits, int T, int E,
                                                      int d) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float zs[kRK][kRT];       // [k][token]
   __shared__ float ws[kRK][kRE + 4];   // [k][expert]
   const int t0 = blockIdx.x * kRT, e0 = blockIdx.y * kRE;
@@ -77,6 +79,8 @@ __global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ z
 // ties), then the weights softmax(selected logits).
 __global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                             int32_t* __restrict__ idx, float* __restrict__ w) {
+  pdl_trigger();
+  pdl_wait();
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -131,6 +135,8 @@ __global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int 
 
 __global__ void expert_hist_kernel(const int32_t* __restrict__ idx, int n, int E,
                                    int32_t* __restrict__ counts) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ int32_t h[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
   __syncthreads();
@@ -152,6 +158,8 @@ __global__ void __launch_bounds__(256) expert_scatter_kernel(const int32_t* __re
                                                              int32_t* __restrict__ offsets,
                                                              int32_t* __restrict__ perm,
                                                              int32_t* __restrict__ inv) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int32_t warp_tot[8];
   __shared__ int32_t base_s;
   const int e = blockIdx.x;
@@ -197,6 +205,8 @@ __global__ void __launch_bounds__(256) expert_scatter_kernel(const int32_t* __re
 // zp[pos] = z[perm[pos] / k]  (16-bit rows of d elements), one warp per row
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ z, const int32_t* __restrict__ perm,
                                    int n, int k, int d, uint16_t* __restrict__ zp) {
+  pdl_trigger();
+  pdl_wait();
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= n) return;
@@ -210,7 +220,9 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ z, const int32_t
 __global__ void combine_kernel(const f16* __restrict__ yp, const int32_t* __restrict__ inv,
                                const float* __restrict__ w, const float* __restrict__ r32,
                                const bf16* __restrict__ r, int T, int k, int d,
-                               bf16* __restrict__ y) {
+                               bf16* __restrict__ y, float* __restrict__ y32) {
+  pdl_trigger();
+  pdl_wait();
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -244,12 +256,19 @@ __global__ void combine_kernel(const f16* __restrict__ yp, const int32_t* __rest
         o[2 * e + 1] = f.y + acc[2 * e + 1];
       }
     }
-    uint4 out;
-    out.x = pack_bf16x2(o[0], o[1]);
-    out.y = pack_bf16x2(o[2], o[3]);
-    out.z = pack_bf16x2(o[4], o[5]);
-    out.w = pack_bf16x2(o[6], o[7]);
-    reinterpret_cast<uint4*>(y + (size_t)t * d)[c] = out;
+    if (y) {
+      uint4 out;
+      out.x = pack_bf16x2(o[0], o[1]);
+      out.y = pack_bf16x2(o[2], o[3]);
+      out.z = pack_bf16x2(o[4], o[5]);
+      out.w = pack_bf16x2(o[6], o[7]);
+      reinterpret_cast<uint4*>(y + (size_t)t * d)[c] = out;
+    }
+    if (y32) {
+      float4* o4 = reinterpret_cast<float4*>(y32 + (size_t)t * d);
+      o4[2 * c] = make_float4(o[0], o[1], o[2], o[3]);
+      o4[2 * c + 1] = make_float4(o[4], o[5], o[6], o[7]);
+    }
   }
 }
 
@@ -257,7 +276,7 @@ inline int nblk(long long n, int t) { return (int)((n + t - 1) / t); }
 
 }  // namespace
 
-qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* y, int T,
+qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* y, float* y32, int T,
                         int32_t* topk_idx_out, float* topk_w_out, float* logits_out, uint8_t* ws,
                         const WorkspaceLayout& W, cudaStream_t st) {
   const qwen_layer_config& c = L->cfg;
@@ -281,21 +300,23 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
   // 1. RMSNorm_2 -> Z (FP16) and Z32 (FP32 router input)
   if ((s = rmsnorm_launch(r, L->gamma_mlp, z, true, z32, r32, T, d, c.rms_eps, st))) return s;
   // 2. router logits in FP32
-  router_kernel<<<dim3(nblk(T, kRT), nblk(E, kRE)), 256, 0, st>>>(z32, L->w_router, L->b_router,
-                                                                  logits, T, E, d);
+  launch_k(router_kernel, dim3(nblk(T, kRT), nblk(E, kRE)), dim3(256), 0, st, (const float*)z32,
+           (const bf16*)L->w_router, (const float*)L->b_router, logits, T, E, d);
   count_launches();
   // 3. top-k + softmax over the selected logits
-  topk_kernel<<<nblk(32LL * T, 256), 256, 0, st>>>(logits, T, E, k, idx, wts);
+  launch_k(topk_kernel, dim3(nblk(32LL * T, 256)), dim3(256), 0, st, (const float*)logits, T, E, k,
+           idx, wts);
   count_launches();
   // 4. permutation by expert (stable in token order) and gather of Z rows
   if (cudaMemsetAsync(counts, 0, (size_t)E * sizeof(int32_t), st) != cudaSuccess)
     return QWEN_ERR_CUDA;
-  expert_hist_kernel<<<nblk(n, 1024) < 148 ? nblk(n, 1024) : 148, 1024, E * sizeof(int32_t), st>>>(
-      idx, n, E, counts);
-  expert_scatter_kernel<<<E, 256, 0, st>>>(idx, n, E, counts, offsets, perm, inv);
-  gather_rows_kernel<<<nblk(32LL * n, 256), 256, 0, st>>>(reinterpret_cast<const uint16_t*>(z),
-                                                          perm, n, k, d,
-                                                          reinterpret_cast<uint16_t*>(zp));
+  launch_k(expert_hist_kernel, dim3(nblk(n, 1024) < 148 ? nblk(n, 1024) : 148), dim3(1024),
+           E * sizeof(int32_t), st, (const int32_t*)idx, n, E, counts);
+  launch_k(expert_scatter_kernel, dim3(E), dim3(256), 0, st, (const int32_t*)idx, n, E,
+           (const int32_t*)counts, offsets, perm, inv);
+  launch_k(gather_rows_kernel, dim3(nblk(32LL * n, 256)), dim3(256), 0, st,
+           reinterpret_cast<const uint16_t*>(z), (const int32_t*)perm, n, k, d,
+           reinterpret_cast<uint16_t*>(zp));
   count_launches(3);
   if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;
   // 5. grouped expert GEMMs: gate/up with SiLU*up, then down
@@ -316,7 +337,8 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
   ed.n_groups = E;
   if ((s = gemm_tc(hp, mf, L->w_down, mf, n, d, mf, true, ed, err, st))) return s;
   // 6. weighted combine + residual
-  combine_kernel<<<nblk(32LL * T, 256), 256, 0, st>>>(yp, inv, wts, r32, r, T, k, d, y);
+  launch_k(combine_kernel, dim3(nblk(32LL * T, 256)), dim3(256), 0, st, (const f16*)yp,
+           (const int32_t*)inv, (const float*)wts, r32, r, T, k, d, y, y32);
   count_launches();
   if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;
   // optional copies of the routing for inspection

@@ -15,6 +15,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
                                                       void* __restrict__ y, bool y_f16,
                                                       float* __restrict__ y32, int rows, int d,
                                                       float eps, size_t xs) {
+  pdl_trigger();
+  pdl_wait();
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -94,11 +96,14 @@ qwen_status rmsnorm_launch(const bf16* x, const bf16* gamma, void* y, bool y_f16
   const int threads = 256;
   const int blocks = (rows * 32 + threads - 1) / threads;
   if (d <= 2048)
-    rmsnorm_kernel<8><<<blocks, threads, 0, st>>>(x, x32, gamma, y, y_f16, y32, rows, d, eps, xs);
+    launch_k(rmsnorm_kernel<8>, dim3(blocks), dim3(threads), 0, st, x, x32, gamma, y, y_f16, y32,
+             rows, d, eps, xs);
   else if (d <= 4096)
-    rmsnorm_kernel<16><<<blocks, threads, 0, st>>>(x, x32, gamma, y, y_f16, y32, rows, d, eps, xs);
+    launch_k(rmsnorm_kernel<16>, dim3(blocks), dim3(threads), 0, st, x, x32, gamma, y, y_f16, y32,
+             rows, d, eps, xs);
   else
-    rmsnorm_kernel<32><<<blocks, threads, 0, st>>>(x, x32, gamma, y, y_f16, y32, rows, d, eps, xs);
+    launch_k(rmsnorm_kernel<32>, dim3(blocks), dim3(threads), 0, st, x, x32, gamma, y, y_f16, y32,
+             rows, d, eps, xs);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
