@@ -99,8 +99,8 @@ WorkspaceLayout workspace_layout(const qwen_layer_config& c, int B, int T) {
     W.yp = take(mk * d * 2);
   }
   if (T == 1) {
-    int chunk = 0, splits = 0;
-    decode_attn_plan(c, B, &chunk, &splits);
+    int splits = 0;
+    decode_attn_plan(c, B, &splits);
     W.part = take(decode_part_bytes(c, B));
     W.attn_o = take((size_t)B * c.n_q_heads * splits * dh * 4);
     W.attn_ml = take((size_t)B * c.n_q_heads * splits * 2 * 4);
@@ -501,10 +501,10 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
     QWEN_STAGE_RUN(QWEN_STAGE_QKV, gemm_tc(xh, d, L->w_qkv, d, B, nqkv, d, true, e, err, st));
   }
   // split-KV attention over slots 0..cache_len[b], then the merge
-  int chunk = 0, splits = 0;
-  decode_attn_plan(c, B, &chunk, &splits);
+  int splits = 0;
+  decode_attn_plan(c, B, &splits);
   QWEN_STAGE_RUN(QWEN_STAGE_ATTN,
-                 attention_decode(q, kc, vc, cache_len, B, Hq, Hkv, dh, c.max_seq, chunk, splits,
+                 attention_decode(q, kc, vc, cache_len, B, Hq, Hkv, dh, c.max_seq, splits,
                                   reinterpret_cast<float*>(ws + W.attn_o),
                                   reinterpret_cast<float*>(ws + W.attn_ml), attn, err, st));
   // O projection + residual -> R (FP32)

@@ -11,11 +11,16 @@
 // swizzle) through a 4-stage ring; the tiny contraction runs on mma.sync
 // (m16n8k16, BF16 -> FP32) with the group's heads as the 16 rows.
 //
-// Work unit = (sequence b, KV head g, key chunk sp).  A persistent CTA walks
-// its units; 4 compute warps each take 16 keys of every block and keep their own
-// running max / sum / O; the warps merge through shared memory and the unit's
-// unnormalised partial (m, l, O) goes to a workspace.  A merge kernel combines
-// the chunks of each head in a fixed order (deterministic).
+// Work unit = (sequence b, KV head g, split sp): the sequence's 64-key blocks
+// are divided evenly among `splits` units.  A persistent CTA walks its units;
+// the producer warp streams each unit's query rows (bulk copy) and K/V blocks
+// (TMA) through rings of equal depth, so it can run ahead across unit
+// boundaries.  4 compute warps each take 16 keys of every block and keep their
+// own running max / sum / O; the warps merge through shared memory and the
+// unit's unnormalised partial (m, l, O) goes to a workspace.  A merge kernel
+// combines the splits of each head in a fixed order (deterministic).
+#include <cmath>
+
 #include "common.cuh"
 #include "internal.h"
 #include "layer.h"
@@ -66,14 +71,20 @@ struct DecAttnCfg {
   static constexpr int BOX_BYTES = kKB * 128;          // 64 keys x 64 dims
   static constexpr int KV_BYTES = (DH / 64) * BOX_BYTES;
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;      // K then V
-  static constexpr int SCRATCH_FLOATS = kCW * 16 * (DH + 2);
-  static constexpr int SMEM_BYTES = 1024 + kDStages * STAGE_BYTES + SCRATCH_FLOATS * 4 + 256;
+  static constexpr int Q_BYTES = 16 * DH * 2;           // one unit's query rows (<= 16 heads)
+  // merge scratch, double-buffered by unit parity: per warp its O fragments
+  // lane-major ([DH/2][32] floats) and per head row (max, sum)
+  static constexpr int FRAG_FLOATS = (DH / 2) * 32;
+  static constexpr int SCRATCH_FLOATS = 2 * kCW * (FRAG_FLOATS + 16 * 2);
+  static constexpr int LEN_SLOTS = 1024;  // cache lengths staged in shared memory
+  static constexpr int SMEM_BYTES = 1024 + kDStages * STAGE_BYTES + kDStages * Q_BYTES +
+                                    SCRATCH_FLOATS * 4 + LEN_SLOTS * 4 + 256;
 };
 
 struct DecAttnArgs {
   const bf16* q;  // [B][Hq][DH]
   const int32_t* cache_len;
-  int B, Hq, Hkv, max_seq, chunk, splits;
+  int B, Hq, Hkv, max_seq, splits;
   float scale_log2;
   float* part_o;   // [B*Hq][splits][DH]
   float* part_ml;  // [B*Hq][splits][2]
@@ -92,10 +103,15 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float* scratch = reinterpret_cast<float*>(smem + kDStages * C::STAGE_BYTES);
+  bf16* sQ = reinterpret_cast<bf16*>(smem + kDStages * C::STAGE_BYTES);  // [kDStages][16][DH]
+  float* scratch =
+      reinterpret_cast<float*>(smem + kDStages * C::STAGE_BYTES + kDStages * C::Q_BYTES);
   uint64_t* full = reinterpret_cast<uint64_t*>(scratch + C::SCRATCH_FLOATS);
   uint64_t* empty = full + kDStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kDStages);
+  uint64_t* q_full = empty + kDStages;   // [kDStages]
+  uint64_t* q_empty = q_full + kDStages; // [kDStages]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(q_empty + kDStages);
+  int* s_len = const_cast<int*>(abort_flag) + 4;  // [LEN_SLOTS] cache lengths
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.Hq / a.Hkv;
@@ -106,9 +122,19 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kCW);
     }
+    for (int s = 0; s < kDStages; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], kCW);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
+  // query rows beyond the group stay zero (the bulk copies fill rows < G only)
+  for (int i = threadIdx.x; i < kDStages * C::Q_BYTES / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(sQ)[i] = make_uint4(0, 0, 0, 0);
+  // every unit needs its sequence's cache length: stage them once
+  for (int i = threadIdx.x; i < a.B && i < C::LEN_SLOTS; i += blockDim.x) s_len[i] = a.cache_len[i];
+  fence_proxy_async_smem();
   __syncthreads();
 
   if (warp == kCW) {
@@ -118,12 +144,21 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
       tma_prefetch_desc(&tmV);
       int stage = 0;
       uint32_t phase = 0;
-      for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      int lu = 0;  // local unit counter
+      for (int u = blockIdx.x; u < units; u += gridDim.x, ++lu) {
         const int pair = u / a.splits, sp = u - pair * a.splits;
-        const int b = pair / a.Hkv;
-        const int n_keys = min(a.cache_len[b] + 1, a.max_seq);
-        const int k0 = sp * a.chunk, k1 = min(k0 + a.chunk, n_keys);
+        const int b = pair / a.Hkv, g = pair - b * a.Hkv;
+        const int n_keys = min((b < C::LEN_SLOTS ? s_len[b] : a.cache_len[b]) + 1, a.max_seq);
+        const int nb = (n_keys + kKB - 1) / kKB;
+        const int k0 = kKB * (int)((long long)sp * nb / a.splits);
+        const int k1 = min(kKB * (int)((long long)(sp + 1) * nb / a.splits), n_keys);
         const int row0 = pair * a.max_seq;  // (b * Hkv + g) * max_seq
+        // the unit's G query rows (contiguous in q) into its slot of the Q ring
+        const int qs = lu % kDStages;
+        if (!mbar_wait(&q_empty[qs], ((lu / kDStages) & 1) ^ 1u, abort_flag, a.err)) goto prod_done;
+        mbar_arrive_expect_tx(&q_full[qs], (uint32_t)(G * DH * 2));
+        bulk_load(sQ + qs * 16 * DH, a.q + ((size_t)b * a.Hq + (size_t)g * G) * DH,
+                  (uint32_t)(G * DH * 2), &q_full[qs]);
         for (int blk = k0; blk < k1; blk += kKB) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err)) goto prod_done;
           uint8_t* st = smem + stage * C::STAGE_BYTES;
@@ -156,26 +191,33 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
   int stage = 0;
   uint32_t phase = 0;
   const uint32_t smem_base = smem_u32(smem);
-  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+  int lu = 0;
+  for (int u = blockIdx.x; u < units; u += gridDim.x, ++lu) {
     const int pair = u / a.splits, sp = u - pair * a.splits;
     const int b = pair / a.Hkv, g = pair - b * a.Hkv;
     // the new token sits in slot cache_len[b]: keys 0..cache_len[b] (clamped to the cache)
-    const int n_keys = min(a.cache_len[b] + 1, a.max_seq);
+    const int n_keys = min((b < C::LEN_SLOTS ? s_len[b] : a.cache_len[b]) + 1, a.max_seq);
     const int L = n_keys - 1;  // last visible key
-    const int k0 = sp * a.chunk, k1 = min(k0 + a.chunk, n_keys);
+    const int nb = (n_keys + kKB - 1) / kKB;
+    const int k0 = kKB * (int)((long long)sp * nb / a.splits);
+    const int k1 = min(kKB * (int)((long long)(sp + 1) * nb / a.splits), n_keys);
     const int h0 = g * G;
-    // Q fragments (rows = heads of the group, zero beyond G)
+    // Q fragments (rows = heads of the group, zero beyond G) from the slot the
+    // producer filled.  The slot is released at the end of the unit: only then
+    // are the shared-memory loads certain to have completed (their consumers,
+    // the S MMAs, have issued), so the next bulk copy cannot overtake them.
     uint32_t qa[DH / 16][4];
+    const int qs = lu % kDStages;
     {
-      const uint32_t* qrow0 = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * a.Hq + h0 + gid) * DH);
-      const uint32_t* qrow1 = reinterpret_cast<const uint32_t*>(a.q + ((size_t)b * a.Hq + h0 + gid + 8) * DH);
-      const bool v0 = gid < G, v1 = gid + 8 < G;
+      if (!mbar_wait(&q_full[qs], (lu / kDStages) & 1, abort_flag, a.err)) break;
+      const uint32_t* qrow0 = reinterpret_cast<const uint32_t*>(sQ + (qs * 16 + gid) * DH);
+      const uint32_t* qrow1 = reinterpret_cast<const uint32_t*>(sQ + (qs * 16 + gid + 8) * DH);
 #pragma unroll
       for (int kk = 0; kk < DH / 16; ++kk) {
-        qa[kk][0] = v0 ? qrow0[(16 * kk + 2 * tq) / 2] : 0u;
-        qa[kk][1] = v1 ? qrow1[(16 * kk + 2 * tq) / 2] : 0u;
-        qa[kk][2] = v0 ? qrow0[(16 * kk + 8 + 2 * tq) / 2] : 0u;
-        qa[kk][3] = v1 ? qrow1[(16 * kk + 8 + 2 * tq) / 2] : 0u;
+        qa[kk][0] = qrow0[(16 * kk + 2 * tq) / 2];
+        qa[kk][1] = qrow1[(16 * kk + 2 * tq) / 2];
+        qa[kk][2] = qrow0[(16 * kk + 8 + 2 * tq) / 2];
+        qa[kk][3] = qrow1[(16 * kk + 8 + 2 * tq) / 2];
       }
     }
     float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
@@ -286,49 +328,76 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
       }
     }
     if (*abort_flag) break;
-    // ---- merge the 4 warps of this unit through shared memory
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&q_empty[qs]);
+    // ---- merge the warps of this unit: fragments lane-major into the scratch
+    // buffer of this unit's parity, one barrier, then each warp combines a
+    // share of the fragment entries across all warps (the other buffer may
+    // still be read by slower threads of the previous unit; the barrier of
+    // the next unit orders reuse of this one)
 #pragma unroll
     for (int rI = 0; rI < 2; ++rI) {
       l_r[rI] += __shfl_xor_sync(0xffffffffu, l_r[rI], 1);
       l_r[rI] += __shfl_xor_sync(0xffffffffu, l_r[rI], 2);
     }
-    float* my = scratch + (size_t)warp * 16 * (DH + 2);
+    float* buf = scratch + (lu & 1) * kCW * (C::FRAG_FLOATS + 32);
+    float* frag = buf + warp * C::FRAG_FLOATS;
+    float* ml = buf + kCW * C::FRAG_FLOATS;  // [kCW][16 rows][2]
+#pragma unroll
+    for (int i = 0; i < DH / 8; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) frag[(4 * i + e) * 32 + lane] = o[i][e];
+    if (tq == 0) {
+      ml[(warp * 16 + gid) * 2] = m_r[0];
+      ml[(warp * 16 + gid) * 2 + 1] = l_r[0];
+      ml[(warp * 16 + gid + 8) * 2] = m_r[1];
+      ml[(warp * 16 + gid + 8) * 2 + 1] = l_r[1];
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kCW * 32) : "memory");
+    constexpr int PER_W = (DH / 2) / kCW;  // fragment entries each warp combines
+    float Mr[2], wr[2][kCW], Lr[2];
 #pragma unroll
     for (int rI = 0; rI < 2; ++rI) {
-      const int hrow = gid + 8 * rI;
-      float* row = my + hrow * (DH + 2);
-#pragma unroll
-      for (int i = 0; i < DH / 8; ++i) {
-        row[8 * i + 2 * tq] = o[i][2 * rI];
-        row[8 * i + 2 * tq + 1] = o[i][2 * rI + 1];
-      }
-      if (tq == 0) {
-        row[DH] = m_r[rI];
-        row[DH + 1] = l_r[rI];
-      }
-    }
-    asm volatile("bar.sync 1, %0;" ::"r"(kCW * 32) : "memory");
-    for (int idx = threadIdx.x; idx < G * DH; idx += kCW * 32) {
-      const int hrow = idx / DH, dd = idx - hrow * DH;
+      const int row = gid + 8 * rI;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kCW; ++w) M = fmaxf(M, scratch[(w * 16 + hrow) * (DH + 2) + DH]);
-      float acc = 0.f, lsum = 0.f;
+      for (int w = 0; w < kCW; ++w) M = fmaxf(M, ml[(w * 16 + row) * 2]);
+      float L = 0.f;
 #pragma unroll
       for (int w = 0; w < kCW; ++w) {
-        const float* row = scratch + (w * 16 + hrow) * (DH + 2);
-        const float f = (row[DH] == -INFINITY) ? 0.f : ex2f(row[DH] - M);
-        acc += f * row[dd];
-        lsum += f * row[DH + 1];
+        const float mw = ml[(w * 16 + row) * 2];
+        wr[rI][w] = (mw == -INFINITY) ? 0.f : ex2f(mw - M);
+        L += wr[rI][w] * ml[(w * 16 + row) * 2 + 1];
       }
-      const size_t ph = (size_t)(b * a.Hq + h0 + hrow) * a.splits + sp;
-      a.part_o[ph * DH + dd] = acc;
-      if (dd == 0) {
-        a.part_ml[ph * 2] = M;
-        a.part_ml[ph * 2 + 1] = lsum;
+      Mr[rI] = M;
+      Lr[rI] = L;
+    }
+#pragma unroll
+    for (int j = 0; j < PER_W; ++j) {
+      const int i = warp * PER_W + j;       // fragment entry
+      const int e = i & 3, nb = i >> 2;
+      const int rI = e >> 1;
+      const int row = gid + 8 * rI;
+      const int col = 8 * nb + 2 * tq + (e & 1);
+      float acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < kCW; ++w) acc += wr[rI][w] * buf[w * C::FRAG_FLOATS + i * 32 + lane];
+      if (row < G) {
+        const size_t ph = (size_t)(b * a.Hq + h0 + row) * a.splits + sp;
+        a.part_o[ph * DH + col] = acc;
       }
     }
-    asm volatile("bar.sync 1, %0;" ::"r"(kCW * 32) : "memory");
+    if (warp == 0 && tq == 0) {
+#pragma unroll
+      for (int rI = 0; rI < 2; ++rI) {
+        const int row = gid + 8 * rI;
+        if (row < G) {
+          const size_t ph = (size_t)(b * a.Hq + h0 + row) * a.splits + sp;
+          a.part_ml[ph * 2] = Mr[rI];
+          a.part_ml[ph * 2 + 1] = Lr[rI];
+        }
+      }
+    }
   }
 }
 
@@ -391,16 +460,24 @@ static bool tmap_cache(CUtensorMap* m, const void* base, uint64_t rows, int dh) 
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-void decode_attn_plan(const qwen_layer_config& c, int B, int* chunk, int* splits) {
+// Splits per (sequence, KV head): minimise the estimated makespan
+// ceil(units / CTAs) * (blocks per unit + per-unit overhead), with one
+// block-equivalent of overhead per unit (query fetch, warp merge, partials).
+void decode_attn_plan(const qwen_layer_config& c, int B, int* splits) {
   const int sms = device_sm_count();
   const long long pairs = (long long)B * c.n_kv_heads;
-  long long target = (16LL * sms + pairs - 1) / pairs;  // splits per (b, g)
-  if (target < 1) target = 1;
-  long long ch = (c.max_seq + target - 1) / target;
-  ch = ((ch + kKB - 1) / kKB) * kKB;
-  if (ch < kKB) ch = kKB;
-  *chunk = (int)ch;
-  *splits = (int)((c.max_seq + ch - 1) / ch);
+  const int nb = (c.max_seq + kKB - 1) / kKB;
+  int best = 1;
+  double best_t = 1e30;
+  for (int s = 1; s <= nb && s <= 256; ++s) {
+    const double per_cta = std::ceil((double)(pairs * s) / sms);
+    const double t = per_cta * ((double)nb / s + 1.0);
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best = s;
+    }
+  }
+  *splits = best;
 }
 
 template <int DH>
@@ -429,10 +506,10 @@ static qwen_status launch_attn_dec(const CUtensorMap& tk, const CUtensorMap& tv,
 
 qwen_status attention_decode(const bf16* q, const bf16* kc, const bf16* vc,
                              const int32_t* cache_len, int B, int Hq, int Hkv, int dh, int max_seq,
-                             int chunk, int splits, float* part_o, float* part_ml, f16* out,
+                             int splits, float* part_o, float* part_ml, f16* out,
                              int* err, cudaStream_t st) {
   if (B == 0) return QWEN_OK;
-  if (Hq / Hkv > 16 || chunk % kKB) return QWEN_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16 || splits < 1) return QWEN_ERR_UNSUPPORTED;
   CUtensorMap tk, tv;
   if (!tmap_cache(&tk, kc, (uint64_t)B * Hkv * max_seq, dh)) return QWEN_ERR_CUDA;
   if (!tmap_cache(&tv, vc, (uint64_t)B * Hkv * max_seq, dh)) return QWEN_ERR_CUDA;
@@ -443,7 +520,6 @@ qwen_status attention_decode(const bf16* q, const bf16* kc, const bf16* vc,
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.max_seq = max_seq;
-  a.chunk = chunk;
   a.splits = splits;
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)dh);
   a.part_o = part_o;

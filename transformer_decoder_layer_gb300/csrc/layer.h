@@ -76,8 +76,8 @@ qwen_status moe_forward(qwen_layer_s* L, const __nv_bfloat16* r, const float* r3
 int decode_splits(int N, int K);
 // Bytes of FP32 partials the decode GEMM of the layer needs for batch B.
 size_t decode_part_bytes(const qwen_layer_config& c, int B);
-// Attention split-KV plan: keys per split and number of splits for batch B.
-void decode_attn_plan(const qwen_layer_config& c, int B, int* chunk, int* splits);
+// Attention split-KV plan: number of splits per (sequence, KV head) for batch B.
+void decode_attn_plan(const qwen_layer_config& c, int B, int* splits);
 
 // part[s][b][n] = sum over split s's k-range of W[n, k] X[b, k].
 // W [N, K], X [B, K] (row stride ldx).
@@ -101,7 +101,7 @@ qwen_status reduce_f32(const float* part, int splits, int B, int N, float* out, 
 // slot cache_len[b] and attends slots 0..cache_len[b].  out [B][Hq*dh].
 qwen_status attention_decode(const __nv_bfloat16* q, const __nv_bfloat16* kc,
                              const __nv_bfloat16* vc, const int32_t* cache_len, int B, int Hq,
-                             int Hkv, int dh, int max_seq, int chunk, int splits, float* part_o,
+                             int Hkv, int dh, int max_seq, int splits, float* part_o,
                              float* part_ml, __half* out, int* err, cudaStream_t st);
 
 }  // namespace qwen
