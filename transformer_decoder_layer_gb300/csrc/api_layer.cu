@@ -79,6 +79,10 @@ WorkspaceLayout workspace_layout(const qwen_layer_config& c, int B, int T) {
   };
   W.xh = take(M * d * 2);
   W.q = take(M * nq * 2);
+  if (T > 1) {  // FP16 copies of the call's K/V rows for the prefill attention
+    W.k16 = take(M * (size_t)c.n_kv_heads * dh * 2);
+    W.v16 = take(M * (size_t)c.n_kv_heads * dh * 2);
+  }
   W.attn = take(M * nq * 2);
   W.r32 = take(M * d * 4);  // residual stream R kept in FP32
   W.z = take(M * d * 2);
@@ -488,7 +492,8 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
   QWEN_STAGE_RUN(QWEN_STAGE_NORM1, rmsnorm_launch(x, L->gamma_attn, xh, true, nullptr, x32, B,
                                                   d, c.rms_eps, st));
   // Q/K/V, then bias, QK-norm, RoPE, Q store and K/V append at slot cache_len[b]
-  const QkvParams qp = make_qkv_params(L, positions, cache_len, q, kc, vc, 1);
+  const QkvParams qp = make_qkv_params(L, positions, cache_len, q, false, kc, vc, nullptr,
+                                       nullptr, 1);
   if (swap) {
     QWEN_STAGE_RUN(QWEN_STAGE_QKV, decode_proj(L->w_qkv, xh, B, nqkv, d, part, err, st, S));
     QWEN_STAGE_RUN(QWEN_STAGE_QKV_FINISH, reduce_qkv(part, S, B, nqkv, qp, err, st));
@@ -508,6 +513,20 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
                                   reinterpret_cast<float*>(ws + W.attn_o),
                                   reinterpret_cast<float*>(ws + W.attn_ml), attn, err, st));
   // O projection + residual -> R (FP32)
+  if (swap && !c.n_experts) {
+    // O projection; its split reduction + residual is fused with RMSNorm_2
+    QWEN_STAGE_RUN(QWEN_STAGE_O, decode_proj(L->w_o, attn, B, d, nq, part, err, st, S));
+    QWEN_STAGE_RUN(QWEN_STAGE_O_FINISH,
+                   reduce_resid_norm(part, S, B, d, x, x32, r32, L->gamma_mlp, c.rms_eps, z, st));
+    // gate/up in one K split with SiLU*up in the epilogue -> H, then down
+    QWEN_STAGE_RUN(QWEN_STAGE_GATE_UP,
+                   gemm_decode_splitk(L->w_gu, z, d, B, 2 * f, d, 1, /*op_f16=*/true, nullptr,
+                                      err, st, /*w_static=*/true, hbuf));
+    QWEN_STAGE_RUN(QWEN_STAGE_DOWN, decode_proj(L->w_down, hbuf, B, d, f, part, err, st, S));
+    QWEN_STAGE_RUN(QWEN_STAGE_DOWN_FINISH,
+                   reduce_resid(part, S, B, d, nullptr, r32, y, y32, st));
+    return QWEN_OK;
+  }
   if (swap) {
     QWEN_STAGE_RUN(QWEN_STAGE_O, decode_proj(L->w_o, attn, B, d, nq, part, err, st, S));
     QWEN_STAGE_RUN(QWEN_STAGE_O_FINISH, reduce_resid(part, S, B, d, x, x32, nullptr, r32, st));
@@ -565,7 +584,9 @@ qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, const float* x32, bf16
   const int M = B * T, d = c.d, dh = c.head_dim, Hq = c.n_q_heads, Hkv = c.n_kv_heads;
   const int nq = Hq * dh, nqkv = nq + 2 * Hkv * dh, f = c.ffn;
   f16* xh = reinterpret_cast<f16*>(ws + W.xh);
-  bf16* q = reinterpret_cast<bf16*>(ws + W.q);
+  f16* q = reinterpret_cast<f16*>(ws + W.q);
+  f16* k16 = reinterpret_cast<f16*>(ws + W.k16);
+  f16* v16 = reinterpret_cast<f16*>(ws + W.v16);
   f16* attn = reinterpret_cast<f16*>(ws + W.attn);
   float* r32 = reinterpret_cast<float*>(ws + W.r32);
   f16* z = reinterpret_cast<f16*>(ws + W.z);
@@ -579,11 +600,11 @@ qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, const float* x32, bf16
   GemmEpilogue e{};
   e.mode = EPI_QKV;
   e.b_static = 1;
-  e.qkv = make_qkv_params(L, positions, slot0, q, kc, vc, T);
+  e.qkv = make_qkv_params(L, positions, slot0, q, true, kc, vc, k16, v16, T);
   QWEN_STAGE_RUN(QWEN_STAGE_QKV, gemm_tc(xh, d, L->w_qkv, d, M, nqkv, d, true, e, err, st));
   // causal GQA attention over the cache
-  QWEN_STAGE_RUN(QWEN_STAGE_ATTN, attention_prefill(q, kc, vc, slot0, attn, B, T, Hq, Hkv, dh,
-                                                    c.max_seq, err, st));
+  QWEN_STAGE_RUN(QWEN_STAGE_ATTN, attention_prefill(q, kc, vc, k16, v16, slot0, attn, B, T, Hq,
+                                                    Hkv, dh, c.max_seq, err, st));
   // O projection + residual; R stays in FP32 (it reaches Y unchanged through
   // the second residual, so rounding it to BF16 would put that rounding on Y)
   GemmEpilogue eo{};
@@ -624,7 +645,7 @@ qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, const float* x32, bf16
 }
 
 QkvParams make_qkv_params(const qwen_layer_s* L, const int32_t* positions, const int32_t* slot0,
-                          bf16* q, bf16* kc, bf16* vc, int T) {
+                          void* q, bool q_f16, bf16* kc, bf16* vc, f16* k16, f16* v16, int T) {
   const qwen_layer_config& c = L->cfg;
   QkvParams p{};
   p.bias = L->b_qkv;
@@ -634,8 +655,11 @@ QkvParams make_qkv_params(const qwen_layer_s* L, const int32_t* positions, const
   p.positions = positions;
   p.slot0 = slot0;
   p.q_out = q;
+  p.q_f16 = q_f16 ? 1 : 0;
   p.k_cache = kc;
   p.v_cache = vc;
+  p.k16 = k16;
+  p.v16 = v16;
   p.T = T;
   p.Hq = c.n_q_heads;
   p.Hkv = c.n_kv_heads;

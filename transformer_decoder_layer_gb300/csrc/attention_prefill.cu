@@ -8,6 +8,13 @@
 // repeat) and tiles above the diagonal are skipped.  §12 of the Qwen3 page: the
 // [T,T] probability matrix is never written to memory.
 //
+// Operands: the queries and the keys/values this call computed are FP16 (the
+// QKV epilogue writes FP16 copies of the new K/V rows besides the BF16 cache),
+// so S = Q K^T and O += P V run on FP16 tensor-core operands with P in FP16.
+// Key tiles that reach below the sequence's first new slot (chunked prefill
+// onto a filled cache) come from the BF16 cache instead; for those the
+// softmax warps convert Q to a BF16 copy once and P is rounded to BF16.
+//
 // One CTA = one (sequence b, query head h, tile of 128 query rows).
 //   warp 0      TMA: Q tile once, then K/V tiles of 128 keys (2-stage ring)
 //   warp 1      TMEM allocator + MMA issuer:
@@ -15,8 +22,9 @@
 //                 O  += P_j V_j  -> TMEM (dh cols), P_j from shared memory,
 //                 V_j read MN-major (dh contiguous) straight from the cache tile
 //   warps 2..5  softmax: thread = query row; online max/sum in FP32 with the
-//               rescale of O deferred until the max grows by 2^8; P -> BF16 in
-//               the 128-byte-swizzled K-major layout the MMA reads; final O / l.
+//               rescale of O deferred until the max grows by 2^8; P -> FP16
+//               (BF16 for cache tiles) in the 128-byte-swizzled K-major layout
+//               the MMA reads; final O / l.
 #include "common.cuh"
 #include "internal.h"
 
@@ -39,9 +47,10 @@ __device__ __forceinline__ float ex2(float x) {
 
 template <int DH>
 struct AttnCfg {
-  static constexpr int TILE_BYTES = kKT * DH * 2;  // one [128 x DH] bf16 tile
-  static constexpr int Q_OFF = 0;
-  static constexpr int P_OFF = TILE_BYTES;                   // P [128 x 128] bf16
+  static constexpr int TILE_BYTES = kKT * DH * 2;  // one [128 x DH] 16-bit tile
+  static constexpr int Q_OFF = 0;                            // Q (FP16)
+  static constexpr int QB_OFF = TILE_BYTES;                  // BF16 copy of Q
+  static constexpr int P_OFF = 2 * TILE_BYTES;               // P [128 x 128] 16-bit
   static constexpr int K_OFF = P_OFF + kQT * kKT * 2;        // 2 stages
   static constexpr int V_OFF = K_OFF + 2 * TILE_BYTES;       // 2 stages
   static constexpr int BAR_OFF = V_OFF + 2 * TILE_BYTES;
@@ -65,7 +74,9 @@ template <int DH>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, AttnArgs a) {
+                        const __grid_constant__ CUtensorMap tmV,
+                        const __grid_constant__ CUtensorMap tmK16,
+                        const __grid_constant__ CUtensorMap tmV16, AttnArgs a) {
   pdl_trigger();
   pdl_wait();
   using C = AttnCfg<DH>;
@@ -73,6 +84,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem + C::Q_OFF;
+  uint8_t* sQb = smem + C::QB_OFF;
   uint8_t* sP = smem + C::P_OFF;
   uint8_t* sK = smem + C::K_OFF;
   uint8_t* sV = smem + C::V_OFF;
@@ -85,7 +97,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* s_free = bars + 9;    // [2]
   uint64_t* p_full = bars + 11;
   uint64_t* o_done = bars + 12;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  uint64_t* qb_ready = bars + 13;  // BF16 copy of Q written (chunked prefill only)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -102,7 +115,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int kmax = s0 + q_last;                // largest visible key slot
   const int n_kv = kmax / kKT + 1;             // key tiles 0..n_kv-1
   const int q_row0 = (b * a.Hq + h) * a.T + t0;        // row in the Q view
-  const int kv_row0 = (b * a.Hkv + g) * a.max_seq;     // row in the K/V view
+  const int kv_row0 = (b * a.Hkv + g) * a.max_seq;     // row in the cache view
+  const int kv16_row0 = (b * a.Hkv + g) * a.T - s0;    // + key slot = row in the fresh view
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -115,6 +129,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     mbar_init(p_full, 128);
     mbar_init(o_done, 1);
+    mbar_init(qb_ready, 128);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -132,6 +147,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmK16);
+      tma_prefetch_desc(&tmV16);
       mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
 #pragma unroll
       for (int c = 0; c < DH / 64; ++c)
@@ -139,16 +156,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int j = 0; j < n_kv; ++j) {
         const int st = j & 1;
         if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1u, abort_flag, a.err)) break;
+        // tiles entirely at or above the first new slot come from the FP16
+        // copies of this call's rows, the others from the BF16 cache
+        const bool fresh = j * kKT >= s0;
+        const CUtensorMap* mk = fresh ? &tmK16 : &tmK;
+        const CUtensorMap* mv = fresh ? &tmV16 : &tmV;
+        const int row = fresh ? kv16_row0 + j * kKT : kv_row0 + j * kKT;
         mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < DH / 64; ++c)
-          tma_load_2d(sK + st * C::TILE_BYTES + c * kKT * 128, &tmK, &k_full[st], c * 64,
-                      kv_row0 + j * kKT);
+          tma_load_2d(sK + st * C::TILE_BYTES + c * kKT * 128, mk, &k_full[st], c * 64, row);
         mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < DH / 64; ++c)
-          tma_load_2d(sV + st * C::TILE_BYTES + c * kKT * 128, &tmV, &v_full[st], c * 64,
-                      kv_row0 + j * kKT);
+          tma_load_2d(sV + st * C::TILE_BYTES + c * kKT * 128, mv, &v_full[st], c * 64, row);
       }
       // drain: every issued tile is consumed before exit
       for (int j = n_kv; j < n_kv + 2; ++j) {
@@ -157,26 +178,36 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(kQT, kKT);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(kQT, DH, false, /*b_mn_major=*/true);
-      const uint32_t q0 = smem_u32(sQ);
-      auto issue_s = [&](int j) {
+      constexpr uint32_t idesc_s16 = idesc_f32acc(kQT, kKT, true);
+      constexpr uint32_t idesc_sb = idesc_f32acc(kQT, kKT, false);
+      constexpr uint32_t idesc_o16 = idesc_f32acc(kQT, DH, true, false, /*b_mn_major=*/true);
+      constexpr uint32_t idesc_ob = idesc_f32acc(kQT, DH, false, false, /*b_mn_major=*/true);
+      bool qb_waited = false;
+      auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
+        const bool fresh = j * kKT >= s0;
+        if (!fresh && !qb_waited) {
+          if (!mbar_wait(qb_ready, 0, abort_flag, a.err)) return false;
+          tc_fence_after();
+          qb_waited = true;
+        }
+        const uint32_t q0 = smem_u32(fresh ? sQ : sQb);
         const uint32_t k0 = smem_u32(sK + st * C::TILE_BYTES);
         const uint32_t d = tmem + C::S_COL0 + st * kKT;
 #pragma unroll
         for (int k = 0; k < DH / 16; ++k) {
           const uint32_t off = (k >> 2) * (kQT * 128) + (k & 3) * 32;
           umma_f16(d, smem_desc_sw128(q0 + off, 16, 1024), smem_desc_sw128(k0 + off, 16, 1024),
-                   idesc_s, k != 0);
+                   fresh ? idesc_s16 : idesc_sb, k != 0);
         }
         umma_commit(&s_full[st]);
+        return true;
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, a.err) &&
                 mbar_wait(&k_full[0], 0, abort_flag, a.err);
       if (ok) {
         tc_fence_after();
-        issue_s(0);
+        ok = issue_s(0);
       }
       const uint32_t p0 = smem_u32(sP);
       for (int j = 0; ok && j < n_kv; ++j) {
@@ -186,7 +217,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (!mbar_wait(&k_full[st1], (j1 >> 1) & 1, abort_flag, a.err)) break;
           if (j1 >= 2 && !mbar_wait(&s_free[st1], ((j1 >> 1) - 1) & 1, abort_flag, a.err)) break;
           tc_fence_after();
-          issue_s(j1);
+          if (!issue_s(j1)) break;
         }
         if (!mbar_wait(p_full, j & 1, abort_flag, a.err)) break;
         if (!mbar_wait(&v_full[st], (j >> 1) & 1, abort_flag, a.err)) break;
@@ -200,7 +231,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           // dh block 16 KB away (LBO), next 8 keys 1 KB away (SBO)
           const uint32_t vb = v0 + k * 16 * 128;
           umma_f16(tmem + C::O_COL, smem_desc_sw128(pa, 16, 1024),
-                   smem_desc_sw128(vb, kKT * 128, 1024), idesc_o, (j | k) != 0);
+                   smem_desc_sw128(vb, kKT * 128, 1024), (j * kKT >= s0) ? idesc_o16 : idesc_ob,
+                   (j | k) != 0);
         }
         umma_commit(o_done);
         umma_commit(&kv_empty[st]);
@@ -215,7 +247,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
     float m_used = -INFINITY, l_sum = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    if (s0 > 0) {
+      // some key tiles come from the BF16 cache: convert this row of Q once
+      // (element by element, so the swizzled placement is kept)
+      if (!mbar_wait(q_full, 0, abort_flag, a.err)) ok = false;
+      if (ok) {
+#pragma unroll
+        for (int blk = 0; blk < DH / 64; ++blk) {
+          const uint4* src = reinterpret_cast<const uint4*>(sQ + blk * (kQT * 128) + r * 128);
+          uint4* dst = reinterpret_cast<uint4*>(sQb + blk * (kQT * 128) + r * 128);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 u = src[c];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = unpack_f16x2(w[e]);
+              o[e] = pack_bf16x2(f.x, f.y);
+            }
+            dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(qb_ready);
+      }
+    }
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const bool fresh = j * kKT >= s0;
       const int st = j & 1;
       if (!mbar_wait(&s_full[st], (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
       tc_fence_after();
@@ -246,14 +305,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         l_sum *= alpha;
         m_used = m_new;
       }
-      // P = 2^(s - m) rounded to bf16; l sums the rounded values
+      // P = 2^(s - m) rounded to the tile's operand type; l sums the rounded values
       uint32_t pk[kKT / 2];
 #pragma unroll
       for (int i = 0; i < kKT / 2; ++i) {
         const float p0 = ex2(s[2 * i] - m_used);
         const float p1 = ex2(s[2 * i + 1] - m_used);
-        pk[i] = pack_bf16x2(p0, p1);
-        const float2 rp = unpack_bf16x2(pk[i]);
+        pk[i] = pack2(p0, p1, fresh);
+        const float2 rp = fresh ? unpack_f16x2(pk[i]) : unpack_bf16x2(pk[i]);
         l_sum += rp.x + rp.y;
       }
       if (j > 0) {
@@ -356,21 +415,23 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-static bool tmap_rows_dh(CUtensorMap* m, const void* base, uint64_t rows, int dh) {
+static bool tmap_rows_dh(CUtensorMap* m, const void* base, uint64_t rows, int dh, bool f16) {
   auto enc = encode_fn();
   if (!enc || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
   cuuint64_t dims[2] = {(cuuint64_t)dh, rows};
   cuuint64_t strides[1] = {(cuuint64_t)dh * 2};
   cuuint32_t box[2] = {64, 128};
   cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int DH>
 static qwen_status launch_dh(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                             const AttnArgs& a, cudaStream_t st) {
+                             const CUtensorMap& k16, const CUtensorMap& v16, const AttnArgs& a,
+                             cudaStream_t st) {
   auto kern = attn_prefill_kernel<DH>;
   static bool attr = false;
   if (!attr) {
@@ -381,26 +442,30 @@ static qwen_status launch_dh(const CUtensorMap& q, const CUtensorMap& k, const C
   }
   const int n_qt = (a.T + kQT - 1) / kQT;
   const int grid = n_qt * a.B * a.Hq;
-  launch_k(kern, dim3(grid), dim3(kAttnThreads), AttnCfg<DH>::SMEM_BYTES, st, q, k, v, a);
+  launch_k(kern, dim3(grid), dim3(kAttnThreads), AttnCfg<DH>::SMEM_BYTES, st, q, k, v, k16, v16,
+           a);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
 // q [B][Hq][T][dh], caches [B][Hkv][max_seq][dh], out [B*T][Hq*dh].
-qwen_status attention_prefill(const bf16* q, const bf16* k_cache, const bf16* v_cache,
-                              const int32_t* slot0, f16* out, int B, int T, int Hq, int Hkv,
-                              int dh, int max_seq, int* err, cudaStream_t st) {
+qwen_status attention_prefill(const f16* q, const bf16* k_cache, const bf16* v_cache,
+                              const f16* k16, const f16* v16, const int32_t* slot0, f16* out,
+                              int B, int T, int Hq, int Hkv, int dh, int max_seq, int* err,
+                              cudaStream_t st) {
   if (B == 0 || T == 0) return QWEN_OK;
-  CUtensorMap tq, tk, tv;
-  if (!tmap_rows_dh(&tq, q, (uint64_t)B * Hq * T, dh)) return QWEN_ERR_CUDA;
-  if (!tmap_rows_dh(&tk, k_cache, (uint64_t)B * Hkv * max_seq, dh)) return QWEN_ERR_CUDA;
-  if (!tmap_rows_dh(&tv, v_cache, (uint64_t)B * Hkv * max_seq, dh)) return QWEN_ERR_CUDA;
+  CUtensorMap tq, tk, tv, tk16, tv16;
+  if (!tmap_rows_dh(&tq, q, (uint64_t)B * Hq * T, dh, true)) return QWEN_ERR_CUDA;
+  if (!tmap_rows_dh(&tk, k_cache, (uint64_t)B * Hkv * max_seq, dh, false)) return QWEN_ERR_CUDA;
+  if (!tmap_rows_dh(&tv, v_cache, (uint64_t)B * Hkv * max_seq, dh, false)) return QWEN_ERR_CUDA;
+  if (!tmap_rows_dh(&tk16, k16, (uint64_t)B * Hkv * T, dh, true)) return QWEN_ERR_CUDA;
+  if (!tmap_rows_dh(&tv16, v16, (uint64_t)B * Hkv * T, dh, true)) return QWEN_ERR_CUDA;
   AttnArgs a;
   a.B = B; a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.max_seq = max_seq;
   a.slot0 = slot0; a.out = out; a.err = err;
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)dh);
-  if (dh == 128) return launch_dh<128>(tq, tk, tv, a, st);
-  if (dh == 64) return launch_dh<64>(tq, tk, tv, a, st);
+  if (dh == 128) return launch_dh<128>(tq, tk, tv, tk16, tv16, a, st);
+  if (dh == 64) return launch_dh<64>(tq, tk, tv, tk16, tv16, a, st);
   return QWEN_ERR_UNSUPPORTED;
 }
 

@@ -25,30 +25,40 @@ constexpr int kDBM = 128;
 constexpr int kDBK = 64;
 constexpr int kDThreads = 192;
 
-template <int BP>
+// Epilogues of the decode GEMM: FP32 split partials, or (one split only) the
+// SwiGLU of an interleaved gate/up tile written straight to H.
+enum DecEpi : int { DEC_PARTIAL = 0, DEC_SWIGLU = 1 };
+
+template <int BP, int EPI>
 struct DecCfg {
   static constexpr int A_BYTES = kDBM * kDBK * 2;  // 16 KB of weight per stage
   static constexpr int B_BYTES = BP * kDBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 12 ? 12 : (200 * 1024) / STAGE_BYTES;
-  static constexpr int TMEM_COLS = 2 * BP < 32 ? 32 : 2 * BP;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+  // gate half of a tile handed to the up warps: [64 rows][BP] FP32
+  static constexpr int XCH_BYTES = EPI == DEC_SWIGLU ? 64 * BP * 4 : 0;
+  static constexpr int RING = (200 * 1024 - XCH_BYTES) / STAGE_BYTES;
+  static constexpr int STAGES = RING > 12 ? 12 : RING;
+  // the epilogue reads 32 columns at a time, so with BP = 16 the second
+  // accumulator's read reaches column 47: allocate at least 64 columns
+  static constexpr int TMEM_COLS = 2 * BP < 64 ? 64 : 2 * BP;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + XCH_BYTES + 256;
 };
 
 }  // namespace
 
-template <int BP>
+template <int BP, int EPI>
 __global__ void __launch_bounds__(kDThreads, 1)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        int B, int N, int K, int splits, uint32_t idesc, int w_static,
-                       float* __restrict__ part, int* err) {
-  using C = DecCfg<BP>;
+                       float* __restrict__ part, f16* __restrict__ hout, int* err) {
+  using C = DecCfg<BP, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + C::STAGES * C::A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+  float* xch = reinterpret_cast<float*>(sB + C::STAGES * C::B_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES + C::XCH_BYTES);
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
@@ -182,23 +192,63 @@ __global__ void __launch_bounds__(kDThreads, 1)
       const int acc = local & 1;
       if (!mbar_wait(&tfull[acc], (local >> 1) & 1, abort_flag, err)) break;
       tc_fence_after();
-      // part[s][b][n]: for each batch column the 32 lanes (consecutive weight
-      // rows n) write 128 contiguous bytes
       const int n = n0 + q * 32 + lane;
-      float* dst = part + (size_t)s * B * N + n;
+      if constexpr (EPI == DEC_PARTIAL) {
+        // part[s][b][n]: for each batch column the 32 lanes (consecutive
+        // weight rows n) write 128 contiguous bytes
+        float* dst = part + (size_t)s * B * N + n;
 #pragma unroll 1
-      for (int c = 0; c < BP; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BP + c, r);
-        tmem_ld_wait();
-        if (n < N) {
+        for (int c = 0; c < BP; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BP + c, r);
+          tmem_ld_wait();
+          if (n < N) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c + i < B) dst[(size_t)(c + i) * N] = __uint_as_float(r[i]);
+            for (int i = 0; i < 32; ++i)
+              if (c + i < B) dst[(size_t)(c + i) * N] = __uint_as_float(r[i]);
+          }
         }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+      } else {
+        // tile rows 0-63 are gate rows (warps q = 0, 1), rows 64-127 the up rows
+        // of the same 64 features (q = 2, 3): gate values go through shared
+        // memory, the up warps form h = SiLU(gate) * up and store H[b][f]
+        const int f_tile = (n0 >> 7) * 64;  // first feature of this tile
+        if (q < 2) {
+#pragma unroll 1
+          for (int c = 0; c < BP; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BP + c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i)  // xch holds BP columns (16 when BP = 16)
+              if (c + i < BP) xch[(c + i) * 64 + q * 32 + lane] = __uint_as_float(r[i]);
+          }
+        }
+        asm volatile("bar.sync 2, 128;" ::: "memory");
+        if (q >= 2) {
+          const int fr = (q - 2) * 32 + lane;  // feature within the tile
+          const int fdim = N / 2;
+#pragma unroll 1
+          for (int c = 0; c < BP; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BP + c, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (c + i < B && f_tile + fr < fdim) {
+                const float gv = xch[(c + i) * 64 + fr];
+                hout[(size_t)(c + i) * fdim + f_tile + fr] =
+                    __float2half_rn(silu_f(gv) * __uint_as_float(r[i]));
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+        asm volatile("bar.sync 2, 128;" ::: "memory");  // xch free for the next tile
       }
-      tc_fence_before();
-      mbar_arrive(&tempty[acc]);
     }
   }
   tc_fence_before();
@@ -222,6 +272,7 @@ __global__ void reduce_resid_kernel(const float* __restrict__ part, int splits, 
   if (i >= N * B) return;
   const size_t plane = (size_t)B * N;
   float acc = 0.f;
+#pragma unroll 8
   for (int s = 0; s < splits; ++s) acc += part[s * plane + i];
   acc += resid32 ? resid32[i] : __bfloat162float(resid[i]);
   if (out) out[i] = __float2bfloat16_rn(acc);
@@ -304,7 +355,7 @@ __global__ void reduce_qkv_kernel(const float* __restrict__ part, int splits, in
   }
   bf16* dst;
   if (kind == 0) {
-    dst = p.q_out + ((size_t)b * p.Hq + head) * DH;  // T == 1
+    dst = static_cast<bf16*>(p.q_out) + ((size_t)b * p.Hq + head) * DH;  // T == 1, BF16
   } else {
     const int slot = p.slot0[b];
     if (slot < 0 || slot >= p.max_seq) {
@@ -316,6 +367,58 @@ __global__ void reduce_qkv_kernel(const float* __restrict__ part, int splits, in
   }
 #pragma unroll
   for (int e = 0; e < PER; ++e) dst[lane + 32 * e] = __float2bfloat16_rn(v[e]);
+}
+
+// One CTA per sequence row b: R[b] = sum_s part[s][b] + residual (FP32 out),
+// then Z[b] = gamma * R[b] / sqrt(mean(R[b]^2) + eps) as the FP16 operand of
+// the next projection: the O-projection reduction fused with RMSNorm_2.
+template <int PER>
+__global__ void __launch_bounds__(1024) reduce_resid_norm_kernel(
+    const float* __restrict__ part, int splits, int B, int N, const bf16* __restrict__ resid,
+    const float* __restrict__ resid32, float* __restrict__ out32, const bf16* __restrict__ gamma,
+    float eps, f16* __restrict__ z) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[32];
+  const int b = blockIdx.x;
+  const size_t plane = (size_t)B * N;
+  const size_t row = (size_t)b * N;
+  float v[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int n = threadIdx.x + 1024 * j;
+    v[j] = 0.f;
+    if (n < N) v[j] = resid32 ? resid32[row + n] : __bfloat162float(resid[row + n]);
+  }
+#pragma unroll 4
+  for (int s = 0; s < splits; ++s) {
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int n = threadIdx.x + 1024 * j;
+      if (n < N) v[j] += part[s * plane + row + n];
+    }
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int n = threadIdx.x + 1024 * j;
+    if (n < N) {
+      out32[row + n] = v[j];
+      ss = fmaf(v[j], v[j], ss);
+    }
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < 32; ++w) tot += red[w];
+  const float rstd = rsqrtf(tot / (float)N + eps);
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int n = threadIdx.x + 1024 * j;
+    if (n < N) z[row + n] = __float2half_rn(__bfloat162float(gamma[n]) * (v[j] * rstd));
+  }
 }
 
 __global__ void reduce_f32_kernel(const float* __restrict__ part, int splits, int B, int N,
@@ -404,30 +507,31 @@ size_t decode_part_bytes(const qwen_layer_config& c, int B) {
   return m;
 }
 
-template <int BP>
+template <int BP, int EPI>
 static qwen_status launch_dec(const CUtensorMap& tw, const CUtensorMap& tx, int B, int N, int K,
-                              int splits, bool op_f16, bool w_static, float* part, int* err,
-                              cudaStream_t st) {
-  auto kern = gemm_decode_kernel<BP>;
+                              int splits, bool op_f16, bool w_static, float* part, f16* hout,
+                              int* err, cudaStream_t st) {
+  using C = DecCfg<BP, EPI>;
+  auto kern = gemm_decode_kernel<BP, EPI>;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DecCfg<BP>::SMEM_BYTES) != cudaSuccess)
+                             C::SMEM_BYTES) != cudaSuccess)
       return QWEN_ERR_CUDA;
     attr = true;
   }
   const int units = ((N + kDBM - 1) / kDBM) * splits;
   const int sms = device_sm_count();
   const int grid = units < sms ? units : sms;
-  launch_k(kern, dim3(grid), dim3(kDThreads), DecCfg<BP>::SMEM_BYTES, st, tw, tx, B, N, K, splits,
-           idesc_f32acc(kDBM, BP, op_f16), w_static ? 1 : 0, part, err);
+  launch_k(kern, dim3(grid), dim3(kDThreads), C::SMEM_BYTES, st, tw, tx, B, N, K, splits,
+           idesc_f32acc(kDBM, BP, op_f16), w_static ? 1 : 0, part, hout, err);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
 qwen_status gemm_decode_splitk(const void* W, const void* X, int ldx, int B, int N, int K,
                                int splits, bool op_f16, float* part, int* err, cudaStream_t st,
-                               bool w_static) {
+                               bool w_static, f16* swiglu_out) {
   if (B <= 0 || B > 256) return QWEN_ERR_UNSUPPORTED;
   if ((K & 7) || splits < 1) return QWEN_ERR_UNSUPPORTED;
   const int bp = pad_batch(B);
@@ -435,11 +539,15 @@ qwen_status gemm_decode_splitk(const void* W, const void* X, int ldx, int B, int
   if (!tmap2d(&tw, W, (uint64_t)N, (uint64_t)K, (uint64_t)K, kDBM, op_f16)) return QWEN_ERR_CUDA;
   if (!tmap2d(&tx, X, (uint64_t)B, (uint64_t)K, (uint64_t)ldx, bp, op_f16)) return QWEN_ERR_CUDA;
   switch (bp) {
-    case 16: return launch_dec<16>(tw, tx, B, N, K, splits, op_f16, w_static, part, err, st);
-    case 32: return launch_dec<32>(tw, tx, B, N, K, splits, op_f16, w_static, part, err, st);
-    case 64: return launch_dec<64>(tw, tx, B, N, K, splits, op_f16, w_static, part, err, st);
-    case 128: return launch_dec<128>(tw, tx, B, N, K, splits, op_f16, w_static, part, err, st);
-    default: return launch_dec<256>(tw, tx, B, N, K, splits, op_f16, w_static, part, err, st);
+    case 16: return swiglu_out ? launch_dec<16, DEC_SWIGLU>(tw, tx, B, N, K, 1, op_f16, w_static, nullptr, swiglu_out, err, st) : launch_dec<16, DEC_PARTIAL>(tw, tx, B, N, K, splits, op_f16, w_static, part, nullptr, err, st);
+    case 32: return swiglu_out ? launch_dec<32, DEC_SWIGLU>(tw, tx, B, N, K, 1, op_f16, w_static, nullptr, swiglu_out, err, st) : launch_dec<32, DEC_PARTIAL>(tw, tx, B, N, K, splits, op_f16, w_static, part, nullptr, err, st);
+    case 64: return swiglu_out ? launch_dec<64, DEC_SWIGLU>(tw, tx, B, N, K, 1, op_f16, w_static, nullptr, swiglu_out, err, st) : launch_dec<64, DEC_PARTIAL>(tw, tx, B, N, K, splits, op_f16, w_static, part, nullptr, err, st);
+    case 128: return swiglu_out ? launch_dec<128, DEC_SWIGLU>(tw, tx, B, N, K, 1, op_f16, w_static, nullptr, swiglu_out, err, st) : launch_dec<128, DEC_PARTIAL>(tw, tx, B, N, K, splits, op_f16, w_static, part, nullptr, err, st);
+    default:
+      return swiglu_out ? launch_dec<256, DEC_SWIGLU>(tw, tx, B, N, K, 1, op_f16, w_static, nullptr,
+                                                      swiglu_out, err, st)
+                        : launch_dec<256, DEC_PARTIAL>(tw, tx, B, N, K, splits, op_f16, w_static,
+                                                       part, nullptr, err, st);
   }
 }
 
@@ -469,6 +577,20 @@ qwen_status reduce_qkv(const float* part, int splits, int B, int Nqkv, const Qkv
   else
     launch_k(reduce_qkv_kernel<64>, dim3(blocks_for(threads, 128)), dim3(128), 0, st, part, splits,
              B, Nqkv, p, err);
+  count_launches();
+  return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
+}
+
+qwen_status reduce_resid_norm(const float* part, int splits, int B, int N, const bf16* resid,
+                              const float* resid32, float* out32, const bf16* gamma, float eps,
+                              f16* z, cudaStream_t st) {
+  if (N > 1024 * 8) return QWEN_ERR_UNSUPPORTED;
+  if (N <= 1024 * 4)
+    launch_k(reduce_resid_norm_kernel<4>, dim3(B), dim3(1024), 0, st, part, splits, B, N, resid,
+             resid32, out32, gamma, eps, z);
+  else
+    launch_k(reduce_resid_norm_kernel<8>, dim3(B), dim3(1024), 0, st, part, splits, B, N, resid,
+             resid32, out32, gamma, eps, z);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }

@@ -29,9 +29,12 @@ struct QkvParams {
   const float2* rope;      // [max_position][dh/2] (cos, sin)
   const int32_t* positions;  // [M]
   const int32_t* slot0;      // [B]: cache slot of the sequence's first new token
-  __nv_bfloat16* q_out;    // [B][Hq][T][dh]
+  void* q_out;             // [B][Hq][T][dh], FP16 when q_f16 else BF16
+  int q_f16;
   __nv_bfloat16* k_cache;  // [B][Hkv][max_seq][dh]
   __nv_bfloat16* v_cache;
+  __half* k16;             // optional FP16 copies of this call's K/V rows,
+  __half* v16;             // [B][Hkv][T][dh] (prefill attention reads them)
   int T, Hq, Hkv, dh, max_seq, max_position;
   float eps;
 };
@@ -95,8 +98,11 @@ qwen_status gemm_tc(const void* A, int lda, const void* B, int ldb, int M, int N
 // Causal GQA flash attention for prefill: q [B][Hq][T][dh], caches
 // [B][Hkv][max_seq][dh], out [B*T][Hq*dh]; query t of sequence b sits in cache
 // slot slot0[b] + t and sees slots <= its own.
-qwen_status attention_prefill(const __nv_bfloat16* q, const __nv_bfloat16* k_cache,
-                              const __nv_bfloat16* v_cache, const int32_t* slot0,
+// q and the fresh K/V copies (k16/v16: this call's T rows per (b, KV head)) are
+// FP16; key tiles that reach below slot0[b] are read from the BF16 cache.
+qwen_status attention_prefill(const __half* q, const __nv_bfloat16* k_cache,
+                              const __nv_bfloat16* v_cache, const __half* k16,
+                              const __half* v16, const int32_t* slot0,
                               __half* out, int B, int T, int Hq, int Hkv, int dh,
                               int max_seq, int* err, cudaStream_t st);
 

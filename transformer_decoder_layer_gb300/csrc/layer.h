@@ -15,7 +15,7 @@ struct PackedLayout {
 };
 
 struct WorkspaceLayout {
-  size_t xh, q, attn, r32, z, h;
+  size_t xh, q, k16, v16, attn, r32, z, h;
   // MoE
   size_t z32, logits, topk_idx, topk_w, counts, offsets, perm, inv, zp, hp, yp;
   // decode (T == 1)
@@ -51,7 +51,8 @@ PackedLayout packed_layout(const qwen_layer_config& c);
 WorkspaceLayout workspace_layout(const qwen_layer_config& c, int B, int T);
 
 QkvParams make_qkv_params(const qwen_layer_s* L, const int32_t* positions, const int32_t* slot0,
-                          __nv_bfloat16* q, __nv_bfloat16* kc, __nv_bfloat16* vc, int T);
+                          void* q, bool q_f16, __nv_bfloat16* kc, __nv_bfloat16* vc,
+                          __half* k16, __half* v16, int T);
 
 // x (BF16) or x32 (FP32) is the input; y (BF16) and/or y32 (FP32) the output.
 qwen_status layer_prefill(qwen_layer_s* L, const __nv_bfloat16* x, const float* x32,
@@ -83,13 +84,19 @@ void decode_attn_plan(const qwen_layer_config& c, int B, int* splits);
 // W [N, K], X [B, K] (row stride ldx).
 // w_static: W is never written by the kernel launched just before (the packed
 // layer weights), so its first tiles may be fetched before waiting on it.
+// swiglu_out: W is an interleaved gate/up weight (64-row blocks); run with one
+// split and write H[b][f] = SiLU(gate) * up (FP16) instead of partials.
 qwen_status gemm_decode_splitk(const void* W, const void* X, int ldx, int B, int N, int K,
                                int splits, bool op_f16, float* part, int* err, cudaStream_t st,
-                               bool w_static = false);
+                               bool w_static = false, __half* swiglu_out = nullptr);
 
 // Reductions over the splits followed by the step's epilogue.
 qwen_status reduce_resid(const float* part, int splits, int B, int N, const __nv_bfloat16* resid,
                          const float* resid32, __nv_bfloat16* out, float* out32, cudaStream_t st);
+// R = sum of splits + residual (FP32, out32), then Z = RMSNorm(R) (FP16).
+qwen_status reduce_resid_norm(const float* part, int splits, int B, int N,
+                              const __nv_bfloat16* resid, const float* resid32, float* out32,
+                              const __nv_bfloat16* gamma, float eps, __half* z, cudaStream_t st);
 qwen_status reduce_swiglu(const float* part, int splits, int B, int f, __half* h,
                           cudaStream_t st);
 qwen_status reduce_qkv(const float* part, int splits, int B, int Nqkv, const QkvParams& p,

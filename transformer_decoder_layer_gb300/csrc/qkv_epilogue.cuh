@@ -66,28 +66,33 @@ __device__ __forceinline__ void qkv_head_finish(float (&v)[DH], int m, int head,
     }
   }
   const int b = m / p.T, t = m - (m / p.T) * p.T;
-  bf16* dst;
-  if (kind == 0) {
-    dst = p.q_out + (((size_t)b * p.Hq + head) * p.T + t) * DH;
-  } else {
-    const int slot = p.slot0[b] + t;
-    if (slot < 0 || slot >= p.max_seq) {
-      record_error(err, QWEN_ERR_RANGE);
-      return;
-    }
-    const int g = kind == 1 ? head - p.Hq : head - p.Hq - p.Hkv;
-    dst = (kind == 1 ? p.k_cache : p.v_cache) + (((size_t)b * p.Hkv + g) * p.max_seq + slot) * DH;
-  }
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  auto store = [&](void* dst, bool f16_out) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int i = 0; i < DH / 8; ++i) {
-    uint4 o;
-    o.x = pack_bf16x2(v[8 * i], v[8 * i + 1]);
-    o.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-    o.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-    o.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
-    d4[i] = o;
+    for (int i = 0; i < DH / 8; ++i) {
+      uint4 o;
+      o.x = pack2(v[8 * i], v[8 * i + 1], f16_out);
+      o.y = pack2(v[8 * i + 2], v[8 * i + 3], f16_out);
+      o.z = pack2(v[8 * i + 4], v[8 * i + 5], f16_out);
+      o.w = pack2(v[8 * i + 6], v[8 * i + 7], f16_out);
+      d4[i] = o;
+    }
+  };
+  if (kind == 0) {
+    store(static_cast<uint16_t*>(p.q_out) + (((size_t)b * p.Hq + head) * p.T + t) * DH,
+          p.q_f16 != 0);
+    return;
   }
+  const int slot = p.slot0[b] + t;
+  if (slot < 0 || slot >= p.max_seq) {
+    record_error(err, QWEN_ERR_RANGE);
+    return;
+  }
+  const int g = kind == 1 ? head - p.Hq : head - p.Hq - p.Hkv;
+  store((kind == 1 ? p.k_cache : p.v_cache) + (((size_t)b * p.Hkv + g) * p.max_seq + slot) * DH,
+        false);
+  __half* fresh = kind == 1 ? p.k16 : p.v16;
+  if (fresh) store(fresh + (((size_t)b * p.Hkv + g) * p.T + t) * DH, true);
 }
 
 }  // namespace qwen
