@@ -347,6 +347,50 @@ def host_cores():
         return os.cpu_count() or 1
 
 
+# ------------------------------------------------------------------ profiling
+
+def profile_run(args):
+    """Eager steps with nothing else on the device: per decode step the kernels
+    launch in stage order (norm1, QKV, QKV finish, attention, merge, O, O finish
+    + norm2, gate/up + SwiGLU, down, down finish); a prefill step launches
+    norm1, QKV, attention, O, norm2, gate/up, down."""
+    import torch
+
+    import synth
+    import transformer_decoder_layer_gb300 as q
+    dev = torch.device("cuda")
+    if args.profile == "decode":
+        shape = synth.QWEN25_7B
+        w = {k: v.to(dev) for k, v in synth.layer_weights(shape, "bench").items()}
+        B = args.batch
+        cfg = q.LayerConfig(shape, max_tokens=B, max_batch=B, max_seq=CACHE_FILLED + 1,
+                            max_position=CACHE_FILLED + 1)
+        layer = q.Layer(cfg, w)
+        bench = DecodeBench(q, torch, shape, B, layer, CACHE_FILLED + 1)
+        for _ in range(args.steps):
+            bench.step()
+    else:
+        shape = synth.QWEN3_8B
+        T = args.tokens
+        w = {k: v.to(dev) for k, v in synth.layer_weights(shape, "bench_prefill").items()}
+        cfg = q.LayerConfig(shape, max_tokens=T, max_batch=1, max_seq=T, max_position=T)
+        layer = q.Layer(cfg, w)
+        x = synth.activations([1, T, shape.d], "bench_prefill", f"x1_{T}").to(dev)
+        kc = torch.zeros((1, shape.n_kv_heads, T, shape.head_dim), dtype=torch.bfloat16,
+                         device=dev)
+        vc = torch.zeros_like(kc)
+        pos = torch.arange(T, dtype=torch.int32, device=dev)
+        start = torch.zeros(1, dtype=torch.int32, device=dev)
+        y = torch.empty_like(x)
+        ws = layer.workspace(1, T)
+        for _ in range(args.steps):
+            layer.prefill(x, pos, start, kc, vc, out=y, workspace=ws)
+    torch.cuda.synchronize()
+    assert layer.poll_error() == 0
+    print(json.dumps({"profile": args.profile, "steps": args.steps,
+                      "launches": int(q.launch_count())}))
+
+
 # ------------------------------------------------------------------ main
 
 def main():
@@ -359,7 +403,13 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
+                    help="run --steps untimed eager steps of one workload and exit "
+                         "(a short, deterministic launch sequence for a profiler capture)")
+    ap.add_argument("--tokens", type=int, default=4096, help="prefill length for --profile")
     args = ap.parse_args()
+    if args.profile:
+        return profile_run(args)
     args.warmup = max(args.warmup, 3)
 
     import synth
