@@ -72,6 +72,16 @@ def test_qwen3_style_dh128_prefill():
     assert_parity(v, vr, what="V cache")
 
 
+def test_qwen3_style_dh128_chunked_prefill():
+    """dh=128 chunk appended to filled caches (slots 45 and 200): keys come from
+    the BF16 cache, partly written by this call."""
+    y, ref, k, kr, v, vr = _prefill_case(QWEN3_SMALL, "q3chunk", 2, 150, cache_start=[200, 45],
+                                         max_seq=400, prefilled=[200, 45])
+    assert_parity(y, ref, what="Y")
+    assert_parity(k, kr, what="K cache")
+    assert_parity(v, vr, what="V cache")
+
+
 def test_qwen25_style_bias_prefill():
     """qkv bias, no QK-norm, G=7, dh=128."""
     shape = synth.LayerConfig(d=896, n_q_heads=14, n_kv_heads=2, head_dim=128, ffn=1792,

@@ -8,24 +8,31 @@
 // repeat) and tiles above the diagonal are skipped.  §12 of the Qwen3 page: the
 // [T,T] probability matrix is never written to memory.
 //
-// Operands: the queries and the keys/values this call computed are FP16 (the
-// QKV epilogue writes FP16 copies of the new K/V rows besides the BF16 cache),
-// so S = Q K^T and O += P V run on FP16 tensor-core operands with P in FP16.
-// Key tiles that reach below the sequence's first new slot (chunked prefill
-// onto a filled cache) come from the BF16 cache instead; for those the
-// softmax warps convert Q to a BF16 copy once and P is rounded to BF16.
+// One CTA = one sequence b, one KV group g, two query heads of that group (A
+// and B; B absent for the last head of an odd-sized group) and one tile of 128
+// query rows.  Both heads read every staged K/V tile, and the two heads form
+// two independent chains that keep the tensor pipe busy while the other head's
+// softmax runs:
+//   warp 0      TMA: Q_A, Q_B once, then K and V tiles of 128 keys (2 stages each)
+//   warp 1      TMEM allocator + MMA issuer, per key tile j:
+//                 O_A += P_A V_j, S_A = Q_A K_{j+1}^T, O_B += P_B V_j, S_B = ...
+//               S_x lives in TMEM (128 columns per head); the softmax writes P_x
+//               back over the first 64 of them and the P.V MMA takes its A
+//               operand straight from TMEM.  S_x(j+1) is issued only after
+//               O_x += P_x(j) V_j has completed (it overwrites P_x(j)).
+//   warps 2-5   softmax of head A, warps 6-9 softmax of head B: one thread per
+//               query row; online max / sum in FP32 with the rescale of O
+//               deferred until the running max grows by 2^8; a quarter of the
+//               exponentials run on the FMA pipe (fast_exp2.cuh), the rest on
+//               the special-function unit; final O / l.
 //
-// One CTA = one (sequence b, query head h, tile of 128 query rows).
-//   warp 0      TMA: Q tile once, then K/V tiles of 128 keys (2-stage ring)
-//   warp 1      TMEM allocator + MMA issuer:
-//                 S_j = Q K_j^T  -> TMEM (two S buffers, 128 cols each)
-//                 O  += P_j V_j  -> TMEM (dh cols), P_j from shared memory,
-//                 V_j read MN-major (dh contiguous) straight from the cache tile
-//   warps 2..5  softmax: thread = query row; online max/sum in FP32 with the
-//               rescale of O deferred until the max grows by 2^8; P -> FP16
-//               (BF16 for cache tiles) in the 128-byte-swizzled K-major layout
-//               the MMA reads; final O / l.
+// Operands: when the sequence starts at slot 0 every key comes from this call,
+// so Q, K, V and P are FP16 (the QKV epilogue writes FP16 copies of the new K/V
+// rows besides the BF16 cache).  A chunk appended to a filled cache reads the
+// BF16 cache instead; then Q is converted to BF16 in shared memory once and P
+// is rounded to BF16.
 #include "common.cuh"
+#include "fast_exp2.cuh"
 #include "internal.h"
 
 #include <cudaTypedefs.h>
@@ -34,10 +41,12 @@ namespace qwen {
 
 namespace {
 
-constexpr int kQT = 128;  // query rows per CTA
-constexpr int kKT = 128;  // keys per tile
-constexpr int kAttnThreads = 192;
+constexpr int kQT = 128;      // query rows per CTA
+constexpr int kKT = 128;      // keys per tile
+constexpr int kStages = 2;    // K and V ring depth
+constexpr int kAttnThreads = 320;
 constexpr float kRescaleLog2 = 8.0f;  // defer O rescale until the max grew by 2^8
+constexpr int kPolyPer16 = 4;         // exponentials per 16 evaluated on the FMA pipe
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -45,18 +54,98 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 128 consecutive TMEM columns of this warp's 32 lanes -> registers; the wait
+// for the load sits in the same statement, so no use can move above it.
+__device__ __forceinline__ void tmem_ld128_wait(uint32_t taddr, uint32_t (&r)[128]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {"
+      "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+      "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, "
+      "%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, "
+      "%80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95, "
+      "%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, "
+      "%112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127"
+      "}, [%128];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]),
+        "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]),
+        "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]),
+        "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]),
+        "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]),
+        "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]),
+        "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]),
+        "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]),
+        "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+      "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31"
+      "}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16: A is M rows (TMEM lanes) x 16
+// 16-bit elements packed two per 32-bit column.
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 template <int DH>
 struct AttnCfg {
   static constexpr int TILE_BYTES = kKT * DH * 2;  // one [128 x DH] 16-bit tile
-  static constexpr int Q_OFF = 0;                            // Q (FP16)
-  static constexpr int QB_OFF = TILE_BYTES;                  // BF16 copy of Q
-  static constexpr int P_OFF = 2 * TILE_BYTES;               // P [128 x 128] 16-bit
-  static constexpr int K_OFF = P_OFF + kQT * kKT * 2;        // 2 stages
-  static constexpr int V_OFF = K_OFF + 2 * TILE_BYTES;       // 2 stages
-  static constexpr int BAR_OFF = V_OFF + 2 * TILE_BYTES;
+  static constexpr int Q_OFF = 0;                  // Q_A, Q_B
+  static constexpr int K_OFF = 2 * TILE_BYTES;     // kStages tiles
+  static constexpr int V_OFF = K_OFF + kStages * TILE_BYTES;
+  static constexpr int BAR_OFF = V_OFF + kStages * TILE_BYTES;
   static constexpr int SMEM_BYTES = 1024 + BAR_OFF + 256;
-  static constexpr int S_COL0 = 0;    // S buffers at columns 0 and 128
-  static constexpr int O_COL = 256;   // O accumulator
+  // TMEM columns: S_A [0,128), S_B [128,256) (P_x over the first 64 of S_x),
+  // O_A [256, 256+DH), O_B [256+DH, 256+2DH)
+  static constexpr int S_COL = 0;
+  static constexpr int O_COL = 256;
   static constexpr int TMEM_COLS = 512;
 };
 
@@ -84,52 +173,60 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem + C::Q_OFF;
-  uint8_t* sQb = smem + C::QB_OFF;
-  uint8_t* sP = smem + C::P_OFF;
   uint8_t* sK = smem + C::K_OFF;
   uint8_t* sV = smem + C::V_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;    // [2]
-  uint64_t* v_full = bars + 3;    // [2]
-  uint64_t* kv_empty = bars + 5;  // [2]
-  uint64_t* s_full = bars + 7;    // [2]
-  uint64_t* s_free = bars + 9;    // [2]
-  uint64_t* p_full = bars + 11;
-  uint64_t* o_done = bars + 12;
-  uint64_t* qb_ready = bars + 13;  // BF16 copy of Q written (chunked prefill only)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* q_conv = bars + 1;    // BF16 conversion of Q done (appended chunks only)
+  uint64_t* k_full = bars + 2;    // [kStages]
+  uint64_t* k_empty = bars + 4;   // [kStages]
+  uint64_t* v_full = bars + 6;    // [kStages]
+  uint64_t* v_empty = bars + 8;   // [kStages]
+  uint64_t* s_full = bars + 10;   // [2] per head
+  uint64_t* p_full = bars + 12;   // [2] per head
+  uint64_t* o_done = bars + 14;   // [2] per head
+  uint64_t* mma_idle = bars + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // heaviest (last) query tiles first
+  // work unit: heaviest (last) query tiles first
+  const int gs = a.Hq / a.Hkv;
+  const int npair = (gs + 1) >> 1;
   const int n_qt = (a.T + kQT - 1) / kQT;
-  const int bh_count = a.B * a.Hq;
-  const int qt = n_qt - 1 - blockIdx.x / bh_count;
-  const int bh = blockIdx.x % bh_count;
-  const int b = bh / a.Hq, h = bh - b * a.Hq;
-  const int g = h / (a.Hq / a.Hkv);
+  const int per_qt = a.B * a.Hkv * npair;
+  const int qt = n_qt - 1 - (int)blockIdx.x / per_qt;
+  int u = (int)blockIdx.x % per_qt;
+  const int pr = u % npair;
+  u /= npair;
+  const int g = u % a.Hkv;
+  const int b = u / a.Hkv;
+  const int hA = g * gs + 2 * pr;
+  const int nq = (2 * pr + 1 < gs) ? 2 : 1;  // heads in this CTA
   const int t0 = qt * kQT;
   const int s0 = a.slot0[b];
-  const int q_last = min(t0 + kQT, a.T) - 1;   // last valid query row of the tile
-  const int kmax = s0 + q_last;                // largest visible key slot
-  const int n_kv = kmax / kKT + 1;             // key tiles 0..n_kv-1
-  const int q_row0 = (b * a.Hq + h) * a.T + t0;        // row in the Q view
-  const int kv_row0 = (b * a.Hkv + g) * a.max_seq;     // row in the cache view
-  const int kv16_row0 = (b * a.Hkv + g) * a.T - s0;    // + key slot = row in the fresh view
+  const bool fresh = s0 == 0;                 // all keys are this call's: FP16 operands
+  const int q_last = min(t0 + kQT, a.T) - 1;  // last valid query row of the tile
+  const int kmax = s0 + q_last;               // largest visible key slot
+  const int n_kv = kmax / kKT + 1;            // key tiles 0..n_kv-1
+  // row of key slot 0 in the K/V view (FP16 copies of this call, or the cache)
+  const int kv_row0 = fresh ? (b * a.Hkv + g) * a.T : (b * a.Hkv + g) * a.max_seq;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    mbar_init(q_conv, 128 * nq);
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
       mbar_init(&v_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 128);
+      mbar_init(&v_empty[i], 1);
     }
-    mbar_init(p_full, 128);
-    mbar_init(o_done, 1);
-    mbar_init(qb_ready, 128);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 128);
+      mbar_init(&o_done[x], 1);
+    }
+    mbar_init(mma_idle, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -144,216 +241,211 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
+      const CUtensorMap* mk = fresh ? &tmK16 : &tmK;
+      const CUtensorMap* mv = fresh ? &tmV16 : &tmV;
       tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
-      tma_prefetch_desc(&tmK16);
-      tma_prefetch_desc(&tmV16);
-      mbar_arrive_expect_tx(q_full, C::TILE_BYTES);
+      tma_prefetch_desc(mk);
+      tma_prefetch_desc(mv);
+      mbar_arrive_expect_tx(q_full, nq * C::TILE_BYTES);
+      for (int x = 0; x < nq; ++x) {
 #pragma unroll
-      for (int c = 0; c < DH / 64; ++c)
-        tma_load_2d(sQ + c * kQT * 128, &tmQ, q_full, c * 64, q_row0);
+        for (int c = 0; c < DH / 64; ++c)
+          tma_load_2d(sQ + x * C::TILE_BYTES + c * kQT * 128, &tmQ, q_full, c * 64,
+                      (b * a.Hq + hA + x) * a.T + t0);
+      }
+      int nk = 0, nv = 0;  // tiles issued
       for (int j = 0; j < n_kv; ++j) {
-        const int st = j & 1;
-        if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1u, abort_flag, a.err)) break;
-        // tiles entirely at or above the first new slot come from the FP16
-        // copies of this call's rows, the others from the BF16 cache
-        const bool fresh = j * kKT >= s0;
-        const CUtensorMap* mk = fresh ? &tmK16 : &tmK;
-        const CUtensorMap* mv = fresh ? &tmV16 : &tmV;
-        const int row = fresh ? kv16_row0 + j * kKT : kv_row0 + j * kKT;
+        const int st = j % kStages;
+        const uint32_t ph = ((j / kStages) & 1) ^ 1u;
+        const int row = kv_row0 + j * kKT;
+        if (!mbar_wait(&k_empty[st], ph, abort_flag, a.err)) break;
         mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < DH / 64; ++c)
           tma_load_2d(sK + st * C::TILE_BYTES + c * kKT * 128, mk, &k_full[st], c * 64, row);
+        ++nk;
+        if (!mbar_wait(&v_empty[st], ph, abort_flag, a.err)) break;
         mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < DH / 64; ++c)
           tma_load_2d(sV + st * C::TILE_BYTES + c * kKT * 128, mv, &v_full[st], c * 64, row);
+        ++nv;
       }
-      // drain: every issued tile is consumed before exit
-      for (int j = n_kv; j < n_kv + 2; ++j) {
-        if (!mbar_wait(&kv_empty[j & 1], ((j >> 1) & 1) ^ 1u, abort_flag, a.err)) break;
-      }
+      // the CTA does not retire while a copy is still landing (also on abort)
+      for (int j = max(0, nk - kStages); j < nk; ++j)
+        mbar_wait_drain(&k_full[j % kStages], (j / kStages) & 1, a.err);
+      for (int j = max(0, nv - kStages); j < nv; ++j)
+        mbar_wait_drain(&v_full[j % kStages], (j / kStages) & 1, a.err);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s16 = idesc_f32acc(kQT, kKT, true);
-      constexpr uint32_t idesc_sb = idesc_f32acc(kQT, kKT, false);
-      constexpr uint32_t idesc_o16 = idesc_f32acc(kQT, DH, true, false, /*b_mn_major=*/true);
-      constexpr uint32_t idesc_ob = idesc_f32acc(kQT, DH, false, false, /*b_mn_major=*/true);
-      bool qb_waited = false;
-      auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        const bool fresh = j * kKT >= s0;
-        if (!fresh && !qb_waited) {
-          if (!mbar_wait(qb_ready, 0, abort_flag, a.err)) return false;
-          tc_fence_after();
-          qb_waited = true;
-        }
-        const uint32_t q0 = smem_u32(fresh ? sQ : sQb);
-        const uint32_t k0 = smem_u32(sK + st * C::TILE_BYTES);
-        const uint32_t d = tmem + C::S_COL0 + st * kKT;
+      const uint32_t idesc_s = idesc_f32acc(kQT, kKT, fresh);
+      const uint32_t idesc_o = idesc_f32acc(kQT, DH, fresh, false, /*b_mn_major=*/true);
+      auto issue_s = [&](int x, int j) {
+        const uint32_t q0 = smem_u32(sQ + x * C::TILE_BYTES);
+        const uint32_t k0 = smem_u32(sK + (j % kStages) * C::TILE_BYTES);
+        const uint32_t d = tmem + C::S_COL + x * kKT;
 #pragma unroll
         for (int k = 0; k < DH / 16; ++k) {
           const uint32_t off = (k >> 2) * (kQT * 128) + (k & 3) * 32;
           umma_f16(d, smem_desc_sw128(q0 + off, 16, 1024), smem_desc_sw128(k0 + off, 16, 1024),
-                   fresh ? idesc_s16 : idesc_sb, k != 0);
+                   idesc_s, k != 0);
         }
-        umma_commit(&s_full[st]);
-        return true;
+        umma_commit(&s_full[x]);
       };
-      bool ok = mbar_wait(q_full, 0, abort_flag, a.err) &&
-                mbar_wait(&k_full[0], 0, abort_flag, a.err);
-      if (ok) {
-        tc_fence_after();
-        ok = issue_s(0);
-      }
-      const uint32_t p0 = smem_u32(sP);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j & 1;
-        if (j + 1 < n_kv) {
-          const int j1 = j + 1, st1 = j1 & 1;
-          if (!mbar_wait(&k_full[st1], (j1 >> 1) & 1, abort_flag, a.err)) break;
-          if (j1 >= 2 && !mbar_wait(&s_free[st1], ((j1 >> 1) - 1) & 1, abort_flag, a.err)) break;
-          tc_fence_after();
-          if (!issue_s(j1)) break;
-        }
-        if (!mbar_wait(p_full, j & 1, abort_flag, a.err)) break;
-        if (!mbar_wait(&v_full[st], (j >> 1) & 1, abort_flag, a.err)) break;
-        tc_fence_after();
-        const uint32_t v0 = smem_u32(sV + st * C::TILE_BYTES);
+      auto issue_pv = [&](int x, int j) {
+        const uint32_t v0 = smem_u32(sV + (j % kStages) * C::TILE_BYTES);
 #pragma unroll
         for (int k = 0; k < kKT / 16; ++k) {
-          // A = P rows x keys (K-major, two 64-key swizzle blocks of 16 KB)
-          const uint32_t pa = p0 + (k >> 2) * (kQT * 128) + (k & 3) * 32;
-          // B = V keys x dh read MN-major: 16 keys = 16 rows of 128 B; next 64-wide
-          // dh block 16 KB away (LBO), next 8 keys 1 KB away (SBO)
-          const uint32_t vb = v0 + k * 16 * 128;
-          umma_f16(tmem + C::O_COL, smem_desc_sw128(pa, 16, 1024),
-                   smem_desc_sw128(vb, kKT * 128, 1024), (j * kKT >= s0) ? idesc_o16 : idesc_ob,
-                   (j | k) != 0);
+          // A = P (16 keys = 8 TMEM columns per step); B = V keys x dh read
+          // MN-major: 16 keys = 16 rows of 128 B, next 64-wide dh block 16 KB
+          // away (LBO), next 8 keys 1 KB away (SBO)
+          umma_f16_tmem_a(tmem + C::O_COL + x * DH, tmem + C::S_COL + x * kKT + k * 8,
+                          smem_desc_sw128(v0 + k * 16 * 128, kKT * 128, 1024), idesc_o,
+                          (j | k) != 0);
         }
-        umma_commit(o_done);
-        umma_commit(&kv_empty[st]);
+        umma_commit(&o_done[x]);
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, a.err);
+      if (ok && !fresh) ok = mbar_wait(q_conv, 0, abort_flag, a.err);
+      if (ok) ok = mbar_wait(&k_full[0], 0, abort_flag, a.err);
+      if (ok) {
+        tc_fence_after();
+        for (int x = 0; x < nq; ++x) issue_s(x, 0);
+        umma_commit(&k_empty[0]);
       }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int st = j % kStages;
+        const bool more = j + 1 < n_kv;
+        if (!mbar_wait(&v_full[st], (j / kStages) & 1, abort_flag, a.err)) break;
+        for (int x = 0; x < nq; ++x) {
+          if (!mbar_wait(&p_full[x], j & 1, abort_flag, a.err)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(x, j);
+          if (x == nq - 1) umma_commit(&v_empty[st]);
+          if (more) {
+            if (x == 0 && !mbar_wait(&k_full[(j + 1) % kStages], ((j + 1) / kStages) & 1,
+                                     abort_flag, a.err)) {
+              ok = false;
+              break;
+            }
+            // S_x(j+1) overwrites the columns P_x(j) is read from
+            if (!mbar_wait(&o_done[x], j & 1, abort_flag, a.err)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(x, j + 1);
+            if (x == nq - 1) umma_commit(&k_empty[(j + 1) % kStages]);
+          }
+        }
+      }
+      // retire only after every issued MMA has completed (also on abort)
+      umma_commit(mma_idle);
+      mbar_wait_drain(mma_idle, 0, a.err);
     }
   } else {
-    // softmax / epilogue warps
-    const int qw = warp & 3;
-    const int r = qw * 32 + lane;  // query row within the tile
+    // softmax / epilogue warps: head x, row r of the query tile
+    const int x = (warp - 2) >> 2;
+    const int qw = warp & 3;        // TMEM lane quadrant of this warp
+    const int r = qw * 32 + lane;   // query row within the tile
     const int t = t0 + r;
-    const int s_q = s0 + t;        // this row's cache slot
+    const int s_q = s0 + t;         // this row's cache slot
+    const int s_row0 = s0 + t0;     // slot of the tile's first row
     const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + C::S_COL + x * kKT;
+    const uint32_t o_addr = tmem + lane_base + C::O_COL + x * DH;
     float m_used = -INFINITY, l_sum = 0.f;
-    bool ok = true;
-    if (s0 > 0) {
-      // some key tiles come from the BF16 cache: convert this row of Q once
+    bool ok = x < nq;
+    if (ok && !fresh) {
+      // keys come from the BF16 cache: convert this row of Q once, in place
       // (element by element, so the swizzled placement is kept)
-      if (!mbar_wait(q_full, 0, abort_flag, a.err)) ok = false;
+      ok = mbar_wait(q_full, 0, abort_flag, a.err);
       if (ok) {
 #pragma unroll
         for (int blk = 0; blk < DH / 64; ++blk) {
-          const uint4* src = reinterpret_cast<const uint4*>(sQ + blk * (kQT * 128) + r * 128);
-          uint4* dst = reinterpret_cast<uint4*>(sQb + blk * (kQT * 128) + r * 128);
+          uint4* row = reinterpret_cast<uint4*>(sQ + x * C::TILE_BYTES + blk * (kQT * 128) +
+                                                r * 128);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            const uint4 u = src[c];
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            const uint4 u4 = row[c];
+            const uint32_t w[4] = {u4.x, u4.y, u4.z, u4.w};
             uint32_t o[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float2 f = unpack_f16x2(w[e]);
               o[e] = pack_bf16x2(f.x, f.y);
             }
-            dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+            row[c] = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(qb_ready);
+        mbar_arrive(q_conv);
       }
     }
     for (int j = 0; ok && j < n_kv; ++j) {
-      const bool fresh = j * kKT >= s0;
-      const int st = j & 1;
-      if (!mbar_wait(&s_full[st], (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
+      if (!mbar_wait(&s_full[x], j & 1, abort_flag, a.err)) { ok = false; break; }
       tc_fence_after();
       float s[kKT];
+      {
+        uint32_t raw[kKT];
+        tmem_ld128_wait(s_addr, raw);
+#pragma unroll
+        for (int i = 0; i < kKT; ++i) s[i] = __uint_as_float(raw[i]);
+      }
+      const int key0 = j * kKT;
+      if (key0 + kKT - 1 > s_row0) {
+        // a tile that reaches past the first row's slot: causal mask
+#pragma unroll
+        for (int i = 0; i < kKT; ++i) s[i] = (key0 + i <= s_q) ? s[i] : -INFINITY;
+      }
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < kKT; i += 8) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) m4[c] = max3(m4[c], s[i + 2 * c], s[i + 2 * c + 1]);
+      }
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2;
+      float alpha = 1.f;
+      if (mx > m_used + kRescaleLog2) {
+        alpha = ex2(m_used - mx);  // 0 on the first tile (m_used = -inf)
+        l_sum *= alpha;
+        m_used = mx;
+      }
+      // P = 2^(s * scale - m), FP32 row sum, rounded to the operand type and
+      // written over the first 64 columns of S_x (two values per column)
+      const float neg_m = -m_used;
 #pragma unroll
       for (int c = 0; c < kKT / 32; ++c) {
-        uint32_t rr[32];
-        tmem_ld32(tmem + lane_base + C::S_COL0 + st * kKT + 32 * c, rr);
-        tmem_ld_wait();
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[32 * c + i] = __uint_as_float(rr[i]);
+        for (int i = 0; i < 16; ++i) {
+          const int e = 32 * c + 2 * i;
+          const float z0 = fmaf(s[e], a.scale_log2, neg_m);
+          const float z1 = fmaf(s[e + 1], a.scale_log2, neg_m);
+          const bool poly = ((2 * i) & 15) < kPolyPer16;
+          const float p0 = poly ? exp2_fma(z0) : ex2(z0);
+          const float p1 = poly ? exp2_fma(z1) : ex2(z1);
+          l_sum += p0 + p1;
+          pk[i] = pack2(p0, p1, fresh);
+        }
+        tmem_st16(s_addr + 16 * c, pk);
       }
-      tc_fence_before();
-      mbar_arrive(&s_free[st]);
-      // scale (log2 domain) and causal mask
-      const int key0 = j * kKT;
-      float mx = -INFINITY;
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O_x is quiescent until p_full: O_x += P_x(j-1) V completed before
+        // S_x(j) was issued, and O_x += P_x(j) V waits for this thread
+#pragma unroll 1
+        for (int c = 0; c < DH / 32; ++c) {
+          uint32_t oo[32];
+          tmem_ld32_wait(o_addr + 32 * c, oo);
 #pragma unroll
-      for (int i = 0; i < kKT; ++i) {
-        const float v = (key0 + i <= s_q) ? s[i] * a.scale_log2 : -INFINITY;
-        s[i] = v;
-        mx = fmaxf(mx, v);
-      }
-      float alpha = 1.f;
-      if (mx > m_used + kRescaleLog2 || m_used == -INFINITY) {
-        const float m_new = fmaxf(mx, m_used);
-        alpha = (m_used == -INFINITY) ? 0.f : ex2(m_used - m_new);
-        l_sum *= alpha;
-        m_used = m_new;
-      }
-      // P = 2^(s - m) rounded to the tile's operand type; l sums the rounded values
-      uint32_t pk[kKT / 2];
-#pragma unroll
-      for (int i = 0; i < kKT / 2; ++i) {
-        const float p0 = ex2(s[2 * i] - m_used);
-        const float p1 = ex2(s[2 * i + 1] - m_used);
-        pk[i] = pack2(p0, p1, fresh);
-        const float2 rp = fresh ? unpack_f16x2(pk[i]) : unpack_bf16x2(pk[i]);
-        l_sum += rp.x + rp.y;
-      }
-      if (j > 0) {
-        // PV of the previous tile must be done before P is overwritten and O rescaled
-        if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, a.err)) { ok = false; break; }
-        tc_fence_after();
-        const bool need = __any_sync(0xffffffffu, alpha != 1.f);
-        if (need) {
-#pragma unroll
-          for (int c = 0; c < DH / 32; ++c) {
-            uint32_t oo[32];
-            const uint32_t addr = tmem + lane_base + C::O_COL + 32 * c;
-            tmem_ld32(addr, oo);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) oo[i] = __float_as_uint(__uint_as_float(oo[i]) * alpha);
-            tmem_st32(addr, oo);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < 32; ++i) oo[i] = __float_as_uint(__uint_as_float(oo[i]) * alpha);
+          tmem_st32(o_addr + 32 * c, oo);
         }
       }
-      // P row -> shared memory, 128-byte swizzle: 16-byte chunk c of row r sits at
-      // chunk c ^ (r & 7) of the row's 128-byte line
-#pragma unroll
-      for (int blk = 0; blk < 2; ++blk) {
-        uint8_t* rowp = sP + blk * (kQT * 128) + r * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int e = blk * 32 + c * 4;  // index into pk (pairs)
-          uint4 v;
-          v.x = pk[e];
-          v.y = pk[e + 1];
-          v.z = pk[e + 2];
-          v.w = pk[e + 3];
-          *reinterpret_cast<uint4*>(rowp + ((c ^ (r & 7)) << 4)) = v;
-        }
-      }
-      // keys past the CTA's last visible slot may hold stale cache contents:
-      // zero their V rows so 0 * (non-finite) cannot reach O
-      if (key0 + kKT - 1 > kmax) {
-        if (!mbar_wait(&v_full[st], (j >> 1) & 1, abort_flag, a.err)) { ok = false; break; }
+      tmem_st_wait();
+      if (x == 0 && key0 + kKT - 1 > kmax) {
+        // keys past the CTA's last visible slot may hold stale cache contents:
+        // zero their V rows so 0 * (non-finite) cannot reach O
+        const int st = j % kStages;
+        if (!mbar_wait(&v_full[st], (j / kStages) & 1, abort_flag, a.err)) { ok = false; break; }
         if (key0 + r > kmax) {
 #pragma unroll
           for (int c = 0; c < DH / 64; ++c) {
@@ -362,21 +454,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int q = 0; q < 8; ++q) vr[q] = make_uint4(0, 0, 0, 0);
           }
         }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[x]);
     }
-    if (ok && mbar_wait(o_done, (n_kv - 1) & 1, abort_flag, a.err)) {
+    if (ok && mbar_wait(&o_done[x], (n_kv - 1) & 1, abort_flag, a.err)) {
       tc_fence_after();
       const float inv_l = 1.f / l_sum;
       const bool row_ok = t < a.T;
-      f16* dst = a.out + ((size_t)b * a.T + t) * (size_t)(a.Hq * DH) + (size_t)h * DH;
-#pragma unroll
+      f16* dst = a.out + ((size_t)b * a.T + t) * (size_t)(a.Hq * DH) + (size_t)(hA + x) * DH;
+#pragma unroll 1
       for (int c = 0; c < DH / 32; ++c) {
         uint32_t oo[32];
-        tmem_ld32(tmem + lane_base + C::O_COL + 32 * c, oo);
-        tmem_ld_wait();
+        tmem_ld32_wait(o_addr + 32 * c, oo);
         if (row_ok) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -441,7 +532,8 @@ static qwen_status launch_dh(const CUtensorMap& q, const CUtensorMap& k, const C
     attr = true;
   }
   const int n_qt = (a.T + kQT - 1) / kQT;
-  const int grid = n_qt * a.B * a.Hq;
+  const int npair = (a.Hq / a.Hkv + 1) / 2;
+  const int grid = n_qt * a.B * a.Hkv * npair;
   launch_k(kern, dim3(grid), dim3(kAttnThreads), AttnCfg<DH>::SMEM_BYTES, st, q, k, v, k16, v16,
            a);
   count_launches();

@@ -102,6 +102,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Drain wait at the end of a role: like mbar_wait but it keeps waiting (within
+// the time limit) when another thread raised *abort, so copies and MMAs still in
+// flight land before the CTA releases its shared and tensor memory.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int* err) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      record_error(err, QWEN_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
 // ----------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
