@@ -10,21 +10,22 @@
 //
 // One CTA = one sequence b, one KV group g, two query heads of that group (A
 // and B; B absent for the last head of an odd-sized group) and one tile of 128
-// query rows.  Both heads read every staged K/V tile, and the two heads form
-// two independent chains that keep the tensor pipe busy while the other head's
-// softmax runs:
-//   warp 0      TMA: Q_A, Q_B once, then K and V tiles of 128 keys (2 stages each)
-//   warp 1      TMEM allocator + MMA issuer, per key tile j:
-//                 O_A += P_A V_j, S_A = Q_A K_{j+1}^T, O_B += P_B V_j, S_B = ...
-//               S_x lives in TMEM (128 columns per head); the softmax writes P_x
-//               back over the first 64 of them and the P.V MMA takes its A
-//               operand straight from TMEM.  S_x(j+1) is issued only after
-//               O_x += P_x(j) V_j has completed (it overwrites P_x(j)).
-//   warps 2-5   softmax of head A, warps 6-9 softmax of head B: one thread per
+// query rows.  Both heads read every staged K/V tile: a single SM's TMA
+// delivers about 64 bytes per cycle, and one head alone would need a 64 KB K/V
+// tile per 1024 cycles of MMA work; two heads halve that.
+//   warp 0      TMA: Q_A, Q_B once, then K (2 stages) and V (1 stage) tiles of
+//               128 keys, in the order K(j+1), V(j)
+//   warps 1, 2  MMA issuers of head A and head B (TMEM allocation by warp 1):
+//               S_x(j+1) = Q_x K_{j+1}^T as soon as the softmax has read S_x(j)
+//               into registers, and O_x += P_x(j) V_j once it has written P_x(j)
+//               to shared memory.  Each issuer runs its loop as a converged warp
+//               and issues from one elected lane: a lone lane next to busy
+//               softmax warps gets too few issue slots.
+//   warps 3-6   softmax of head A, warps 7-10 softmax of head B: one thread per
 //               query row; online max / sum in FP32 with the rescale of O
-//               deferred until the running max grows by 2^8; a quarter of the
-//               exponentials run on the FMA pipe (fast_exp2.cuh), the rest on
-//               the special-function unit; final O / l.
+//               deferred until the running max grows by 2^8; P in the
+//               128-byte-swizzled K-major layout the MMA reads; final O / l.
+// Tensor memory: S_A, S_B (128 columns each), O_A, O_B (dh columns each).
 //
 // Operands: when the sequence starts at slot 0 every key comes from this call,
 // so Q, K, V and P are FP16 (the QKV epilogue writes FP16 copies of the new K/V
@@ -32,7 +33,6 @@
 // BF16 cache instead; then Q is converted to BF16 in shared memory once and P
 // is rounded to BF16.
 #include "common.cuh"
-#include "fast_exp2.cuh"
 #include "internal.h"
 
 #include <cudaTypedefs.h>
@@ -43,10 +43,9 @@ namespace {
 
 constexpr int kQT = 128;      // query rows per CTA
 constexpr int kKT = 128;      // keys per tile
-constexpr int kStages = 2;    // K and V ring depth
-constexpr int kAttnThreads = 320;
+constexpr int kKStages = 2;   // K ring; V has a single stage
+constexpr int kAttnThreads = 352;
 constexpr float kRescaleLog2 = 8.0f;  // defer O rescale until the max grew by 2^8
-constexpr int kPolyPer16 = 4;         // exponentials per 16 evaluated on the FMA pipe
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -112,41 +111,20 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem], kind::f16: A is M rows (TMEM lanes) x 16
-// 16-bit elements packed two per 32-bit column.
-__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 template <int DH>
 struct AttnCfg {
   static constexpr int TILE_BYTES = kKT * DH * 2;  // one [128 x DH] 16-bit tile
+  static constexpr int P_BYTES = kQT * kKT * 2;    // one [128 x 128] 16-bit P tile
   static constexpr int Q_OFF = 0;                  // Q_A, Q_B
-  static constexpr int K_OFF = 2 * TILE_BYTES;     // kStages tiles
-  static constexpr int V_OFF = K_OFF + kStages * TILE_BYTES;
-  static constexpr int BAR_OFF = V_OFF + kStages * TILE_BYTES;
+  static constexpr int K_OFF = 2 * TILE_BYTES;     // kKStages tiles
+  static constexpr int V_OFF = K_OFF + kKStages * TILE_BYTES;
+  static constexpr int P_OFF = V_OFF + TILE_BYTES;  // P_A, P_B
+  static constexpr int BAR_OFF = P_OFF + 2 * P_BYTES;
   static constexpr int SMEM_BYTES = 1024 + BAR_OFF + 256;
-  // TMEM columns: S_A [0,128), S_B [128,256) (P_x over the first 64 of S_x),
-  // O_A [256, 256+DH), O_B [256+DH, 256+2DH)
-  static constexpr int S_COL = 0;
-  static constexpr int O_COL = 256;
+  static constexpr int S_COL = 0;     // S_x at x * 128
+  static constexpr int O_COL = 256;   // O_x at 256 + x * DH
   static constexpr int TMEM_COLS = 512;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
 struct AttnArgs {
@@ -175,18 +153,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* sQ = smem + C::Q_OFF;
   uint8_t* sK = smem + C::K_OFF;
   uint8_t* sV = smem + C::V_OFF;
+  uint8_t* sP = smem + C::P_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* q_full = bars + 0;
   uint64_t* q_conv = bars + 1;    // BF16 conversion of Q done (appended chunks only)
-  uint64_t* k_full = bars + 2;    // [kStages]
-  uint64_t* k_empty = bars + 4;   // [kStages]
-  uint64_t* v_full = bars + 6;    // [kStages]
-  uint64_t* v_empty = bars + 8;   // [kStages]
-  uint64_t* s_full = bars + 10;   // [2] per head
-  uint64_t* p_full = bars + 12;   // [2] per head
-  uint64_t* o_done = bars + 14;   // [2] per head
-  uint64_t* mma_idle = bars + 16;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+  uint64_t* k_full = bars + 2;    // [2]
+  uint64_t* k_empty = bars + 4;   // [2]
+  uint64_t* v_full = bars + 6;
+  uint64_t* v_empty = bars + 7;
+  uint64_t* s_full = bars + 8;    // [2] per head: S_x(j) in TMEM
+  uint64_t* s_free = bars + 10;   // [2] per head: S_x(j) read into registers
+  uint64_t* p_full = bars + 12;   // [2] per head: P_x(j) in shared memory
+  uint64_t* o_done = bars + 14;   // [2] per head: O_x += P_x(j) V_j complete
+  uint64_t* mma_idle = bars + 16; // [2] per head
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -215,18 +195,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_conv, 128 * nq);
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
-      mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
+      mbar_init(&k_empty[i], nq);  // released by each head's issuer
     }
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, nq);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
+      mbar_init(&s_free[x], 128);
       mbar_init(&p_full[x], 128);
       mbar_init(&o_done[x], 1);
+      mbar_init(&mma_idle[x], 1);
     }
-    mbar_init(mma_idle, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -240,110 +221,121 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
+    // TMA producer, converged; one elected lane issues
+    const CUtensorMap* mk = fresh ? &tmK16 : &tmK;
+    const CUtensorMap* mv = fresh ? &tmV16 : &tmV;
     if (lane == 0) {
-      const CUtensorMap* mk = fresh ? &tmK16 : &tmK;
-      const CUtensorMap* mv = fresh ? &tmV16 : &tmV;
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(mk);
       tma_prefetch_desc(mv);
-      mbar_arrive_expect_tx(q_full, nq * C::TILE_BYTES);
-      for (int x = 0; x < nq; ++x) {
-#pragma unroll
-        for (int c = 0; c < DH / 64; ++c)
-          tma_load_2d(sQ + x * C::TILE_BYTES + c * kQT * 128, &tmQ, q_full, c * 64,
-                      (b * a.Hq + hA + x) * a.T + t0);
-      }
-      int nk = 0, nv = 0;  // tiles issued
-      for (int j = 0; j < n_kv; ++j) {
-        const int st = j % kStages;
-        const uint32_t ph = ((j / kStages) & 1) ^ 1u;
-        const int row = kv_row0 + j * kKT;
-        if (!mbar_wait(&k_empty[st], ph, abort_flag, a.err)) break;
-        mbar_arrive_expect_tx(&k_full[st], C::TILE_BYTES);
-#pragma unroll
-        for (int c = 0; c < DH / 64; ++c)
-          tma_load_2d(sK + st * C::TILE_BYTES + c * kKT * 128, mk, &k_full[st], c * 64, row);
-        ++nk;
-        if (!mbar_wait(&v_empty[st], ph, abort_flag, a.err)) break;
-        mbar_arrive_expect_tx(&v_full[st], C::TILE_BYTES);
-#pragma unroll
-        for (int c = 0; c < DH / 64; ++c)
-          tma_load_2d(sV + st * C::TILE_BYTES + c * kKT * 128, mv, &v_full[st], c * 64, row);
-        ++nv;
-      }
-      // the CTA does not retire while a copy is still landing (also on abort)
-      for (int j = max(0, nk - kStages); j < nk; ++j)
-        mbar_wait_drain(&k_full[j % kStages], (j / kStages) & 1, a.err);
-      for (int j = max(0, nv - kStages); j < nv; ++j)
-        mbar_wait_drain(&v_full[j % kStages], (j / kStages) & 1, a.err);
     }
-  } else if (warp == 1) {
-    if (lane == 0) {
+    __syncwarp();
+    mbar_arrive_expect_tx_w(q_full, nq * C::TILE_BYTES);
+    for (int x = 0; x < nq; ++x) {
+#pragma unroll
+      for (int c = 0; c < DH / 64; ++c)
+        tma_load_2d_w(sQ + x * C::TILE_BYTES + c * kQT * 128, &tmQ, q_full, c * 64,
+                      (b * a.Hq + hA + x) * a.T + t0);
+    }
+    int nk = 0, nv = 0;  // tiles issued
+    auto load_k = [&](int j) -> bool {
+      const int st = j % kKStages;
+      if (!mbar_wait_w(&k_empty[st], ((j / kKStages) & 1) ^ 1u, abort_flag, a.err)) return false;
+      mbar_arrive_expect_tx_w(&k_full[st], C::TILE_BYTES);
+#pragma unroll
+      for (int c = 0; c < DH / 64; ++c)
+        tma_load_2d_w(sK + st * C::TILE_BYTES + c * kKT * 128, mk, &k_full[st], c * 64,
+                      kv_row0 + j * kKT);
+      ++nk;
+      return true;
+    };
+    auto load_v = [&](int j) -> bool {
+      if (!mbar_wait_w(v_empty, (j & 1) ^ 1u, abort_flag, a.err)) return false;
+      mbar_arrive_expect_tx_w(v_full, C::TILE_BYTES);
+#pragma unroll
+      for (int c = 0; c < DH / 64; ++c)
+        tma_load_2d_w(sV + c * kKT * 128, mv, v_full, c * 64, kv_row0 + j * kKT);
+      ++nv;
+      return true;
+    };
+    // K(j+1) goes ahead of V(j): S(j+1) is issued early in the softmax of tile j,
+    // P(j).V only at its end
+    if (load_k(0)) {
+      for (int j = 0; j < n_kv; ++j) {
+        if (j + 1 < n_kv && !load_k(j + 1)) break;
+        if (!load_v(j)) break;
+      }
+    }
+    // the CTA does not retire while a copy is still landing (also on abort)
+    for (int j = max(0, nk - kKStages); j < nk; ++j)
+      mbar_wait_drain(&k_full[j % kKStages], (j / kKStages) & 1, a.err);
+    if (nv > 0) mbar_wait_drain(v_full, (nv - 1) & 1, a.err);
+  } else if (warp <= 2) {
+    const int x = warp - 1;  // head whose MMAs this warp issues
+    if (x < nq) {
       const uint32_t idesc_s = idesc_f32acc(kQT, kKT, fresh);
       const uint32_t idesc_o = idesc_f32acc(kQT, DH, fresh, false, /*b_mn_major=*/true);
-      auto issue_s = [&](int x, int j) {
-        const uint32_t q0 = smem_u32(sQ + x * C::TILE_BYTES);
-        const uint32_t k0 = smem_u32(sK + (j % kStages) * C::TILE_BYTES);
-        const uint32_t d = tmem + C::S_COL + x * kKT;
+      // descriptors computed once; each MMA adds a constant (start address >> 4
+      // stays below 2^14, so the add never carries out of its field)
+      const uint64_t dq = smem_desc_sw128(smem_u32(sQ + x * C::TILE_BYTES), 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dv = smem_desc_sw128(smem_u32(sV), kKT * 128, 1024);
+      const uint64_t dp = smem_desc_sw128(smem_u32(sP + x * C::P_BYTES), 16, 1024);
+      const uint32_t d_s = tmem + C::S_COL + x * kKT;
+      const uint32_t d_o = tmem + C::O_COL + x * DH;
+      auto issue_s = [&](int j) {
+        const uint64_t b0 = dk0 + (uint64_t)((j % kKStages) * (C::TILE_BYTES >> 4));
 #pragma unroll
         for (int k = 0; k < DH / 16; ++k) {
-          const uint32_t off = (k >> 2) * (kQT * 128) + (k & 3) * 32;
-          umma_f16(d, smem_desc_sw128(q0 + off, 16, 1024), smem_desc_sw128(k0 + off, 16, 1024),
-                   idesc_s, k != 0);
+          // 16 dh columns = 32 B within a 128-B swizzle row; next 64-wide block 16 KB on
+          const uint32_t off = ((k >> 2) * (kQT * 128) + (k & 3) * 32) >> 4;
+          umma_f16_w(d_s, dq + off, b0 + off, idesc_s, k != 0);
         }
-        umma_commit(&s_full[x]);
+        umma_commit_w(&s_full[x]);
+        // release the stage only if it will be refilled (nothing is left in
+        // flight towards this CTA's barriers when it ends)
+        if (j + kKStages < n_kv) umma_commit_w(&k_empty[j % kKStages]);
       };
-      auto issue_pv = [&](int x, int j) {
-        const uint32_t v0 = smem_u32(sV + (j % kStages) * C::TILE_BYTES);
+      auto issue_pv = [&](int j) {
 #pragma unroll
         for (int k = 0; k < kKT / 16; ++k) {
-          // A = P (16 keys = 8 TMEM columns per step); B = V keys x dh read
-          // MN-major: 16 keys = 16 rows of 128 B, next 64-wide dh block 16 KB
-          // away (LBO), next 8 keys 1 KB away (SBO)
-          umma_f16_tmem_a(tmem + C::O_COL + x * DH, tmem + C::S_COL + x * kKT + k * 8,
-                          smem_desc_sw128(v0 + k * 16 * 128, kKT * 128, 1024), idesc_o,
-                          (j | k) != 0);
+          // A = P rows x keys (K-major, two 64-key swizzle blocks of 16 KB);
+          // B = V keys x dh read MN-major: 16 keys = 16 rows of 128 B, next
+          // 64-wide dh block 16 KB away (LBO), next 8 keys 1 KB away (SBO)
+          const uint32_t pa = ((k >> 2) * (kQT * 128) + (k & 3) * 32) >> 4;
+          umma_f16_w(d_o, dp + pa, dv + ((k * 16 * 128) >> 4), idesc_o, (j | k) != 0);
         }
-        umma_commit(&o_done[x]);
+        umma_commit_w(&o_done[x]);
+        if (j + 1 < n_kv) umma_commit_w(v_empty);
       };
-      bool ok = mbar_wait(q_full, 0, abort_flag, a.err);
-      if (ok && !fresh) ok = mbar_wait(q_conv, 0, abort_flag, a.err);
-      if (ok) ok = mbar_wait(&k_full[0], 0, abort_flag, a.err);
+      bool ok = mbar_wait_w(q_full, 0, abort_flag, a.err);
+      if (ok && !fresh) ok = mbar_wait_w(q_conv, 0, abort_flag, a.err);
+      if (ok) ok = mbar_wait_w(&k_full[0], 0, abort_flag, a.err);
       if (ok) {
         tc_fence_after();
-        for (int x = 0; x < nq; ++x) issue_s(x, 0);
-        umma_commit(&k_empty[0]);
+        issue_s(0);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
-        const int st = j % kStages;
-        const bool more = j + 1 < n_kv;
-        if (!mbar_wait(&v_full[st], (j / kStages) & 1, abort_flag, a.err)) break;
-        for (int x = 0; x < nq; ++x) {
-          if (!mbar_wait(&p_full[x], j & 1, abort_flag, a.err)) { ok = false; break; }
+        if (j + 1 < n_kv) {
+          const int j1 = j + 1;
+          if (!mbar_wait_w(&k_full[j1 % kKStages], (j1 / kKStages) & 1, abort_flag, a.err)) break;
+          // S_x(j+1) overwrites S_x(j): the softmax has it in registers
+          if (!mbar_wait_w(&s_free[x], j & 1, abort_flag, a.err)) break;
           tc_fence_after();
-          issue_pv(x, j);
-          if (x == nq - 1) umma_commit(&v_empty[st]);
-          if (more) {
-            if (x == 0 && !mbar_wait(&k_full[(j + 1) % kStages], ((j + 1) / kStages) & 1,
-                                     abort_flag, a.err)) {
-              ok = false;
-              break;
-            }
-            // S_x(j+1) overwrites the columns P_x(j) is read from
-            if (!mbar_wait(&o_done[x], j & 1, abort_flag, a.err)) { ok = false; break; }
-            tc_fence_after();
-            issue_s(x, j + 1);
-            if (x == nq - 1) umma_commit(&k_empty[(j + 1) % kStages]);
-          }
+          issue_s(j1);
         }
+        if (!mbar_wait_w(v_full, j & 1, abort_flag, a.err)) break;
+        if (!mbar_wait_w(&p_full[x], j & 1, abort_flag, a.err)) break;
+        tc_fence_after();
+        issue_pv(j);
       }
       // retire only after every issued MMA has completed (also on abort)
-      umma_commit(mma_idle);
-      mbar_wait_drain(mma_idle, 0, a.err);
+      umma_commit_w(&mma_idle[x]);
+      mbar_wait_drain(&mma_idle[x], 0, a.err);
     }
   } else {
     // softmax / epilogue warps: head x, row r of the query tile
-    const int x = (warp - 2) >> 2;
+    const int x = (warp - 3) >> 2;
     const int qw = warp & 3;        // TMEM lane quadrant of this warp
     const int r = qw * 32 + lane;   // query row within the tile
     const int t = t0 + r;
@@ -352,6 +344,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + C::S_COL + x * kKT;
     const uint32_t o_addr = tmem + lane_base + C::O_COL + x * DH;
+    uint8_t* prow = sP + x * C::P_BYTES + r * 128;  // this row in P's two swizzle blocks
     float m_used = -INFINITY, l_sum = 0.f;
     bool ok = x < nq;
     if (ok && !fresh) {
@@ -390,6 +383,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int i = 0; i < kKT; ++i) s[i] = __uint_as_float(raw[i]);
       }
+      tc_fence_before();
+      mbar_arrive(&s_free[x]);  // S_x(j+1) may now be computed into the same columns
       const int key0 = j * kKT;
       if (key0 + kKT - 1 > s_row0) {
         // a tile that reaches past the first row's slot: causal mask
@@ -409,28 +404,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         l_sum *= alpha;
         m_used = mx;
       }
-      // P = 2^(s * scale - m), FP32 row sum, rounded to the operand type and
-      // written over the first 64 columns of S_x (two values per column)
+      // P = 2^(s * scale - m), FP32 row sum, rounded to the operand type, stored
+      // in the 128-byte swizzle: 16-byte chunk c of row r sits at chunk
+      // c ^ (r & 7) of the row's 128-byte line.  Keys 0-63 are packed before
+      // the wait for the previous P.V (which still reads the buffer), keys
+      // 64-127 are stored as they are computed.
       const float neg_m = -m_used;
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < kKT / 32; ++c) {
-        uint32_t pk[16];
+      for (int i = 0; i < 32; ++i) {
+        const float p0 = ex2(fmaf(s[2 * i], a.scale_log2, neg_m));
+        const float p1 = ex2(fmaf(s[2 * i + 1], a.scale_log2, neg_m));
+        l_sum += p0 + p1;
+        pk[i] = pack2(p0, p1, fresh);
+      }
+      if (j > 0) {
+        // O_x += P_x(j-1) V must be done: it reads the P buffer, and O is
+        // rescaled below (O_x += P_x(j) V waits for this thread)
+        if (!mbar_wait(&o_done[x], (j - 1) & 1, abort_flag, a.err)) { ok = false; break; }
+        tc_fence_after();
+      }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int e = 32 * c + 2 * i;
-          const float z0 = fmaf(s[e], a.scale_log2, neg_m);
-          const float z1 = fmaf(s[e + 1], a.scale_log2, neg_m);
-          const bool poly = ((2 * i) & 15) < kPolyPer16;
-          const float p0 = poly ? exp2_fma(z0) : ex2(z0);
-          const float p1 = poly ? exp2_fma(z1) : ex2(z1);
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = 64 + 8 * c + 2 * q;
+          const float p0 = ex2(fmaf(s[e], a.scale_log2, neg_m));
+          const float p1 = ex2(fmaf(s[e + 1], a.scale_log2, neg_m));
           l_sum += p0 + p1;
-          pk[i] = pack2(p0, p1, fresh);
+          w[q] = pack2(p0, p1, fresh);
         }
-        tmem_st16(s_addr + 16 * c, pk);
+        *reinterpret_cast<uint4*>(prow + kQT * 128 + ((c ^ (r & 7)) << 4)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
       }
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        // O_x is quiescent until p_full: O_x += P_x(j-1) V completed before
-        // S_x(j) was issued, and O_x += P_x(j) V waits for this thread
 #pragma unroll 1
         for (int c = 0; c < DH / 32; ++c) {
           uint32_t oo[32];
@@ -439,23 +451,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int i = 0; i < 32; ++i) oo[i] = __float_as_uint(__uint_as_float(oo[i]) * alpha);
           tmem_st32(o_addr + 32 * c, oo);
         }
+        tmem_st_wait();
       }
-      tmem_st_wait();
-      if (x == 0 && key0 + kKT - 1 > kmax) {
+      if (key0 + kKT - 1 > kmax) {
         // keys past the CTA's last visible slot may hold stale cache contents:
-        // zero their V rows so 0 * (non-finite) cannot reach O
-        const int st = j % kStages;
-        if (!mbar_wait(&v_full[st], (j / kStages) & 1, abort_flag, a.err)) { ok = false; break; }
+        // zero their V rows so 0 * (non-finite) cannot reach O (both heads'
+        // threads write the same zeros; each head's P.V waits for its own)
+        if (!mbar_wait(v_full, j & 1, abort_flag, a.err)) { ok = false; break; }
         if (key0 + r > kmax) {
 #pragma unroll
           for (int c = 0; c < DH / 64; ++c) {
-            uint4* vr = reinterpret_cast<uint4*>(sV + st * C::TILE_BYTES + c * kKT * 128 + r * 128);
+            uint4* vr = reinterpret_cast<uint4*>(sV + c * kKT * 128 + r * 128);
 #pragma unroll
             for (int q = 0; q < 8; ++q) vr[q] = make_uint4(0, 0, 0, 0);
           }
         }
-        fence_proxy_async_smem();
       }
+      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[x]);
     }
