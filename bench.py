@@ -38,6 +38,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "prefill tokens/s & decode µs/step per layer; % of BF16 tensor / HBM roofline"
 CACHE_FILLED = 4096
+# DRAM bytes (read + write) of one gate/up decode launch at B=32, from the ncu
+# capture summarised in profiles/gemm_decode_gateup_qwen25_7b_b32.md; to be
+# replaced whenever that kernel changes
+GATE_UP_TRAFFIC_B32 = 272086272 + 4292864
 
 
 def load_peaks():
@@ -487,7 +491,7 @@ def main():
     achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": "gemm_decode_kernel (gate/up, swap-AB split-K)",
                 "achieved": round(achieved, 1), "peak": hbm_gbs, "unit": "GB/s",
-                "frac": round(achieved / hbm_gbs, 3), "traffic": None,
+                "frac": round(achieved / hbm_gbs, 3), "traffic": GATE_UP_TRAFFIC_B32 if B == 32 else None,
                 "peak_kind": f"{peak_kind} hbm_gbs",
                 "algorithmic_bytes": gu_bytes, "avg_ms": round(gu_ms, 4),
                 "timing": "CUDA events around the gate/up stage in each of K graph-replayed steps",
