@@ -259,45 +259,6 @@ __device__ __forceinline__ bool mbar_wait_w(uint64_t* bar, uint32_t parity, vola
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, err));
 }
 
-// ---- thread-block clusters
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Every thread of every CTA in the cluster arrives and waits (release/acquire).
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-
-// 2-D tiled load multicast to the CTAs of `mask`: the box lands at the same
-// shared-memory offset in each, and each CTA's mbarrier at `bar`'s offset
-// receives the byte count.  One elected lane of a converged warp issues.
-__device__ __forceinline__ void tma_load_2d_mc_w(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                                 int c0, int c1, uint16_t mask) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;\n\t}" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
-      : "memory");
-}
-
-// tcgen05.commit arriving on the mbarrier at `bar`'s offset in each CTA of `mask`.
-__device__ __forceinline__ void umma_commit_mc_w(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
 // Instruction descriptor for kind::f16 with an FP32 accumulator.
 //   bits 4-5 D format (1 = F32), 7-9 A format and 10-12 B format (0 = F16,
 //   1 = BF16; A and B always share one type), 15/16 A/B major (0 = K-major,
