@@ -125,12 +125,12 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ workload
 
-def decode_bytes(shape, B):
+def decode_bytes(shape, B, cached=CACHE_FILLED):
     """Algorithmic bytes of one decode step: weights + KV read + KV write + X/Y."""
     d, hq, hkv, dh, f = shape.d, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn
     nq, nkv = hq * dh, hkv * dh
     weights = 2 * (d * (nq + 2 * nkv) + d * nq + 3 * d * f) + 4 * (nq + 2 * nkv) * shape.qkv_bias
-    kv_read = B * 2 * hkv * CACHE_FILLED * dh * 2
+    kv_read = B * 2 * hkv * cached * dh * 2
     kv_write = B * 2 * nkv * 2
     xy = B * d * 2 * 2
     return weights + kv_read + kv_write + xy
@@ -300,6 +300,177 @@ def prefill_bench(q, torch, shape, B, T, steps, warmup, peak_tflops, tag="bench_
     }
 
 
+# ------------------------------------------------------------------ other configurations
+
+def gpu_layer_weights(torch, shape, seed):
+    """Random-init weights of one layer generated on the device (seeded; the
+    distributions of synth.layer_weights: N(0, 0.02) projections and biases,
+    1 + N(0, 0.1) gammas, N(0, 0.5) router bias), BF16 [out, in]."""
+    g = torch.Generator(device="cuda").manual_seed(seed)
+
+    def n(shp, std, mean=0.0, dtype=torch.bfloat16):
+        return (torch.randn(shp, generator=g, device="cuda") * std + mean).to(dtype)
+    d, hq, hkv, dh, f = shape.d, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn
+    w = {"gamma_attn": n([d], 0.1, 1.0), "gamma_mlp": n([d], 0.1, 1.0),
+         "w_q": n([hq * dh, d], 0.02), "w_k": n([hkv * dh, d], 0.02),
+         "w_v": n([hkv * dh, d], 0.02), "w_o": n([d, hq * dh], 0.02)}
+    if shape.qk_norm:
+        w["gamma_q"], w["gamma_k"] = n([dh], 0.1, 1.0), n([dh], 0.1, 1.0)
+    if shape.qkv_bias:
+        w["b_q"], w["b_k"], w["b_v"] = n([hq * dh], 0.02), n([hkv * dh], 0.02), n([hkv * dh], 0.02)
+    if shape.n_experts:
+        e = shape.n_experts
+        w["w_router"] = n([e, d], 0.02)
+        if shape.router_bias:
+            w["b_router"] = n([e], 0.5).float()
+        w["w_gate"], w["w_up"] = n([e, f, d], 0.02), n([e, f, d], 0.02)
+        w["w_down"] = n([e, d, f], 0.02)
+    else:
+        w["w_gate"], w["w_up"], w["w_down"] = n([f, d], 0.02), n([f, d], 0.02), n([d, f], 0.02)
+    return w
+
+
+def stack_bench(q, torch, hbm_gbs, peak_tflops, steps, warmup):
+    """The 28-layer Qwen2.5-7B-shaped stack with final norm and last-token
+    lm_head: decode at B=32 against 2048 cached tokens per layer (CUDA graph of
+    the whole step), and one prefill of T=1024."""
+    import synth
+    shape, L, V = synth.QWEN25_7B, synth.QWEN25_7B_LAYERS, synth.QWEN25_7B_VOCAB
+    B, CACHED, T = 32, 2048, 1024
+    g = torch.Generator(device="cuda").manual_seed(5)
+    gamma_f = (torch.randn([shape.d], generator=g, device="cuda") * 0.1 + 1.0).bfloat16()
+    w_lm = (torch.randn([V, shape.d], generator=g, device="cuda") * 0.02).bfloat16()
+    st = q.Stack(shape, (gpu_layer_weights(torch, shape, 1000 + l) for l in range(L)), gamma_f,
+                 w_lm, max_batch=B, max_seq=CACHED + 1, max_tokens=T)
+    for l in range(L):
+        st.k[l][:, :, :CACHED].normal_(generator=g)
+        st.v[l][:, :, :CACHED].normal_(generator=g)
+    x = torch.randn([B, shape.d], generator=g, device="cuda").bfloat16()
+    pos = torch.full((B,), CACHED, dtype=torch.int32, device="cuda")
+    logits = torch.empty((B, V), dtype=torch.float32, device="cuda")
+    for _ in range(warmup):
+        st.decode(x, pos, pos, logits=logits)
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        for _ in range(steps):
+            st.decode(x, pos, pos, logits=logits)
+    graph.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    del graph
+    layer_bytes = decode_bytes(shape, B, cached=CACHED)
+    head_bytes = V * shape.d * 2 + B * V * 4
+    total = L * layer_bytes + head_bytes
+    dec = {"workload": f"28-layer qwen2.5-7b-shaped stack decode B={B}, {CACHED} cached tokens "
+                       "per layer, final norm + lm_head (152064) on the last position",
+           "ms_per_step": round(ms, 4), "bytes_per_step": total,
+           "GB_per_s": round(total / (ms * 1e-3) / 1e9, 1),
+           "frac_hbm": round(total / (ms * 1e-3) / 1e9 / hbm_gbs, 3)}
+    # prefill of one sequence of T tokens, logits of the last one
+    xp = torch.randn([1, T, shape.d], generator=g, device="cuda").bfloat16()
+    pp = torch.arange(T, dtype=torch.int32, device="cuda")
+    start = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):
+        st.prefill(xp, pp, start)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(3):
+        a.record()
+        st.prefill(xp, pp, start)
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    assert st.poll_error() == 0
+    pms = statistics.median(times)
+    P = linear_params(shape)
+    flops_exec = L * (2 * P * T + 2 * shape.n_q_heads * shape.head_dim * T * (T + 1)) \
+        + 2 * V * shape.d
+    flops_metric = L * (2 * P * T + 4 * T * T * shape.n_q_heads * shape.head_dim) + 2 * V * shape.d
+    pre = {"workload": f"28-layer qwen2.5-7b-shaped stack prefill B=1 T={T}, last-token logits",
+           "ms": round(pms, 3), "tokens_per_s": round(T / (pms * 1e-3), 1),
+           "tflops_metric": round(flops_metric / (pms * 1e-3) / 1e12, 1),
+           "tflops_executed": round(flops_exec / (pms * 1e-3) / 1e12, 1),
+           "frac_of_peak_executed": round(flops_exec / (pms * 1e-3) / 1e12 / peak_tflops, 3)}
+    del st
+    return {"decode": dec, "prefill": pre}
+
+
+def moe_prefill_bench(q, torch, peak_tflops, steps=5, warmup=2):
+    """Qwen3-30B-A3B-shaped MoE layer prefill, T=4096 (router bias N(0, 0.5) skews
+    the expert loads)."""
+    import synth
+    shape, T = synth.QWEN3_30B_A3B, 4096
+    w = gpu_layer_weights(torch, shape, 4000)
+    cfg = q.LayerConfig(shape, max_tokens=T, max_batch=1, max_seq=T, max_position=T)
+    layer = q.Layer(cfg, w)
+    g = torch.Generator(device="cuda").manual_seed(4)
+    x = torch.randn([1, T, shape.d], generator=g, device="cuda").bfloat16()
+    kc = torch.zeros((1, shape.n_kv_heads, T, shape.head_dim), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    pos = torch.arange(T, dtype=torch.int32, device="cuda")
+    start = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = torch.empty_like(x)
+    ws = layer.workspace(1, T)
+    for _ in range(warmup):
+        layer.prefill(x, pos, start, kc, vc, out=y, workspace=ws)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(steps):
+        a.record()
+        layer.prefill(x, pos, start, kc, vc, out=y, workspace=ws)
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    assert layer.poll_error() == 0
+    ms = statistics.median(times)
+    d, hq, hkv, dh = shape.d, shape.n_q_heads, shape.n_kv_heads, shape.head_dim
+    attn_lin = d * hq * dh + 2 * d * hkv * dh + hq * dh * d
+    experts = shape.top_k * 3 * d * shape.ffn
+    flops_exec = 2 * T * (attn_lin + shape.n_experts * d + experts) + 2 * hq * dh * T * (T + 1)
+    flops_metric = 2 * T * (attn_lin + shape.n_experts * d + experts) + 4 * T * T * hq * dh
+    return {"workload": f"qwen3-30b-a3b-shaped MoE layer prefill T={T} (128 experts, top-8, "
+                        "mf=768, skewed router bias)",
+            "ms": round(ms, 4), "tokens_per_s": round(T / (ms * 1e-3), 1),
+            "tflops_metric": round(flops_metric / (ms * 1e-3) / 1e12, 1),
+            "tflops_executed": round(flops_exec / (ms * 1e-3) / 1e12, 1),
+            "frac_of_peak_executed": round(flops_exec / (ms * 1e-3) / 1e12 / peak_tflops, 3)}
+
+
+def tiny_prefill_bench(q, torch, steps=20, warmup=3):
+    """The tiny Qwen3-style layer (d=512, B=1, T=128): launch-bound, reported in us."""
+    import synth
+    shape, T = synth.TINY, 128
+    w = gpu_layer_weights(torch, shape, 1)
+    layer = q.Layer(q.LayerConfig(shape, max_tokens=T, max_batch=1, max_seq=T, max_position=T), w)
+    x = torch.randn([1, T, shape.d], device="cuda").bfloat16()
+    kc = torch.zeros((1, shape.n_kv_heads, T, shape.head_dim), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    pos = torch.arange(T, dtype=torch.int32, device="cuda")
+    start = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = torch.empty_like(x)
+    ws = layer.workspace(1, T)
+    for _ in range(warmup):
+        layer.prefill(x, pos, start, kc, vc, out=y, workspace=ws)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        layer.prefill(x, pos, start, kc, vc, out=y, workspace=ws)
+    b.record()
+    torch.cuda.synchronize()
+    return {"workload": "tiny qwen3-style layer prefill B=1 T=128 (d=512, Hq=8, Hkv=2, dh=64)",
+            "us": round(a.elapsed_time(b) * 1e3 / steps, 2)}
+
+
 # ------------------------------------------------------------------ oracle timing
 
 class OracleDecode:
@@ -406,6 +577,7 @@ def main():
     ap.add_argument("--batch", type=int, default=32)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
                     help="run --steps untimed eager steps of one workload and exit "
@@ -530,6 +702,13 @@ def main():
         for (pb, pt) in ((1, 4096), (1, 1024), (8, 1024), (1, 16384)):
             pf.append(prefill_bench(q, torch, synth.QWEN3_8B, pb, pt, 5, 3, bf16_tf))
         line["prefill"] = pf
+    if rank == 0 and not args.no_prefill:
+        line["moe_prefill"] = moe_prefill_bench(q, torch, bf16_tf)
+        line["tiny_prefill"] = tiny_prefill_bench(q, torch)
+    if rank == 0 and not args.no_stack:
+        del layer, w
+        torch.cuda.empty_cache()
+        line["stack"] = stack_bench(q, torch, hbm_gbs, bf16_tf, 10, 3)
     if rank == 0 and world == 1:
         per_seq, n = oracle_decode_seconds_per_seq(shape, B, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(per_seq * B * 1e6, 1), "unit": "us/step",
