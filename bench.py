@@ -528,7 +528,9 @@ def profile_run(args):
     """Eager steps with nothing else on the device: per decode step the kernels
     launch in stage order (norm1, QKV, QKV finish, attention, merge, O, O finish
     + norm2, gate/up + SwiGLU, down, down finish); a prefill step launches
-    norm1, QKV, attention, O, norm2, gate/up, down."""
+    norm1, QKV, attention, O, norm2, gate/up, down; a MoE step (Qwen3-30B-A3B
+    shape) replaces the MLP by router, top-k, permutation, grouped expert GEMMs
+    and combine."""
     import torch
 
     import synth
@@ -544,6 +546,21 @@ def profile_run(args):
         bench = DecodeBench(q, torch, shape, B, layer, CACHE_FILLED + 1)
         for _ in range(args.steps):
             bench.step()
+    elif args.profile == "moe":
+        shape, T = synth.QWEN3_30B_A3B, args.tokens
+        w = gpu_layer_weights(torch, shape, 4000)
+        cfg = q.LayerConfig(shape, max_tokens=T, max_batch=1, max_seq=T, max_position=T)
+        layer = q.Layer(cfg, w)
+        x = torch.randn([1, T, shape.d], device=dev).bfloat16()
+        kc = torch.zeros((1, shape.n_kv_heads, T, shape.head_dim), dtype=torch.bfloat16,
+                         device=dev)
+        vc = torch.zeros_like(kc)
+        pos = torch.arange(T, dtype=torch.int32, device=dev)
+        start = torch.zeros(1, dtype=torch.int32, device=dev)
+        y = torch.empty_like(x)
+        ws = layer.workspace(1, T)
+        for _ in range(args.steps):
+            layer.prefill(x, pos, start, kc, vc, out=y, workspace=ws)
     else:
         shape = synth.QWEN3_8B
         T = args.tokens
@@ -579,7 +596,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--profile", choices=["decode", "prefill"], default=None,
+    ap.add_argument("--profile", choices=["decode", "prefill", "moe"], default=None,
                     help="run --steps untimed eager steps of one workload and exit "
                          "(a short, deterministic launch sequence for a profiler capture)")
     ap.add_argument("--tokens", type=int, default=4096, help="prefill length for --profile")

@@ -71,7 +71,7 @@ typedef struct {
   int32_t qk_norm;      /* 1: Qwen3 per-head RMSNorm on Q and K                */
   double rope_theta;    /* RoPE base, 1e6 for the Qwen configurations          */
   float rms_eps;        /* epsilon of every RMSNorm (also QK-norm)             */
-  int32_t n_experts;    /* E; 0 = dense MLP                                    */
+  int32_t n_experts;    /* E; 0 = dense MLP; else a multiple of 8, <= 248     */
   int32_t top_k;        /* k experts per token (MoE)                           */
   int32_t norm_topk_prob; /* must be 1: softmax over the k selected logits     */
   int32_t router_bias;  /* 1: per-expert FP32 bias added to the router logits  */

@@ -25,7 +25,9 @@ bool config_valid(const qwen_layer_config& c) {
   if (!(c.rope_theta > 0.0) || !(c.rms_eps >= 0.f)) return false;
   if (c.qkv_bias != 0 && c.qkv_bias != 1) return false;
   if (c.qk_norm != 0 && c.qk_norm != 1) return false;
-  if (c.n_experts < 0 || c.n_experts > 256) return false;
+  // the router is one tensor-core GEMM with N = E (a multiple of 8), and the
+  // grouped expert GEMM schedules at most 248 groups
+  if (c.n_experts < 0 || c.n_experts > 248 || (c.n_experts & 7)) return false;
   if (c.n_experts > 0) {
     if (c.top_k < 1 || c.top_k > 8 || c.top_k > c.n_experts) return false;
     if (c.norm_topk_prob != 1) return false;
@@ -58,7 +60,7 @@ PackedLayout packed_layout(const qwen_layer_config& c) {
     L.w_down = take(d * f * 2);
   } else {
     const size_t e = c.n_experts;
-    L.w_router = take(e * d * 2);
+    L.w_router = take(e * 2 * d * 2);  // FP16 [E][2d], each row twice
     L.b_router = take(e * 4);
     L.w_gu = take(e * 2 * f * d * 2);
     L.w_down = take(e * d * f * 2);
@@ -85,16 +87,16 @@ WorkspaceLayout workspace_layout(const qwen_layer_config& c, int B, int T) {
   }
   W.attn = take(M * nq * 2);
   W.r32 = take(M * d * 4);  // residual stream R kept in FP32
-  W.z = take(M * d * 2);
+  // MoE: Z rows are [Z_hi | Z_lo] (2d FP16), the router's split-precision operand
+  W.z = take(M * d * 2 * (c.n_experts ? 2 : 1));
   if (c.n_experts == 0) {
     W.h = take(M * f * 2);
   } else {
     const size_t e = c.n_experts, k = c.top_k, mk = M * k;
-    W.z32 = take(M * d * 4);
     W.logits = take(M * e * 4);
     W.topk_idx = take(mk * 4);
     W.topk_w = take(mk * 4);
-    W.counts = take(e * 4);
+    W.blk_counts = take(moe_perm_blocks(mk) * e * 4);
     W.offsets = take((e + 1) * 4);
     W.perm = take(mk * 4);
     W.inv = take(mk * 4);
@@ -132,7 +134,7 @@ static bool copy_d2d(void* dst, const void* src, size_t bytes, cudaStream_t st) 
 // block i and block 2i+1 = up block i, so one GEMM tile holds both halves of
 // every SwiGLU output feature.
 __global__ void pack_rows_f16_kernel(f16* __restrict__ dst, const bf16* __restrict__ src,
-                                     size_t rows, int d, int mode) {
+                                     size_t rows, int d, int mode, size_t ldd, size_t coff) {
   const int cpr = d / 8;  // 16-byte chunks per row
   const size_t nch = rows * (size_t)cpr;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nch;
@@ -148,17 +150,19 @@ __global__ void pack_rows_f16_kernel(f16* __restrict__ dst, const bf16* __restri
       const float2 f = unpack_bf16x2(w[j]);
       o[j] = pack_f16x2(fminf(fmaxf(f.x, -65504.f), 65504.f), fminf(fmaxf(f.y, -65504.f), 65504.f));
     }
-    reinterpret_cast<uint4*>(dst)[dr * cpr + c] = make_uint4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<uint4*>(dst + dr * ldd + coff)[c] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
+// Rows of BF16 [rows][d] -> FP16, written `ldd` elements apart (0 = d) from
+// column `coff` (mode 1/2: gate/up rows interleaved in 64-row blocks).
 static bool pack_rows(f16* dst, const void* src, size_t rows, size_t d, int mode,
-                      cudaStream_t st) {
+                      cudaStream_t st, size_t ldd = 0, size_t coff = 0) {
   if (rows == 0) return true;
   const size_t nch = rows * (d / 8);
   const int blocks = (int)((nch + 255) / 256 < 65535 ? (nch + 255) / 256 : 65535);
   pack_rows_f16_kernel<<<blocks, 256, 0, st>>>(dst, static_cast<const bf16*>(src), rows, (int)d,
-                                               mode);
+                                               mode, ldd ? ldd : d, coff);
   count_launches();
   return cudaGetLastError() == cudaSuccess;
 }
@@ -222,7 +226,7 @@ qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_wei
   h->w_o = reinterpret_cast<f16*>(P + L.w_o);
   h->w_gu = reinterpret_cast<f16*>(P + L.w_gu);
   h->w_down = reinterpret_cast<f16*>(P + L.w_down);
-  h->w_router = moe ? reinterpret_cast<bf16*>(P + L.w_router) : nullptr;
+  h->w_router = moe ? reinterpret_cast<f16*>(P + L.w_router) : nullptr;
   h->b_router = (moe && c.router_bias) ? reinterpret_cast<float*>(P + L.b_router) : nullptr;
 
   bool ok = cudaMemsetAsync(h->status, 0, 256, st) == cudaSuccess;
@@ -251,7 +255,8 @@ qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_wei
   ok = ok && pack_rows(h->w_gu, w->w_up, n_exp * f, d, 2, st);
   ok = ok && pack_rows(h->w_down, w->w_down, n_exp * d, f, 0, st);
   if (moe) {
-    ok = ok && copy_d2d(h->w_router, w->w_router, n_exp * d * 2, st);
+    ok = ok && pack_rows(h->w_router, w->w_router, n_exp, d, 0, st, 2 * d, 0);
+    ok = ok && pack_rows(h->w_router, w->w_router, n_exp, d, 0, st, 2 * d, d);
     if (c.router_bias) ok = ok && copy_d2d(h->b_router, w->b_router, n_exp * 4, st);
   }
   // RoPE table: (cos, sin) of p * theta^(-2i/dh), angles and trig in FP64.

@@ -17,7 +17,7 @@ struct PackedLayout {
 struct WorkspaceLayout {
   size_t xh, q, k16, v16, attn, r32, z, h;
   // MoE
-  size_t z32, logits, topk_idx, topk_w, counts, offsets, perm, inv, zp, hp, yp;
+  size_t logits, topk_idx, topk_w, blk_counts, offsets, perm, inv, zp, hp, yp;
   // decode (T == 1)
   size_t part, attn_o, attn_ml;
   size_t total;
@@ -37,7 +37,9 @@ struct qwen_layer_s {
   float* b_qkv;
   __half* w_o;
   __half *w_gu, *w_down;  // gate/up rows interleaved in 64-row blocks
-  __nv_bfloat16* w_router;
+  // router weights as FP16 [E][2d], each row twice ([W_r | W_r]): the logits
+  // are one GEMM over [Z_hi | Z_lo] (Z split into two FP16 parts)
+  __half* w_router;
   float* b_router;
   // optional per-stage events (qwen_layer_set_trace)
   bool tracing = false;
@@ -77,6 +79,9 @@ qwen_status moe_forward(qwen_layer_s* L, const __nv_bfloat16* r, const float* r3
 int decode_splits(int N, int K);
 // Bytes of FP32 partials the decode GEMM of the layer needs for batch B.
 size_t decode_part_bytes(const qwen_layer_config& c, int B);
+
+// CTAs of the MoE permutation for `entries` (token, slot) pairs (1024 each).
+int moe_perm_blocks(size_t entries);
 // Attention split-KV plan: number of splits per (sequence, KV head) for batch B.
 void decode_attn_plan(const qwen_layer_config& c, int B, int* splits);
 

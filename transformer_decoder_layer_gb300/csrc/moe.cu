@@ -8,12 +8,18 @@
 // then the residual add.  Selection ties go to the lower expert index.
 //
 // Steps (all on the caller's stream, no host synchronisation):
-//   1. RMSNorm_2 of R -> Z (FP16 GEMM operand) and Z32 (FP32, for the router)
-//   2. router: logits = Z32 W_r^T + b_r in FP32 (SIMT FMA, smem-tiled)
-//   3. top-k: one warp per token, k rounds of a warp arg-max
-//   4. permutation: expert histogram (integer atomics, order-free), then one
-//      CTA per expert writes its (token, slot) entries in token order (stable
-//      counting sort) and the group offsets; gather of Z rows
+//   1. RMSNorm_2 of R -> Z as two FP16 parts per row, [Z_hi | Z_lo]: Z_hi is
+//      the experts' GEMM operand, Z_hi + Z_lo carries the FP32 value to ~2^-22
+//   2. router: logits = [Z_hi | Z_lo] [W_r | W_r]^T on the tensor cores (one
+//      GEMM over K = 2d, FP32 accumulate), i.e. Z W_r^T with FP32-grade inputs:
+//      the logits differ from an FP32 evaluation by ~1e-6, far below the 1e-3
+//      selection gaps the top-k must reproduce
+//   3. top-k: one warp per token, k rounds of a warp arg-max; adds b_r and
+//      writes the biased logits back
+//   4. permutation (stable counting sort by expert, in entry order t*k + j):
+//      per-block expert counts, then per block the starting position of each
+//      expert (all counts of earlier experts, plus this expert's counts in
+//      earlier blocks) and warp-level ranks; gather of Z_hi rows
 //   5. grouped GEMM gate/up (+SiLU*up) and grouped GEMM down over per-expert
 //      row ranges, one persistent tensor-core kernel each
 //   6. combine: Y[t] = R[t] + sum_j w[t][j] Y_e[pos(t, j)] in slot order
@@ -25,60 +31,11 @@ namespace qwen {
 
 namespace {
 
-constexpr int kRT = 32;   // router: tokens per CTA
-constexpr int kRE = 128;  // router: experts per CTA
-constexpr int kRK = 32;   // router: k chunk
+constexpr int kPermBlock = 1024;  // permutation entries per CTA
 
-__global__ void __launch_bounds__(256) router_kernel(const float* __restrict__ z32,
-                                                     const bf16* __restrict__ wr,
-                                                     const float* __restrict__ br,
-                                                     float* __restrict__ logits, int T, int E,
-                                                     int d) {
-  pdl_trigger();
-  pdl_wait();
-  __shared__ float zs[kRK][kRT];       // [k][token]
-  __shared__ float ws[kRK][kRE + 4];   // [k][expert]
-  const int t0 = blockIdx.x * kRT, e0 = blockIdx.y * kRE;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // experts 4tx.., tokens 4ty..
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < d; k0 += kRK) {
-    for (int i = threadIdx.x; i < kRT * kRK; i += 256) {
-      const int t = i / kRK, kk = i % kRK;
-      zs[kk][t] = (t0 + t < T) ? z32[(size_t)(t0 + t) * d + k0 + kk] : 0.f;
-    }
-    for (int i = threadIdx.x; i < kRE * kRK; i += 256) {
-      const int e = i / kRK, kk = i % kRK;
-      ws[kk][e] = (e0 + e < E) ? __bfloat162float(wr[(size_t)(e0 + e) * d + k0 + kk]) : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < kRK; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&zs[kk][4 * ty]);
-      const float4 b = *reinterpret_cast<const float4*>(&ws[kk][4 * tx]);
-      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + 4 * ty + i;
-    if (t >= T) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + 4 * tx + j;
-      if (e < E) logits[(size_t)t * E + e] = acc[i][j] + (br ? br[e] : 0.f);
-    }
-  }
-}
-
-// One warp per token: k rounds of arg-max (larger logit first, lower index on
-// ties), then the weights softmax(selected logits).
-__global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k,
-                            int32_t* __restrict__ idx, float* __restrict__ w) {
+// logits [T][E] are Z W_r^T on entry and Z W_r^T + b_r on exit.
+__global__ void topk_kernel(float* __restrict__ logits, const float* __restrict__ bias, int T,
+                            int E, int k, int32_t* __restrict__ idx, float* __restrict__ w) {
   pdl_trigger();
   pdl_wait();
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -88,8 +45,16 @@ __global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int 
   float v[8];
   unsigned taken = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    v[i] = (i < per && lane + 32 * i < E) ? logits[(size_t)t * E + lane + 32 * i] : -INFINITY;
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    if (i < per && e < E) {
+      float x = logits[(size_t)t * E + e] + (bias ? bias[e] : 0.f);
+      logits[(size_t)t * E + e] = x;
+      v[i] = x == x ? x : -INFINITY;  // a NaN logit is never preferred
+    } else {
+      v[i] = -INFINITY;
+    }
+  }
   float sel[8];
   int sel_i[8];
   for (int j = 0; j < k; ++j) {
@@ -133,85 +98,83 @@ __global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int 
   }
 }
 
-__global__ void expert_hist_kernel(const int32_t* __restrict__ idx, int n, int E,
-                                   int32_t* __restrict__ counts) {
+// Per-block expert counts: block g counts entries [g*1024, (g+1)*1024).
+__global__ void __launch_bounds__(kPermBlock) perm_count_kernel(const int32_t* __restrict__ idx,
+                                                                int n, int E,
+                                                                int32_t* __restrict__ blk_counts) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ int32_t h[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) h[e] = 0;
   __syncthreads();
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-    const int e = idx[i];
-    if (e >= 0 && e < E) atomicAdd(&h[e], 1);
-  }
+  const int i = blockIdx.x * kPermBlock + threadIdx.x;
+  if (i < n) atomicAdd(&h[min(max(idx[i], 0), E - 1)], 1);
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    if (h[e]) atomicAdd(&counts[e], h[e]);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) blk_counts[(size_t)blockIdx.x * E + e] = h[e];
 }
 
-// One CTA per expert: stable positions of its entries (entry = t*k + j, in
-// entry order), perm[pos] = entry, inv[entry] = pos.  CTA 0 also writes the
-// group offsets [E+1].
-__global__ void __launch_bounds__(256) expert_scatter_kernel(const int32_t* __restrict__ idx,
-                                                             int n, int E,
-                                                             const int32_t* __restrict__ counts,
-                                                             int32_t* __restrict__ offsets,
-                                                             int32_t* __restrict__ perm,
-                                                             int32_t* __restrict__ inv) {
+// Stable positions: entry i of block g with expert e goes to
+//   offsets[e] + (entries of e in blocks < g) + (entries of e before i in block g),
+// the last term from warp match masks plus the counts of earlier warps.
+// perm[pos] = entry, inv[entry] = pos; block 0 writes offsets[0..E].
+__global__ void __launch_bounds__(kPermBlock) perm_scatter_kernel(
+    const int32_t* __restrict__ idx, int n, int E, int G, const int32_t* __restrict__ blk_counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
   pdl_trigger();
   pdl_wait();
-  __shared__ int32_t warp_tot[8];
-  __shared__ int32_t base_s;
-  const int e = blockIdx.x;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int i = 0; i < e; ++i) acc += counts[i];
-    base_s = acc;
-    if (e == 0) {
-      int o = 0;
-      for (int i = 0; i < E; ++i) {
-        offsets[i] = o;
-        o += counts[i];
-      }
-      offsets[E] = o;
+  extern __shared__ int32_t sm[];
+  int32_t* tot = sm;               // [E] all entries of e
+  int32_t* base = sm + E;          // [E] first position of e for this block
+  int32_t* wcnt = sm + 2 * E;      // [32][E] entries of e per warp of this block
+  const int g = blockIdx.x, lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int all = 0, before = 0;
+    for (int b = 0; b < G; ++b) {
+      const int c = blk_counts[(size_t)b * E + e];
+      all += c;
+      before += b < g ? c : 0;
     }
+    tot[e] = all;
+    base[e] = before;
   }
+  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
-  int base = base_s;
-  for (int c0 = 0; c0 < n; c0 += 256) {
-    const int i = c0 + threadIdx.x;
-    const bool hit = i < n && idx[i] == e;
-    const unsigned bal = __ballot_sync(0xffffffffu, hit);
-    const int rank_in_warp = __popc(bal & ((1u << lane) - 1u));
-    if (lane == 0) warp_tot[wid] = __popc(bal);
-    __syncthreads();
-    int before = 0, total = 0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      before += (w < wid) ? warp_tot[w] : 0;
-      total += warp_tot[w];
+  if (threadIdx.x == 0) {
+    int o = 0;
+    for (int e = 0; e < E; ++e) {
+      if (g == 0) offsets[e] = o;
+      base[e] += o;
+      o += tot[e];
     }
-    if (hit) {
-      const int pos = base + before + rank_in_warp;
-      perm[pos] = i;
-      inv[i] = pos;
-    }
-    base += total;
-    __syncthreads();
+    if (g == 0) offsets[E] = o;
+  }
+  const int i = g * kPermBlock + threadIdx.x;
+  const bool valid = i < n;
+  const int e = valid ? min(max(idx[i], 0), E - 1) : -1;
+  const unsigned same = __match_any_sync(0xffffffffu, e);
+  const int rank_w = __popc(same & ((1u << lane) - 1u));
+  if (valid && rank_w == 0) wcnt[wid * E + e] = __popc(same);
+  __syncthreads();
+  if (valid) {
+    int pos = base[e] + rank_w;
+    for (int w = 0; w < wid; ++w) pos += wcnt[w * E + e];
+    perm[pos] = i;
+    inv[i] = pos;
   }
 }
 
-// zp[pos] = z[perm[pos] / k]  (16-bit rows of d elements), one warp per row
-__global__ void gather_rows_kernel(const uint16_t* __restrict__ z, const int32_t* __restrict__ perm,
-                                   int n, int k, int d, uint16_t* __restrict__ zp) {
+// zp[pos] = z[perm[pos] / k]  (16-bit rows of d elements; z rows `zs` apart),
+// one warp per row
+__global__ void gather_rows_kernel(const uint16_t* __restrict__ z, size_t zs,
+                                   const int32_t* __restrict__ perm, int n, int k, int d,
+                                   uint16_t* __restrict__ zp) {
   pdl_trigger();
   pdl_wait();
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= n) return;
   const int t = perm[row] / k;
-  const uint4* src = reinterpret_cast<const uint4*>(z + (size_t)t * d);
+  const uint4* src = reinterpret_cast<const uint4*>(z + (size_t)t * zs);
   uint4* dst = reinterpret_cast<uint4*>(zp + (size_t)row * d);
   for (int c = lane; c < d / 8; c += 32) dst[c] = src[c];
 }
@@ -276,6 +239,8 @@ inline int nblk(long long n, int t) { return (int)((n + t - 1) / t); }
 
 }  // namespace
 
+int moe_perm_blocks(size_t entries) { return (int)((entries + kPermBlock - 1) / kPermBlock); }
+
 qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* y, float* y32, int T,
                         int32_t* topk_idx_out, float* topk_w_out, float* logits_out, uint8_t* ws,
                         const WorkspaceLayout& W, cudaStream_t st) {
@@ -283,12 +248,11 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
   const int d = c.d, E = c.n_experts, k = c.top_k, mf = c.ffn;
   const int n = T * k;
   int* err = L->status;
-  f16* z = reinterpret_cast<f16*>(ws + W.z);
-  float* z32 = reinterpret_cast<float*>(ws + W.z32);
+  f16* z = reinterpret_cast<f16*>(ws + W.z);  // rows [Z_hi | Z_lo], 2d apart
   float* logits = reinterpret_cast<float*>(ws + W.logits);
   int32_t* idx = reinterpret_cast<int32_t*>(ws + W.topk_idx);
   float* wts = reinterpret_cast<float*>(ws + W.topk_w);
-  int32_t* counts = reinterpret_cast<int32_t*>(ws + W.counts);
+  int32_t* blk_counts = reinterpret_cast<int32_t*>(ws + W.blk_counts);
   int32_t* offsets = reinterpret_cast<int32_t*>(ws + W.offsets);
   int32_t* perm = reinterpret_cast<int32_t*>(ws + W.perm);
   int32_t* inv = reinterpret_cast<int32_t*>(ws + W.inv);
@@ -297,25 +261,29 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
   f16* yp = reinterpret_cast<f16*>(ws + W.yp);
   qwen_status s;
 
-  // 1. RMSNorm_2 -> Z (FP16) and Z32 (FP32 router input)
-  if ((s = rmsnorm_launch(r, L->gamma_mlp, z, true, z32, r32, T, d, c.rms_eps, st))) return s;
-  // 2. router logits in FP32
-  launch_k(router_kernel, dim3(nblk(T, kRT), nblk(E, kRE)), dim3(256), 0, st, (const float*)z32,
-           (const bf16*)L->w_router, (const float*)L->b_router, logits, T, E, d);
+  // 1. RMSNorm_2 -> [Z_hi | Z_lo] (FP16 parts of the FP32 result)
+  if ((s = rmsnorm_launch(r, L->gamma_mlp, z, true, nullptr, r32, T, d, c.rms_eps, st, 0,
+                          2 * (size_t)d, z + d)))
+    return s;
+  // 2. router logits: one tensor-core GEMM over K = 2d against [W_r | W_r]
+  GemmEpilogue er{};
+  er.mode = EPI_F32;
+  er.out32 = logits;
+  er.ldo32 = E;
+  er.b_static = 1;
+  if ((s = gemm_tc(z, 2 * d, L->w_router, 2 * d, T, E, 2 * d, true, er, err, st))) return s;
+  // 3. top-k (+ router bias) + softmax over the selected logits
+  launch_k(topk_kernel, dim3(nblk(32LL * T, 256)), dim3(256), 0, st, logits,
+           (const float*)L->b_router, T, E, k, idx, wts);
   count_launches();
-  // 3. top-k + softmax over the selected logits
-  launch_k(topk_kernel, dim3(nblk(32LL * T, 256)), dim3(256), 0, st, (const float*)logits, T, E, k,
-           idx, wts);
-  count_launches();
-  // 4. permutation by expert (stable in token order) and gather of Z rows
-  if (cudaMemsetAsync(counts, 0, (size_t)E * sizeof(int32_t), st) != cudaSuccess)
-    return QWEN_ERR_CUDA;
-  launch_k(expert_hist_kernel, dim3(nblk(n, 1024) < 148 ? nblk(n, 1024) : 148), dim3(1024),
-           E * sizeof(int32_t), st, (const int32_t*)idx, n, E, counts);
-  launch_k(expert_scatter_kernel, dim3(E), dim3(256), 0, st, (const int32_t*)idx, n, E,
-           (const int32_t*)counts, offsets, perm, inv);
+  // 4. permutation by expert (stable in entry order) and gather of Z_hi rows
+  const int G = moe_perm_blocks(n);
+  launch_k(perm_count_kernel, dim3(G), dim3(kPermBlock), E * sizeof(int32_t), st,
+           (const int32_t*)idx, n, E, blk_counts);
+  launch_k(perm_scatter_kernel, dim3(G), dim3(kPermBlock), (2 + 32) * E * sizeof(int32_t), st,
+           (const int32_t*)idx, n, E, G, (const int32_t*)blk_counts, offsets, perm, inv);
   launch_k(gather_rows_kernel, dim3(nblk(32LL * n, 256)), dim3(256), 0, st,
-           reinterpret_cast<const uint16_t*>(z), (const int32_t*)perm, n, k, d,
+           reinterpret_cast<const uint16_t*>(z), 2 * (size_t)d, (const int32_t*)perm, n, k, d,
            reinterpret_cast<uint16_t*>(zp));
   count_launches(3);
   if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;

@@ -14,7 +14,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
                                                       const bf16* __restrict__ gamma,
                                                       void* __restrict__ y, bool y_f16,
                                                       float* __restrict__ y32, int rows, int d,
-                                                      float eps, size_t xs) {
+                                                      float eps, size_t xs, size_t ys,
+                                                      __half* __restrict__ y_lo) {
   pdl_trigger();
   pdl_wait();
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -58,7 +59,8 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
   ss = warp_sum(ss);
   const float rstd = rsqrtf(ss / (float)d + eps);
   const uint4* gr = reinterpret_cast<const uint4*>(gamma);
-  uint4* yr = reinterpret_cast<uint4*>(static_cast<uint16_t*>(y) + (size_t)row * d);
+  uint4* yr = reinterpret_cast<uint4*>(static_cast<uint16_t*>(y) + (size_t)row * ys);
+  uint4* lr = y_lo ? reinterpret_cast<uint4*>(y_lo + (size_t)row * ys) : nullptr;
 #pragma unroll
   for (int i = 0; i < MAXC; ++i) {
     const int c = lane + 32 * i;
@@ -78,6 +80,17 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
       out.z = pack2(o[4], o[5], y_f16);
       out.w = pack2(o[6], o[7], y_f16);
       yr[c] = out;
+      if (lr) {
+        // residual of the FP16 rounding, itself rounded to FP16
+        const uint32_t hw[4] = {out.x, out.y, out.z, out.w};
+        uint32_t lo[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 h = unpack_f16x2(hw[j]);
+          lo[j] = pack_f16x2(o[2 * j] - h.x, o[2 * j + 1] - h.y);
+        }
+        lr[c] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
       if (y32) {
         float4* y4 = reinterpret_cast<float4*>(y32 + (size_t)row * d);
         y4[2 * c] = make_float4(o[0], o[1], o[2], o[3]);
@@ -89,21 +102,23 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
 
 qwen_status rmsnorm_launch(const bf16* x, const bf16* gamma, void* y, bool y_f16, float* y32,
                            const float* x32, int rows, int d, float eps, cudaStream_t st,
-                           size_t x_stride) {
+                           size_t x_stride, size_t y_stride, __half* y_lo) {
   if (rows == 0) return QWEN_OK;
   if (d <= 0 || (d & 7) || d > 8192) return QWEN_ERR_UNSUPPORTED;
   const size_t xs = x_stride ? x_stride : (size_t)d;
+  const size_t ys = y_stride ? y_stride : (size_t)d;
+  if (y_lo && !y_f16) return QWEN_ERR_INVALID_ARG;
   const int threads = 256;
   const int blocks = (rows * 32 + threads - 1) / threads;
   if (d <= 2048)
     launch_k(rmsnorm_kernel<8>, dim3(blocks), dim3(threads), 0, st, x, x32, gamma, y, y_f16, y32,
-             rows, d, eps, xs);
+             rows, d, eps, xs, ys, y_lo);
   else if (d <= 4096)
     launch_k(rmsnorm_kernel<16>, dim3(blocks), dim3(threads), 0, st, x, x32, gamma, y, y_f16, y32,
-             rows, d, eps, xs);
+             rows, d, eps, xs, ys, y_lo);
   else
     launch_k(rmsnorm_kernel<32>, dim3(blocks), dim3(threads), 0, st, x, x32, gamma, y, y_f16, y32,
-             rows, d, eps, xs);
+             rows, d, eps, xs, ys, y_lo);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
