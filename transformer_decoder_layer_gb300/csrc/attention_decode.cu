@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      const uint64_t pol = l2_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       int lu = 0;  // local unit counter
@@ -165,8 +166,10 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
 #pragma unroll
           for (int c = 0; c < DH / 64; ++c) {
-            tma_load_2d(st + c * C::BOX_BYTES, &tmK, &full[stage], c * 64, row0 + blk);
-            tma_load_2d(st + C::KV_BYTES + c * C::BOX_BYTES, &tmV, &full[stage], c * 64, row0 + blk);
+            // the cache is read once per step: evicted first
+            tma_load_2d_hint(st + c * C::BOX_BYTES, &tmK, &full[stage], c * 64, row0 + blk, pol);
+            tma_load_2d_hint(st + C::KV_BYTES + c * C::BOX_BYTES, &tmV, &full[stage], c * 64,
+                             row0 + blk, pol);
           }
           if (++stage == kDStages) {
             stage = 0;

@@ -104,6 +104,9 @@ __global__ void __launch_bounds__(kDThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmW);
       tma_prefetch_desc(&tmX);
+      // weights are read once per step: evicted first, so the activations
+      // the small kernels between the GEMMs read stay in L2
+      const uint64_t wpol = l2_evict_first();
       // weights are never written by the kernels before this one: stream the
       // first stages of weight tiles while the previous kernel finishes
       int pre = 0;
@@ -113,7 +116,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         pre = min(C::STAGES, kb1 - kb0);
         for (int i = 0; i < pre; ++i) {
           mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
-          tma_load_2d(sA + i * C::A_BYTES, &tmW, &full[i], (kb0 + i) * kDBK, n0);
+          tma_load_2d_hint(sA + i * C::A_BYTES, &tmW, &full[i], (kb0 + i) * kDBK, n0, wpol);
         }
       }
       pdl_wait();
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
           } else {
             if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) goto prod_done;
             mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-            tma_load_2d(sA + stage * C::A_BYTES, &tmW, &full[stage], kb * kDBK, n0);
+            tma_load_2d_hint(sA + stage * C::A_BYTES, &tmW, &full[stage], kb * kDBK, n0, wpol);
             tma_load_2d(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * kDBK, 0);
           }
           if (++stage == C::STAGES) {
