@@ -445,6 +445,98 @@ def moe_prefill_bench(q, torch, peak_tflops, steps=5, warmup=2):
             "frac_of_peak_executed": round(flops_exec / (ms * 1e-3) / 1e12 / peak_tflops, 3)}
 
 
+def moe_decode_bench(q, torch, hbm_gbs, steps=20, warmup=3, cached=4096):
+    """Qwen3-30B-A3B-shaped MoE layer decode against `cached` tokens: bytes =
+    attention and router weights + the experts the batch touches + KV."""
+    import synth
+    shape = synth.QWEN3_30B_A3B
+    w = gpu_layer_weights(torch, shape, 4000)
+    S = cached + 1
+    layer = q.Layer(q.LayerConfig(shape, max_tokens=64, max_batch=64, max_seq=S, max_position=S), w)
+    g = torch.Generator(device="cuda").manual_seed(7)
+    out = {}
+    d, hq, hkv, dh, E, k, mf = (shape.d, shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
+                                shape.n_experts, shape.top_k, shape.ffn)
+    attn_w = 2 * (d * (hq + 2 * hkv) * dh + hq * dh * d) + 2 * E * d * 2
+    for B in (1, 8, 32):
+        kc = torch.randn((B, hkv, S, dh), generator=g, device="cuda").bfloat16()
+        vc = torch.randn_like(kc)
+        x = torch.randn([B, d], generator=g, device="cuda").bfloat16()
+        pos = torch.full((B,), cached, dtype=torch.int32, device="cuda")
+        y = torch.empty_like(x)
+        ws = layer.workspace(B, 1)
+        idx = torch.empty((B, k), dtype=torch.int32, device="cuda")
+        layer.decode(x, pos, pos, kc, vc, out=y, workspace=ws)
+        # experts touched: the step's input rows routed through the same router
+        # (a proxy for the routing of norm(R) inside the step)
+        layer.moe_ffn(x, out=torch.empty_like(x), topk_idx=idx)
+        touched = int(torch.unique(idx).numel())
+        for _ in range(warmup):
+            layer.decode(x, pos, pos, kc, vc, out=y, workspace=ws)
+        torch.cuda.synchronize()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for _ in range(steps):
+                layer.decode(x, pos, pos, kc, vc, out=y, workspace=ws)
+        graph.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / steps
+        del graph
+        nbytes = attn_w + touched * 3 * d * mf * 2 + B * 2 * hkv * cached * dh * 2
+        out[f"B={B}"] = {"us_per_step": round(us, 2), "experts_touched": touched,
+                         "bytes_per_step": nbytes, "GB_per_s": round(nbytes / (us * 1e-6) / 1e9, 1),
+                         "frac_hbm": round(nbytes / (us * 1e-6) / 1e9 / hbm_gbs, 3)}
+    assert layer.poll_error() == 0
+    return {"workload": f"qwen3-30b-a3b-shaped MoE layer decode, {cached} cached tokens", **out}
+
+
+def long_decode_bench(q, torch, hbm_gbs, B=8, cached=32768, steps=20, warmup=3):
+    """Qwen2.5-7B-shaped layer decode with a long cache (the KV read outgrows the
+    weights)."""
+    import synth
+    shape = synth.QWEN25_7B
+    w = gpu_layer_weights(torch, shape, 1)
+    S = cached + 1
+    layer = q.Layer(q.LayerConfig(shape, max_tokens=B, max_batch=B, max_seq=S, max_position=S), w)
+    g = torch.Generator(device="cuda").manual_seed(8)
+    kc = torch.randn((B, shape.n_kv_heads, S, shape.head_dim), generator=g, device="cuda").bfloat16()
+    vc = torch.randn_like(kc)
+    x = torch.randn([B, shape.d], generator=g, device="cuda").bfloat16()
+    pos = torch.full((B,), cached, dtype=torch.int32, device="cuda")
+    y = torch.empty_like(x)
+    ws = layer.workspace(B, 1)
+    for _ in range(warmup):
+        layer.decode(x, pos, pos, kc, vc, out=y, workspace=ws)
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        for _ in range(steps):
+            layer.decode(x, pos, pos, kc, vc, out=y, workspace=ws)
+    graph.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    assert layer.poll_error() == 0
+    us = a.elapsed_time(b) * 1e3 / steps
+    nbytes = decode_bytes(shape, B, cached=cached)
+    return {"workload": f"qwen2.5-7b-shaped layer decode B={B}, {cached} cached tokens",
+            "us_per_step": round(us, 2), "bytes_per_step": nbytes,
+            "GB_per_s": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "frac_hbm": round(nbytes / (us * 1e-6) / 1e9 / hbm_gbs, 3)}
+
+
 def tiny_prefill_bench(q, torch, steps=20, warmup=3):
     """The tiny Qwen3-style layer (d=512, B=1, T=128): launch-bound, reported in us."""
     import synth
@@ -546,6 +638,20 @@ def profile_run(args):
         bench = DecodeBench(q, torch, shape, B, layer, CACHE_FILLED + 1)
         for _ in range(args.steps):
             bench.step()
+    elif args.profile == "moe_decode":
+        shape, B, cached = synth.QWEN3_30B_A3B, args.batch, CACHE_FILLED
+        w = gpu_layer_weights(torch, shape, 4000)
+        S = cached + 1
+        cfg = q.LayerConfig(shape, max_tokens=B, max_batch=B, max_seq=S, max_position=S)
+        layer = q.Layer(cfg, w)
+        kc = torch.randn((B, shape.n_kv_heads, S, shape.head_dim), device=dev).bfloat16()
+        vc = torch.randn_like(kc)
+        x = torch.randn([B, shape.d], device=dev).bfloat16()
+        pos = torch.full((B,), cached, dtype=torch.int32, device=dev)
+        y = torch.empty_like(x)
+        ws = layer.workspace(B, 1)
+        for _ in range(args.steps):
+            layer.decode(x, pos, pos, kc, vc, out=y, workspace=ws)
     elif args.profile == "moe":
         shape, T = synth.QWEN3_30B_A3B, args.tokens
         w = gpu_layer_weights(torch, shape, 4000)
@@ -596,7 +702,7 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-stack", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--profile", choices=["decode", "prefill", "moe"], default=None,
+    ap.add_argument("--profile", choices=["decode", "prefill", "moe", "moe_decode"], default=None,
                     help="run --steps untimed eager steps of one workload and exit "
                          "(a short, deterministic launch sequence for a profiler capture)")
     ap.add_argument("--tokens", type=int, default=4096, help="prefill length for --profile")
@@ -722,6 +828,9 @@ def main():
     if rank == 0 and not args.no_prefill:
         line["moe_prefill"] = moe_prefill_bench(q, torch, bf16_tf)
         line["tiny_prefill"] = tiny_prefill_bench(q, torch)
+    if rank == 0 and not args.no_sweep:
+        line["moe_decode"] = moe_decode_bench(q, torch, hbm_gbs)
+        line["long_decode"] = long_decode_bench(q, torch, hbm_gbs)
     if rank == 0 and not args.no_stack:
         del layer, w
         torch.cuda.empty_cache()

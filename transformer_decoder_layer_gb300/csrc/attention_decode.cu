@@ -411,24 +411,36 @@ __global__ void attn_decode_merge_kernel(const float* __restrict__ part_o,
                                          f16* __restrict__ out) {
   pdl_trigger();
   pdl_wait();
+  extern __shared__ float merge_f[];  // [warps][splits]: the weight of each split
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= BH) return;
+  float* fs = merge_f + (threadIdx.x >> 5) * splits;
   const float* ml = part_ml + (size_t)wid * splits * 2;
-  float M = -INFINITY;
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, ml[2 * s]);
+  // the lanes share the splits for the global max and the row sum
+  float mloc = -INFINITY;
+  for (int s = lane; s < splits; s += 32) mloc = fmaxf(mloc, ml[2 * s]);
+  const float M = warp_max(mloc);
+  float lloc = 0.f;
+  for (int s = lane; s < splits; s += 32) {
+    const float m = ml[2 * s];
+    const float f = (m == -INFINITY) ? 0.f : ex2f(m - M);  // empty split: weight 0
+    lloc += f * ml[2 * s + 1];
+    fs[s] = f;
+  }
+  const float lsum = warp_sum(lloc);
+  __syncwarp();
   float acc[DH / 32];
 #pragma unroll
   for (int i = 0; i < DH / 32; ++i) acc[i] = 0.f;
-  float lsum = 0.f;
+  const float* po = part_o + (size_t)wid * splits * DH + lane;
+#pragma unroll 4
   for (int s = 0; s < splits; ++s) {
-    const float m = ml[2 * s];
-    if (m == -INFINITY) continue;
-    const float f = ex2f(m - M);
-    lsum += f * ml[2 * s + 1];
-    const float* po = part_o + ((size_t)wid * splits + s) * DH;
+    const float f = fs[s];
+    if (f != 0.f) {  // an empty split's partial output is never read
 #pragma unroll
-    for (int i = 0; i < DH / 32; ++i) acc[i] += f * po[lane + 32 * i];
+      for (int i = 0; i < DH / 32; ++i) acc[i] = fmaf(f, po[(size_t)s * DH + 32 * i], acc[i]);
+    }
   }
   const float inv = 1.f / lsum;
 #pragma unroll
@@ -501,7 +513,8 @@ static qwen_status launch_attn_dec(const CUtensorMap& tk, const CUtensorMap& tv,
   count_launches();
   if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;
   const int BH = a.B * a.Hq;
-  launch_k(attn_decode_merge_kernel<DH>, dim3((BH * 32 + 255) / 256), dim3(256), 0, st,
+  launch_k(attn_decode_merge_kernel<DH>, dim3((BH * 32 + 255) / 256), dim3(256),
+           (size_t)(256 / 32) * a.splits * sizeof(float), st,
            (const float*)a.part_o, (const float*)a.part_ml, BH, a.splits, out);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;

@@ -506,6 +506,8 @@ size_t decode_part_bytes(const qwen_layer_config& c, int B) {
   if (c.n_experts == 0) {
     upd(2 * f, d);
     upd(d, f);
+  } else {
+    upd(c.n_experts, 2 * d);  // the router over [Z_hi | Z_lo]
   }
   return m;
 }

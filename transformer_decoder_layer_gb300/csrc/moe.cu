@@ -186,52 +186,62 @@ __global__ void combine_kernel(const f16* __restrict__ yp, const int32_t* __rest
                                bf16* __restrict__ y, float* __restrict__ y32) {
   pdl_trigger();
   pdl_wait();
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
-  for (int c = lane; c < d / 8; c += 32) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const float wj = w[(size_t)t * k + j];
-      const int pos = inv[(size_t)t * k + j];
-      const uint4 u = reinterpret_cast<const uint4*>(yp + (size_t)pos * d)[c];
-      const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+  // one thread per 8-column chunk of one token; the k expert rows are loaded
+  // together (k <= 8) and summed in slot order
+  const int nch = d / 8;
+  const long long gi = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gi >= (long long)T * nch) return;
+  const int t = (int)(gi / nch), c = (int)(gi - (long long)t * nch);
+  uint4 u[8];
+  float wj[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < k) {
+      wj[j] = w[(size_t)t * k + j];
+      u[j] = reinterpret_cast<const uint4*>(yp + (size_t)inv[(size_t)t * k + j] * d)[c];
+    }
+  }
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < k) {
+      const uint32_t q[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 f = unpack_f16x2(q[e]);
-        acc[2 * e] = fmaf(wj, f.x, acc[2 * e]);
-        acc[2 * e + 1] = fmaf(wj, f.y, acc[2 * e + 1]);
+        acc[2 * e] = fmaf(wj[j], f.x, acc[2 * e]);
+        acc[2 * e + 1] = fmaf(wj[j], f.y, acc[2 * e + 1]);
       }
     }
-    float o[8];
-    if (r32) {
-      const float4 a = reinterpret_cast<const float4*>(r32 + (size_t)t * d)[2 * c];
-      const float4 b = reinterpret_cast<const float4*>(r32 + (size_t)t * d)[2 * c + 1];
-      o[0] = a.x + acc[0]; o[1] = a.y + acc[1]; o[2] = a.z + acc[2]; o[3] = a.w + acc[3];
-      o[4] = b.x + acc[4]; o[5] = b.y + acc[5]; o[6] = b.z + acc[6]; o[7] = b.w + acc[7];
-    } else {
-      const uint4 u = reinterpret_cast<const uint4*>(r + (size_t)t * d)[c];
-      const uint32_t q[4] = {u.x, u.y, u.z, u.w};
+  }
+  float o[8];
+  if (r32) {
+    const float4 a = reinterpret_cast<const float4*>(r32 + (size_t)t * d)[2 * c];
+    const float4 b = reinterpret_cast<const float4*>(r32 + (size_t)t * d)[2 * c + 1];
+    o[0] = a.x + acc[0]; o[1] = a.y + acc[1]; o[2] = a.z + acc[2]; o[3] = a.w + acc[3];
+    o[4] = b.x + acc[4]; o[5] = b.y + acc[5]; o[6] = b.z + acc[6]; o[7] = b.w + acc[7];
+  } else {
+    const uint4 ur = reinterpret_cast<const uint4*>(r + (size_t)t * d)[c];
+    const uint32_t q[4] = {ur.x, ur.y, ur.z, ur.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = unpack_bf16x2(q[e]);
-        o[2 * e] = f.x + acc[2 * e];
-        o[2 * e + 1] = f.y + acc[2 * e + 1];
-      }
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = unpack_bf16x2(q[e]);
+      o[2 * e] = f.x + acc[2 * e];
+      o[2 * e + 1] = f.y + acc[2 * e + 1];
     }
-    if (y) {
-      uint4 out;
-      out.x = pack_bf16x2(o[0], o[1]);
-      out.y = pack_bf16x2(o[2], o[3]);
-      out.z = pack_bf16x2(o[4], o[5]);
-      out.w = pack_bf16x2(o[6], o[7]);
-      reinterpret_cast<uint4*>(y + (size_t)t * d)[c] = out;
-    }
-    if (y32) {
-      float4* o4 = reinterpret_cast<float4*>(y32 + (size_t)t * d);
-      o4[2 * c] = make_float4(o[0], o[1], o[2], o[3]);
-      o4[2 * c + 1] = make_float4(o[4], o[5], o[6], o[7]);
-    }
+  }
+  if (y) {
+    uint4 out;
+    out.x = pack_bf16x2(o[0], o[1]);
+    out.y = pack_bf16x2(o[2], o[3]);
+    out.z = pack_bf16x2(o[4], o[5]);
+    out.w = pack_bf16x2(o[6], o[7]);
+    reinterpret_cast<uint4*>(y + (size_t)t * d)[c] = out;
+  }
+  if (y32) {
+    float4* o4 = reinterpret_cast<float4*>(y32 + (size_t)t * d);
+    o4[2 * c] = make_float4(o[0], o[1], o[2], o[3]);
+    o4[2 * c + 1] = make_float4(o[4], o[5], o[6], o[7]);
   }
 }
 
@@ -265,13 +275,24 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
   if ((s = rmsnorm_launch(r, L->gamma_mlp, z, true, nullptr, r32, T, d, c.rms_eps, st, 0,
                           2 * (size_t)d, z + d)))
     return s;
-  // 2. router logits: one tensor-core GEMM over K = 2d against [W_r | W_r]
-  GemmEpilogue er{};
-  er.mode = EPI_F32;
-  er.out32 = logits;
-  er.ldo32 = E;
-  er.b_static = 1;
-  if ((s = gemm_tc(z, 2 * d, L->w_router, 2 * d, T, E, 2 * d, true, er, err, st))) return s;
+  // 2. router logits: one tensor-core GEMM over K = 2d against [W_r | W_r];
+  // decode-sized batches use the swap-AB split-K GEMM (one 128-row weight tile
+  // would otherwise run its whole K on a single SM)
+  if (T <= 256 && W.part != 0) {
+    const int S = decode_splits(E, 2 * d);
+    float* part = reinterpret_cast<float*>(ws + W.part);
+    if ((s = gemm_decode_splitk(L->w_router, z, 2 * d, T, E, 2 * d, S, true, part, err, st,
+                                /*w_static=*/true)))
+      return s;
+    if ((s = reduce_f32(part, S, T, E, logits, E, st))) return s;
+  } else {
+    GemmEpilogue er{};
+    er.mode = EPI_F32;
+    er.out32 = logits;
+    er.ldo32 = E;
+    er.b_static = 1;
+    if ((s = gemm_tc(z, 2 * d, L->w_router, 2 * d, T, E, 2 * d, true, er, err, st))) return s;
+  }
   // 3. top-k (+ router bias) + softmax over the selected logits
   launch_k(topk_kernel, dim3(nblk(32LL * T, 256)), dim3(256), 0, st, logits,
            (const float*)L->b_router, T, E, k, idx, wts);
@@ -305,7 +326,7 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
   ed.n_groups = E;
   if ((s = gemm_tc(hp, mf, L->w_down, mf, n, d, mf, true, ed, err, st))) return s;
   // 6. weighted combine + residual
-  launch_k(combine_kernel, dim3(nblk(32LL * T, 256)), dim3(256), 0, st, (const f16*)yp,
+  launch_k(combine_kernel, dim3(nblk((long long)T * (d / 8), 256)), dim3(256), 0, st, (const f16*)yp,
            (const int32_t*)inv, (const float*)wts, r32, r, T, k, d, y, y32);
   count_launches();
   if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;
