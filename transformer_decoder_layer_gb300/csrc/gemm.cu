@@ -309,8 +309,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // warps 0 and 1 run converged and issue from one elected lane (a lone lane
+  // next to busy epilogue warps gets too few issue slots)
   if (warp == 0) {
-    if (lane == 0) {
+    {
       // stream the first B (weight) tiles while the previous kernel finishes
       int pre = 0;
       TileInfo ti;
@@ -318,8 +320,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           get_tile(blockIdx.x, M, N, BN, n_nblk, epi, s_tile_prefix, ti)) {
         pre = min(C::STAGES, n_kblk);
         for (int i = 0; i < pre; ++i) {
-          mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
-          tma_load_2d(sB + i * C::B_BYTES, &tmB, &full[i], i * kBK, ti.b_row0);
+          mbar_arrive_expect_tx_w(&full[i], C::STAGE_BYTES);
+          tma_load_2d_w(sB + i * C::B_BYTES, &tmB, &full[i], i * kBK, ti.b_row0);
         }
       }
       pdl_wait();
@@ -330,12 +332,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
            tile += gridDim.x) {
         for (int kb = 0; kb < n_kblk; ++kb, ++g) {
           if (g < pre) {
-            tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * kBK, ti.m0);
+            tma_load_2d_w(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * kBK, ti.m0);
           } else {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) goto producer_done;
-            mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-            tma_load_2d(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * kBK, ti.m0);
-            tma_load_2d(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * kBK, ti.b_row0);
+            if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, err)) goto producer_done;
+            mbar_arrive_expect_tx_w(&full[stage], C::STAGE_BYTES);
+            tma_load_2d_w(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * kBK, ti.m0);
+            tma_load_2d_w(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * kBK, ti.b_row0);
           }
           if (++stage == C::STAGES) {
             stage = 0;
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // drain: wait until the MMA warp has consumed every stage we filled, so
       // no TMA write is still in flight when the CTA exits
       for (int s = 0; s < C::STAGES; ++s) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) break;
+        if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, err)) break;
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -355,7 +357,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     producer_done:;
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -364,12 +366,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
            tile += gridDim.x, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, err)) break;
+        if (!mbar_wait_w(&tempty[acc], acc_phase ^ 1u, abort_flag, err)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         bool ok = true;
         for (int kb = 0; kb < n_kblk; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, err)) {
+          if (!mbar_wait_w(&full[stage], phase, abort_flag, err)) {
             ok = false;
             break;
           }
@@ -380,16 +382,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int k = 0; k < kBK / 16; ++k) {
             const uint64_t ad = smem_desc_sw128(a0 + 32 * k, 16, 1024);
             const uint64_t bd = smem_desc_sw128(b0 + 32 * k, 16, 1024);
-            umma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            umma_f16_w(d_tmem, ad, bd, idesc, (kb | k) != 0);
           }
-          umma_commit(&empty[stage]);
+          umma_commit_w(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(&tfull[acc]);
+        umma_commit_w(&tfull[acc]);
       }
     }
   } else {
