@@ -138,10 +138,13 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
   __syncthreads();
 
   if (warp == kCW) {
-    // ---------------- producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
+    // ---------------- producer (converged; one elected lane issues)
+    {
+      if (lane == 0) {
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+      }
+      __syncwarp();
       const uint64_t pol = l2_evict_first();
       int stage = 0;
       uint32_t phase = 0;
@@ -156,19 +159,19 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
         const int row0 = pair * a.max_seq;  // (b * Hkv + g) * max_seq
         // the unit's G query rows (contiguous in q) into its slot of the Q ring
         const int qs = lu % kDStages;
-        if (!mbar_wait(&q_empty[qs], ((lu / kDStages) & 1) ^ 1u, abort_flag, a.err)) goto prod_done;
-        mbar_arrive_expect_tx(&q_full[qs], (uint32_t)(G * DH * 2));
-        bulk_load(sQ + qs * 16 * DH, a.q + ((size_t)b * a.Hq + (size_t)g * G) * DH,
+        if (!mbar_wait_w(&q_empty[qs], ((lu / kDStages) & 1) ^ 1u, abort_flag, a.err)) goto prod_done;
+        mbar_arrive_expect_tx_w(&q_full[qs], (uint32_t)(G * DH * 2));
+        bulk_load_w(sQ + qs * 16 * DH, a.q + ((size_t)b * a.Hq + (size_t)g * G) * DH,
                   (uint32_t)(G * DH * 2), &q_full[qs]);
         for (int blk = k0; blk < k1; blk += kKB) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err)) goto prod_done;
+          if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, a.err)) goto prod_done;
           uint8_t* st = smem + stage * C::STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          mbar_arrive_expect_tx_w(&full[stage], C::STAGE_BYTES);
 #pragma unroll
           for (int c = 0; c < DH / 64; ++c) {
             // the cache is read once per step: evicted first
-            tma_load_2d_hint(st + c * C::BOX_BYTES, &tmK, &full[stage], c * 64, row0 + blk, pol);
-            tma_load_2d_hint(st + C::KV_BYTES + c * C::BOX_BYTES, &tmV, &full[stage], c * 64,
+            tma_load_2d_hint_w(st + c * C::BOX_BYTES, &tmK, &full[stage], c * 64, row0 + blk, pol);
+            tma_load_2d_hint_w(st + C::KV_BYTES + c * C::BOX_BYTES, &tmV, &full[stage], c * 64,
                              row0 + blk, pol);
           }
           if (++stage == kDStages) {
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
         }
       }
       for (int i = 0; i < kDStages; ++i) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.err)) break;
+        if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, a.err)) break;
         if (++stage == kDStages) {
           stage = 0;
           phase ^= 1u;

@@ -100,8 +100,9 @@ __global__ void __launch_bounds__(kDThreads, 1)
     kb1 = (int)(((long long)(s + 1) * n_kblk) / splits);
   };
 
+  // warps 0 and 1 run converged and issue from one elected lane
   if (warp == 0) {
-    if (lane == 0) {
+    {
       tma_prefetch_desc(&tmW);
       tma_prefetch_desc(&tmX);
       // weights are read once per step: evicted first, so the activations
@@ -115,8 +116,8 @@ __global__ void __launch_bounds__(kDThreads, 1)
         unit_range(blockIdx.x, n0, kb0, kb1, s);
         pre = min(C::STAGES, kb1 - kb0);
         for (int i = 0; i < pre; ++i) {
-          mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
-          tma_load_2d_hint(sA + i * C::A_BYTES, &tmW, &full[i], (kb0 + i) * kDBK, n0, wpol);
+          mbar_arrive_expect_tx_w(&full[i], C::STAGE_BYTES);
+          tma_load_2d_hint_w(sA + i * C::A_BYTES, &tmW, &full[i], (kb0 + i) * kDBK, n0, wpol);
         }
       }
       pdl_wait();
@@ -128,12 +129,12 @@ __global__ void __launch_bounds__(kDThreads, 1)
         unit_range(u, n0, kb0, kb1, s);
         for (int kb = kb0; kb < kb1; ++kb, ++g) {
           if (g < pre) {
-            tma_load_2d(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * kDBK, 0);
+            tma_load_2d_w(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * kDBK, 0);
           } else {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) goto prod_done;
-            mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-            tma_load_2d_hint(sA + stage * C::A_BYTES, &tmW, &full[stage], kb * kDBK, n0, wpol);
-            tma_load_2d(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * kDBK, 0);
+            if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, err)) goto prod_done;
+            mbar_arrive_expect_tx_w(&full[stage], C::STAGE_BYTES);
+            tma_load_2d_hint_w(sA + stage * C::A_BYTES, &tmW, &full[stage], kb * kDBK, n0, wpol);
+            tma_load_2d_w(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * kDBK, 0);
           }
           if (++stage == C::STAGES) {
             stage = 0;
@@ -142,7 +143,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         }
       }
       for (int i = 0; i < C::STAGES; ++i) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) break;
+        if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, err)) break;
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -151,7 +152,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
     prod_done:;
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -159,12 +160,12 @@ __global__ void __launch_bounds__(kDThreads, 1)
         int n0, kb0, kb1, s;
         unit_range(u, n0, kb0, kb1, s);
         const int acc = local & 1;
-        if (!mbar_wait(&tempty[acc], ((local >> 1) & 1) ^ 1u, abort_flag, err)) break;
+        if (!mbar_wait_w(&tempty[acc], ((local >> 1) & 1) ^ 1u, abort_flag, err)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * BP;
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, err)) {
+          if (!mbar_wait_w(&full[stage], phase, abort_flag, err)) {
             ok = false;
             break;
           }
@@ -173,16 +174,16 @@ __global__ void __launch_bounds__(kDThreads, 1)
           const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
           for (int k = 0; k < kDBK / 16; ++k)
-            umma_f16(d, smem_desc_sw128(a0 + 32 * k, 16, 1024), smem_desc_sw128(b0 + 32 * k, 16, 1024),
+            umma_f16_w(d, smem_desc_sw128(a0 + 32 * k, 16, 1024), smem_desc_sw128(b0 + 32 * k, 16, 1024),
                      idesc, (kb != kb0) || k);
-          umma_commit(&empty[stage]);
+          umma_commit_w(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(&tfull[acc]);
+        umma_commit_w(&tfull[acc]);
       }
     }
   } else {
