@@ -27,6 +27,7 @@ from .layer import (  # noqa: F401
     rmsnorm,
     linear,
     silu,
+    sigmoid,
     rope_angles,
     apply_rope_rotate_half,
     gqa_attention,

@@ -256,13 +256,16 @@ def layer_forward(x, w, cfg, positions, k_cache, v_cache, slots,
 # Mixture of experts
 # --------------------------------------------------------------------------
 
-def router_topk(z, w_router, b_router, k):
-    """Router logits, top-k selection and softmax over the selected logits.
+def router_topk(z, w_router, b_router, k, norm_topk_prob=True):
+    """Router logits, top-k selection and the gating weights.
 
     [P1] §10.2 and [P2] "Router 机制": logits = z W_router (+ bias), one score
-    per expert for every expert.  With norm_topk_prob the k weights are the
-    selected probabilities renormalised, which equals a softmax over the k
-    selected logits; ranking by probability equals ranking by logit.
+    per expert for every expert; probs = softmax over all experts; the k
+    largest are selected (ranking by probability equals ranking by logit).
+    With norm_topk_prob the k weights are the selected probabilities
+    renormalised to sum 1, which equals a softmax over the k selected logits;
+    without it ([P1] §10.2, Qwen2) they are the selected probabilities as they
+    are (their sum is below 1).
     Returns (logits [T,E], idx [T,k] int64, weights [T,k], gap [T]) where gap
     is the k-th minus the (k+1)-th largest logit (inf when k == E).
     """
@@ -271,9 +274,13 @@ def router_topk(z, w_router, b_router, k):
     order = np.argsort(-logits, axis=1, kind="stable")
     idx = order[:, :k]
     sel = np.take_along_axis(logits, idx, axis=1)
-    m = np.max(sel, axis=1, keepdims=True)
-    e = np.exp(sel - m)
-    wts = e / np.sum(e, axis=1, keepdims=True)
+    if norm_topk_prob:
+        m = np.max(sel, axis=1, keepdims=True)
+        e = np.exp(sel - m)
+        wts = e / np.sum(e, axis=1, keepdims=True)
+    else:
+        m = np.max(logits, axis=1, keepdims=True)
+        wts = np.exp(sel - m) / np.sum(np.exp(logits - m), axis=1, keepdims=True)
     if k < logits.shape[1]:
         kth = sel[:, k - 1]
         nxt = np.take_along_axis(logits, order[:, k:k + 1], axis=1)[:, 0]
@@ -288,18 +295,27 @@ def _expert(z, wg, wu, wd):
     return linear(silu(linear(z, wg)) * linear(z, wu), wd)
 
 
+def sigmoid(x):
+    """The logistic function 1 / (1 + e^-x)."""
+    return 1.0 / (1.0 + np.exp(-x))
+
+
 def moe_block(r, w, cfg, routing=None):
-    """Y = R + sum_j w_j * Expert_{idx_j}(Z), Z = RMSNorm_2(R).
+    """Y = R + sum_j w_j * Expert_{idx_j}(Z) [+ g * SharedExpert(Z)],
+    Z = RMSNorm_2(R).
 
     [P1] §10.2 (the weighted sum is a plain element-wise sum, no further
-    normalisation) and [P2] "MoE 的最终输出".  ``routing`` may supply
-    (idx, weights) to evaluate the experts under a given selection.
+    normalisation) and [P2] "MoE 的最终输出".  With a shared expert ([P1]
+    §10.1, Qwen2-MoE): a SwiGLU of width ``shared_ffn`` on the same Z whose
+    output is scaled per token by g = sigmoid(Z W_sg), W_sg one column without
+    bias, and added to the routed sum.  ``routing`` may supply (idx, weights)
+    to evaluate the experts under a given selection.
     Returns (Y, logits, idx, weights, gap, z).
     """
     r = np.asarray(r, dtype=np.float64)
     z = rmsnorm(r, w["gamma_mlp"], cfg["rms_eps"])
     logits, idx, wts, gap = router_topk(z, w["w_router"], w.get("b_router"),
-                                        cfg["top_k"])
+                                        cfg["top_k"], cfg.get("norm_topk_prob", 1))
     if routing is not None:
         idx, wts = routing
     t, kk = idx.shape
@@ -310,6 +326,10 @@ def moe_block(r, w, cfg, routing=None):
     acc = np.zeros_like(r)
     for j in range(kk):  # summed in slot order
         acc = acc + wts[:, j:j + 1] * eo[:, j, :]
+    if cfg.get("shared_ffn", 0):
+        g = sigmoid(z @ np.asarray(w["w_shared_expert_gate"], dtype=np.float64))
+        acc = acc + g[:, None] * _expert(z, w["w_shared_gate"], w["w_shared_up"],
+                                         w["w_shared_down"])
     return r + acc, logits, idx, wts, gap, z
 
 

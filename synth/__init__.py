@@ -36,6 +36,7 @@ class LayerConfig:
     top_k: int = 0
     norm_topk_prob: int = 1
     router_bias: int = 0
+    shared_ffn: int = 0      # width of the shared expert (Qwen2-MoE); 0 = none
 
     def as_dict(self):
         return dataclasses.asdict(self)
@@ -102,6 +103,12 @@ def layer_weights(cfg: LayerConfig, tag: str, base: int = 0) -> dict:
         w["w_gate"] = normal_bf16([e, f, d], s("w_gate"), 0.02)
         w["w_up"] = normal_bf16([e, f, d], s("w_up"), 0.02)
         w["w_down"] = normal_bf16([e, d, f], s("w_down"), 0.02)
+        if cfg.shared_ffn:
+            sf = cfg.shared_ffn
+            w["w_shared_gate"] = normal_bf16([sf, d], s("w_shared_gate"), 0.02)
+            w["w_shared_up"] = normal_bf16([sf, d], s("w_shared_up"), 0.02)
+            w["w_shared_down"] = normal_bf16([d, sf], s("w_shared_down"), 0.02)
+            w["w_shared_expert_gate"] = normal_bf16([d], s("w_shared_expert_gate"), 0.02)
     else:
         w["w_gate"] = normal_bf16([f, d], s("w_gate"), 0.02)
         w["w_up"] = normal_bf16([f, d], s("w_up"), 0.02)

@@ -434,6 +434,60 @@ def test_moe_output_is_gated_sum_of_chosen_experts():
     assert np.allclose(y - r, wts[0, 0] * singles[0] + wts[0, 1] * singles[1], atol=1e-13)
 
 
+def test_topk_without_renormalisation_is_the_full_softmax_probability():
+    """Qwen2.5-7B 结构拆解 §10.2, norm_topk_prob = false: the k weights are the
+    selected experts' probabilities under the softmax over all experts.
+
+    E = 2, k = 1: the one weight is the logistic of the logit difference; and
+    in general the renormalised weights are these divided by their sum."""
+    rng = np.random.default_rng(30)
+    z = rng.standard_normal((5, 4))
+    w_r = rng.standard_normal((2, 4))
+    logits, idx, wts, _ = O.router_topk(z, w_r, None, 1, norm_topk_prob=False)
+    other = 1 - idx[:, 0]
+    diff = logits[np.arange(5), idx[:, 0]] - logits[np.arange(5), other]
+    assert np.allclose(wts[:, 0], 1 / (1 + np.exp(-diff)), rtol=1e-13)
+    w_r = rng.standard_normal((6, 4))
+    _, idx_n, wts_n, _ = O.router_topk(z, w_r, None, 3, norm_topk_prob=True)
+    _, idx_r, wts_r, _ = O.router_topk(z, w_r, None, 3, norm_topk_prob=False)
+    assert np.array_equal(idx_n, idx_r)
+    assert np.all(wts_r.sum(axis=1) < 1)
+    assert np.allclose(wts_r / wts_r.sum(axis=1, keepdims=True), wts_n, rtol=1e-13)
+
+
+def test_shared_expert_is_a_sigmoid_gated_dense_swiglu():
+    """Qwen2.5-7B 结构拆解 §10.1: y_shared = sigmoid(x W_sg) SharedExpert(x),
+    added to the routed sum; the shared expert is a plain SwiGLU.
+
+    One routed expert (weight 1) plus a shared expert: with W_sg = 0 the gate is
+    exactly 1/2, so y - r = MLP_routed + MLP_shared / 2, each term checked
+    against the dense MLP block; a large positive gate logit gives ~1."""
+    rng = np.random.default_rng(31)
+    d, f, sf = 6, 8, 12
+    gam = 1 + 0.1 * rng.standard_normal(d)
+    w = {"gamma_mlp": gam, "w_router": np.zeros((1, d)),
+         "w_gate": rng.standard_normal((1, f, d)), "w_up": rng.standard_normal((1, f, d)),
+         "w_down": rng.standard_normal((1, d, f)),
+         "w_shared_gate": rng.standard_normal((sf, d)), "w_shared_up": rng.standard_normal((sf, d)),
+         "w_shared_down": rng.standard_normal((d, sf)), "w_shared_expert_gate": np.zeros(d)}
+    cfg = dict(rms_eps=1e-6, top_k=1, shared_ffn=sf)
+    r = rng.standard_normal((3, d))
+    y = O.moe_block(r, w, cfg)[0]
+    routed = O.mlp_block(r, {"gamma_mlp": gam, "w_gate": w["w_gate"][0], "w_up": w["w_up"][0],
+                             "w_down": w["w_down"][0]}, cfg) - r
+    shared = O.mlp_block(r, {"gamma_mlp": gam, "w_gate": w["w_shared_gate"],
+                             "w_up": w["w_shared_up"], "w_down": w["w_shared_down"]}, cfg) - r
+    assert np.allclose(y - r, routed + 0.5 * shared, atol=1e-12)
+    w["w_shared_expert_gate"] = 50.0 * np.sign(O.rmsnorm(r, gam, 1e-6)[0])
+    z0 = O.rmsnorm(r, gam, 1e-6)[0]
+    g = O.sigmoid(z0 @ w["w_shared_expert_gate"])
+    assert g > 1 - 1e-12
+    y0 = O.moe_block(r[:1], w, cfg)[0]
+    assert np.allclose(y0 - r[:1], routed[:1] + g * shared[:1], atol=1e-10)
+    with np.errstate(over="ignore"):
+        assert O.sigmoid(0.0) == 0.5 and O.sigmoid(-800.0) == 0.0
+
+
 # ---------------------------------------------------------------- head
 
 
