@@ -15,9 +15,11 @@
  *   SwiGLU MLP: (SiLU(Z Wg^T) * (Z Wu^T)) Wd^T (§10).  KV cache: K (after
  *   QK-norm and RoPE) and V of every position, appended ("Qwen2.5-7B 结构拆解"
  *   §09.1; Qwen3 layer page §12).  MoE: router logits z Wr^T (+ per-expert
- *   bias), top-k, softmax over the k selected logits, weighted sum of SwiGLU
- *   experts ("Qwen2.5-7B 结构拆解" §10.2; "MoE 初步" lecture, Router /
- *   Expert sections).
+ *   bias), top-k, softmax over the k selected logits (or, Qwen2-MoE, the
+ *   selected entries of the softmax over all E), weighted sum of SwiGLU
+ *   experts, plus an optional shared SwiGLU expert scaled per token by
+ *   sigmoid(z W_sg) ("Qwen2.5-7B 结构拆解" §10.1, §10.2; "MoE 初步" lecture,
+ *   Router / Expert sections).
  *
  * Conventions shared by every entry point:
  *   - Every tensor argument is a DEVICE pointer unless marked "host".  BF16
@@ -73,19 +75,26 @@ typedef struct {
   float rms_eps;        /* epsilon of every RMSNorm (also QK-norm)             */
   int32_t n_experts;    /* E; 0 = dense MLP; else a multiple of 8, <= 248     */
   int32_t top_k;        /* k experts per token (MoE)                           */
-  int32_t norm_topk_prob; /* must be 1: softmax over the k selected logits     */
+  int32_t norm_topk_prob; /* 1: gate weights = softmax over the k selected
+                           * logits; 0: the selected entries of the softmax over
+                           * all E logits, as they are (Qwen2-MoE)             */
   int32_t router_bias;  /* 1: per-expert FP32 bias added to the router logits  */
   int32_t max_tokens;   /* capacity: largest B*T of one prefill call           */
   int32_t max_batch;    /* capacity: largest B of one call                     */
   int32_t max_seq;      /* KV cache slots per sequence                         */
   int32_t max_position; /* RoPE table length: positions must be < this         */
+  int32_t shared_ffn;   /* sf: width of the shared expert (MoE only); 0 = none;
+                         * else % 64 == 0                                       */
 } qwen_layer_config;
 
 /* Source weights (device, BF16, [out, in] row-major) handed to create.  NULL
  * where the config says absent.  Dense: w_gate/w_up [f, d], w_down [d, f].
  * MoE: w_gate/w_up [E, mf, d], w_down [E, d, mf], w_router [E, d] BF16,
- * b_router [E] FP32.  The library copies them into its packed buffer; the
- * caller may free these after the stream passed to create has synchronised. */
+ * b_router [E] FP32.  Shared expert (shared_ffn = sf > 0): w_shared_gate and
+ * w_shared_up [sf, d], w_shared_down [d, sf], w_shared_expert_gate [d] (the
+ * one-column gate W_sg, no bias), all BF16.  The library copies them into its
+ * packed buffer; the caller may free these after the stream passed to create
+ * has synchronised. */
 typedef struct {
   const void* gamma_attn; /* [d]   RMSNorm_1 gamma                       */
   const void* gamma_mlp;  /* [d]   RMSNorm_2 gamma                       */
@@ -103,6 +112,10 @@ typedef struct {
   const void* w_down;
   const void* w_router;   /* MoE only                                    */
   const float* b_router;  /* MoE with router_bias                        */
+  const void* w_shared_gate;        /* [sf, d]  (shared_ffn)             */
+  const void* w_shared_up;          /* [sf, d]  (shared_ffn)             */
+  const void* w_shared_down;        /* [d, sf]  (shared_ffn)             */
+  const void* w_shared_expert_gate; /* [d]      (shared_ffn)             */
 } qwen_layer_weights;
 
 typedef struct qwen_layer_s* qwen_layer_t;
@@ -171,7 +184,8 @@ QWEN_API qwen_status qwen_layer_decode_ex(qwen_layer_t layer, const void* x, con
                                           void* k_cache, void* v_cache, void* workspace,
                                           size_t workspace_bytes, void* stream);
 
-/* MoE block alone on T tokens: Y = R + sum_j w_j Expert_{idx_j}(RMSNorm_2(R)).
+/* MoE block alone on T tokens: Y = R + sum_j w_j Expert_{idx_j}(Z)
+ * [+ sigmoid(Z W_sg) SharedExpert(Z)],  Z = RMSNorm_2(R).
  *   r        [T, d] BF16 residual-stream input; y [T, d] BF16 output.
  *   r_fp32   optional [T, d] FP32 copy of r used for the norm and router
  *            (NULL: r is widened from BF16).

@@ -63,3 +63,30 @@ def test_config_struct_layout_matches_c(built_lib):
     dh2 = q.LayerConfig(dict(d=4, n_q_heads=2, n_kv_heads=1, head_dim=2, ffn=6),
                         max_tokens=3, max_batch=1, max_seq=3, max_position=3)
     assert L.qwen_layer_packed_bytes(ctypes.byref(dh2.c)) == 0
+
+
+def test_shared_expert_config_reaches_the_library(built_lib):
+    """Host-only: shared_ffn (the last config field) changes the packed size by
+    exactly the shared expert's FP16 weights plus 8 router rows, the shared gate
+    and its padding, so the field is read where the binding writes it."""
+    import transformer_decoder_layer_gb300 as q
+    L = q.lib()
+    d, sf = 512, 512
+    moe = dict(d=d, n_q_heads=8, n_kv_heads=2, head_dim=64, ffn=256, n_experts=16, top_k=4)
+
+    def packed(**kw):
+        c = q.LayerConfig(dict(moe, **kw), max_tokens=64, max_batch=1, max_seq=64,
+                          max_position=64)
+        return L.qwen_layer_packed_bytes(ctypes.byref(c.c))
+
+    base = packed()
+    assert base > 0
+    assert packed(norm_topk_prob=0) == base
+    router_rows = 8 * 2 * d * 2
+    assert packed(shared_ffn=sf, norm_topk_prob=0) - base == router_rows + 3 * sf * d * 2
+    assert packed(shared_ffn=100) == 0            # not a multiple of 64
+    assert packed(norm_topk_prob=2) == 0
+    dense = q.LayerConfig(dict(d=d, n_q_heads=8, n_kv_heads=2, head_dim=64, ffn=256,
+                               shared_ffn=sf), max_tokens=64, max_batch=1, max_seq=64,
+                          max_position=64)
+    assert L.qwen_layer_packed_bytes(ctypes.byref(dense.c)) == 0  # shared expert needs MoE

@@ -20,6 +20,20 @@ GAP = 1e-3
 
 SMALL_MOE = synth.LayerConfig(d=512, n_q_heads=8, n_kv_heads=2, head_dim=64, ffn=256, qk_norm=1,
                               n_experts=16, top_k=4, router_bias=1)
+# Qwen2-MoE-like: q/k/v bias, weights without renormalisation, shared expert
+SMALL_QWEN2_MOE = synth.LayerConfig(d=512, n_q_heads=8, n_kv_heads=2, head_dim=64, ffn=128,
+                                    qkv_bias=1, n_experts=16, top_k=4, norm_topk_prob=0,
+                                    shared_ffn=512)
+
+
+def _gate_weights(logits, sel_idx, norm):
+    """Gate weights of a given selection from the oracle's logits."""
+    sel = np.take_along_axis(logits, sel_idx.astype(np.int64), axis=1)
+    if norm:
+        p = np.exp(sel - sel.max(1, keepdims=True))
+        return p / p.sum(1, keepdims=True)
+    m = logits.max(1, keepdims=True)
+    return np.exp(sel - m) / np.exp(logits - m).sum(1, keepdims=True)
 
 
 def _moe_reference(r64, w64, cfg, gpu_idx):
@@ -27,9 +41,7 @@ def _moe_reference(r64, w64, cfg, gpu_idx):
     y, logits, idx, wts, gap, z = oracle.moe_block(r64, w64, cfg)
     amb = gap <= GAP
     if amb.any():
-        sel = np.take_along_axis(logits, gpu_idx.astype(np.int64), axis=1)
-        p = np.exp(sel - sel.max(1, keepdims=True))
-        p /= p.sum(1, keepdims=True)
+        p = _gate_weights(logits, gpu_idx, cfg.get("norm_topk_prob", 1))
         idx2 = np.where(amb[:, None], gpu_idx, idx)
         wts2 = np.where(amb[:, None], p, wts)
         y = oracle.moe_block(r64, w64, cfg, routing=(idx2, wts2))[0]
@@ -54,16 +66,21 @@ def _run_moe_ffn(shape, tag, T, fp32_input=False):
     return f64(y.float()), ref, gi, wts.cpu().numpy(), lg.cpu().numpy(), logits, oidx, owts, gap
 
 
-def _check_routing(gi, gw, glog, logits, oidx, owts, gap):
+def _check_routing(gi, gw, glog, logits, oidx, owts, gap, norm=1):
     clear = gap > GAP
     assert clear.mean() > 0.8, "too few unambiguous tokens for a meaningful check"
     assert np.array_equal(gi[clear], oidx[clear]), (
         f"top-k mismatch on {np.sum(np.any(gi[clear] != oidx[clear], axis=1))} unambiguous tokens")
     assert np.allclose(gw[clear], owts[clear], atol=1e-5)
     assert np.allclose(glog, logits, atol=2e-5, rtol=1e-5)
-    # every selection is a valid top-k: distinct experts, weights sum to one
+    # every selection is a valid top-k: distinct experts, and its weights are
+    # those of the oracle's logits at the selected experts
     assert all(len(set(row)) == len(row) for row in gi)
-    assert np.allclose(gw.sum(1), 1.0, atol=1e-5)
+    assert np.allclose(gw, _gate_weights(logits, gi, norm), atol=1e-5)
+    if norm:
+        assert np.allclose(gw.sum(1), 1.0, atol=1e-5)
+    else:  # probabilities of a softmax over all E: the k selected sum below 1
+        assert np.all(gw.sum(1) < 1.0)
 
 
 def test_moe_ffn_small_ragged():
@@ -71,6 +88,21 @@ def test_moe_ffn_small_ragged():
     y, ref, gi, gw, glog, logits, oidx, owts, gap = _run_moe_ffn(SMALL_MOE, "moe_s", 300)
     _check_routing(gi, gw, glog, logits, oidx, owts, gap)
     assert_parity(y, ref, what="MoE Y")
+
+
+def test_moe_ffn_shared_expert_without_renormalisation():
+    """Qwen2-MoE block: full-softmax gate weights and a sigmoid-gated shared
+    expert (sf = 512), T=300 ragged over 16 experts."""
+    shape = SMALL_QWEN2_MOE
+    y, ref, gi, gw, glog, logits, oidx, owts, gap = _run_moe_ffn(shape, "q2moe", 300)
+    _check_routing(gi, gw, glog, logits, oidx, owts, gap, norm=0)
+    assert_parity(y, ref, what="Qwen2-MoE Y")
+    # the shared expert is not lost in the tolerance: the oracle without it fails
+    w64 = synth.weights_f64(synth.layer_weights(shape, "q2moe"))
+    r = synth.activations([300, shape.d], "q2moe", "r")
+    no_shared = oracle.moe_block(f64(r), w64, dict(shape.as_dict(), shared_ffn=0))[0]
+    with pytest.raises(AssertionError):
+        assert_parity(y, no_shared, what="Qwen2-MoE Y without the shared expert")
 
 
 def test_moe_ffn_fp32_residual_input():
@@ -139,22 +171,33 @@ def test_moe_layer_prefill_qwen3_30b_a3b(a3b_weights):
     _moe_layer_case(synth.QWEN3_30B_A3B, a3b_weights, "a3bl", 1, T, rows)
 
 
-def test_moe_layer_decode():
-    """MoE layer decode (tiny per-expert groups), B=8 against 100 cached slots."""
-    shape = SMALL_MOE
+def test_moe_layer_prefill_shared_expert():
+    shape = SMALL_QWEN2_MOE
+    rows = np.array([0, 1, 63, 64, 65, 127, 128, 200, 255])
+    _moe_layer_case(shape, synth.layer_weights(shape, "q2moel"), "q2moel", 2, 256, rows)
+
+
+@pytest.mark.parametrize("shape,tag", [(SMALL_MOE, "moed"), (SMALL_QWEN2_MOE, "q2moed")],
+                         ids=["qwen3", "qwen2_shared"])
+def test_moe_layer_decode(shape, tag):
+    """MoE layer decode (tiny per-expert groups), B=8 against 100 cached slots;
+    the Qwen2-MoE case runs the shared expert through the split-K GEMMs."""
     B, L = 8, 100
-    w_cpu = synth.layer_weights(shape, "moed")
-    x = synth.activations([B, shape.d], "moed")
-    kc, vc = synth.kv_cache(B, shape.n_kv_heads, L + 1, shape.head_dim, L, "moed")
+    w_cpu = synth.layer_weights(shape, tag)
+    x = synth.activations([B, shape.d], tag)
+    kc, vc = synth.kv_cache(B, shape.n_kv_heads, L + 1, shape.head_dim, L, tag)
     g = GpuLayer(shape, w_cpu, max_tokens=B, max_batch=B, max_seq=L + 1, max_position=L + 1)
     kd, vd = kc.cuda(), vc.cuda()
     y = g.decode(x, np.full(B, L), [L] * B, kd, vd)
     w64 = synth.weights_f64(w_cpu)
     cfg = shape.as_dict()
     yg = f64(y.float())
+    checked = 0
     for b in range(B):
         kk, vv = f64(kc)[b].copy(), f64(vc)[b].copy()
         yo, r, (logits, idx, wts, gap) = oracle.moe_layer_forward(
             f64(x)[b][None], w64, cfg, np.array([L]), kk, vv, np.array([L]))
         if gap[0] > 10 * GAP:
             assert_parity(yg[b][None], yo, what=f"decode Y b={b}")
+            checked += 1
+    assert checked >= B // 2

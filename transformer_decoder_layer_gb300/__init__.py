@@ -40,11 +40,13 @@ class _Config(ctypes.Structure):
         ("norm_topk_prob", ctypes.c_int32), ("router_bias", ctypes.c_int32),
         ("max_tokens", ctypes.c_int32), ("max_batch", ctypes.c_int32),
         ("max_seq", ctypes.c_int32), ("max_position", ctypes.c_int32),
+        ("shared_ffn", ctypes.c_int32),
     ]
 
 
 _WEIGHT_FIELDS = ["gamma_attn", "gamma_mlp", "gamma_q", "gamma_k", "w_q", "w_k", "w_v", "b_q",
-                  "b_k", "b_v", "w_o", "w_gate", "w_up", "w_down", "w_router", "b_router"]
+                  "b_k", "b_v", "w_o", "w_gate", "w_up", "w_down", "w_router", "b_router",
+                  "w_shared_gate", "w_shared_up", "w_shared_down", "w_shared_expert_gate"]
 
 
 class _Weights(ctypes.Structure):
@@ -224,7 +226,8 @@ class LayerConfig:
             rms_eps=float(get("rms_eps", 1.0e-6)), n_experts=get("n_experts"),
             top_k=get("top_k"), norm_topk_prob=get("norm_topk_prob", 1),
             router_bias=get("router_bias"), max_tokens=int(max_tokens),
-            max_batch=int(max_batch), max_seq=int(max_seq), max_position=int(max_position))
+            max_batch=int(max_batch), max_seq=int(max_seq), max_position=int(max_position),
+            shared_ffn=get("shared_ffn"))
 
     def __getattr__(self, k):
         return getattr(self.__dict__["c"], k)

@@ -30,8 +30,11 @@ bool config_valid(const qwen_layer_config& c) {
   if (c.n_experts < 0 || c.n_experts > 248 || (c.n_experts & 7)) return false;
   if (c.n_experts > 0) {
     if (c.top_k < 1 || c.top_k > 8 || c.top_k > c.n_experts) return false;
-    if (c.norm_topk_prob != 1) return false;
+    if (c.norm_topk_prob != 0 && c.norm_topk_prob != 1) return false;
   }
+  // shared expert: MoE layers only, width a multiple of 64 (SwiGLU tiles)
+  if (c.shared_ffn < 0 || c.shared_ffn % 64) return false;
+  if (c.shared_ffn > 0 && c.n_experts == 0) return false;
   if (c.max_tokens <= 0 || c.max_batch <= 0 || c.max_seq <= 0 || c.max_position <= 0) return false;
   return true;
 }
@@ -60,10 +63,15 @@ PackedLayout packed_layout(const qwen_layer_config& c) {
     L.w_down = take(d * f * 2);
   } else {
     const size_t e = c.n_experts;
-    L.w_router = take(e * 2 * d * 2);  // FP16 [E][2d], each row twice
+    L.w_router = take((size_t)router_rows(c) * 2 * d * 2);  // FP16 rows, each twice
     L.b_router = take(e * 4);
     L.w_gu = take(e * 2 * f * d * 2);
     L.w_down = take(e * d * f * 2);
+    if (c.shared_ffn) {
+      const size_t sf = c.shared_ffn;
+      L.w_sgu = take(2 * sf * d * 2);
+      L.w_sdown = take(d * sf * 2);
+    }
   }
   L.total = o;
   return L;
@@ -93,7 +101,7 @@ WorkspaceLayout workspace_layout(const qwen_layer_config& c, int B, int T) {
     W.h = take(M * f * 2);
   } else {
     const size_t e = c.n_experts, k = c.top_k, mk = M * k;
-    W.logits = take(M * e * 4);
+    W.logits = take(M * (size_t)router_rows(c) * 4);
     W.topk_idx = take(mk * 4);
     W.topk_w = take(mk * 4);
     W.blk_counts = take(moe_perm_blocks(mk) * e * 4);
@@ -103,6 +111,11 @@ WorkspaceLayout workspace_layout(const qwen_layer_config& c, int B, int T) {
     W.zp = take(mk * d * 2);
     W.hp = take(mk * f * 2);
     W.yp = take(mk * d * 2);
+    if (c.shared_ffn) {
+      W.hs = take(M * (size_t)c.shared_ffn * 2);
+      W.ys32 = take(M * d * 4);
+      W.gscale = take(M * 4);
+    }
   }
   if (T == 1) {
     int splits = 0;
@@ -204,6 +217,9 @@ qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_wei
   if (c.qk_norm && (!w->gamma_q || !w->gamma_k)) return QWEN_ERR_INVALID_ARG;
   if (c.qkv_bias && (!w->b_q || !w->b_k || !w->b_v)) return QWEN_ERR_INVALID_ARG;
   if (moe && (!w->w_router || (c.router_bias && !w->b_router))) return QWEN_ERR_INVALID_ARG;
+  if (c.shared_ffn && (!w->w_shared_gate || !w->w_shared_up || !w->w_shared_down ||
+                       !w->w_shared_expert_gate))
+    return QWEN_ERR_INVALID_ARG;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* P = static_cast<uint8_t*>(packed);
@@ -228,6 +244,8 @@ qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_wei
   h->w_down = reinterpret_cast<f16*>(P + L.w_down);
   h->w_router = moe ? reinterpret_cast<f16*>(P + L.w_router) : nullptr;
   h->b_router = (moe && c.router_bias) ? reinterpret_cast<float*>(P + L.b_router) : nullptr;
+  h->w_sgu = c.shared_ffn ? reinterpret_cast<f16*>(P + L.w_sgu) : nullptr;
+  h->w_sdown = c.shared_ffn ? reinterpret_cast<f16*>(P + L.w_sdown) : nullptr;
 
   bool ok = cudaMemsetAsync(h->status, 0, 256, st) == cudaSuccess;
   ok = ok && copy_d2d(h->gamma_attn, w->gamma_attn, d * 2, st);
@@ -255,9 +273,22 @@ qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_wei
   ok = ok && pack_rows(h->w_gu, w->w_up, n_exp * f, d, 2, st);
   ok = ok && pack_rows(h->w_down, w->w_down, n_exp * d, f, 0, st);
   if (moe) {
+    const size_t rr = router_rows(c);
+    if (rr > n_exp)  // the shared gate row and the zero padding after it
+      ok = ok && cudaMemsetAsync(h->w_router + n_exp * 2 * d, 0, (rr - n_exp) * 2 * d * 2, st) ==
+                     cudaSuccess;
     ok = ok && pack_rows(h->w_router, w->w_router, n_exp, d, 0, st, 2 * d, 0);
     ok = ok && pack_rows(h->w_router, w->w_router, n_exp, d, 0, st, 2 * d, d);
     if (c.router_bias) ok = ok && copy_d2d(h->b_router, w->b_router, n_exp * 4, st);
+  }
+  if (c.shared_ffn) {
+    const size_t sf = c.shared_ffn;
+    f16* gate_row = h->w_router + n_exp * 2 * d;  // W_sg as router row E
+    ok = ok && pack_rows(gate_row, w->w_shared_expert_gate, 1, d, 0, st, 2 * d, 0);
+    ok = ok && pack_rows(gate_row, w->w_shared_expert_gate, 1, d, 0, st, 2 * d, d);
+    ok = ok && pack_rows(h->w_sgu, w->w_shared_gate, sf, d, 1, st);
+    ok = ok && pack_rows(h->w_sgu, w->w_shared_up, sf, d, 2, st);
+    ok = ok && pack_rows(h->w_sdown, w->w_shared_down, d, sf, 0, st);
   }
   // RoPE table: (cos, sin) of p * theta^(-2i/dh), angles and trig in FP64.
   // Qwen3 layer page, §6 (frequency equation).
@@ -506,7 +537,6 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
     GemmEpilogue e{};
     e.mode = EPI_QKV;
     e.b_static = 1;
-  e.b_static = 1;
     e.qkv = qp;
     QWEN_STAGE_RUN(QWEN_STAGE_QKV, gemm_tc(xh, d, L->w_qkv, d, B, nqkv, d, true, e, err, st));
   }

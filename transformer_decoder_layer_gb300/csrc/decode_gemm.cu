@@ -508,7 +508,8 @@ size_t decode_part_bytes(const qwen_layer_config& c, int B) {
     upd(2 * f, d);
     upd(d, f);
   } else {
-    upd(c.n_experts, 2 * d);  // the router over [Z_hi | Z_lo]
+    upd(router_rows(c), 2 * d);  // the router over [Z_hi | Z_lo]
+    if (c.shared_ffn) upd(d, c.shared_ffn);  // the shared expert's down projection
   }
   return m;
 }

@@ -11,13 +11,15 @@ namespace qwen {
 
 struct PackedLayout {
   size_t status, rope, gamma_attn, gamma_mlp, gamma_q, gamma_k, w_qkv, b_qkv, w_o, w_gu, w_down,
-      w_router, b_router, total;
+      w_router, b_router, w_sgu, w_sdown, total;
 };
 
 struct WorkspaceLayout {
   size_t xh, q, k16, v16, attn, r32, z, h;
   // MoE
   size_t logits, topk_idx, topk_w, blk_counts, offsets, perm, inv, zp, hp, yp;
+  // MoE shared expert: H_s [M][sf] FP16, its output [M][d] FP32, gate g [M]
+  size_t hs, ys32, gscale;
   // decode (T == 1)
   size_t part, attn_o, attn_ml;
   size_t total;
@@ -37,10 +39,14 @@ struct qwen_layer_s {
   float* b_qkv;
   __half* w_o;
   __half *w_gu, *w_down;  // gate/up rows interleaved in 64-row blocks
-  // router weights as FP16 [E][2d], each row twice ([W_r | W_r]): the logits
-  // are one GEMM over [Z_hi | Z_lo] (Z split into two FP16 parts)
+  // router weights as FP16 [router_rows][2d], each row twice ([W_r | W_r]):
+  // the logits are one GEMM over [Z_hi | Z_lo] (Z split into two FP16 parts).
+  // With a shared expert, row E holds its gate column W_sg (rows E+1.. are
+  // zero), so logit E is the shared gate's pre-activation.
   __half* w_router;
   float* b_router;
+  // shared expert: gate/up interleaved like w_gu, FP16 [2sf][d]; down [d][sf]
+  __half *w_sgu, *w_sdown;
   // optional per-stage events (qwen_layer_set_trace)
   bool tracing = false;
   void* trace[2 * QWEN_STAGE_COUNT] = {};
@@ -49,6 +55,11 @@ struct qwen_layer_s {
 namespace qwen {
 
 bool config_valid(const qwen_layer_config& c);
+// Rows of the router GEMM: E, plus 8 (the shared gate and zero padding) when
+// the layer has a shared expert.
+inline int router_rows(const qwen_layer_config& c) {
+  return c.n_experts + (c.shared_ffn > 0 ? 8 : 0);
+}
 PackedLayout packed_layout(const qwen_layer_config& c);
 WorkspaceLayout workspace_layout(const qwen_layer_config& c, int B, int T);
 

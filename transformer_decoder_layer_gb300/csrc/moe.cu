@@ -3,9 +3,12 @@
 //
 // "Qwen2.5-7B 结构拆解" §10.2: router logits = x W_router, top-k, and with
 // norm_topk_prob the k weights are renormalised (equal to a softmax over the k
-// selected logits, "MoE 初步" lecture, Router section); each expert is a SwiGLU;
-// the output is the plain weighted element-wise sum of the k expert outputs,
-// then the residual add.  Selection ties go to the lower expert index.
+// selected logits, "MoE 初步" lecture, Router section); without it (Qwen2) they
+// are the selected probabilities of the softmax over all experts.  Each expert
+// is a SwiGLU; the output is the plain weighted element-wise sum of the k
+// expert outputs, plus (§10.1, Qwen2-MoE) a shared SwiGLU expert of width sf
+// scaled per token by g = sigmoid(z W_sg), then the residual add.  Selection
+// ties go to the lower expert index.
 //
 // Steps (all on the caller's stream, no host synchronisation):
 //   1. RMSNorm_2 of R -> Z as two FP16 parts per row, [Z_hi | Z_lo]: Z_hi is
@@ -15,14 +18,17 @@
 //      the logits differ from an FP32 evaluation by ~1e-6, far below the 1e-3
 //      selection gaps the top-k must reproduce
 //   3. top-k: one warp per token, k rounds of a warp arg-max; adds b_r and
-//      writes the biased logits back
+//      writes the biased logits back.  The shared gate W_sg rides along as
+//      router row E, so its logit comes out of the same GEMM
 //   4. permutation (stable counting sort by expert, in entry order t*k + j):
 //      per-block expert counts, then per block the starting position of each
 //      expert (all counts of earlier experts, plus this expert's counts in
 //      earlier blocks) and warp-level ranks; gather of Z_hi rows
 //   5. grouped GEMM gate/up (+SiLU*up) and grouped GEMM down over per-expert
 //      row ranges, one persistent tensor-core kernel each
+//   5b. shared expert: dense gate/up (+SiLU*up) and down GEMMs on Z_hi, FP32 out
 //   6. combine: Y[t] = R[t] + sum_j w[t][j] Y_e[pos(t, j)] in slot order
+//      (+ g[t] Y_s[t])
 #include "common.cuh"
 #include "internal.h"
 #include "layer.h"
@@ -33,14 +39,20 @@ namespace {
 
 constexpr int kPermBlock = 1024;  // permutation entries per CTA
 
-// logits [T][E] are Z W_r^T on entry and Z W_r^T + b_r on exit.
-__global__ void topk_kernel(float* __restrict__ logits, const float* __restrict__ bias, int T,
-                            int E, int k, int32_t* __restrict__ idx, float* __restrict__ w) {
+// logits rows are `ldl` apart; columns [0, E) are Z W_r^T on entry and
+// Z W_r^T + b_r on exit.  Gate weights: norm != 0, a softmax over the k
+// selected logits; norm == 0, the selected entries of the softmax over all E
+// logits.  With gscale, column E holds the shared expert's gate logit and
+// gscale[t] = sigmoid of it.
+__global__ void topk_kernel(float* __restrict__ logits, int ldl, const float* __restrict__ bias,
+                            int T, int E, int k, int norm, int32_t* __restrict__ idx,
+                            float* __restrict__ w, float* __restrict__ gscale) {
   pdl_trigger();
   pdl_wait();
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
+  float* lrow = logits + (size_t)t * ldl;
   const int per = (E + 31) / 32;  // <= 8
   float v[8];
   unsigned taken = 0;
@@ -48,8 +60,8 @@ __global__ void topk_kernel(float* __restrict__ logits, const float* __restrict_
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
     if (i < per && e < E) {
-      float x = logits[(size_t)t * E + e] + (bias ? bias[e] : 0.f);
-      logits[(size_t)t * E + e] = x;
+      float x = lrow[e] + (bias ? bias[e] : 0.f);
+      lrow[e] = x;
       v[i] = x == x ? x : -INFINITY;  // a NaN logit is never preferred
     } else {
       v[i] = -INFINITY;
@@ -83,18 +95,25 @@ __global__ void topk_kernel(float* __restrict__ logits, const float* __restrict_
     sel[j] = bv;
     sel_i[j] = bi;
   }
+  // sel[0] is the largest logit of the row
+  float all = 0.f;  // sum over all E of exp(logit - max), for norm == 0
+  if (!norm) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) all += v[i] == -INFINITY ? 0.f : expf(v[i] - sel[0]);
+    all = warp_sum(all);
+  }
   if (lane == 0) {
-    float m = sel[0];
-    for (int j = 1; j < k; ++j) m = fmaxf(m, sel[j]);
     float s = 0.f, p[8];
     for (int j = 0; j < k; ++j) {
-      p[j] = __expf(sel[j] - m);
+      p[j] = expf(sel[j] - sel[0]);
       s += p[j];
     }
+    const float den = norm ? s : all;
     for (int j = 0; j < k; ++j) {
       idx[(size_t)t * k + j] = sel_i[j];
-      w[(size_t)t * k + j] = p[j] / s;
+      w[(size_t)t * k + j] = p[j] / den;
     }
+    if (gscale) gscale[t] = 1.f / (1.f + expf(-lrow[E]));
   }
 }
 
@@ -179,9 +198,11 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ z, size_t zs,
   for (int c = lane; c < d / 8; c += 32) dst[c] = src[c];
 }
 
-// y[t] = R[t] + sum_j w[t][j] * yp[inv[t*k + j]], summed in slot order j.
+// y[t] = R[t] + (sum_j w[t][j] * yp[inv[t*k + j]] summed in slot order j
+//        [+ gs[t] * ys[t], the gated shared expert, when ys is given]).
 __global__ void combine_kernel(const f16* __restrict__ yp, const int32_t* __restrict__ inv,
-                               const float* __restrict__ w, const float* __restrict__ r32,
+                               const float* __restrict__ w, const float* __restrict__ ys,
+                               const float* __restrict__ gs, const float* __restrict__ r32,
                                const bf16* __restrict__ r, int T, int k, int d,
                                bf16* __restrict__ y, float* __restrict__ y32) {
   pdl_trigger();
@@ -213,6 +234,15 @@ __global__ void combine_kernel(const f16* __restrict__ yp, const int32_t* __rest
         acc[2 * e + 1] = fmaf(wj[j], f.y, acc[2 * e + 1]);
       }
     }
+  }
+  if (ys) {
+    const float g = gs[t];
+    const float4 a = reinterpret_cast<const float4*>(ys + (size_t)t * d)[2 * c];
+    const float4 b = reinterpret_cast<const float4*>(ys + (size_t)t * d)[2 * c + 1];
+    acc[0] = fmaf(g, a.x, acc[0]); acc[1] = fmaf(g, a.y, acc[1]);
+    acc[2] = fmaf(g, a.z, acc[2]); acc[3] = fmaf(g, a.w, acc[3]);
+    acc[4] = fmaf(g, b.x, acc[4]); acc[5] = fmaf(g, b.y, acc[5]);
+    acc[6] = fmaf(g, b.z, acc[6]); acc[7] = fmaf(g, b.w, acc[7]);
   }
   float o[8];
   if (r32) {
@@ -255,7 +285,8 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
                         int32_t* topk_idx_out, float* topk_w_out, float* logits_out, uint8_t* ws,
                         const WorkspaceLayout& W, cudaStream_t st) {
   const qwen_layer_config& c = L->cfg;
-  const int d = c.d, E = c.n_experts, k = c.top_k, mf = c.ffn;
+  const int d = c.d, E = c.n_experts, k = c.top_k, mf = c.ffn, sf = c.shared_ffn;
+  const int R = router_rows(c);  // E, or E + 8 with the shared gate at column E
   const int n = T * k;
   int* err = L->status;
   f16* z = reinterpret_cast<f16*>(ws + W.z);  // rows [Z_hi | Z_lo], 2d apart
@@ -269,33 +300,38 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
   f16* zp = reinterpret_cast<f16*>(ws + W.zp);
   f16* hp = reinterpret_cast<f16*>(ws + W.hp);
   f16* yp = reinterpret_cast<f16*>(ws + W.yp);
+  f16* hs = sf ? reinterpret_cast<f16*>(ws + W.hs) : nullptr;
+  float* ys32 = sf ? reinterpret_cast<float*>(ws + W.ys32) : nullptr;
+  float* gsc = sf ? reinterpret_cast<float*>(ws + W.gscale) : nullptr;
+  float* part = reinterpret_cast<float*>(ws + W.part);
+  // decode-sized batches use the swap-AB split-K GEMMs (one 128-row weight
+  // tile would otherwise run its whole K on a single SM)
+  const bool small = T <= 256 && W.part != 0;
   qwen_status s;
 
   // 1. RMSNorm_2 -> [Z_hi | Z_lo] (FP16 parts of the FP32 result)
   if ((s = rmsnorm_launch(r, L->gamma_mlp, z, true, nullptr, r32, T, d, c.rms_eps, st, 0,
                           2 * (size_t)d, z + d)))
     return s;
-  // 2. router logits: one tensor-core GEMM over K = 2d against [W_r | W_r];
-  // decode-sized batches use the swap-AB split-K GEMM (one 128-row weight tile
-  // would otherwise run its whole K on a single SM)
-  if (T <= 256 && W.part != 0) {
-    const int S = decode_splits(E, 2 * d);
-    float* part = reinterpret_cast<float*>(ws + W.part);
-    if ((s = gemm_decode_splitk(L->w_router, z, 2 * d, T, E, 2 * d, S, true, part, err, st,
+  // 2. router logits (and the shared gate's, column E): one tensor-core GEMM
+  // over K = 2d against [W_r | W_r]
+  if (small) {
+    const int S = decode_splits(R, 2 * d);
+    if ((s = gemm_decode_splitk(L->w_router, z, 2 * d, T, R, 2 * d, S, true, part, err, st,
                                 /*w_static=*/true)))
       return s;
-    if ((s = reduce_f32(part, S, T, E, logits, E, st))) return s;
+    if ((s = reduce_f32(part, S, T, R, logits, R, st))) return s;
   } else {
     GemmEpilogue er{};
     er.mode = EPI_F32;
     er.out32 = logits;
-    er.ldo32 = E;
+    er.ldo32 = R;
     er.b_static = 1;
-    if ((s = gemm_tc(z, 2 * d, L->w_router, 2 * d, T, E, 2 * d, true, er, err, st))) return s;
+    if ((s = gemm_tc(z, 2 * d, L->w_router, 2 * d, T, R, 2 * d, true, er, err, st))) return s;
   }
-  // 3. top-k (+ router bias) + softmax over the selected logits
-  launch_k(topk_kernel, dim3(nblk(32LL * T, 256)), dim3(256), 0, st, logits,
-           (const float*)L->b_router, T, E, k, idx, wts);
+  // 3. top-k (+ router bias), gate weights, shared gate sigmoid
+  launch_k(topk_kernel, dim3(nblk(32LL * T, 256)), dim3(256), 0, st, logits, R,
+           (const float*)L->b_router, T, E, k, c.norm_topk_prob, idx, wts, gsc);
   count_launches();
   // 4. permutation by expert (stable in entry order) and gather of Z_hi rows
   const int G = moe_perm_blocks(n);
@@ -325,9 +361,37 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
   ed.group_offsets = offsets;
   ed.n_groups = E;
   if ((s = gemm_tc(hp, mf, L->w_down, mf, n, d, mf, true, ed, err, st))) return s;
-  // 6. weighted combine + residual
+  // 5b. shared expert on Z_hi: H_s = SiLU(Z W_sg^T) * (Z W_su^T), Y_s = H_s W_sd^T (FP32)
+  if (sf) {
+    if (small) {
+      if ((s = gemm_decode_splitk(L->w_sgu, z, 2 * d, T, 2 * sf, d, 1, true, nullptr, err, st,
+                                  /*w_static=*/true, hs)))
+        return s;
+      const int S = decode_splits(d, sf);
+      if ((s = gemm_decode_splitk(L->w_sdown, hs, sf, T, d, sf, S, true, part, err, st,
+                                  /*w_static=*/true)))
+        return s;
+      if ((s = reduce_f32(part, S, T, d, ys32, d, st))) return s;
+    } else {
+      GemmEpilogue sg{};
+      sg.mode = EPI_SWIGLU;
+      sg.out = hs;
+      sg.out_f16 = 1;
+      sg.ldo = sf;
+      sg.b_static = 1;
+      if ((s = gemm_tc(z, 2 * d, L->w_sgu, d, T, 2 * sf, d, true, sg, err, st))) return s;
+      GemmEpilogue sd{};
+      sd.mode = EPI_F32;
+      sd.out32 = ys32;
+      sd.ldo32 = d;
+      sd.b_static = 1;
+      if ((s = gemm_tc(hs, sf, L->w_sdown, sf, T, d, sf, true, sd, err, st))) return s;
+    }
+  }
+  // 6. weighted combine (+ gated shared expert) + residual
   launch_k(combine_kernel, dim3(nblk((long long)T * (d / 8), 256)), dim3(256), 0, st, (const f16*)yp,
-           (const int32_t*)inv, (const float*)wts, r32, r, T, k, d, y, y32);
+           (const int32_t*)inv, (const float*)wts, (const float*)ys32, (const float*)gsc, r32, r,
+           T, k, d, y, y32);
   count_launches();
   if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;
   // optional copies of the routing for inspection
@@ -337,8 +401,9 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
   if (topk_w_out &&
       cudaMemcpyAsync(topk_w_out, wts, (size_t)n * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
     return QWEN_ERR_CUDA;
-  if (logits_out && cudaMemcpyAsync(logits_out, logits, (size_t)T * E * 4,
-                                    cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+  if (logits_out && cudaMemcpy2DAsync(logits_out, (size_t)E * 4, logits, (size_t)R * 4,
+                                      (size_t)E * 4, T, cudaMemcpyDeviceToDevice,
+                                      st) != cudaSuccess)
     return QWEN_ERR_CUDA;
   return QWEN_OK;
 }
