@@ -325,6 +325,11 @@ def gpu_layer_weights(torch, shape, seed):
             w["b_router"] = n([e], 0.5).float()
         w["w_gate"], w["w_up"] = n([e, f, d], 0.02), n([e, f, d], 0.02)
         w["w_down"] = n([e, d, f], 0.02)
+        if shape.shared_ffn:
+            sf = shape.shared_ffn
+            w["w_shared_gate"], w["w_shared_up"] = n([sf, d], 0.02), n([sf, d], 0.02)
+            w["w_shared_down"] = n([d, sf], 0.02)
+            w["w_shared_expert_gate"] = n([d], 0.02)
     else:
         w["w_gate"], w["w_up"], w["w_down"] = n([f, d], 0.02), n([f, d], 0.02), n([d, f], 0.02)
     return w
@@ -403,11 +408,23 @@ def stack_bench(q, torch, hbm_gbs, peak_tflops, steps, warmup):
     return {"decode": dec, "prefill": pre}
 
 
-def moe_prefill_bench(q, torch, peak_tflops, steps=5, warmup=2):
-    """Qwen3-30B-A3B-shaped MoE layer prefill, T=4096 (router bias N(0, 0.5) skews
-    the expert loads)."""
+MOE_WORKLOADS = {
+    "qwen3": ("qwen3-30b-a3b-shaped", "128 experts, top-8, mf=768, skewed router bias"),
+    "qwen2": ("qwen2-57b-a14b-shaped", "64 experts, top-8, mf=2560, shared expert sf=20480, "
+                                       "no renormalisation"),
+}
+
+
+def moe_shape(which):
     import synth
-    shape, T = synth.QWEN3_30B_A3B, 4096
+    return synth.QWEN3_30B_A3B if which == "qwen3" else synth.QWEN2_57B_A14B
+
+
+def moe_prefill_bench(q, torch, peak_tflops, which="qwen3", steps=5, warmup=2):
+    """MoE layer prefill at T=4096: Qwen3-30B-A3B-shaped (router bias N(0, 0.5)
+    skews the expert loads) or Qwen2-57B-A14B-shaped (shared expert)."""
+    shape, T = moe_shape(which), 4096
+    name, desc = MOE_WORKLOADS[which]
     w = gpu_layer_weights(torch, shape, 4000)
     cfg = q.LayerConfig(shape, max_tokens=T, max_batch=1, max_seq=T, max_position=T)
     layer = q.Layer(cfg, w)
@@ -434,22 +451,23 @@ def moe_prefill_bench(q, torch, peak_tflops, steps=5, warmup=2):
     ms = statistics.median(times)
     d, hq, hkv, dh = shape.d, shape.n_q_heads, shape.n_kv_heads, shape.head_dim
     attn_lin = d * hq * dh + 2 * d * hkv * dh + hq * dh * d
-    experts = shape.top_k * 3 * d * shape.ffn
-    flops_exec = 2 * T * (attn_lin + shape.n_experts * d + experts) + 2 * hq * dh * T * (T + 1)
-    flops_metric = 2 * T * (attn_lin + shape.n_experts * d + experts) + 4 * T * T * hq * dh
-    return {"workload": f"qwen3-30b-a3b-shaped MoE layer prefill T={T} (128 experts, top-8, "
-                        "mf=768, skewed router bias)",
+    experts = shape.top_k * 3 * d * shape.ffn + 3 * d * shape.shared_ffn
+    router = (shape.n_experts + (1 if shape.shared_ffn else 0)) * d
+    flops_exec = 2 * T * (attn_lin + router + experts) + 2 * hq * dh * T * (T + 1)
+    flops_metric = 2 * T * (attn_lin + router + experts) + 4 * T * T * hq * dh
+    del layer, w
+    return {"workload": f"{name} MoE layer prefill T={T} ({desc})",
             "ms": round(ms, 4), "tokens_per_s": round(T / (ms * 1e-3), 1),
             "tflops_metric": round(flops_metric / (ms * 1e-3) / 1e12, 1),
             "tflops_executed": round(flops_exec / (ms * 1e-3) / 1e12, 1),
             "frac_of_peak_executed": round(flops_exec / (ms * 1e-3) / 1e12 / peak_tflops, 3)}
 
 
-def moe_decode_bench(q, torch, hbm_gbs, steps=20, warmup=3, cached=4096):
-    """Qwen3-30B-A3B-shaped MoE layer decode against `cached` tokens: bytes =
-    attention and router weights + the experts the batch touches + KV."""
-    import synth
-    shape = synth.QWEN3_30B_A3B
+def moe_decode_bench(q, torch, hbm_gbs, which="qwen3", steps=20, warmup=3, cached=4096):
+    """MoE layer decode against `cached` tokens: bytes = attention and router
+    weights (+ the shared expert) + the experts the batch touches + KV."""
+    shape = moe_shape(which)
+    name, desc = MOE_WORKLOADS[which]
     w = gpu_layer_weights(torch, shape, 4000)
     S = cached + 1
     layer = q.Layer(q.LayerConfig(shape, max_tokens=64, max_batch=64, max_seq=S, max_position=S), w)
@@ -457,7 +475,9 @@ def moe_decode_bench(q, torch, hbm_gbs, steps=20, warmup=3, cached=4096):
     out = {}
     d, hq, hkv, dh, E, k, mf = (shape.d, shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
                                 shape.n_experts, shape.top_k, shape.ffn)
-    attn_w = 2 * (d * (hq + 2 * hkv) * dh + hq * dh * d) + 2 * E * d * 2
+    router_rows = E + (8 if shape.shared_ffn else 0)  # FP16 [W_r | W_r] rows read
+    attn_w = (2 * (d * (hq + 2 * hkv) * dh + hq * dh * d) + 2 * router_rows * d * 2
+              + 3 * d * shape.shared_ffn * 2)
     for B in (1, 8, 32):
         kc = torch.randn((B, hkv, S, dh), generator=g, device="cuda").bfloat16()
         vc = torch.randn_like(kc)
@@ -494,7 +514,8 @@ def moe_decode_bench(q, torch, hbm_gbs, steps=20, warmup=3, cached=4096):
                          "bytes_per_step": nbytes, "GB_per_s": round(nbytes / (us * 1e-6) / 1e9, 1),
                          "frac_hbm": round(nbytes / (us * 1e-6) / 1e9 / hbm_gbs, 3)}
     assert layer.poll_error() == 0
-    return {"workload": f"qwen3-30b-a3b-shaped MoE layer decode, {cached} cached tokens", **out}
+    del layer, w
+    return {"workload": f"{name} MoE layer decode, {cached} cached tokens ({desc})", **out}
 
 
 def long_decode_bench(q, torch, hbm_gbs, B=8, cached=32768, steps=20, warmup=3):
@@ -621,8 +642,8 @@ def profile_run(args):
     launch in stage order (norm1, QKV, QKV finish, attention, merge, O, O finish
     + norm2, gate/up + SwiGLU, down, down finish); a prefill step launches
     norm1, QKV, attention, O, norm2, gate/up, down; a MoE step (Qwen3-30B-A3B
-    shape) replaces the MLP by router, top-k, permutation, grouped expert GEMMs
-    and combine."""
+    or Qwen2-57B-A14B shape) replaces the MLP by router, top-k, permutation,
+    grouped expert GEMMs, the shared expert's GEMMs (Qwen2) and combine."""
     import torch
 
     import synth
@@ -639,7 +660,7 @@ def profile_run(args):
         for _ in range(args.steps):
             bench.step()
     elif args.profile == "moe_decode":
-        shape, B, cached = synth.QWEN3_30B_A3B, args.batch, CACHE_FILLED
+        shape, B, cached = moe_shape(args.moe_shape), args.batch, CACHE_FILLED
         w = gpu_layer_weights(torch, shape, 4000)
         S = cached + 1
         cfg = q.LayerConfig(shape, max_tokens=B, max_batch=B, max_seq=S, max_position=S)
@@ -653,7 +674,7 @@ def profile_run(args):
         for _ in range(args.steps):
             layer.decode(x, pos, pos, kc, vc, out=y, workspace=ws)
     elif args.profile == "moe":
-        shape, T = synth.QWEN3_30B_A3B, args.tokens
+        shape, T = moe_shape(args.moe_shape), args.tokens
         w = gpu_layer_weights(torch, shape, 4000)
         cfg = q.LayerConfig(shape, max_tokens=T, max_batch=1, max_seq=T, max_position=T)
         layer = q.Layer(cfg, w)
@@ -706,6 +727,9 @@ def main():
                     help="run --steps untimed eager steps of one workload and exit "
                          "(a short, deterministic launch sequence for a profiler capture)")
     ap.add_argument("--tokens", type=int, default=4096, help="prefill length for --profile")
+    ap.add_argument("--moe-shape", choices=["qwen3", "qwen2"], default="qwen3",
+                    help="MoE layer shape for --profile moe / moe_decode: Qwen3-30B-A3B or "
+                         "Qwen2-57B-A14B (shared expert)")
     args = ap.parse_args()
     if args.profile:
         return profile_run(args)
@@ -827,9 +851,11 @@ def main():
         line["prefill"] = pf
     if rank == 0 and not args.no_prefill:
         line["moe_prefill"] = moe_prefill_bench(q, torch, bf16_tf)
+        line["moe_prefill_shared"] = moe_prefill_bench(q, torch, bf16_tf, "qwen2")
         line["tiny_prefill"] = tiny_prefill_bench(q, torch)
     if rank == 0 and not args.no_sweep:
         line["moe_decode"] = moe_decode_bench(q, torch, hbm_gbs)
+        line["moe_decode_shared"] = moe_decode_bench(q, torch, hbm_gbs, "qwen2")
         line["long_decode"] = long_decode_bench(q, torch, hbm_gbs)
     if rank == 0 and not args.no_stack:
         del layer, w

@@ -52,6 +52,12 @@ QWEN3_8B = LayerConfig(d=4096, n_q_heads=32, n_kv_heads=8, head_dim=128, ffn=122
 QWEN3_30B_A3B = LayerConfig(d=2048, n_q_heads=32, n_kv_heads=4, head_dim=128, ffn=768,
                             qk_norm=1, n_experts=128, top_k=8, norm_topk_prob=1,
                             router_bias=1)
+# Qwen2-57B-A14B MoE layer: 64 experts, top-8, mf=2560, a shared expert of width
+# 20480 with a sigmoid gate, weights without renormalisation; attention shapes
+# those of Qwen2.5-7B ("Qwen2.5-7B 结构拆解" §10, §10.1).
+QWEN2_57B_A14B = LayerConfig(d=3584, n_q_heads=28, n_kv_heads=4, head_dim=128, ffn=2560,
+                             qkv_bias=1, n_experts=64, top_k=8, norm_topk_prob=0,
+                             shared_ffn=20480)
 QWEN25_7B_VOCAB = 152064
 QWEN25_7B_LAYERS = 28
 

@@ -72,7 +72,9 @@ def _check_routing(gi, gw, glog, logits, oidx, owts, gap, norm=1):
     assert np.array_equal(gi[clear], oidx[clear]), (
         f"top-k mismatch on {np.sum(np.any(gi[clear] != oidx[clear], axis=1))} unambiguous tokens")
     assert np.allclose(gw[clear], owts[clear], atol=1e-5)
-    assert np.allclose(glog, logits, atol=2e-5, rtol=1e-5)
+    # the selection claim needs logit errors well below the 1e-3 gap; the
+    # router's FP32 accumulation over K = 2d grows with d (about 3e-5 at d=3584)
+    assert np.abs(glog - logits).max() < 1e-4
     # every selection is a valid top-k: distinct experts, and its weights are
     # those of the oracle's logits at the selected experts
     assert all(len(set(row)) == len(row) for row in gi)
@@ -136,6 +138,46 @@ def test_moe_ffn_qwen3_30b_a3b_full(a3b_weights):
     # the router bias skews expert loads, as the workload intends
     loads = np.bincount(gi.reshape(-1), minlength=128)
     assert loads.max() > 2 * loads.mean()
+
+
+class _PerExpertF64:
+    """w[e] widened to float64 on demand (the full expert stack in FP64 would
+    not fit the test's memory)."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __getitem__(self, e):
+        return synth.to_f64(self.t[e])
+
+
+def test_moe_ffn_qwen2_57b_a14b_full():
+    """Qwen2-57B-A14B-shaped MoE block at T=4096 (64 experts, top-8, mf=2560,
+    shared expert sf=20480, no renormalisation): routing of every token, Y on
+    sampled tokens."""
+    shape = synth.QWEN2_57B_A14B
+    T, E, k = 4096, shape.n_experts, shape.top_k
+    w_cpu = synth.layer_weights(shape, "q2full")
+    r = synth.activations([T, shape.d], "q2full", "r")
+    g = GpuLayer(shape, w_cpu, max_tokens=T, max_batch=1, max_seq=8, max_position=8)
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    wts = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    lg = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    y = g.layer.moe_ffn(r.cuda(), topk_idx=idx, topk_w=wts, logits=lg)
+    assert g.layer.poll_error() == 0
+    del g
+    gi, r64 = idx.cpu().numpy(), f64(r)
+    w64 = {n: (_PerExpertF64(t) if n in ("w_gate", "w_up", "w_down") else synth.to_f64(t))
+           for n, t in w_cpu.items()}
+    cfg = shape.as_dict()
+    z = oracle.rmsnorm(r64, w64["gamma_mlp"], cfg["rms_eps"])
+    logits, oidx, owts, gap = oracle.router_topk(z, w64["w_router"], None, k, 0)
+    _check_routing(gi, wts.cpu().numpy(), lg.cpu().numpy(), logits, oidx, owts, gap, norm=0)
+    rows = np.unique(np.r_[0, 1, 127, 128, 2048, 4095,
+                           np.random.default_rng(2).integers(0, T, 26)])
+    rows = rows[gap[rows] > GAP]
+    ref = oracle.moe_block(r64[rows], w64, cfg)[0]
+    assert_parity(f64(y.float())[rows], ref, what="Qwen2-57B-A14B MoE Y")
 
 
 def _moe_layer_case(shape, w_cpu, tag, B, T, rows):
