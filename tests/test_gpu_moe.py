@@ -219,12 +219,16 @@ def test_moe_layer_prefill_shared_expert():
     _moe_layer_case(shape, synth.layer_weights(shape, "q2moel"), "q2moel", 2, 256, rows)
 
 
-@pytest.mark.parametrize("shape,tag", [(SMALL_MOE, "moed"), (SMALL_QWEN2_MOE, "q2moed")],
-                         ids=["qwen3", "qwen2_shared"])
-def test_moe_layer_decode(shape, tag):
-    """MoE layer decode (tiny per-expert groups), B=8 against 100 cached slots;
-    the Qwen2-MoE case runs the shared expert through the split-K GEMMs."""
-    B, L = 8, 100
+@pytest.mark.parametrize("shape,tag,B", [(SMALL_MOE, "moed", 8), (SMALL_QWEN2_MOE, "q2moed", 8),
+                                         (SMALL_MOE, "moed1", 1), (SMALL_MOE, "moed64", 64),
+                                         (SMALL_QWEN2_MOE, "q2moed65", 65)],
+                         ids=["qwen3", "qwen2_shared", "qwen3_b1", "qwen3_b64", "qwen2_b65"])
+def test_moe_layer_decode(shape, tag, B):
+    """MoE layer decode against 100 cached slots.  Up to 64 tokens the experts
+    run as the grouped swap-AB decode GEMM (B=64 is its largest padding); 65
+    tokens take the 128-row grouped GEMM.  The Qwen2-MoE cases run the shared
+    expert through the split-K GEMMs."""
+    L = 100
     w_cpu = synth.layer_weights(shape, tag)
     x = synth.activations([B, shape.d], tag)
     kc, vc = synth.kv_cache(B, shape.n_kv_heads, L + 1, shape.head_dim, L, tag)

@@ -106,6 +106,7 @@ WorkspaceLayout workspace_layout(const qwen_layer_config& c, int B, int T) {
     W.topk_w = take(mk * 4);
     W.blk_counts = take(moe_perm_blocks(mk) * e * 4);
     W.offsets = take((e + 1) * 4);
+    W.act = take((e + 1) * 4);
     W.perm = take(mk * 4);
     W.inv = take(mk * 4);
     W.zp = take(mk * d * 2);
@@ -563,8 +564,11 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
     return QWEN_OK;
   }
   if (swap) {
+    // MoE: the split reduction + residual also writes [Z_hi | Z_lo] = RMSNorm_2(R)
     QWEN_STAGE_RUN(QWEN_STAGE_O, decode_proj(L->w_o, attn, B, d, nq, part, err, st, S));
-    QWEN_STAGE_RUN(QWEN_STAGE_O_FINISH, reduce_resid(part, S, B, d, x, x32, nullptr, r32, st));
+    QWEN_STAGE_RUN(QWEN_STAGE_O_FINISH,
+                   reduce_resid_norm(part, S, B, d, x, x32, r32, L->gamma_mlp, c.rms_eps, z, st,
+                                     2 * (size_t)d, z + d));
   } else {
     GemmEpilogue e{};
     e.mode = EPI_RESID;
@@ -577,8 +581,8 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
     QWEN_STAGE_RUN(QWEN_STAGE_O, gemm_tc(attn, nq, L->w_o, nq, B, d, nq, true, e, err, st));
   }
   if (c.n_experts) {
-    QWEN_STAGE_RUN(QWEN_STAGE_MOE,
-                   moe_forward(L, nullptr, r32, y, y32, B, nullptr, nullptr, nullptr, ws, W, st));
+    QWEN_STAGE_RUN(QWEN_STAGE_MOE, moe_forward(L, nullptr, r32, y, y32, B, nullptr, nullptr,
+                                               nullptr, ws, W, st, /*z_ready=*/swap));
     return QWEN_OK;
   }
   // RMSNorm_2 -> Z, gate/up + SiLU*up -> H, down + residual -> Y

@@ -10,6 +10,16 @@
 // are in flight.  Each unit writes FP32 partials part[s][n][b]; a reduction
 // kernel sums the splits in a fixed order (deterministic) and applies the
 // step's epilogue (residual add, SiLU*up, or the fused QKV finish).
+//
+// Grouped mode (mixture-of-experts decode): W is a stack of E weights [E][N][K]
+// and X holds the routed rows grouped by expert, rows [offsets[e],
+// offsets[e+1]) for expert e.  A unit is (non-empty expert, n-tile, k-split);
+// its X tile starts at the expert's first row and results are kept for that
+// expert's rows only, so each touched expert's weights stream from HBM once.
+// Token mode (grouped, SwiGLU only): X holds the T token rows themselves;
+// every expert's tile multiplies all of them and the epilogue keeps the
+// tokens routed to the expert, writing each to its sorted row inv[t*k + j]
+// (idx[t*k + j] == e), so no gathered copy of X is needed.
 #include "common.cuh"
 #include "internal.h"
 #include "layer.h"
@@ -46,11 +56,18 @@ struct DecCfg {
 
 }  // namespace
 
+// B: rows of X (all routed rows in grouped mode, the tokens in token mode).
+// gact (grouped mode, else null): [0] = number of non-empty experts, then
+// their ids; goff: [E + 1] row offsets; tidx/tinv (token mode, else null):
+// [B][tk] expert ids and sorted rows of each (token, slot).  All are written
+// by the kernel before this one.
 template <int BP, int EPI>
 __global__ void __launch_bounds__(kDThreads, 1)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        int B, int N, int K, int splits, uint32_t idesc, int w_static,
-                       float* __restrict__ part, f16* __restrict__ hout, int* err) {
+                       float* __restrict__ part, f16* __restrict__ hout,
+                       const int32_t* gact, const int32_t* goff, const int32_t* tidx,
+                       const int32_t* tinv, int tk, int* err) {
   using C = DecCfg<BP, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -69,7 +86,11 @@ __global__ void __launch_bounds__(kDThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = (N + kDBM - 1) / kDBM;
   const int n_kblk = (K + kDBK - 1) / kDBK;
-  const int units = n_tiles * splits;
+  const int per_group = n_tiles * splits;
+  const bool grouped = gact != nullptr;
+  const bool tokens = tidx != nullptr;  // token mode (grouped SwiGLU only)
+  // grouped: the unit count is device data, read after pdl_wait by each role
+  int units = grouped ? 0 : per_group;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -92,10 +113,26 @@ __global__ void __launch_bounds__(kDThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  auto unit_range = [&](int u, int& n0, int& kb0, int& kb1, int& s) {
-    const int tile = u / splits;
-    s = u - tile * splits;
+  // unit u -> weight row of its tile (wrow), n0 within the expert's N, the
+  // k-block range of split s, and the X rows [row0, row0 + m) it serves
+  auto unit_range = [&](int u, int& wrow, int& n0, int& kb0, int& kb1, int& s, int& row0,
+                        int& m, int& e) {
+    const int a = u / per_group;
+    const int r = u - a * per_group;
+    const int tile = r / splits;
+    s = r - tile * splits;
     n0 = tile * kDBM;
+    if (grouped) {
+      e = gact[1 + a];
+      row0 = tokens ? 0 : goff[e];
+      m = tokens ? B : goff[e + 1] - row0;
+      wrow = e * N + n0;
+    } else {
+      e = 0;
+      row0 = 0;
+      m = B;
+      wrow = n0;
+    }
     kb0 = (int)(((long long)s * n_kblk) / splits);
     kb1 = (int)(((long long)(s + 1) * n_kblk) / splits);
   };
@@ -111,30 +148,31 @@ __global__ void __launch_bounds__(kDThreads, 1)
       // weights are never written by the kernels before this one: stream the
       // first stages of weight tiles while the previous kernel finishes
       int pre = 0;
-      if (w_static && blockIdx.x < units) {
-        int n0, kb0, kb1, s;
-        unit_range(blockIdx.x, n0, kb0, kb1, s);
+      if (w_static && !grouped && blockIdx.x < units) {
+        int wrow, n0, kb0, kb1, s, row0, m, e;
+        unit_range(blockIdx.x, wrow, n0, kb0, kb1, s, row0, m, e);
         pre = min(C::STAGES, kb1 - kb0);
         for (int i = 0; i < pre; ++i) {
           mbar_arrive_expect_tx_w(&full[i], C::STAGE_BYTES);
-          tma_load_2d_hint_w(sA + i * C::A_BYTES, &tmW, &full[i], (kb0 + i) * kDBK, n0, wpol);
+          tma_load_2d_hint_w(sA + i * C::A_BYTES, &tmW, &full[i], (kb0 + i) * kDBK, wrow, wpol);
         }
       }
       pdl_wait();
+      if (grouped) units = gact[0] * per_group;
       int stage = 0;
       uint32_t phase = 0;
       int g = 0;
       for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        int n0, kb0, kb1, s;
-        unit_range(u, n0, kb0, kb1, s);
+        int wrow, n0, kb0, kb1, s, row0, m, e;
+        unit_range(u, wrow, n0, kb0, kb1, s, row0, m, e);
         for (int kb = kb0; kb < kb1; ++kb, ++g) {
           if (g < pre) {
-            tma_load_2d_w(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * kDBK, 0);
+            tma_load_2d_w(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * kDBK, row0);
           } else {
             if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, err)) goto prod_done;
             mbar_arrive_expect_tx_w(&full[stage], C::STAGE_BYTES);
-            tma_load_2d_hint_w(sA + stage * C::A_BYTES, &tmW, &full[stage], kb * kDBK, n0, wpol);
-            tma_load_2d_w(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * kDBK, 0);
+            tma_load_2d_hint_w(sA + stage * C::A_BYTES, &tmW, &full[stage], kb * kDBK, wrow, wpol);
+            tma_load_2d_w(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * kDBK, row0);
           }
           if (++stage == C::STAGES) {
             stage = 0;
@@ -153,12 +191,16 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
   } else if (warp == 1) {
     {
+      if (grouped) {
+        pdl_wait();
+        units = gact[0] * per_group;
+      }
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
-        int n0, kb0, kb1, s;
-        unit_range(u, n0, kb0, kb1, s);
+        int wrow, n0, kb0, kb1, s, row0, m, e;
+        unit_range(u, wrow, n0, kb0, kb1, s, row0, m, e);
         const int acc = local & 1;
         if (!mbar_wait_w(&tempty[acc], ((local >> 1) & 1) ^ 1u, abort_flag, err)) break;
         tc_fence_after();
@@ -188,19 +230,24 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
   } else {
     pdl_wait();  // the partials may still be read by the previous kernel
+    if (grouped) units = gact[0] * per_group;
     const int q = warp & 3;
     int local = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
-      int n0, kb0, kb1, s;
-      unit_range(u, n0, kb0, kb1, s);
+      int wrow, n0, kb0, kb1, s, row0, m, e;
+      unit_range(u, wrow, n0, kb0, kb1, s, row0, m, e);
+      if (m > BP) {  // the host sizes BP for the largest group: never taken
+        record_error(err, QWEN_ERR_CAPACITY);
+        m = BP;
+      }
       const int acc = local & 1;
       if (!mbar_wait(&tfull[acc], (local >> 1) & 1, abort_flag, err)) break;
       tc_fence_after();
       const int n = n0 + q * 32 + lane;
       if constexpr (EPI == DEC_PARTIAL) {
-        // part[s][b][n]: for each batch column the 32 lanes (consecutive
-        // weight rows n) write 128 contiguous bytes
-        float* dst = part + (size_t)s * B * N + n;
+        // part[s][row][n]: for each X row the 32 lanes (consecutive weight
+        // rows n) write 128 contiguous bytes
+        float* dst = part + (size_t)s * B * N + (size_t)row0 * N + n;
 #pragma unroll 1
         for (int c = 0; c < BP; c += 32) {
           uint32_t r[32];
@@ -209,7 +256,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
           if (n < N) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (c + i < B) dst[(size_t)(c + i) * N] = __uint_as_float(r[i]);
+              if (c + i < m) dst[(size_t)(c + i) * N] = __uint_as_float(r[i]);
           }
         }
         tc_fence_before();
@@ -239,11 +286,21 @@ __global__ void __launch_bounds__(kDThreads, 1)
             uint32_t r[32];
             tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BP + c, r);
             tmem_ld_wait();
+            // output row of column c + lane: the X row itself, or in token
+            // mode the sorted row of the token's slot that chose this expert
+            int orow = c + lane < m ? row0 + c + lane : -1;
+            if (tokens && orow >= 0) {
+              int found = -1;
+              for (int j = 0; j < tk; ++j)
+                if (tidx[(size_t)orow * tk + j] == e) found = tinv[(size_t)orow * tk + j];
+              orow = found;
+            }
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              if (c + i < B && f_tile + fr < fdim) {
+              const int row = __shfl_sync(0xffffffffu, orow, i);
+              if (row >= 0 && f_tile + fr < fdim) {
                 const float gv = xch[(c + i) * 64 + fr];
-                hout[(size_t)(c + i) * fdim + f_tile + fr] =
+                hout[(size_t)row * fdim + f_tile + fr] =
                     __float2half_rn(silu_f(gv) * __uint_as_float(r[i]));
               }
             }
@@ -380,7 +437,7 @@ template <int PER>
 __global__ void __launch_bounds__(1024) reduce_resid_norm_kernel(
     const float* __restrict__ part, int splits, int B, int N, const bf16* __restrict__ resid,
     const float* __restrict__ resid32, float* __restrict__ out32, const bf16* __restrict__ gamma,
-    float eps, f16* __restrict__ z) {
+    float eps, f16* __restrict__ z, size_t zs, f16* __restrict__ z_lo) {
   pdl_trigger();
   pdl_wait();
   __shared__ float red[32];
@@ -418,10 +475,16 @@ __global__ void __launch_bounds__(1024) reduce_resid_norm_kernel(
 #pragma unroll
   for (int w = 0; w < 32; ++w) tot += red[w];
   const float rstd = rsqrtf(tot / (float)N + eps);
+  const size_t zrow = (size_t)b * zs;
 #pragma unroll
   for (int j = 0; j < PER; ++j) {
     const int n = threadIdx.x + 1024 * j;
-    if (n < N) z[row + n] = __float2half_rn(__bfloat162float(gamma[n]) * (v[j] * rstd));
+    if (n < N) {
+      const float o = __bfloat162float(gamma[n]) * (v[j] * rstd);
+      const f16 hi = __float2half_rn(o);
+      z[zrow + n] = hi;
+      if (z_lo) z_lo[zrow + n] = __float2half_rn(o - __half2float(hi));
+    }
   }
 }
 
@@ -474,9 +537,9 @@ static int pad_batch(int B) {
   return 256;
 }
 
-int decode_splits(int N, int K) {
+int decode_splits(int N, int K, int groups) {
   const int sms = device_sm_count();
-  const int tiles = (N + kDBM - 1) / kDBM;
+  const int tiles = (N + kDBM - 1) / kDBM * groups;
   const int kblk = (K + kDBK - 1) / kDBK;
   int best = 1;
   double best_score = -1.0;
@@ -510,6 +573,12 @@ size_t decode_part_bytes(const qwen_layer_config& c, int B) {
   } else {
     upd(router_rows(c), 2 * d);  // the router over [Z_hi | Z_lo]
     if (c.shared_ffn) upd(d, c.shared_ffn);  // the shared expert's down projection
+    if (B <= kMoeDecodeMaxRows) {  // grouped expert down projection, B*k rows
+      const int rows = B * c.top_k;
+      const int groups = rows < c.n_experts ? rows : c.n_experts;
+      const size_t need = (size_t)decode_splits(d, f, groups) * rows * d * 4;
+      if (need > m) m = need;
+    }
   }
   return m;
 }
@@ -517,7 +586,9 @@ size_t decode_part_bytes(const qwen_layer_config& c, int B) {
 template <int BP, int EPI>
 static qwen_status launch_dec(const CUtensorMap& tw, const CUtensorMap& tx, int B, int N, int K,
                               int splits, bool op_f16, bool w_static, float* part, f16* hout,
-                              int* err, cudaStream_t st) {
+                              const int32_t* gact, const int32_t* goff, const int32_t* tidx,
+                              const int32_t* tinv, int tk, int max_groups, int* err,
+                              cudaStream_t st) {
   using C = DecCfg<BP, EPI>;
   auto kern = gemm_decode_kernel<BP, EPI>;
   static bool attr = false;
@@ -527,35 +598,75 @@ static qwen_status launch_dec(const CUtensorMap& tw, const CUtensorMap& tx, int 
       return QWEN_ERR_CUDA;
     attr = true;
   }
-  const int units = ((N + kDBM - 1) / kDBM) * splits;
+  const int units = ((N + kDBM - 1) / kDBM) * splits * max_groups;
   const int sms = device_sm_count();
   const int grid = units < sms ? units : sms;
   launch_k(kern, dim3(grid), dim3(kDThreads), C::SMEM_BYTES, st, tw, tx, B, N, K, splits,
-           idesc_f32acc(kDBM, BP, op_f16), w_static ? 1 : 0, part, hout, err);
+           idesc_f32acc(kDBM, BP, op_f16), w_static ? 1 : 0, part, hout, gact, goff, tidx, tinv,
+           tk, err);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
+}
+
+// Shared host path of the dense and grouped decode GEMMs.  W rows: N, or
+// E * N stacked experts (grouped); X: B rows, ldx apart; BP covers max_m rows.
+static qwen_status decode_gemm_launch(const void* W, int w_rows, const void* X, int ldx, int B,
+                                      int max_m, int N, int K, int splits, bool op_f16,
+                                      bool w_static, float* part, f16* hout,
+                                      const int32_t* gact, const int32_t* goff,
+                                      const int32_t* tidx, const int32_t* tinv, int tk,
+                                      int max_groups, int* err, cudaStream_t st) {
+  if (B <= 0 || max_m <= 0 || max_m > 256) return QWEN_ERR_UNSUPPORTED;
+  if ((K & 7) || splits < 1 || max_groups < 1) return QWEN_ERR_UNSUPPORTED;
+  const int bp = pad_batch(max_m);
+  CUtensorMap tw, tx;
+  if (!tmap2d(&tw, W, (uint64_t)w_rows, (uint64_t)K, (uint64_t)K, kDBM, op_f16))
+    return QWEN_ERR_CUDA;
+  if (!tmap2d(&tx, X, (uint64_t)B, (uint64_t)K, (uint64_t)ldx, bp, op_f16)) return QWEN_ERR_CUDA;
+#define QWEN_DEC_CASE(BPV)                                                                        \
+  case BPV:                                                                                       \
+    return hout ? launch_dec<BPV, DEC_SWIGLU>(tw, tx, B, N, K, 1, op_f16, w_static, nullptr,      \
+                                              hout, gact, goff, tidx, tinv, tk, max_groups, err,  \
+                                              st)                                                 \
+                : launch_dec<BPV, DEC_PARTIAL>(tw, tx, B, N, K, splits, op_f16, w_static, part,   \
+                                               nullptr, gact, goff, nullptr, nullptr, 0,          \
+                                               max_groups, err, st);
+  switch (bp) {
+    QWEN_DEC_CASE(16)
+    QWEN_DEC_CASE(32)
+    QWEN_DEC_CASE(64)
+    QWEN_DEC_CASE(128)
+    QWEN_DEC_CASE(256)
+    default: return QWEN_ERR_UNSUPPORTED;
+  }
+#undef QWEN_DEC_CASE
 }
 
 qwen_status gemm_decode_splitk(const void* W, const void* X, int ldx, int B, int N, int K,
                                int splits, bool op_f16, float* part, int* err, cudaStream_t st,
                                bool w_static, f16* swiglu_out) {
-  if (B <= 0 || B > 256) return QWEN_ERR_UNSUPPORTED;
-  if ((K & 7) || splits < 1) return QWEN_ERR_UNSUPPORTED;
-  const int bp = pad_batch(B);
-  CUtensorMap tw, tx;
-  if (!tmap2d(&tw, W, (uint64_t)N, (uint64_t)K, (uint64_t)K, kDBM, op_f16)) return QWEN_ERR_CUDA;
-  if (!tmap2d(&tx, X, (uint64_t)B, (uint64_t)K, (uint64_t)ldx, bp, op_f16)) return QWEN_ERR_CUDA;
-  switch (bp) {
-    case 16: return swiglu_out ? launch_dec<16, DEC_SWIGLU>(tw, tx, B, N, K, 1, op_f16, w_static, nullptr, swiglu_out, err, st) : launch_dec<16, DEC_PARTIAL>(tw, tx, B, N, K, splits, op_f16, w_static, part, nullptr, err, st);
-    case 32: return swiglu_out ? launch_dec<32, DEC_SWIGLU>(tw, tx, B, N, K, 1, op_f16, w_static, nullptr, swiglu_out, err, st) : launch_dec<32, DEC_PARTIAL>(tw, tx, B, N, K, splits, op_f16, w_static, part, nullptr, err, st);
-    case 64: return swiglu_out ? launch_dec<64, DEC_SWIGLU>(tw, tx, B, N, K, 1, op_f16, w_static, nullptr, swiglu_out, err, st) : launch_dec<64, DEC_PARTIAL>(tw, tx, B, N, K, splits, op_f16, w_static, part, nullptr, err, st);
-    case 128: return swiglu_out ? launch_dec<128, DEC_SWIGLU>(tw, tx, B, N, K, 1, op_f16, w_static, nullptr, swiglu_out, err, st) : launch_dec<128, DEC_PARTIAL>(tw, tx, B, N, K, splits, op_f16, w_static, part, nullptr, err, st);
-    default:
-      return swiglu_out ? launch_dec<256, DEC_SWIGLU>(tw, tx, B, N, K, 1, op_f16, w_static, nullptr,
-                                                      swiglu_out, err, st)
-                        : launch_dec<256, DEC_PARTIAL>(tw, tx, B, N, K, splits, op_f16, w_static,
-                                                       part, nullptr, err, st);
-  }
+  return decode_gemm_launch(W, N, X, ldx, B, B, N, K, splits, op_f16, w_static, part, swiglu_out,
+                            nullptr, nullptr, nullptr, nullptr, 0, 1, err, st);
+}
+
+qwen_status gemm_decode_grouped(const void* W, int E, const void* X, int rows, int max_m, int N,
+                                int K, int splits, const int32_t* act, const int32_t* offsets,
+                                int max_groups, float* part, f16* swiglu_out, int* err,
+                                cudaStream_t st) {
+  if (!act || !offsets || E <= 0) return QWEN_ERR_INVALID_ARG;
+  return decode_gemm_launch(W, E * N, X, K, rows, max_m, N, K, splits, /*op_f16=*/true,
+                            /*w_static=*/true, part, swiglu_out, act, offsets, nullptr, nullptr, 0,
+                            max_groups, err, st);
+}
+
+qwen_status gemm_decode_grouped_tokens(const void* W, int E, const void* X, int ldx, int T,
+                                       int N, int K, const int32_t* act, const int32_t* idx,
+                                       const int32_t* inv, int k, int max_groups, f16* h_out,
+                                       int* err, cudaStream_t st) {
+  if (!act || !idx || !inv || !h_out || E <= 0 || k < 1) return QWEN_ERR_INVALID_ARG;
+  return decode_gemm_launch(W, E * N, X, ldx, T, T, N, K, 1, /*op_f16=*/true, /*w_static=*/true,
+                            nullptr, h_out, act, nullptr, idx, inv, k,
+                            max_groups, err, st);
 }
 
 static inline int blocks_for(long long n, int t) { return (int)((n + t - 1) / t); }
@@ -590,14 +701,15 @@ qwen_status reduce_qkv(const float* part, int splits, int B, int Nqkv, const Qkv
 
 qwen_status reduce_resid_norm(const float* part, int splits, int B, int N, const bf16* resid,
                               const float* resid32, float* out32, const bf16* gamma, float eps,
-                              f16* z, cudaStream_t st) {
+                              f16* z, cudaStream_t st, size_t z_stride, f16* z_lo) {
   if (N > 1024 * 8) return QWEN_ERR_UNSUPPORTED;
+  const size_t zs = z_stride ? z_stride : (size_t)N;
   if (N <= 1024 * 4)
     launch_k(reduce_resid_norm_kernel<4>, dim3(B), dim3(1024), 0, st, part, splits, B, N, resid,
-             resid32, out32, gamma, eps, z);
+             resid32, out32, gamma, eps, z, zs, z_lo);
   else
     launch_k(reduce_resid_norm_kernel<8>, dim3(B), dim3(1024), 0, st, part, splits, B, N, resid,
-             resid32, out32, gamma, eps, z);
+             resid32, out32, gamma, eps, z, zs, z_lo);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }

@@ -17,7 +17,7 @@ struct PackedLayout {
 struct WorkspaceLayout {
   size_t xh, q, k16, v16, attn, r32, z, h;
   // MoE
-  size_t logits, topk_idx, topk_w, blk_counts, offsets, perm, inv, zp, hp, yp;
+  size_t logits, topk_idx, topk_w, blk_counts, offsets, act, perm, inv, zp, hp, yp;
   // MoE shared expert: H_s [M][sf] FP16, its output [M][d] FP32, gate g [M]
   size_t hs, ys32, gscale;
   // decode (T == 1)
@@ -79,15 +79,21 @@ qwen_status layer_decode(qwen_layer_s* L, const __nv_bfloat16* x, const float* x
                          uint8_t* ws, const WorkspaceLayout& W, cudaStream_t st);
 
 // MoE block: residual input r (BF16) or r32 (FP32); output y (BF16) and/or y32.
+// z_ready: the workspace already holds [Z_hi | Z_lo] = RMSNorm_2(R) (the decode
+// step fuses the norm into the O projection's split reduction).
 qwen_status moe_forward(qwen_layer_s* L, const __nv_bfloat16* r, const float* r32,
                         __nv_bfloat16* y, float* y32, int T, int32_t* topk_idx_out,
                         float* topk_w_out, float* logits_out, uint8_t* ws,
-                        const WorkspaceLayout& W, cudaStream_t st);
+                        const WorkspaceLayout& W, cudaStream_t st, bool z_ready = false);
 
 // ---- decode building blocks (decode_gemm.cu, attention_decode.cu)
 
-// Number of K splits the swap-AB decode GEMM uses for an [N, K] weight.
-int decode_splits(int N, int K);
+// Number of K splits the swap-AB decode GEMM uses for an [N, K] weight (or for
+// `groups` such weights in grouped mode).
+int decode_splits(int N, int K, int groups = 1);
+// MoE blocks on at most this many tokens run the experts through the grouped
+// swap-AB decode GEMM (the tokens sit on the MMA's N side, padded to 16..64).
+constexpr int kMoeDecodeMaxRows = 64;
 // Bytes of FP32 partials the decode GEMM of the layer needs for batch B.
 size_t decode_part_bytes(const qwen_layer_config& c, int B);
 
@@ -106,13 +112,36 @@ qwen_status gemm_decode_splitk(const void* W, const void* X, int ldx, int B, int
                                int splits, bool op_f16, float* part, int* err, cudaStream_t st,
                                bool w_static = false, __half* swiglu_out = nullptr);
 
+// Grouped (mixture-of-experts) decode GEMM.  W: E stacked FP16 [N, K] weights;
+// X: `rows` FP16 rows of K, grouped by expert: rows [offsets[e], offsets[e+1])
+// belong to expert e (offsets [E + 1], device).  act (device): [0] = number of
+// non-empty experts (at most max_groups), then their ids.  No expert has more
+// than max_m rows.  Output: part[s][row][N] FP32 partials, or with swiglu_out
+// (one split, W interleaved gate/up) H[row][N/2] = SiLU(gate) * up as FP16.
+qwen_status gemm_decode_grouped(const void* W, int E, const void* X, int rows, int max_m, int N,
+                                int K, int splits, const int32_t* act, const int32_t* offsets,
+                                int max_groups, float* part, __half* swiglu_out, int* err,
+                                cudaStream_t st);
+
+// Token mode of the grouped decode GEMM for an interleaved gate/up stack W
+// [E][N][K]: X = the T token rows (ldx apart); for each non-empty expert e in
+// act, H[inv[t*k + j]] = SiLU(gate) * up of token t wherever idx[t*k + j] == e
+// (H rows N/2 wide, FP16).
+qwen_status gemm_decode_grouped_tokens(const void* W, int E, const void* X, int ldx, int T,
+                                       int N, int K, const int32_t* act, const int32_t* idx,
+                                       const int32_t* inv, int k, int max_groups, __half* h_out,
+                                       int* err, cudaStream_t st);
+
 // Reductions over the splits followed by the step's epilogue.
 qwen_status reduce_resid(const float* part, int splits, int B, int N, const __nv_bfloat16* resid,
                          const float* resid32, __nv_bfloat16* out, float* out32, cudaStream_t st);
-// R = sum of splits + residual (FP32, out32), then Z = RMSNorm(R) (FP16).
+// R = sum of splits + residual (FP32, out32), then Z = RMSNorm(R) (FP16, rows
+// z_stride apart, 0 = N).  With z_lo the FP16 rounding residual of Z is written
+// there as well (same row stride): the [Z_hi | Z_lo] operand of the router.
 qwen_status reduce_resid_norm(const float* part, int splits, int B, int N,
                               const __nv_bfloat16* resid, const float* resid32, float* out32,
-                              const __nv_bfloat16* gamma, float eps, __half* z, cudaStream_t st);
+                              const __nv_bfloat16* gamma, float eps, __half* z, cudaStream_t st,
+                              size_t z_stride = 0, __half* z_lo = nullptr);
 qwen_status reduce_swiglu(const float* part, int splits, int B, int f, __half* h,
                           cudaStream_t st);
 qwen_status reduce_qkv(const float* part, int splits, int B, int Nqkv, const QkvParams& p,

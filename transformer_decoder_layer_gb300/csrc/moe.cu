@@ -20,14 +20,17 @@
 //   3. top-k: one warp per token, k rounds of a warp arg-max; adds b_r and
 //      writes the biased logits back.  The shared gate W_sg rides along as
 //      router row E, so its logit comes out of the same GEMM
-//   4. permutation (stable counting sort by expert, in entry order t*k + j):
+//   4. shared expert: dense gate/up (+SiLU*up) and down GEMMs on Z_hi, FP32 out
+//   5. permutation (stable counting sort by expert, in entry order t*k + j):
 //      per-block expert counts, then per block the starting position of each
 //      expert (all counts of earlier experts, plus this expert's counts in
-//      earlier blocks) and warp-level ranks; gather of Z_hi rows
-//   5. grouped GEMM gate/up (+SiLU*up) and grouped GEMM down over per-expert
-//      row ranges, one persistent tensor-core kernel each
-//   5b. shared expert: dense gate/up (+SiLU*up) and down GEMMs on Z_hi, FP32 out
-//   6. combine: Y[t] = R[t] + sum_j w[t][j] Y_e[pos(t, j)] in slot order
+//      earlier blocks) and warp-level ranks; the list of non-empty experts;
+//      gather of Z_hi rows
+//   6. grouped GEMM gate/up (+SiLU*up) and grouped GEMM down over per-expert
+//      row ranges, one persistent tensor-core kernel each: 128-row tiles of
+//      routed rows, or for up to 64 tokens the swap-AB decode GEMM per
+//      touched expert (weights streamed once, tokens on the MMA's N side)
+//   7. combine: Y[t] = R[t] + sum_j w[t][j] Y_e[pos(t, j)] in slot order
 //      (+ g[t] Y_s[t])
 #include "common.cuh"
 #include "internal.h"
@@ -38,21 +41,17 @@ namespace qwen {
 namespace {
 
 constexpr int kPermBlock = 1024;  // permutation entries per CTA
+constexpr int kRouteMaxSplits = 8;  // router K splits when the routing is one CTA
 
-// logits rows are `ldl` apart; columns [0, E) are Z W_r^T on entry and
-// Z W_r^T + b_r on exit.  Gate weights: norm != 0, a softmax over the k
-// selected logits; norm == 0, the selected entries of the softmax over all E
-// logits.  With gscale, column E holds the shared expert's gate logit and
-// gscale[t] = sigmoid of it.
-__global__ void topk_kernel(float* __restrict__ logits, int ldl, const float* __restrict__ bias,
-                            int T, int E, int k, int norm, int32_t* __restrict__ idx,
-                            float* __restrict__ w, float* __restrict__ gscale) {
-  pdl_trigger();
-  pdl_wait();
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+// One warp: top-k of the logits row `lrow` (columns [0, E) are Z W_r^T on entry
+// and Z W_r^T + b_r on exit) and its gate weights: norm != 0, a softmax over
+// the k selected logits; norm == 0, the selected entries of the softmax over
+// all E logits.  Lane 0 writes idx_row/w_row [k] and, with g_out, the sigmoid
+// of the shared gate's logit lrow[E].
+__device__ __forceinline__ void topk_warp(float* lrow, const float* __restrict__ bias, int E,
+                                          int k, int norm, int32_t* idx_row, float* w_row,
+                                          float* g_out) {
   const int lane = threadIdx.x & 31;
-  if (t >= T) return;
-  float* lrow = logits + (size_t)t * ldl;
   const int per = (E + 31) / 32;  // <= 8
   float v[8];
   unsigned taken = 0;
@@ -110,11 +109,23 @@ __global__ void topk_kernel(float* __restrict__ logits, int ldl, const float* __
     }
     const float den = norm ? s : all;
     for (int j = 0; j < k; ++j) {
-      idx[(size_t)t * k + j] = sel_i[j];
-      w[(size_t)t * k + j] = p[j] / den;
+      idx_row[j] = sel_i[j];
+      w_row[j] = p[j] / den;
     }
-    if (gscale) gscale[t] = 1.f / (1.f + expf(-lrow[E]));
+    if (g_out) *g_out = 1.f / (1.f + expf(-lrow[E]));
   }
+}
+
+// One warp per token; logits rows are `ldl` apart (column E: the shared gate).
+__global__ void topk_kernel(float* __restrict__ logits, int ldl, const float* __restrict__ bias,
+                            int T, int E, int k, int norm, int32_t* __restrict__ idx,
+                            float* __restrict__ w, float* __restrict__ gscale) {
+  pdl_trigger();
+  pdl_wait();
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (t >= T) return;
+  topk_warp(logits + (size_t)t * ldl, bias, E, k, norm, idx + (size_t)t * k, w + (size_t)t * k,
+            gscale ? gscale + t : nullptr);
 }
 
 // Per-block expert counts: block g counts entries [g*1024, (g+1)*1024).
@@ -135,10 +146,12 @@ __global__ void __launch_bounds__(kPermBlock) perm_count_kernel(const int32_t* _
 // Stable positions: entry i of block g with expert e goes to
 //   offsets[e] + (entries of e in blocks < g) + (entries of e before i in block g),
 // the last term from warp match masks plus the counts of earlier warps.
-// perm[pos] = entry, inv[entry] = pos; block 0 writes offsets[0..E].
+// perm[pos] = entry, inv[entry] = pos; block 0 writes offsets[0..E] and the
+// list of non-empty experts act = [count, ids in increasing order].
 __global__ void __launch_bounds__(kPermBlock) perm_scatter_kernel(
     const int32_t* __restrict__ idx, int n, int E, int G, const int32_t* __restrict__ blk_counts,
-    int32_t* __restrict__ offsets, int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+    int32_t* __restrict__ offsets, int32_t* __restrict__ act, int32_t* __restrict__ perm,
+    int32_t* __restrict__ inv) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ int32_t sm[];
@@ -159,13 +172,19 @@ __global__ void __launch_bounds__(kPermBlock) perm_scatter_kernel(
   for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
   if (threadIdx.x == 0) {
-    int o = 0;
+    int o = 0, na = 0;
     for (int e = 0; e < E; ++e) {
-      if (g == 0) offsets[e] = o;
+      if (g == 0) {
+        offsets[e] = o;
+        if (tot[e]) act[1 + na++] = e;
+      }
       base[e] += o;
       o += tot[e];
     }
-    if (g == 0) offsets[E] = o;
+    if (g == 0) {
+      offsets[E] = o;
+      act[0] = na;
+    }
   }
   const int i = g * kPermBlock + threadIdx.x;
   const bool valid = i < n;
@@ -179,6 +198,97 @@ __global__ void __launch_bounds__(kPermBlock) perm_scatter_kernel(
     for (int w = 0; w < wid; ++w) pos += wcnt[w * E + e];
     perm[pos] = i;
     inv[i] = pos;
+  }
+}
+
+// Decode-sized routing in one CTA of 1024 threads (T * k <= 1024, T <= 64,
+// S <= kRouteMaxSplits):
+//   logits[t] = sum over the S router split partials part[s][t][0..R) (in
+//   split order; one thread per logit), then the top-k of every token (one
+//   warp per token), then the stable counting sort by expert (offsets, list of
+//   non-empty experts, perm, inv) as the separate kernels below do.  No Z rows
+//   are gathered: the expert gate/up GEMM reads the token rows directly.
+__global__ void __launch_bounds__(1024) route_small_kernel(
+    const float* __restrict__ part, int S, int T, int R, const float* __restrict__ bias, int E,
+    int k, int norm, float* __restrict__ logits, int32_t* __restrict__ idx,
+    float* __restrict__ w, float* __restrict__ gscale, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ act, int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ int32_t sm[];
+  int32_t* tot = sm;              // [E] entries per expert
+  int32_t* base = tot + E;        // [E] first sorted position of each expert
+  int32_t* wcnt = base + E;       // [32][E] entries of e per warp
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int n = T * k;
+  const size_t plane = (size_t)T * R;
+  // split sums: all S loads of a logit are issued before the in-order adds
+  for (int i = threadIdx.x; i < T * R; i += blockDim.x) {
+    float p[kRouteMaxSplits];
+#pragma unroll
+    for (int sp = 0; sp < kRouteMaxSplits; ++sp) p[sp] = sp < S ? part[sp * plane + i] : 0.f;
+    float a = 0.f;
+#pragma unroll
+    for (int sp = 0; sp < kRouteMaxSplits; ++sp) a += p[sp];
+    logits[i] = a;
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) tot[e] = 0;
+  for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  for (int t = wid; t < T; t += 32)
+    topk_warp(logits + (size_t)t * R, bias, E, k, norm, idx + (size_t)t * k, w + (size_t)t * k,
+              gscale ? gscale + t : nullptr);
+  __syncthreads();  // idx rows written by lane 0 of each warp are visible
+  const bool valid = threadIdx.x < n;
+  const int e = valid ? min(max(idx[threadIdx.x], 0), E - 1) : -1;
+  if (valid) atomicAdd(&tot[e], 1);
+  const unsigned same = __match_any_sync(0xffffffffu, e);
+  const int rank_w = __popc(same & ((1u << lane) - 1u));
+  if (valid && rank_w == 0) wcnt[wid * E + e] = __popc(same);
+  __syncthreads();
+  if (wid == 0) {
+    // exclusive scan of tot over E <= 256 experts, 8 per lane, and the
+    // compacted list of non-empty experts in increasing order
+    int c[8], sum = 0, nz = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int x = lane * 8 + j;
+      c[j] = x < E ? tot[x] : 0;
+      sum += c[j];
+      nz += c[j] > 0;
+    }
+    int incl = sum, nzi = nz;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      const int u = __shfl_up_sync(0xffffffffu, nzi, o);
+      if (lane >= o) {
+        incl += v;
+        nzi += u;
+      }
+    }
+    int off = incl - sum, na = nzi - nz;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int x = lane * 8 + j;
+      if (x < E) {
+        offsets[x] = off;
+        base[x] = off;
+        if (c[j]) act[1 + na++] = x;
+      }
+      off += c[j];
+    }
+    if (lane == 31) {
+      offsets[E] = incl;
+      act[0] = nzi;
+    }
+  }
+  __syncthreads();
+  if (valid) {
+    int pos = base[e] + rank_w;
+    for (int q = 0; q < wid; ++q) pos += wcnt[q * E + e];
+    perm[pos] = threadIdx.x;
+    inv[threadIdx.x] = pos;
   }
 }
 
@@ -198,9 +308,13 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ z, size_t zs,
   for (int c = lane; c < d / 8; c += 32) dst[c] = src[c];
 }
 
-// y[t] = R[t] + (sum_j w[t][j] * yp[inv[t*k + j]] summed in slot order j
+// y[t] = R[t] + (sum_j w[t][j] * Y_e[inv[t*k + j]] summed in slot order j
 //        [+ gs[t] * ys[t], the gated shared expert, when ys is given]).
-__global__ void combine_kernel(const f16* __restrict__ yp, const int32_t* __restrict__ inv,
+// Expert outputs Y_e: FP16 rows yp, or (PART) the sum over `ys_n` FP32 split
+// partials ypart[s][row][d], splits added in order.
+template <bool PART>
+__global__ void combine_kernel(const f16* __restrict__ yp, const float* __restrict__ ypart,
+                               int y_splits, size_t y_plane, const int32_t* __restrict__ inv,
                                const float* __restrict__ w, const float* __restrict__ ys,
                                const float* __restrict__ gs, const float* __restrict__ r32,
                                const bf16* __restrict__ r, int T, int k, int d,
@@ -213,25 +327,61 @@ __global__ void combine_kernel(const f16* __restrict__ yp, const int32_t* __rest
   const long long gi = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (gi >= (long long)T * nch) return;
   const int t = (int)(gi / nch), c = (int)(gi - (long long)t * nch);
-  uint4 u[8];
-  float wj[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (j < k) {
-      wj[j] = w[(size_t)t * k + j];
-      u[j] = reinterpret_cast<const uint4*>(yp + (size_t)inv[(size_t)t * k + j] * d)[c];
-    }
-  }
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if constexpr (PART) {
+    float v[8][8];
+    float wj[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (j < k) {
-      const uint32_t q[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        wj[j] = w[(size_t)t * k + j];
+        const float4* src =
+            reinterpret_cast<const float4*>(ypart + (size_t)inv[(size_t)t * k + j] * d) + 2 * c;
+        const float4 a = src[0], b = src[1];
+        v[j][0] = a.x; v[j][1] = a.y; v[j][2] = a.z; v[j][3] = a.w;
+        v[j][4] = b.x; v[j][5] = b.y; v[j][6] = b.z; v[j][7] = b.w;
+      }
+    }
+    for (int sp = 1; sp < y_splits; ++sp) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = unpack_f16x2(q[e]);
-        acc[2 * e] = fmaf(wj[j], f.x, acc[2 * e]);
-        acc[2 * e + 1] = fmaf(wj[j], f.y, acc[2 * e + 1]);
+      for (int j = 0; j < 8; ++j) {
+        if (j < k) {
+          const float4* src = reinterpret_cast<const float4*>(
+                                  ypart + sp * y_plane + (size_t)inv[(size_t)t * k + j] * d) +
+                              2 * c;
+          const float4 a = src[0], b = src[1];
+          v[j][0] += a.x; v[j][1] += a.y; v[j][2] += a.z; v[j][3] += a.w;
+          v[j][4] += b.x; v[j][5] += b.y; v[j][6] += b.z; v[j][7] += b.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(wj[j], v[j][e], acc[e]);
+      }
+    }
+  } else {
+    uint4 u[8];
+    float wj[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        wj[j] = w[(size_t)t * k + j];
+        u[j] = reinterpret_cast<const uint4*>(yp + (size_t)inv[(size_t)t * k + j] * d)[c];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        const uint32_t q[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = unpack_f16x2(q[e]);
+          acc[2 * e] = fmaf(wj[j], f.x, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(wj[j], f.y, acc[2 * e + 1]);
+        }
       }
     }
   }
@@ -277,13 +427,30 @@ __global__ void combine_kernel(const f16* __restrict__ yp, const int32_t* __rest
 
 inline int nblk(long long n, int t) { return (int)((n + t - 1) / t); }
 
+// Optional copies of the routing for inspection (logits rows are R apart).
+qwen_status copy_routing(const int32_t* idx, const float* wts, const float* logits,
+                         int32_t* idx_out, float* w_out, float* logits_out, int T, int E, int R,
+                         int k, cudaStream_t st) {
+  const size_t n = (size_t)T * k;
+  if (idx_out &&
+      cudaMemcpyAsync(idx_out, idx, n * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return QWEN_ERR_CUDA;
+  if (w_out && cudaMemcpyAsync(w_out, wts, n * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return QWEN_ERR_CUDA;
+  if (logits_out && cudaMemcpy2DAsync(logits_out, (size_t)E * 4, logits, (size_t)R * 4,
+                                      (size_t)E * 4, T, cudaMemcpyDeviceToDevice,
+                                      st) != cudaSuccess)
+    return QWEN_ERR_CUDA;
+  return QWEN_OK;
+}
+
 }  // namespace
 
 int moe_perm_blocks(size_t entries) { return (int)((entries + kPermBlock - 1) / kPermBlock); }
 
 qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* y, float* y32, int T,
                         int32_t* topk_idx_out, float* topk_w_out, float* logits_out, uint8_t* ws,
-                        const WorkspaceLayout& W, cudaStream_t st) {
+                        const WorkspaceLayout& W, cudaStream_t st, bool z_ready) {
   const qwen_layer_config& c = L->cfg;
   const int d = c.d, E = c.n_experts, k = c.top_k, mf = c.ffn, sf = c.shared_ffn;
   const int R = router_rows(c);  // E, or E + 8 with the shared gate at column E
@@ -295,6 +462,7 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
   float* wts = reinterpret_cast<float*>(ws + W.topk_w);
   int32_t* blk_counts = reinterpret_cast<int32_t*>(ws + W.blk_counts);
   int32_t* offsets = reinterpret_cast<int32_t*>(ws + W.offsets);
+  int32_t* act = reinterpret_cast<int32_t*>(ws + W.act);
   int32_t* perm = reinterpret_cast<int32_t*>(ws + W.perm);
   int32_t* inv = reinterpret_cast<int32_t*>(ws + W.inv);
   f16* zp = reinterpret_cast<f16*>(ws + W.zp);
@@ -305,22 +473,37 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
   float* gsc = sf ? reinterpret_cast<float*>(ws + W.gscale) : nullptr;
   float* part = reinterpret_cast<float*>(ws + W.part);
   // decode-sized batches use the swap-AB split-K GEMMs (one 128-row weight
-  // tile would otherwise run its whole K on a single SM)
+  // tile would otherwise run its whole K on a single SM), and up to 64 tokens
+  // the grouped swap-AB GEMM for the experts (1-8 routed rows per expert
+  // would waste most of a 128-row tile)
   const bool small = T <= 256 && W.part != 0;
+  const bool grouped_dec = small && T <= kMoeDecodeMaxRows;
   qwen_status s;
 
   // 1. RMSNorm_2 -> [Z_hi | Z_lo] (FP16 parts of the FP32 result)
-  if ((s = rmsnorm_launch(r, L->gamma_mlp, z, true, nullptr, r32, T, d, c.rms_eps, st, 0,
-                          2 * (size_t)d, z + d)))
+  if (!z_ready && (s = rmsnorm_launch(r, L->gamma_mlp, z, true, nullptr, r32, T, d, c.rms_eps,
+                                      st, 0, 2 * (size_t)d, z + d)))
     return s;
   // 2. router logits (and the shared gate's, column E): one tensor-core GEMM
   // over K = 2d against [W_r | W_r]
   if (small) {
-    const int S = decode_splits(R, 2 * d);
+    // the one-CTA routing sums the split partials: keep their number small
+    const int S = grouped_dec ? min(decode_splits(R, 2 * d), kRouteMaxSplits)
+                              : decode_splits(R, 2 * d);
     if ((s = gemm_decode_splitk(L->w_router, z, 2 * d, T, R, 2 * d, S, true, part, err, st,
                                 /*w_static=*/true)))
       return s;
-    if ((s = reduce_f32(part, S, T, R, logits, R, st))) return s;
+    if (grouped_dec) {
+      // 3 + 5 in one CTA: split sum, top-k, counting sort (it reads the
+      // router partials, so it runs before the shared expert reuses them)
+      launch_k(route_small_kernel, dim3(1), dim3(1024), 34 * E * sizeof(int32_t), st,
+               (const float*)part, S, T, R, (const float*)L->b_router, E, k, c.norm_topk_prob,
+               logits, idx, wts, gsc, offsets, act, perm, inv);
+      count_launches();
+      if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;
+    } else if ((s = reduce_f32(part, S, T, R, logits, R, st))) {
+      return s;
+    }
   } else {
     GemmEpilogue er{};
     er.mode = EPI_F32;
@@ -330,38 +513,13 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
     if ((s = gemm_tc(z, 2 * d, L->w_router, 2 * d, T, R, 2 * d, true, er, err, st))) return s;
   }
   // 3. top-k (+ router bias), gate weights, shared gate sigmoid
-  launch_k(topk_kernel, dim3(nblk(32LL * T, 256)), dim3(256), 0, st, logits, R,
-           (const float*)L->b_router, T, E, k, c.norm_topk_prob, idx, wts, gsc);
-  count_launches();
-  // 4. permutation by expert (stable in entry order) and gather of Z_hi rows
-  const int G = moe_perm_blocks(n);
-  launch_k(perm_count_kernel, dim3(G), dim3(kPermBlock), E * sizeof(int32_t), st,
-           (const int32_t*)idx, n, E, blk_counts);
-  launch_k(perm_scatter_kernel, dim3(G), dim3(kPermBlock), (2 + 32) * E * sizeof(int32_t), st,
-           (const int32_t*)idx, n, E, G, (const int32_t*)blk_counts, offsets, perm, inv);
-  launch_k(gather_rows_kernel, dim3(nblk(32LL * n, 256)), dim3(256), 0, st,
-           reinterpret_cast<const uint16_t*>(z), 2 * (size_t)d, (const int32_t*)perm, n, k, d,
-           reinterpret_cast<uint16_t*>(zp));
-  count_launches(3);
-  if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;
-  // 5. grouped expert GEMMs: gate/up with SiLU*up, then down
-  GemmEpilogue eg{};
-  eg.mode = EPI_SWIGLU;
-  eg.out = hp;
-  eg.out_f16 = 1;
-  eg.ldo = mf;
-  eg.group_offsets = offsets;
-  eg.n_groups = E;
-  if ((s = gemm_tc(zp, d, L->w_gu, d, n, 2 * mf, d, true, eg, err, st))) return s;
-  GemmEpilogue ed{};
-  ed.mode = EPI_STORE;
-  ed.out = yp;
-  ed.out_f16 = 1;
-  ed.ldo = d;
-  ed.group_offsets = offsets;
-  ed.n_groups = E;
-  if ((s = gemm_tc(hp, mf, L->w_down, mf, n, d, mf, true, ed, err, st))) return s;
-  // 5b. shared expert on Z_hi: H_s = SiLU(Z W_sg^T) * (Z W_su^T), Y_s = H_s W_sd^T (FP32)
+  if (!grouped_dec) {
+    launch_k(topk_kernel, dim3(nblk(32LL * T, 256)), dim3(256), 0, st, logits, R,
+             (const float*)L->b_router, T, E, k, c.norm_topk_prob, idx, wts, gsc);
+    count_launches();
+  }
+  // 4. shared expert on Z_hi: H_s = SiLU(Z W_sg^T) * (Z W_su^T), Y_s = H_s W_sd^T
+  // (FP32); before the routed experts, whose decode partials reuse `part`
   if (sf) {
     if (small) {
       if ((s = gemm_decode_splitk(L->w_sgu, z, 2 * d, T, 2 * sf, d, 1, true, nullptr, err, st,
@@ -388,24 +546,62 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
       if ((s = gemm_tc(hs, sf, L->w_sdown, sf, T, d, sf, true, sd, err, st))) return s;
     }
   }
-  // 6. weighted combine (+ gated shared expert) + residual
-  launch_k(combine_kernel, dim3(nblk((long long)T * (d / 8), 256)), dim3(256), 0, st, (const f16*)yp,
-           (const int32_t*)inv, (const float*)wts, (const float*)ys32, (const float*)gsc, r32, r,
-           T, k, d, y, y32);
+  // 5. permutation by expert (stable in entry order) and gather of Z_hi rows
+  if (!grouped_dec) {
+    const int G = moe_perm_blocks(n);
+    launch_k(perm_count_kernel, dim3(G), dim3(kPermBlock), E * sizeof(int32_t), st,
+             (const int32_t*)idx, n, E, blk_counts);
+    launch_k(perm_scatter_kernel, dim3(G), dim3(kPermBlock), (2 + 32) * E * sizeof(int32_t), st,
+             (const int32_t*)idx, n, E, G, (const int32_t*)blk_counts, offsets, act, perm, inv);
+    launch_k(gather_rows_kernel, dim3(nblk(32LL * n, 256)), dim3(256), 0, st,
+             reinterpret_cast<const uint16_t*>(z), 2 * (size_t)d, (const int32_t*)perm, n, k, d,
+             reinterpret_cast<uint16_t*>(zp));
+    count_launches(3);
+    if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;
+  }
+  // 6. grouped expert GEMMs: gate/up with SiLU*up, then down
+  if (grouped_dec) {
+    // swap-AB per touched expert: gate/up on the token rows of Z_hi (each
+    // expert keeps its routed tokens), down on the sorted H rows; the down
+    // partials are summed by the combine
+    const int groups = n < E ? n : E;
+    if ((s = gemm_decode_grouped_tokens(L->w_gu, E, z, 2 * d, T, 2 * mf, d, act, idx, inv, k,
+                                        groups, hp, err, st)))
+      return s;
+    const int S = decode_splits(d, mf, groups);
+    if ((s = gemm_decode_grouped(L->w_down, E, hp, n, T, d, mf, S, act, offsets, groups, part,
+                                 nullptr, err, st)))
+      return s;
+    launch_k(combine_kernel<true>, dim3(nblk((long long)T * (d / 8), 256)), dim3(256), 0, st,
+             (const f16*)nullptr, (const float*)part, S, (size_t)n * d, (const int32_t*)inv,
+             (const float*)wts, (const float*)ys32, (const float*)gsc, r32, r, T, k, d, y, y32);
+    count_launches();
+    if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;
+    return copy_routing(idx, wts, logits, topk_idx_out, topk_w_out, logits_out, T, E, R, k, st);
+  }
+  GemmEpilogue eg{};
+  eg.mode = EPI_SWIGLU;
+  eg.out = hp;
+  eg.out_f16 = 1;
+  eg.ldo = mf;
+  eg.group_offsets = offsets;
+  eg.n_groups = E;
+  if ((s = gemm_tc(zp, d, L->w_gu, d, n, 2 * mf, d, true, eg, err, st))) return s;
+  GemmEpilogue ed{};
+  ed.mode = EPI_STORE;
+  ed.out = yp;
+  ed.out_f16 = 1;
+  ed.ldo = d;
+  ed.group_offsets = offsets;
+  ed.n_groups = E;
+  if ((s = gemm_tc(hp, mf, L->w_down, mf, n, d, mf, true, ed, err, st))) return s;
+  // 7. weighted combine (+ gated shared expert) + residual
+  launch_k(combine_kernel<false>, dim3(nblk((long long)T * (d / 8), 256)), dim3(256), 0, st,
+           (const f16*)yp, (const float*)nullptr, 1, (size_t)0, (const int32_t*)inv,
+           (const float*)wts, (const float*)ys32, (const float*)gsc, r32, r, T, k, d, y, y32);
   count_launches();
   if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;
-  // optional copies of the routing for inspection
-  if (topk_idx_out &&
-      cudaMemcpyAsync(topk_idx_out, idx, (size_t)n * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-    return QWEN_ERR_CUDA;
-  if (topk_w_out &&
-      cudaMemcpyAsync(topk_w_out, wts, (size_t)n * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-    return QWEN_ERR_CUDA;
-  if (logits_out && cudaMemcpy2DAsync(logits_out, (size_t)E * 4, logits, (size_t)R * 4,
-                                      (size_t)E * 4, T, cudaMemcpyDeviceToDevice,
-                                      st) != cudaSuccess)
-    return QWEN_ERR_CUDA;
-  return QWEN_OK;
+  return copy_routing(idx, wts, logits, topk_idx_out, topk_w_out, logits_out, T, E, R, k, st);
 }
 
 }  // namespace qwen
