@@ -323,6 +323,30 @@ __global__ void __launch_bounds__(kDThreads, 1)
 // ------------------------------------------------------------------ reductions
 // Partials are part[s][b][n]; the splits are summed in order s = 0, 1, ...
 
+// v[e] += src[s * plane + e * estride] for s = 0 .. splits-1 in order, for the
+// first nvalid of the PER values.  The loads of CH splits are issued together
+// before their adds: these reductions are bound by load latency, not bytes.
+template <int PER, int CH>
+__device__ __forceinline__ void add_splits(const float* __restrict__ src, size_t plane,
+                                           int estride, int splits, int nvalid,
+                                           float (&v)[PER]) {
+  for (int s0 = 0; s0 < splits; s0 += CH) {
+    float t[CH][PER];
+#pragma unroll
+    for (int c = 0; c < CH; ++c)
+#pragma unroll
+      for (int e = 0; e < PER; ++e)
+        t[c][e] = (s0 + c < splits && e < nvalid)
+                      ? src[(size_t)(s0 + c) * plane + (size_t)e * estride]
+                      : 0.f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c)
+#pragma unroll
+      for (int e = 0; e < PER; ++e)
+        if (s0 + c < splits) v[e] += t[c][e];
+  }
+}
+
 __global__ void reduce_resid_kernel(const float* __restrict__ part, int splits, int B, int N,
                                     const bf16* __restrict__ resid,
                                     const float* __restrict__ resid32, bf16* __restrict__ out,
@@ -332,12 +356,11 @@ __global__ void reduce_resid_kernel(const float* __restrict__ part, int splits, 
   const int i = blockIdx.x * blockDim.x + threadIdx.x;  // over B * N, n fastest
   if (i >= N * B) return;
   const size_t plane = (size_t)B * N;
-  float acc = 0.f;
-#pragma unroll 8
-  for (int s = 0; s < splits; ++s) acc += part[s * plane + i];
-  acc += resid32 ? resid32[i] : __bfloat162float(resid[i]);
-  if (out) out[i] = __float2bfloat16_rn(acc);
-  if (out32) out32[i] = acc;
+  float acc[1] = {0.f};
+  add_splits<1, 8>(part + i, plane, 0, splits, 1, acc);
+  const float r = acc[0] + (resid32 ? resid32[i] : __bfloat162float(resid[i]));
+  if (out) out[i] = __float2bfloat16_rn(r);
+  if (out32) out32[i] = r;
 }
 
 // h[b][j] = SiLU(gate_j) * up_j with gate row (j/64)*128 + j%64 and up row +64.
@@ -352,12 +375,9 @@ __global__ void reduce_swiglu_kernel(const float* __restrict__ part, int splits,
   const int n_gate = (j >> 6) * 128 + (j & 63);
   const size_t plane = (size_t)B * N;
   const float* src = part + (size_t)b * N + n_gate;
-  float g = 0.f, u = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    g += src[s * plane];
-    u += src[s * plane + 64];
-  }
-  h[i] = __float2half_rn(silu_f(g) * u);
+  float gu[2] = {0.f, 0.f};  // gate, up
+  add_splits<2, 8>(src, plane, 64, splits, 2, gu);
+  h[i] = __float2half_rn(silu_f(gu[0]) * gu[1]);
 }
 
 // One warp per (b, head): lane e holds channels e, e+32, e+64, e+96 (dh = 128)
@@ -380,10 +400,7 @@ __global__ void reduce_qkv_kernel(const float* __restrict__ part, int splits, in
   float v[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) v[e] = 0.f;
-  for (int s = 0; s < splits; ++s) {
-#pragma unroll
-    for (int e = 0; e < PER; ++e) v[e] += src[s * plane + 32 * e];
-  }
+  add_splits<PER, 32 / PER>(src, plane, 32, splits, PER, v);
   const int kind = head < p.Hq ? 0 : (head < p.Hq + p.Hkv ? 1 : 2);
   if (p.bias) {
 #pragma unroll
@@ -451,14 +468,9 @@ __global__ void __launch_bounds__(1024) reduce_resid_norm_kernel(
     v[j] = 0.f;
     if (n < N) v[j] = resid32 ? resid32[row + n] : __bfloat162float(resid[row + n]);
   }
-#pragma unroll 4
-  for (int s = 0; s < splits; ++s) {
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int n = threadIdx.x + 1024 * j;
-      if (n < N) v[j] += part[s * plane + row + n];
-    }
-  }
+  // columns threadIdx.x + 1024 j, j < nvalid, are inside the row
+  const int nvalid = (int)threadIdx.x < N ? min(PER, (N - 1 - (int)threadIdx.x) / 1024 + 1) : 0;
+  add_splits<PER, 32 / PER>(part + row + threadIdx.x, plane, 1024, splits, nvalid, v);
   float ss = 0.f;
 #pragma unroll
   for (int j = 0; j < PER; ++j) {
@@ -496,9 +508,9 @@ __global__ void reduce_f32_kernel(const float* __restrict__ part, int splits, in
   if (i >= N * B) return;
   const int b = i / N, n = i - b * N;
   const size_t plane = (size_t)B * N;
-  float acc = 0.f;
-  for (int s = 0; s < splits; ++s) acc += part[s * plane + i];
-  out[(size_t)b * ldo + n] = acc;
+  float acc[1] = {0.f};
+  add_splits<1, 8>(part + i, plane, 0, splits, 1, acc);
+  out[(size_t)b * ldo + n] = acc[0];
 }
 
 // ------------------------------------------------------------------ host side
