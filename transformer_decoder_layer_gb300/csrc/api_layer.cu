@@ -436,7 +436,7 @@ size_t qwen_head_workspace_bytes(int32_t B, int32_t d, int32_t V) {
   if (B <= 0 || d <= 0 || V <= 0) return 0;
   const size_t xn = align256((size_t)B * d * 2);
   if (B > 256) return xn;
-  return xn + align256((size_t)decode_splits(V, d) * V * (size_t)B * 4);
+  return xn + align256((size_t)decode_splits(V, d, B) * V * (size_t)B * 4);
 }
 
 qwen_status qwen_head_last_token(const void* y, int32_t B, int32_t T, int32_t d,
@@ -464,7 +464,7 @@ qwen_status qwen_head_last_token(const void* y, int32_t B, int32_t T, int32_t d,
   }
   float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                          align256((size_t)B * d * 2));
-  const int S = decode_splits(V, d);
+  const int S = decode_splits(V, d, B);
   if ((s = gemm_decode_splitk(w_lm, xn, d, B, V, d, S, /*op_f16=*/false, part, err, st)))
     return s;
   return reduce_f32(part, S, B, V, logits, V, st);
@@ -501,7 +501,7 @@ static inline void mark(const qwen_layer_s* L, int stage, int end, cudaStream_t 
 // reduction that follows applies the step's epilogue.
 static qwen_status decode_proj(const f16* Wt, const f16* X, int B, int N, int K, float* part,
                                int* err, cudaStream_t st, int& splits) {
-  splits = decode_splits(N, K);
+  splits = decode_splits(N, K, B);
   return gemm_decode_splitk(Wt, X, K, B, N, K, splits, /*op_f16=*/true, part, err, st,
                             /*w_static=*/true);
 }

@@ -549,19 +549,34 @@ static int pad_batch(int B) {
   return 256;
 }
 
-int decode_splits(int N, int K, int groups) {
+// K splits for an [N, K] weight (times `groups` in grouped mode) and B tokens:
+// the split count with the smallest modelled time, where a launch takes the
+// longer of streaming all weight bytes from HBM and the busiest SM pulling its
+// units through TMA, plus the split partials (written, then read by the
+// reduction) and a fixed cost per unit on the busiest SM.  Few splits leave
+// SMs idle; many make small units whose partials and hand-offs cost more than
+// the extra SMs gain.  Rates: measured GB300 copy bandwidth and per-SM TMA
+// ingress (about 6.6 TB/s and 100-120 GB/s; 70 GB/s is used to keep a margin).
+int decode_splits(int N, int K, int B, int groups) {
   const int sms = device_sm_count();
   const int tiles = (N + kDBM - 1) / kDBM * groups;
   const int kblk = (K + kDBK - 1) / kDBK;
+  const int bp = pad_batch(B < 1 ? 1 : (B > 256 ? 256 : B));
+  constexpr double kHbm = 6.6e12, kSmIngress = 7.0e10, kUnitCost = 2.0e-7;
+  const double w_time = (double)tiles * kblk * kDBM * kDBK * 2 / kHbm;
+  const double kblk_bytes = (double)(kDBM + bp) * kDBK * 2;  // weight + X tile
+  const double part_bytes = (double)kDBM * B * 4;            // one unit's partials
   int best = 1;
-  double best_score = -1.0;
-  for (int s = 1; s <= 32 && s <= kblk / 2; ++s) {
+  double best_t = 1e30;
+  for (int s = 1; s <= 32 && (s == 1 || s <= kblk / 2); ++s) {
     const int units = tiles * s;
-    const int waves = (units + sms - 1) / sms;
-    const double eff = (double)units / ((double)waves * sms);
-    const double score = eff - 0.004 * s;  // small preference for fewer partials
-    if (score > best_score + 1e-9) {
-      best_score = score;
+    const int per_sm = (units + sms - 1) / sms;
+    const int kb = (kblk + s - 1) / s;
+    const double sm_time = (double)per_sm * kb * kblk_bytes / kSmIngress;
+    const double t = (w_time > sm_time ? w_time : sm_time) +
+                     (s > 1 ? 2.0 * units * part_bytes / kHbm : 0.0) + per_sm * kUnitCost;
+    if (t < best_t * (1.0 - 1e-9)) {
+      best_t = t;
       best = s;
     }
   }
@@ -573,7 +588,7 @@ size_t decode_part_bytes(const qwen_layer_config& c, int B) {
                nqkv = nq + 2 * (size_t)c.n_kv_heads * c.head_dim, f = c.ffn;
   size_t m = 0;
   auto upd = [&](size_t N, size_t K) {
-    const size_t s = decode_splits((int)N, (int)K);
+    const size_t s = decode_splits((int)N, (int)K, B);
     const size_t need = s * N * (size_t)B * 4;
     if (need > m) m = need;
   };
@@ -588,7 +603,7 @@ size_t decode_part_bytes(const qwen_layer_config& c, int B) {
     if (B <= kMoeDecodeMaxRows) {  // grouped expert down projection, B*k rows
       const int rows = B * c.top_k;
       const int groups = rows < c.n_experts ? rows : c.n_experts;
-      const size_t need = (size_t)decode_splits(d, f, groups) * rows * d * 4;
+      const size_t need = (size_t)decode_splits(d, f, B, groups) * rows * d * 4;
       if (need > m) m = need;
     }
   }

@@ -89,8 +89,8 @@ qwen_status moe_forward(qwen_layer_s* L, const __nv_bfloat16* r, const float* r3
 // ---- decode building blocks (decode_gemm.cu, attention_decode.cu)
 
 // Number of K splits the swap-AB decode GEMM uses for an [N, K] weight (or for
-// `groups` such weights in grouped mode).
-int decode_splits(int N, int K, int groups = 1);
+// `groups` such weights in grouped mode) and B tokens.
+int decode_splits(int N, int K, int B, int groups = 1);
 // MoE blocks on at most this many tokens run the experts through the grouped
 // swap-AB decode GEMM (the tokens sit on the MMA's N side, padded to 16..64).
 constexpr int kMoeDecodeMaxRows = 64;

@@ -488,8 +488,8 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
   // over K = 2d against [W_r | W_r]
   if (small) {
     // the one-CTA routing sums the split partials: keep their number small
-    const int S = grouped_dec ? min(decode_splits(R, 2 * d), kRouteMaxSplits)
-                              : decode_splits(R, 2 * d);
+    const int S = grouped_dec ? min(decode_splits(R, 2 * d, T), kRouteMaxSplits)
+                              : decode_splits(R, 2 * d, T);
     if ((s = gemm_decode_splitk(L->w_router, z, 2 * d, T, R, 2 * d, S, true, part, err, st,
                                 /*w_static=*/true)))
       return s;
@@ -525,7 +525,7 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
       if ((s = gemm_decode_splitk(L->w_sgu, z, 2 * d, T, 2 * sf, d, 1, true, nullptr, err, st,
                                   /*w_static=*/true, hs)))
         return s;
-      const int S = decode_splits(d, sf);
+      const int S = decode_splits(d, sf, T);
       if ((s = gemm_decode_splitk(L->w_sdown, hs, sf, T, d, sf, S, true, part, err, st,
                                   /*w_static=*/true)))
         return s;
@@ -568,7 +568,7 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
     if ((s = gemm_decode_grouped_tokens(L->w_gu, E, z, 2 * d, T, 2 * mf, d, act, idx, inv, k,
                                         groups, hp, err, st)))
       return s;
-    const int S = decode_splits(d, mf, groups);
+    const int S = decode_splits(d, mf, T, groups);
     if ((s = gemm_decode_grouped(L->w_down, E, hp, n, T, d, mf, S, act, offsets, groups, part,
                                  nullptr, err, st)))
       return s;
