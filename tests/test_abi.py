@@ -67,8 +67,9 @@ def test_config_struct_layout_matches_c(built_lib):
 
 def test_shared_expert_config_reaches_the_library(built_lib):
     """Host-only: shared_ffn (the last config field) changes the packed size by
-    exactly the shared expert's FP16 weights plus 8 router rows, the shared gate
-    and its padding, so the field is read where the binding writes it."""
+    exactly the shared expert's FP16 weights (its gate row joins the router,
+    whose rows are padded to 128 either way), so the field is read where the
+    binding writes it."""
     import transformer_decoder_layer_gb300 as q
     L = q.lib()
     d, sf = 512, 512
@@ -82,8 +83,7 @@ def test_shared_expert_config_reaches_the_library(built_lib):
     base = packed()
     assert base > 0
     assert packed(norm_topk_prob=0) == base
-    router_rows = 8 * 2 * d * 2
-    assert packed(shared_ffn=sf, norm_topk_prob=0) - base == router_rows + 3 * sf * d * 2
+    assert packed(shared_ffn=sf, norm_topk_prob=0) - base == 3 * sf * d * 2
     assert packed(shared_ffn=100) == 0            # not a multiple of 64
     assert packed(norm_topk_prob=2) == 0
     dense = q.LayerConfig(dict(d=d, n_q_heads=8, n_kv_heads=2, head_dim=64, ffn=256,

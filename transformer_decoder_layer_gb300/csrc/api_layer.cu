@@ -15,6 +15,7 @@
 namespace qwen {
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+static size_t round128(size_t x) { return (x + 127) & ~static_cast<size_t>(127); }
 
 bool config_valid(const qwen_layer_config& c) {
   if (c.d <= 0 || c.d % 64 || c.d > 8192) return false;
@@ -55,22 +56,24 @@ PackedLayout packed_layout(const qwen_layer_config& c) {
   L.gamma_mlp = take(d * 2);
   L.gamma_q = take(dh * 2);
   L.gamma_k = take(dh * 2);
-  L.w_qkv = take(nqkv * d * 2);
+  // FP16 weights in the blocked layout: every matrix (every expert's) rows
+  // padded to a multiple of 128
   L.b_qkv = take(nqkv * 4);
-  L.w_o = take(d * nq * 2);
+  L.w_qkv = take(round128(nqkv) * d * 2);
+  L.w_o = take(round128(d) * nq * 2);
   if (c.n_experts == 0) {
     L.w_gu = take(2 * f * d * 2);
-    L.w_down = take(d * f * 2);
+    L.w_down = take(round128(d) * f * 2);
   } else {
     const size_t e = c.n_experts;
-    L.w_router = take((size_t)router_rows(c) * 2 * d * 2);  // FP16 rows, each twice
     L.b_router = take(e * 4);
+    L.w_router = take(round128(router_rows(c)) * 2 * d * 2);  // rows [W_r | W_r]
     L.w_gu = take(e * 2 * f * d * 2);
-    L.w_down = take(e * d * f * 2);
+    L.w_down = take(e * round128(d) * f * 2);
     if (c.shared_ffn) {
       const size_t sf = c.shared_ffn;
       L.w_sgu = take(2 * sf * d * 2);
-      L.w_sdown = take(d * sf * 2);
+      L.w_sdown = take(round128(d) * sf * 2);
     }
   }
   L.total = o;
@@ -143,19 +146,33 @@ static bool copy_d2d(void* dst, const void* src, size_t bytes, cudaStream_t st) 
 // Copy BF16 weight rows into the packed FP16 buffer.  BF16 -> FP16 is exact
 // for magnitudes in [2^-14, 65504] (FP16 keeps more mantissa bits); smaller
 // magnitudes land on the FP16 subnormal grid (absolute error <= 2^-25) and
-// larger ones saturate.  Row placement: mode 0 keeps the row order; modes 1
-// and 2 interleave gate (1) and up (2) rows in 64-row blocks, block 2i = gate
-// block i and block 2i+1 = up block i, so one GEMM tile holds both halves of
-// every SwiGLU output feature.
-__global__ void pack_rows_f16_kernel(f16* __restrict__ dst, const bf16* __restrict__ src,
-                                     size_t rows, int d, int mode, size_t ldd, size_t coff) {
-  const int cpr = d / 8;  // 16-byte chunks per row
+// larger ones saturate.
+//
+// Destination: the blocked layout, a [rows][dst_cols] matrix stored as 128 x 64
+// tiles of 16 KB, tile (row / 128, col / 64) at ((row/128) * dst_cols/64 +
+// col/64) * 16 KB, row-major inside the tile.  Weight tiles then stream as
+// whole contiguous 16 KB blocks (measured ~6% faster HBM streaming than 128
+// rows of 128 bytes each from a row-major matrix).
+// Row placement: source row r belongs to group r / gsz (an expert); inside a
+// group, mode 0 keeps the row order and modes 1 and 2 interleave gate (1) and
+// up (2) rows in 64-row blocks, block 2i = gate block i and block 2i+1 = up
+// block i, so one GEMM tile holds both halves of every SwiGLU output feature;
+// group g starts at destination row roff + g * gpad.  Columns go to coff + c.
+__global__ void pack_blocked_f16_kernel(f16* __restrict__ dst, const bf16* __restrict__ src,
+                                        size_t rows, int cols, int mode, size_t gsz, size_t gpad,
+                                        size_t roff, int dst_cols, int coff) {
+  const int cpr = cols / 8;  // 16-byte chunks per source row
   const size_t nch = rows * (size_t)cpr;
+  const size_t kt = (size_t)dst_cols / 64;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nch;
        i += (size_t)gridDim.x * blockDim.x) {
     const size_t r = i / cpr;
     const int c = (int)(i - r * cpr);
-    const size_t dr = mode == 0 ? r : (r / 64) * 128 + (r % 64) + (mode == 2 ? 64 : 0);
+    const size_t g = r / gsz, rin = r - g * gsz;
+    const size_t din = mode == 0 ? rin : (rin / 64) * 128 + (rin % 64) + (mode == 2 ? 64 : 0);
+    const size_t dr = roff + g * gpad + din;
+    const size_t dc = (size_t)coff + 8 * (size_t)c;
+    const size_t off = (((dr / 128) * kt + dc / 64) * 128 + dr % 128) * 64 + dc % 64;
     const uint4 u = reinterpret_cast<const uint4*>(src)[i];
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
     uint32_t o[4];
@@ -164,19 +181,21 @@ __global__ void pack_rows_f16_kernel(f16* __restrict__ dst, const bf16* __restri
       const float2 f = unpack_bf16x2(w[j]);
       o[j] = pack_f16x2(fminf(fmaxf(f.x, -65504.f), 65504.f), fminf(fmaxf(f.y, -65504.f), 65504.f));
     }
-    reinterpret_cast<uint4*>(dst + dr * ldd + coff)[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(dst + off) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
-// Rows of BF16 [rows][d] -> FP16, written `ldd` elements apart (0 = d) from
-// column `coff` (mode 1/2: gate/up rows interleaved in 64-row blocks).
-static bool pack_rows(f16* dst, const void* src, size_t rows, size_t d, int mode,
-                      cudaStream_t st, size_t ldd = 0, size_t coff = 0) {
+// BF16 [rows][cols] -> blocked FP16 (see pack_blocked_f16_kernel); gsz = 0:
+// one group; dst_cols = 0: cols.
+static bool pack_blocked(f16* dst, const void* src, size_t rows, size_t cols, int mode,
+                         cudaStream_t st, size_t gsz = 0, size_t gpad = 0, size_t roff = 0,
+                         size_t dst_cols = 0, size_t coff = 0) {
   if (rows == 0) return true;
-  const size_t nch = rows * (d / 8);
+  const size_t nch = rows * (cols / 8);
   const int blocks = (int)((nch + 255) / 256 < 65535 ? (nch + 255) / 256 : 65535);
-  pack_rows_f16_kernel<<<blocks, 256, 0, st>>>(dst, static_cast<const bf16*>(src), rows, (int)d,
-                                               mode, ldd ? ldd : d, coff);
+  pack_blocked_f16_kernel<<<blocks, 256, 0, st>>>(dst, static_cast<const bf16*>(src), rows,
+                                                  (int)cols, mode, gsz ? gsz : rows, gpad, roff,
+                                                  (int)(dst_cols ? dst_cols : cols), (int)coff);
   count_launches();
   return cudaGetLastError() == cudaSuccess;
 }
@@ -255,9 +274,11 @@ qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_wei
     ok = ok && copy_d2d(h->gamma_q, w->gamma_q, dh * 2, st);
     ok = ok && copy_d2d(h->gamma_k, w->gamma_k, dh * 2, st);
   }
-  ok = ok && pack_rows(h->w_qkv, w->w_q, nq, d, 0, st);
-  ok = ok && pack_rows(h->w_qkv + nq * d, w->w_k, nkv, d, 0, st);
-  ok = ok && pack_rows(h->w_qkv + (nq + nkv) * d, w->w_v, nkv, d, 0, st);
+  // zero the weight area first: the rows that pad matrices to 128 stay zero
+  ok = ok && cudaMemsetAsync(P + L.w_qkv, 0, L.total - L.w_qkv, st) == cudaSuccess;
+  ok = ok && pack_blocked(h->w_qkv, w->w_q, nq, d, 0, st);
+  ok = ok && pack_blocked(h->w_qkv, w->w_k, nkv, d, 0, st, 0, 0, nq);
+  ok = ok && pack_blocked(h->w_qkv, w->w_v, nkv, d, 0, st, 0, 0, nq + nkv);
   if (c.qkv_bias && ok) {
     bf16_to_f32_kernel<<<(int)((nq + 255) / 256), 256, 0, st>>>(
         static_cast<const bf16*>(w->b_q), h->b_qkv, (int)nq);
@@ -268,28 +289,24 @@ qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_wei
     count_launches(3);
     ok = cudaGetLastError() == cudaSuccess;
   }
-  ok = ok && pack_rows(h->w_o, w->w_o, d, nq, 0, st);
+  ok = ok && pack_blocked(h->w_o, w->w_o, d, nq, 0, st);
   const size_t n_exp = moe ? (size_t)c.n_experts : 1;
-  ok = ok && pack_rows(h->w_gu, w->w_gate, n_exp * f, d, 1, st);
-  ok = ok && pack_rows(h->w_gu, w->w_up, n_exp * f, d, 2, st);
-  ok = ok && pack_rows(h->w_down, w->w_down, n_exp * d, f, 0, st);
+  ok = ok && pack_blocked(h->w_gu, w->w_gate, n_exp * f, d, 1, st, f, 2 * f);
+  ok = ok && pack_blocked(h->w_gu, w->w_up, n_exp * f, d, 2, st, f, 2 * f);
+  ok = ok && pack_blocked(h->w_down, w->w_down, n_exp * d, f, 0, st, d, round128(d));
   if (moe) {
-    const size_t rr = router_rows(c);
-    if (rr > n_exp)  // the shared gate row and the zero padding after it
-      ok = ok && cudaMemsetAsync(h->w_router + n_exp * 2 * d, 0, (rr - n_exp) * 2 * d * 2, st) ==
-                     cudaSuccess;
-    ok = ok && pack_rows(h->w_router, w->w_router, n_exp, d, 0, st, 2 * d, 0);
-    ok = ok && pack_rows(h->w_router, w->w_router, n_exp, d, 0, st, 2 * d, d);
+    // rows [W_r | W_r]; with a shared expert W_sg is row E (rows after it zero)
+    ok = ok && pack_blocked(h->w_router, w->w_router, n_exp, d, 0, st, 0, 0, 0, 2 * d, 0);
+    ok = ok && pack_blocked(h->w_router, w->w_router, n_exp, d, 0, st, 0, 0, 0, 2 * d, d);
     if (c.router_bias) ok = ok && copy_d2d(h->b_router, w->b_router, n_exp * 4, st);
   }
   if (c.shared_ffn) {
     const size_t sf = c.shared_ffn;
-    f16* gate_row = h->w_router + n_exp * 2 * d;  // W_sg as router row E
-    ok = ok && pack_rows(gate_row, w->w_shared_expert_gate, 1, d, 0, st, 2 * d, 0);
-    ok = ok && pack_rows(gate_row, w->w_shared_expert_gate, 1, d, 0, st, 2 * d, d);
-    ok = ok && pack_rows(h->w_sgu, w->w_shared_gate, sf, d, 1, st);
-    ok = ok && pack_rows(h->w_sgu, w->w_shared_up, sf, d, 2, st);
-    ok = ok && pack_rows(h->w_sdown, w->w_shared_down, d, sf, 0, st);
+    ok = ok && pack_blocked(h->w_router, w->w_shared_expert_gate, 1, d, 0, st, 0, 0, n_exp, 2 * d, 0);
+    ok = ok && pack_blocked(h->w_router, w->w_shared_expert_gate, 1, d, 0, st, 0, 0, n_exp, 2 * d, d);
+    ok = ok && pack_blocked(h->w_sgu, w->w_shared_gate, sf, d, 1, st, sf, 2 * sf);
+    ok = ok && pack_blocked(h->w_sgu, w->w_shared_up, sf, d, 2, st, sf, 2 * sf);
+    ok = ok && pack_blocked(h->w_sdown, w->w_shared_down, d, sf, 0, st, d, round128(d));
   }
   // RoPE table: (cos, sin) of p * theta^(-2i/dh), angles and trig in FP64.
   // Qwen3 layer page, §6 (frequency equation).
@@ -503,7 +520,7 @@ static qwen_status decode_proj(const f16* Wt, const f16* X, int B, int N, int K,
                                int* err, cudaStream_t st, int& splits) {
   splits = decode_splits(N, K, B);
   return gemm_decode_splitk(Wt, X, K, B, N, K, splits, /*op_f16=*/true, part, err, st,
-                            /*w_static=*/true);
+                            /*w_packed=*/true);
 }
 
 qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16* y, float* y32,
@@ -538,6 +555,7 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
     GemmEpilogue e{};
     e.mode = EPI_QKV;
     e.b_static = 1;
+    e.b_blocked = 1;
     e.qkv = qp;
     QWEN_STAGE_RUN(QWEN_STAGE_QKV, gemm_tc(xh, d, L->w_qkv, d, B, nqkv, d, true, e, err, st));
   }
@@ -557,7 +575,7 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
     // gate/up in one K split with SiLU*up in the epilogue -> H, then down
     QWEN_STAGE_RUN(QWEN_STAGE_GATE_UP,
                    gemm_decode_splitk(L->w_gu, z, d, B, 2 * f, d, 1, /*op_f16=*/true, nullptr,
-                                      err, st, /*w_static=*/true, hbuf));
+                                      err, st, /*w_packed=*/true, hbuf));
     QWEN_STAGE_RUN(QWEN_STAGE_DOWN, decode_proj(L->w_down, hbuf, B, d, f, part, err, st, S));
     QWEN_STAGE_RUN(QWEN_STAGE_DOWN_FINISH,
                    reduce_resid(part, S, B, d, nullptr, r32, y, y32, st));
@@ -573,6 +591,7 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
     GemmEpilogue e{};
     e.mode = EPI_RESID;
     e.b_static = 1;
+    e.b_blocked = 1;
     e.resid = x;
     e.resid32 = x32;
     e.ldr = d;
@@ -599,6 +618,7 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
   GemmEpilogue eg{};
   eg.mode = EPI_SWIGLU;
   eg.b_static = 1;
+  eg.b_blocked = 1;
   eg.out = hbuf;
   eg.out_f16 = 1;
   eg.ldo = f;
@@ -606,6 +626,7 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
   GemmEpilogue ed{};
   ed.mode = EPI_RESID;
   ed.b_static = 1;
+  ed.b_blocked = 1;
   ed.out = y;
   ed.ldo = d;
   ed.resid32 = r32;
@@ -639,6 +660,7 @@ qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, const float* x32, bf16
   GemmEpilogue e{};
   e.mode = EPI_QKV;
   e.b_static = 1;
+  e.b_blocked = 1;
   e.qkv = make_qkv_params(L, positions, slot0, q, true, kc, vc, k16, v16, T);
   QWEN_STAGE_RUN(QWEN_STAGE_QKV, gemm_tc(xh, d, L->w_qkv, d, M, nqkv, d, true, e, err, st));
   // causal GQA attention over the cache
@@ -649,6 +671,7 @@ qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, const float* x32, bf16
   GemmEpilogue eo{};
   eo.mode = EPI_RESID;
   eo.b_static = 1;
+  eo.b_blocked = 1;
   eo.resid = x;
   eo.resid32 = x32;
   eo.ldr = d;
@@ -666,6 +689,7 @@ qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, const float* x32, bf16
   GemmEpilogue eg{};
   eg.mode = EPI_SWIGLU;
   eg.b_static = 1;
+  eg.b_blocked = 1;
   eg.out = hbuf;
   eg.out_f16 = 1;
   eg.ldo = f;
@@ -673,6 +697,7 @@ qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, const float* x32, bf16
   GemmEpilogue ed{};
   ed.mode = EPI_RESID;
   ed.b_static = 1;
+  ed.b_blocked = 1;
   ed.out = y;
   ed.ldo = d;
   ed.resid32 = r32;

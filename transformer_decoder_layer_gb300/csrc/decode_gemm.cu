@@ -64,7 +64,7 @@ struct DecCfg {
 template <int BP, int EPI>
 __global__ void __launch_bounds__(kDThreads, 1)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                       int B, int N, int K, int splits, uint32_t idesc, int w_static,
+                       int B, int N, int K, int splits, uint32_t idesc, int w_packed,
                        float* __restrict__ part, f16* __restrict__ hout,
                        const int32_t* gact, const int32_t* goff, const int32_t* tidx,
                        const int32_t* tinv, int tk, int* err) {
@@ -113,8 +113,9 @@ __global__ void __launch_bounds__(kDThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // unit u -> weight row of its tile (wrow), n0 within the expert's N, the
-  // k-block range of split s, and the X rows [row0, row0 + m) it serves
+  // unit u -> row tile of its weight tile (wrow: the blocked layout's tile
+  // index for packed weights, else the first weight row), n0 within the
+  // expert's N, the k-block range of split s, and the X rows [row0, row0 + m)
   auto unit_range = [&](int u, int& wrow, int& n0, int& kb0, int& kb1, int& s, int& row0,
                         int& m, int& e) {
     const int a = u / per_group;
@@ -126,15 +127,24 @@ __global__ void __launch_bounds__(kDThreads, 1)
       e = gact[1 + a];
       row0 = tokens ? 0 : goff[e];
       m = tokens ? B : goff[e + 1] - row0;
-      wrow = e * N + n0;
+      wrow = w_packed ? e * n_tiles + tile : e * N + n0;
     } else {
       e = 0;
       row0 = 0;
       m = B;
-      wrow = n0;
+      wrow = w_packed ? tile : n0;
     }
     kb0 = (int)(((long long)s * n_kblk) / splits);
     kb1 = (int)(((long long)(s + 1) * n_kblk) / splits);
+  };
+
+  // weight tile of k-block kb: packed weights are in the blocked layout (4-D
+  // map, one 128 x 64 tile), others row-major (2-D map from row wrow)
+  auto load_w = [&](uint8_t* dst, uint64_t* bar, int kb, int wrow, uint64_t pol) {
+    if (w_packed)
+      tma_load_4d_hint_w(dst, &tmW, bar, 0, 0, kb, wrow, pol);
+    else
+      tma_load_2d_hint_w(dst, &tmW, bar, kb * kDBK, wrow, pol);
   };
 
   // warps 0 and 1 run converged and issue from one elected lane
@@ -148,13 +158,13 @@ __global__ void __launch_bounds__(kDThreads, 1)
       // weights are never written by the kernels before this one: stream the
       // first stages of weight tiles while the previous kernel finishes
       int pre = 0;
-      if (w_static && !grouped && blockIdx.x < units) {
+      if (w_packed && !grouped && blockIdx.x < units) {
         int wrow, n0, kb0, kb1, s, row0, m, e;
         unit_range(blockIdx.x, wrow, n0, kb0, kb1, s, row0, m, e);
         pre = min(C::STAGES, kb1 - kb0);
         for (int i = 0; i < pre; ++i) {
           mbar_arrive_expect_tx_w(&full[i], C::STAGE_BYTES);
-          tma_load_2d_hint_w(sA + i * C::A_BYTES, &tmW, &full[i], (kb0 + i) * kDBK, wrow, wpol);
+          load_w(sA + i * C::A_BYTES, &full[i], kb0 + i, wrow, wpol);
         }
       }
       pdl_wait();
@@ -171,7 +181,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
           } else {
             if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, err)) goto prod_done;
             mbar_arrive_expect_tx_w(&full[stage], C::STAGE_BYTES);
-            tma_load_2d_hint_w(sA + stage * C::A_BYTES, &tmW, &full[stage], kb * kDBK, wrow, wpol);
+            load_w(sA + stage * C::A_BYTES, &full[stage], kb, wrow, wpol);
             tma_load_2d_w(sB + stage * C::B_BYTES, &tmX, &full[stage], kb * kDBK, row0);
           }
           if (++stage == C::STAGES) {
@@ -528,6 +538,22 @@ static PFN_cuTensorMapEncodeTiled_v12000 enc_fn() {
   return fn;
 }
 
+// Packed weights: 128 x 64 tiles of 16 KB (see the prefill GEMM), one tile a box.
+static bool tmap_blocked(CUtensorMap* m, const void* base, uint64_t row_tiles, uint64_t K,
+                         bool f16) {
+  auto enc = enc_fn();
+  if (!enc || (reinterpret_cast<uintptr_t>(base) & 15) || (K % kDBK)) return false;
+  const uint64_t kt = K / kDBK;
+  cuuint64_t dims[4] = {(cuuint64_t)kDBK, (cuuint64_t)kDBM, kt, row_tiles};
+  cuuint64_t strides[3] = {kDBK * 2, kDBM * kDBK * 2, kt * kDBM * kDBK * 2};
+  cuuint32_t box[4] = {(cuuint32_t)kDBK, (cuuint32_t)kDBM, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+             const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static bool tmap2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
                    uint32_t box_rows, bool f16) {
   auto enc = enc_fn();
@@ -612,7 +638,7 @@ size_t decode_part_bytes(const qwen_layer_config& c, int B) {
 
 template <int BP, int EPI>
 static qwen_status launch_dec(const CUtensorMap& tw, const CUtensorMap& tx, int B, int N, int K,
-                              int splits, bool op_f16, bool w_static, float* part, f16* hout,
+                              int splits, bool op_f16, bool w_packed, float* part, f16* hout,
                               const int32_t* gact, const int32_t* goff, const int32_t* tidx,
                               const int32_t* tinv, int tk, int max_groups, int* err,
                               cudaStream_t st) {
@@ -629,17 +655,18 @@ static qwen_status launch_dec(const CUtensorMap& tw, const CUtensorMap& tx, int 
   const int sms = device_sm_count();
   const int grid = units < sms ? units : sms;
   launch_k(kern, dim3(grid), dim3(kDThreads), C::SMEM_BYTES, st, tw, tx, B, N, K, splits,
-           idesc_f32acc(kDBM, BP, op_f16), w_static ? 1 : 0, part, hout, gact, goff, tidx, tinv,
+           idesc_f32acc(kDBM, BP, op_f16), w_packed ? 1 : 0, part, hout, gact, goff, tidx, tinv,
            tk, err);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
-// Shared host path of the dense and grouped decode GEMMs.  W rows: N, or
-// E * N stacked experts (grouped); X: B rows, ldx apart; BP covers max_m rows.
-static qwen_status decode_gemm_launch(const void* W, int w_rows, const void* X, int ldx, int B,
+// Shared host path of the dense and grouped decode GEMMs.  W: `groups` stacked
+// [N, K] weights, packed (blocked layout, each weight's rows padded to 128) or
+// row-major; X: B rows, ldx apart; BP covers max_m rows.
+static qwen_status decode_gemm_launch(const void* W, int groups, const void* X, int ldx, int B,
                                       int max_m, int N, int K, int splits, bool op_f16,
-                                      bool w_static, float* part, f16* hout,
+                                      bool w_packed, float* part, f16* hout,
                                       const int32_t* gact, const int32_t* goff,
                                       const int32_t* tidx, const int32_t* tinv, int tk,
                                       int max_groups, int* err, cudaStream_t st) {
@@ -647,15 +674,19 @@ static qwen_status decode_gemm_launch(const void* W, int w_rows, const void* X, 
   if ((K & 7) || splits < 1 || max_groups < 1) return QWEN_ERR_UNSUPPORTED;
   const int bp = pad_batch(max_m);
   CUtensorMap tw, tx;
-  if (!tmap2d(&tw, W, (uint64_t)w_rows, (uint64_t)K, (uint64_t)K, kDBM, op_f16))
+  if (w_packed) {
+    if (!tmap_blocked(&tw, W, (uint64_t)groups * ((N + kDBM - 1) / kDBM), (uint64_t)K, op_f16))
+      return QWEN_ERR_CUDA;
+  } else if (!tmap2d(&tw, W, (uint64_t)groups * N, (uint64_t)K, (uint64_t)K, kDBM, op_f16)) {
     return QWEN_ERR_CUDA;
+  }
   if (!tmap2d(&tx, X, (uint64_t)B, (uint64_t)K, (uint64_t)ldx, bp, op_f16)) return QWEN_ERR_CUDA;
 #define QWEN_DEC_CASE(BPV)                                                                        \
   case BPV:                                                                                       \
-    return hout ? launch_dec<BPV, DEC_SWIGLU>(tw, tx, B, N, K, 1, op_f16, w_static, nullptr,      \
+    return hout ? launch_dec<BPV, DEC_SWIGLU>(tw, tx, B, N, K, 1, op_f16, w_packed, nullptr,      \
                                               hout, gact, goff, tidx, tinv, tk, max_groups, err,  \
                                               st)                                                 \
-                : launch_dec<BPV, DEC_PARTIAL>(tw, tx, B, N, K, splits, op_f16, w_static, part,   \
+                : launch_dec<BPV, DEC_PARTIAL>(tw, tx, B, N, K, splits, op_f16, w_packed, part,   \
                                                nullptr, gact, goff, nullptr, nullptr, 0,          \
                                                max_groups, err, st);
   switch (bp) {
@@ -671,8 +702,8 @@ static qwen_status decode_gemm_launch(const void* W, int w_rows, const void* X, 
 
 qwen_status gemm_decode_splitk(const void* W, const void* X, int ldx, int B, int N, int K,
                                int splits, bool op_f16, float* part, int* err, cudaStream_t st,
-                               bool w_static, f16* swiglu_out) {
-  return decode_gemm_launch(W, N, X, ldx, B, B, N, K, splits, op_f16, w_static, part, swiglu_out,
+                               bool w_packed, f16* swiglu_out) {
+  return decode_gemm_launch(W, 1, X, ldx, B, B, N, K, splits, op_f16, w_packed, part, swiglu_out,
                             nullptr, nullptr, nullptr, nullptr, 0, 1, err, st);
 }
 
@@ -681,8 +712,8 @@ qwen_status gemm_decode_grouped(const void* W, int E, const void* X, int rows, i
                                 int max_groups, float* part, f16* swiglu_out, int* err,
                                 cudaStream_t st) {
   if (!act || !offsets || E <= 0) return QWEN_ERR_INVALID_ARG;
-  return decode_gemm_launch(W, E * N, X, K, rows, max_m, N, K, splits, /*op_f16=*/true,
-                            /*w_static=*/true, part, swiglu_out, act, offsets, nullptr, nullptr, 0,
+  return decode_gemm_launch(W, E, X, K, rows, max_m, N, K, splits, /*op_f16=*/true,
+                            /*w_packed=*/true, part, swiglu_out, act, offsets, nullptr, nullptr, 0,
                             max_groups, err, st);
 }
 
@@ -691,7 +722,7 @@ qwen_status gemm_decode_grouped_tokens(const void* W, int E, const void* X, int 
                                        const int32_t* inv, int k, int max_groups, f16* h_out,
                                        int* err, cudaStream_t st) {
   if (!act || !idx || !inv || !h_out || E <= 0 || k < 1) return QWEN_ERR_INVALID_ARG;
-  return decode_gemm_launch(W, E * N, X, ldx, T, T, N, K, 1, /*op_f16=*/true, /*w_static=*/true,
+  return decode_gemm_launch(W, E, X, ldx, T, T, N, K, 1, /*op_f16=*/true, /*w_packed=*/true,
                             nullptr, h_out, act, nullptr, idx, inv, k,
                             max_groups, err, st);
 }

@@ -38,6 +38,7 @@ struct GemmCfg {
 
 struct TileInfo {
   int m0, n0, row_end, b_row0;
+  int b_tile;  // blocked B: index of the tile's first 128-row block
 };
 
 // Map a linear tile id to output coordinates.  Dense mode: groups of kGroupM
@@ -60,6 +61,7 @@ __device__ __forceinline__ bool get_tile(int tile, int M, int N, int BN, int n_n
     ti.n0 = nb * BN;
     ti.row_end = M;
     ti.b_row0 = ti.n0;
+    ti.b_tile = ti.n0 / 128;
     return true;
   }
   // grouped: s_tile_prefix[g] = m-tiles of groups < g (n_groups+1 entries)
@@ -78,6 +80,7 @@ __device__ __forceinline__ bool get_tile(int tile, int M, int N, int BN, int n_n
   ti.row_end = epi.group_offsets[g + 1];
   ti.n0 = nb * BN;
   ti.b_row0 = g * N + ti.n0;
+  ti.b_tile = g * ((N + 127) / 128) + ti.n0 / 128;  // each group's rows padded to 128
   return true;
 }
 
@@ -309,6 +312,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // B tile of k-block kb: row-major [N, K] (2-D map, BN rows from b_row0) or
+  // the blocked layout of packed weights (4-D map, BN/128 consecutive
+  // 128 x 64 tiles from b_tile)
+  auto load_b = [&](uint8_t* dst, uint64_t* bar, int kb, const TileInfo& t) {
+    if (epi.b_blocked)
+      tma_load_4d_w(dst, &tmB, bar, 0, 0, kb, t.b_tile);
+    else
+      tma_load_2d_w(dst, &tmB, bar, kb * kBK, t.b_row0);
+  };
+
   // warps 0 and 1 run converged and issue from one elected lane (a lone lane
   // next to busy epilogue warps gets too few issue slots)
   if (warp == 0) {
@@ -321,7 +334,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         pre = min(C::STAGES, n_kblk);
         for (int i = 0; i < pre; ++i) {
           mbar_arrive_expect_tx_w(&full[i], C::STAGE_BYTES);
-          tma_load_2d_w(sB + i * C::B_BYTES, &tmB, &full[i], i * kBK, ti.b_row0);
+          load_b(sB + i * C::B_BYTES, &full[i], i, ti);
         }
       }
       pdl_wait();
@@ -337,7 +350,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, err)) goto producer_done;
             mbar_arrive_expect_tx_w(&full[stage], C::STAGE_BYTES);
             tma_load_2d_w(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * kBK, ti.m0);
-            tma_load_2d_w(sB + stage * C::B_BYTES, &tmB, &full[stage], kb * kBK, ti.b_row0);
+            load_b(sB + stage * C::B_BYTES, &full[stage], kb, ti);
           }
           if (++stage == C::STAGES) {
             stage = 0;
@@ -453,6 +466,25 @@ static bool make_tmap_16(CUtensorMap* map, const void* base, uint64_t rows, uint
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The blocked layout of packed weights: 128 x 64 tiles of 16 KB, tile (t, kt)
+// at ((t * K/64) + kt) * 16 KB, rows of 64 elements inside a tile.  4-D map
+// {64 elements, 128 rows, K/64 tiles, row tiles}; a box of `box_tiles`
+// consecutive row tiles lands in shared memory as box_tiles * 128 rows.
+static bool make_tmap_blocked(CUtensorMap* map, const void* base, uint64_t row_tiles, uint64_t K,
+                              uint32_t box_tiles, bool f16) {
+  auto enc = get_encode_fn();
+  if (!enc || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+  const uint64_t kt = K / kBK;
+  cuuint64_t dims[4] = {(cuuint64_t)kBK, 128, kt, row_tiles};
+  cuuint64_t strides[3] = {kBK * 2, 128 * kBK * 2, kt * 128 * kBK * 2};
+  cuuint32_t box[4] = {(cuuint32_t)kBK, 128, 1, box_tiles};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int BN, int EPI>
 static qwen_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K,
                              uint32_t idesc, const GemmEpilogue& epi, int* err, int grid,
@@ -481,7 +513,13 @@ qwen_status gemm_tc(const void* A, int lda, const void* B, int ldb, int M, int N
   CUtensorMap ta, tb;
   if (!make_tmap_16(&ta, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, kBM, op_f16))
     return QWEN_ERR_CUDA;
-  if (!make_tmap_16(&tb, B, b_rows, (uint64_t)K, (uint64_t)ldb, BN, op_f16)) return QWEN_ERR_CUDA;
+  if (epi.b_blocked) {
+    if (K % kBK) return QWEN_ERR_UNSUPPORTED;
+    const uint64_t tiles = (uint64_t)(epi.group_offsets ? epi.n_groups : 1) * ((N + 127) / 128);
+    if (!make_tmap_blocked(&tb, B, tiles, (uint64_t)K, BN / 128, op_f16)) return QWEN_ERR_CUDA;
+  } else if (!make_tmap_16(&tb, B, b_rows, (uint64_t)K, (uint64_t)ldb, BN, op_f16)) {
+    return QWEN_ERR_CUDA;
+  }
   const uint32_t idesc = idesc_f32acc(kBM, BN, op_f16);
   const int sms = device_sm_count();
   int tiles;

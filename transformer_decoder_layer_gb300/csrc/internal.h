@@ -58,6 +58,9 @@ struct GemmEpilogue {
   // B is never written by the kernel launched just before this one (packed
   // layer weights): its first tiles may be fetched before waiting on it.
   int b_static;
+  // B is a packed layer weight in the blocked layout (128 x 64 tiles, each
+  // group's rows padded to a multiple of 128); else row-major with row stride ldb.
+  int b_blocked;
 };
 
 int device_sm_count();

@@ -104,13 +104,15 @@ void decode_attn_plan(const qwen_layer_config& c, int B, int* splits);
 
 // part[s][b][n] = sum over split s's k-range of W[n, k] X[b, k].
 // W [N, K], X [B, K] (row stride ldx).
-// w_static: W is never written by the kernel launched just before (the packed
-// layer weights), so its first tiles may be fetched before waiting on it.
+// w_packed: W is a packed layer weight: stored in the blocked layout (128 x 64
+// tiles, rows padded to 128) and never written by the kernel launched just
+// before, so its first tiles may be fetched before waiting on it.  Otherwise
+// W is row-major [N, K] (the caller's lm_head).
 // swiglu_out: W is an interleaved gate/up weight (64-row blocks); run with one
 // split and write H[b][f] = SiLU(gate) * up (FP16) instead of partials.
 qwen_status gemm_decode_splitk(const void* W, const void* X, int ldx, int B, int N, int K,
                                int splits, bool op_f16, float* part, int* err, cudaStream_t st,
-                               bool w_static = false, __half* swiglu_out = nullptr);
+                               bool w_packed = false, __half* swiglu_out = nullptr);
 
 // Grouped (mixture-of-experts) decode GEMM.  W: E stacked FP16 [N, K] weights;
 // X: `rows` FP16 rows of K, grouped by expert: rows [offsets[e], offsets[e+1])

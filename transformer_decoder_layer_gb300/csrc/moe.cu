@@ -491,7 +491,7 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
     const int S = grouped_dec ? min(decode_splits(R, 2 * d, T), kRouteMaxSplits)
                               : decode_splits(R, 2 * d, T);
     if ((s = gemm_decode_splitk(L->w_router, z, 2 * d, T, R, 2 * d, S, true, part, err, st,
-                                /*w_static=*/true)))
+                                /*w_packed=*/true)))
       return s;
     if (grouped_dec) {
       // 3 + 5 in one CTA: split sum, top-k, counting sort (it reads the
@@ -510,6 +510,7 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
     er.out32 = logits;
     er.ldo32 = R;
     er.b_static = 1;
+    er.b_blocked = 1;
     if ((s = gemm_tc(z, 2 * d, L->w_router, 2 * d, T, R, 2 * d, true, er, err, st))) return s;
   }
   // 3. top-k (+ router bias), gate weights, shared gate sigmoid
@@ -523,11 +524,11 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
   if (sf) {
     if (small) {
       if ((s = gemm_decode_splitk(L->w_sgu, z, 2 * d, T, 2 * sf, d, 1, true, nullptr, err, st,
-                                  /*w_static=*/true, hs)))
+                                  /*w_packed=*/true, hs)))
         return s;
       const int S = decode_splits(d, sf, T);
       if ((s = gemm_decode_splitk(L->w_sdown, hs, sf, T, d, sf, S, true, part, err, st,
-                                  /*w_static=*/true)))
+                                  /*w_packed=*/true)))
         return s;
       if ((s = reduce_f32(part, S, T, d, ys32, d, st))) return s;
     } else {
@@ -537,12 +538,14 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
       sg.out_f16 = 1;
       sg.ldo = sf;
       sg.b_static = 1;
+      sg.b_blocked = 1;
       if ((s = gemm_tc(z, 2 * d, L->w_sgu, d, T, 2 * sf, d, true, sg, err, st))) return s;
       GemmEpilogue sd{};
       sd.mode = EPI_F32;
       sd.out32 = ys32;
       sd.ldo32 = d;
       sd.b_static = 1;
+      sd.b_blocked = 1;
       if ((s = gemm_tc(hs, sf, L->w_sdown, sf, T, d, sf, true, sd, err, st))) return s;
     }
   }
@@ -586,6 +589,7 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
   eg.ldo = mf;
   eg.group_offsets = offsets;
   eg.n_groups = E;
+  eg.b_blocked = 1;
   if ((s = gemm_tc(zp, d, L->w_gu, d, n, 2 * mf, d, true, eg, err, st))) return s;
   GemmEpilogue ed{};
   ed.mode = EPI_STORE;
@@ -594,6 +598,7 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
   ed.ldo = d;
   ed.group_offsets = offsets;
   ed.n_groups = E;
+  ed.b_blocked = 1;
   if ((s = gemm_tc(hp, mf, L->w_down, mf, n, d, mf, true, ed, err, st))) return s;
   // 7. weighted combine (+ gated shared expert) + residual
   launch_k(combine_kernel<false>, dim3(nblk((long long)T * (d / 8), 256)), dim3(256), 0, st,
