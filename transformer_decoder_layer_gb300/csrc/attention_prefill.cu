@@ -30,8 +30,8 @@
 // Operands: when the sequence starts at slot 0 every key comes from this call,
 // so Q, K, V and P are FP16 (the QKV epilogue writes FP16 copies of the new K/V
 // rows besides the BF16 cache).  A chunk appended to a filled cache reads the
-// BF16 cache instead; then Q is converted to BF16 in shared memory once and P
-// is rounded to BF16.
+// BF16 cache instead; then the QKV epilogue has written Q in BF16 and P is
+// rounded to BF16.
 #include "common.cuh"
 #include "internal.h"
 
@@ -137,6 +137,51 @@ struct AttnArgs {
 
 }  // namespace
 
+// One work item: sequence b, KV group g, query heads hA (and hA + 1 when
+// nq = 2), query rows [t0, t0 + 128).  Items are numbered heaviest first (the
+// last query tiles see the most keys).
+struct AttnItem {
+  int b, g, hA, nq, t0, s0, kmax, n_kv, kv_row0;
+  bool fresh;  // every key is this call's (slot0 == 0): FP16 operands
+};
+
+__device__ __forceinline__ AttnItem attn_item(int it, const AttnArgs& a) {
+  const int gs = a.Hq / a.Hkv;
+  const int npair = (gs + 1) >> 1;
+  const int n_qt = (a.T + kQT - 1) / kQT;
+  const int per_qt = a.B * a.Hkv * npair;
+  AttnItem I;
+  const int qt = n_qt - 1 - it / per_qt;
+  int u = it % per_qt;
+  const int pr = u % npair;
+  u /= npair;
+  I.g = u % a.Hkv;
+  I.b = u / a.Hkv;
+  I.hA = I.g * gs + 2 * pr;
+  I.nq = (2 * pr + 1 < gs) ? 2 : 1;
+  I.t0 = qt * kQT;
+  I.s0 = a.slot0[I.b];
+  I.fresh = I.s0 == 0;
+  const int q_last = min(I.t0 + kQT, a.T) - 1;  // last valid query row of the tile
+  I.kmax = I.s0 + q_last;                       // largest visible key slot
+  I.n_kv = I.kmax / kKT + 1;                    // key tiles 0..n_kv-1
+  // row of key slot 0 in the K/V view (FP16 copies of this call, or the cache)
+  I.kv_row0 = I.fresh ? (I.b * a.Hkv + I.g) * a.T : (I.b * a.Hkv + I.g) * a.max_seq;
+  return I;
+}
+
+// Persistent: each CTA walks its items (a snake order, see item_of).  The K/V
+// ring, the S/P/O hand-offs and the Q buffers carry over from item to item
+// (running counters give every barrier phase), so the next item's Q and first
+// K tiles load, and its first S is computed, while the softmax warps still
+// write the previous item's output.
+// Barrier phases are tracked by parity, so no thread may wait on a phase more
+// than one ahead of, or two behind, a barrier's current one.  The barriers both
+// heads share (Q, K and V full / empty) therefore see every phase from both
+// issuers: in an item without head B (the last of an odd-sized group) issuer B
+// still waits for each Q, K and V load and makes head B's release arrival.
+// The softmax warps only wait on their own head's barriers and on V tiles of
+// their own items.
 template <int DH>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_prefill_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -156,56 +201,52 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* sP = smem + C::P_OFF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* q_full = bars + 0;
-  uint64_t* q_conv = bars + 1;    // BF16 conversion of Q done (appended chunks only)
-  uint64_t* k_full = bars + 2;    // [2]
-  uint64_t* k_empty = bars + 4;   // [2]
-  uint64_t* v_full = bars + 6;
-  uint64_t* v_empty = bars + 7;
-  uint64_t* s_full = bars + 8;    // [2] per head: S_x(j) in TMEM
-  uint64_t* s_free = bars + 10;   // [2] per head: S_x(j) read into registers
-  uint64_t* p_full = bars + 12;   // [2] per head: P_x(j) in shared memory
-  uint64_t* o_done = bars + 14;   // [2] per head: O_x += P_x(j) V_j complete
-  uint64_t* mma_idle = bars + 16; // [2] per head
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  uint64_t* q_empty = bars + 2;   // the item's S MMAs no longer read Q
+  uint64_t* k_full = bars + 3;    // [2]
+  uint64_t* k_empty = bars + 5;   // [2]
+  uint64_t* v_full = bars + 7;
+  uint64_t* v_empty = bars + 8;
+  uint64_t* s_full = bars + 9;    // [2] per head: S_x in TMEM
+  uint64_t* s_free = bars + 11;   // [2] per head: S_x read into registers
+  uint64_t* p_full = bars + 13;   // [2] per head: P_x in shared memory
+  uint64_t* o_done = bars + 15;   // [2] per head: O_x += P_x V complete
+  uint64_t* o_free = bars + 17;   // [2] per head: the item's O_x has been read out
+  uint64_t* mma_idle = bars + 19; // [2] per head
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // work unit: heaviest (last) query tiles first
   const int gs = a.Hq / a.Hkv;
-  const int npair = (gs + 1) >> 1;
-  const int n_qt = (a.T + kQT - 1) / kQT;
-  const int per_qt = a.B * a.Hkv * npair;
-  const int qt = n_qt - 1 - (int)blockIdx.x / per_qt;
-  int u = (int)blockIdx.x % per_qt;
-  const int pr = u % npair;
-  u /= npair;
-  const int g = u % a.Hkv;
-  const int b = u / a.Hkv;
-  const int hA = g * gs + 2 * pr;
-  const int nq = (2 * pr + 1 < gs) ? 2 : 1;  // heads in this CTA
-  const int t0 = qt * kQT;
-  const int s0 = a.slot0[b];
-  const bool fresh = s0 == 0;                 // all keys are this call's: FP16 operands
-  const int q_last = min(t0 + kQT, a.T) - 1;  // last valid query row of the tile
-  const int kmax = s0 + q_last;               // largest visible key slot
-  const int n_kv = kmax / kKT + 1;            // key tiles 0..n_kv-1
-  // row of key slot 0 in the K/V view (FP16 copies of this call, or the cache)
-  const int kv_row0 = fresh ? (b * a.Hkv + g) * a.T : (b * a.Hkv + g) * a.max_seq;
+  const int n_items = ((a.T + kQT - 1) / kQT) * a.B * a.Hkv * ((gs + 1) >> 1);
+  // this CTA's ni-th item (-1: none left).  Snake order over the heaviest-first
+  // item list: round r takes items [r G, (r+1) G), CTA k the k-th of them in
+  // even rounds and the (G-1-k)-th in odd rounds, which balances the summed
+  // work about as well as handing out items dynamically.
+  auto item_of = [&](int ni) -> int {
+    const int G = (int)gridDim.x, k = (int)blockIdx.x;
+    for (int r = 0, seen = 0;; ++r) {
+      const int base = r * G;
+      if (base >= n_items) return -1;
+      const int it = base + ((r & 1) ? G - 1 - k : k);
+      if (it < n_items && seen++ == ni) return it;
+    }
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    mbar_init(q_conv, 128 * nq);
+    mbar_init(q_empty, 2);   // each head's issuer, present in the item or not
     for (int i = 0; i < kKStages; ++i) {
       mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], nq);  // released by each head's issuer
+      mbar_init(&k_empty[i], 2);
     }
     mbar_init(v_full, 1);
-    mbar_init(v_empty, nq);
+    mbar_init(v_empty, 2);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
       mbar_init(&s_free[x], 128);
       mbar_init(&p_full[x], 128);
       mbar_init(&o_done[x], 1);
+      mbar_init(&o_free[x], 128);
       mbar_init(&mma_idle[x], 1);
     }
     *abort_flag = 0;
@@ -221,70 +262,102 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // TMA producer, converged; one elected lane issues
-    const CUtensorMap* mk = fresh ? &tmK16 : &tmK;
-    const CUtensorMap* mv = fresh ? &tmV16 : &tmV;
+    // TMA producer, converged; one elected lane issues.  Per item: Q once the
+    // previous item's S MMAs are done with it, then K(0), and per tile j
+    // K(j+1) ahead of V(j): S(j+1) is issued early in the softmax of tile j,
+    // P(j).V only at its end.
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(mk);
-      tma_prefetch_desc(mv);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmK16);
+      tma_prefetch_desc(&tmV16);
     }
     __syncwarp();
-    mbar_arrive_expect_tx_w(q_full, nq * C::TILE_BYTES);
-    for (int x = 0; x < nq; ++x) {
+    int nk = 0, nv = 0, nql = 0;  // K, V and Q loads issued
+    for (int ni = 0, it = item_of(0); it >= 0; it = item_of(++ni)) {
+      const AttnItem I = attn_item(it, a);
+      const CUtensorMap* mk = I.fresh ? &tmK16 : &tmK;
+      const CUtensorMap* mv = I.fresh ? &tmV16 : &tmV;
+      if (ni > 0 && !mbar_wait_w(q_empty, (ni - 1) & 1, abort_flag, a.err)) break;
+      mbar_arrive_expect_tx_w(q_full, I.nq * C::TILE_BYTES);
+      for (int x = 0; x < I.nq; ++x) {
 #pragma unroll
-      for (int c = 0; c < DH / 64; ++c)
-        tma_load_2d_w(sQ + x * C::TILE_BYTES + c * kQT * 128, &tmQ, q_full, c * 64,
-                      (b * a.Hq + hA + x) * a.T + t0);
-    }
-    int nk = 0, nv = 0;  // tiles issued
-    auto load_k = [&](int j) -> bool {
-      const int st = j % kKStages;
-      if (!mbar_wait_w(&k_empty[st], ((j / kKStages) & 1) ^ 1u, abort_flag, a.err)) return false;
-      mbar_arrive_expect_tx_w(&k_full[st], C::TILE_BYTES);
-#pragma unroll
-      for (int c = 0; c < DH / 64; ++c)
-        tma_load_2d_w(sK + st * C::TILE_BYTES + c * kKT * 128, mk, &k_full[st], c * 64,
-                      kv_row0 + j * kKT);
-      ++nk;
-      return true;
-    };
-    auto load_v = [&](int j) -> bool {
-      if (!mbar_wait_w(v_empty, (j & 1) ^ 1u, abort_flag, a.err)) return false;
-      mbar_arrive_expect_tx_w(v_full, C::TILE_BYTES);
-#pragma unroll
-      for (int c = 0; c < DH / 64; ++c)
-        tma_load_2d_w(sV + c * kKT * 128, mv, v_full, c * 64, kv_row0 + j * kKT);
-      ++nv;
-      return true;
-    };
-    // K(j+1) goes ahead of V(j): S(j+1) is issued early in the softmax of tile j,
-    // P(j).V only at its end
-    if (load_k(0)) {
-      for (int j = 0; j < n_kv; ++j) {
-        if (j + 1 < n_kv && !load_k(j + 1)) break;
-        if (!load_v(j)) break;
+        for (int c = 0; c < DH / 64; ++c)
+          tma_load_2d_w(sQ + x * C::TILE_BYTES + c * kQT * 128, &tmQ, q_full, c * 64,
+                        (I.b * a.Hq + I.hA + x) * a.T + I.t0);
       }
+      ++nql;
+      auto load_k = [&](int j) -> bool {
+        const int st = nk % kKStages;
+        if (!mbar_wait_w(&k_empty[st], ((nk / kKStages) & 1) ^ 1u, abort_flag, a.err))
+          return false;
+        mbar_arrive_expect_tx_w(&k_full[st], C::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < DH / 64; ++c)
+          tma_load_2d_w(sK + st * C::TILE_BYTES + c * kKT * 128, mk, &k_full[st], c * 64,
+                        I.kv_row0 + j * kKT);
+        ++nk;
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        if (!mbar_wait_w(v_empty, (nv & 1) ^ 1u, abort_flag, a.err)) return false;
+        mbar_arrive_expect_tx_w(v_full, C::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < DH / 64; ++c)
+          tma_load_2d_w(sV + c * kKT * 128, mv, v_full, c * 64, I.kv_row0 + j * kKT);
+        ++nv;
+        return true;
+      };
+      bool ok = load_k(0);
+      for (int j = 0; ok && j < I.n_kv; ++j) {
+        if (j + 1 < I.n_kv && !load_k(j + 1)) ok = false;
+        if (ok && !load_v(j)) ok = false;
+      }
+      if (!ok) break;
     }
     // the CTA does not retire while a copy is still landing (also on abort)
     for (int j = max(0, nk - kKStages); j < nk; ++j)
       mbar_wait_drain(&k_full[j % kKStages], (j / kKStages) & 1, a.err);
     if (nv > 0) mbar_wait_drain(v_full, (nv - 1) & 1, a.err);
+    if (nql > 0) mbar_wait_drain(q_full, (nql - 1) & 1, a.err);
   } else if (warp <= 2) {
     const int x = warp - 1;  // head whose MMAs this warp issues
-    if (x < nq) {
-      const uint32_t idesc_s = idesc_f32acc(kQT, kKT, fresh);
-      const uint32_t idesc_o = idesc_f32acc(kQT, DH, fresh, false, /*b_mn_major=*/true);
-      // descriptors computed once; each MMA adds a constant (start address >> 4
-      // stays below 2^14, so the add never carries out of its field)
-      const uint64_t dq = smem_desc_sw128(smem_u32(sQ + x * C::TILE_BYTES), 16, 1024);
-      const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t dv = smem_desc_sw128(smem_u32(sV), kKT * 128, 1024);
-      const uint64_t dp = smem_desc_sw128(smem_u32(sP + x * C::P_BYTES), 16, 1024);
-      const uint32_t d_s = tmem + C::S_COL + x * kKT;
-      const uint32_t d_o = tmem + C::O_COL + x * DH;
+    // descriptors computed once; each MMA adds a constant (start address >> 4
+    // stays below 2^14, so the add never carries out of its field)
+    const uint64_t dq = smem_desc_sw128(smem_u32(sQ + x * C::TILE_BYTES), 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+    const uint64_t dv = smem_desc_sw128(smem_u32(sV), kKT * 128, 1024);
+    const uint64_t dp = smem_desc_sw128(smem_u32(sP + x * C::P_BYTES), 16, 1024);
+    const uint32_t d_s = tmem + C::S_COL + x * kKT;
+    const uint32_t d_o = tmem + C::O_COL + x * DH;
+    // kc, vc: this CTA's K and V tiles before the item; c: head x's tiles before
+    // the item; hi: items head x took part in
+    int kc = 0, vc = 0, c = 0, hi = 0;
+    bool ok = true;
+    for (int ni = 0, it = item_of(0); ok && it >= 0; it = item_of(++ni)) {
+      const AttnItem I = attn_item(it, a);
+      if (x >= I.nq) {
+        // head absent: observe each shared load and arrive for this head
+        ok = mbar_wait_w(q_full, ni & 1, abort_flag, a.err);
+        if (ok && lane == 0) mbar_arrive(q_empty);
+        for (int j = 0; ok && j < I.n_kv; ++j) {
+          const int k1 = kc + j, v1 = vc + j;
+          ok = mbar_wait_w(&k_full[k1 % kKStages], (k1 / kKStages) & 1, abort_flag, a.err);
+          if (ok && lane == 0) mbar_arrive(&k_empty[k1 % kKStages]);
+          if (ok) ok = mbar_wait_w(v_full, v1 & 1, abort_flag, a.err);
+          if (ok && lane == 0) mbar_arrive(v_empty);
+        }
+        __syncwarp();
+        kc += I.n_kv;
+        vc += I.n_kv;
+        continue;
+      }
+      const uint32_t idesc_s = idesc_f32acc(kQT, kKT, I.fresh);
+      const uint32_t idesc_o = idesc_f32acc(kQT, DH, I.fresh, false, /*b_mn_major=*/true);
       auto issue_s = [&](int j) {
-        const uint64_t b0 = dk0 + (uint64_t)((j % kKStages) * (C::TILE_BYTES >> 4));
+        const int kidx = kc + j;
+        const uint64_t b0 = dk0 + (uint64_t)((kidx % kKStages) * (C::TILE_BYTES >> 4));
 #pragma unroll
         for (int k = 0; k < DH / 16; ++k) {
           // 16 dh columns = 32 B within a 128-B swizzle row; next 64-wide block 16 KB on
@@ -292,9 +365,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           umma_f16_w(d_s, dq + off, b0 + off, idesc_s, k != 0);
         }
         umma_commit_w(&s_full[x]);
-        // release the stage only if it will be refilled (nothing is left in
-        // flight towards this CTA's barriers when it ends)
-        if (j + kKStages < n_kv) umma_commit_w(&k_empty[j % kKStages]);
+        umma_commit_w(&k_empty[kidx % kKStages]);
+        if (j == I.n_kv - 1) umma_commit_w(q_empty);  // the item's last read of Q
       };
       auto issue_pv = [&](int j) {
 #pragma unroll
@@ -306,192 +378,199 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           umma_f16_w(d_o, dp + pa, dv + ((k * 16 * 128) >> 4), idesc_o, (j | k) != 0);
         }
         umma_commit_w(&o_done[x]);
-        if (j + 1 < n_kv) umma_commit_w(v_empty);
+        umma_commit_w(v_empty);
       };
-      bool ok = mbar_wait_w(q_full, 0, abort_flag, a.err);
-      if (ok && !fresh) ok = mbar_wait_w(q_conv, 0, abort_flag, a.err);
-      if (ok) ok = mbar_wait_w(&k_full[0], 0, abort_flag, a.err);
+      // S(0): Q and K(0) landed, and the previous item's last S read out of TMEM
+      ok = mbar_wait_w(q_full, ni & 1, abort_flag, a.err);
+      if (ok) ok = mbar_wait_w(&k_full[kc % kKStages], (kc / kKStages) & 1, abort_flag, a.err);
+      if (ok && c > 0) ok = mbar_wait_w(&s_free[x], (c - 1) & 1, abort_flag, a.err);
       if (ok) {
         tc_fence_after();
         issue_s(0);
       }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv) {
-          const int j1 = j + 1;
-          if (!mbar_wait_w(&k_full[j1 % kKStages], (j1 / kKStages) & 1, abort_flag, a.err)) break;
+      for (int j = 0; ok && j < I.n_kv; ++j) {
+        if (j + 1 < I.n_kv) {
+          const int k1 = kc + j + 1;
+          if (!mbar_wait_w(&k_full[k1 % kKStages], (k1 / kKStages) & 1, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
           // S_x(j+1) overwrites S_x(j): the softmax has it in registers
-          if (!mbar_wait_w(&s_free[x], j & 1, abort_flag, a.err)) break;
+          if (!mbar_wait_w(&s_free[x], (c + j) & 1, abort_flag, a.err)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          issue_s(j1);
+          issue_s(j + 1);
         }
-        if (!mbar_wait_w(v_full, j & 1, abort_flag, a.err)) break;
-        if (!mbar_wait_w(&p_full[x], j & 1, abort_flag, a.err)) break;
+        if (!mbar_wait_w(v_full, (vc + j) & 1, abort_flag, a.err)) { ok = false; break; }
+        if (!mbar_wait_w(&p_full[x], (c + j) & 1, abort_flag, a.err)) { ok = false; break; }
+        // the first P.V of an item overwrites O_x: the previous item's output
+        // must have been read out
+        if (j == 0 && hi > 0 && !mbar_wait_w(&o_free[x], (hi - 1) & 1, abort_flag, a.err)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         issue_pv(j);
       }
-      // retire only after every issued MMA has completed (also on abort)
-      umma_commit_w(&mma_idle[x]);
-      mbar_wait_drain(&mma_idle[x], 0, a.err);
+      kc += I.n_kv;
+      vc += I.n_kv;
+      c += I.n_kv;
+      ++hi;
     }
+    // retire only after every issued MMA has completed (also on abort)
+    umma_commit_w(&mma_idle[x]);
+    mbar_wait_drain(&mma_idle[x], 0, a.err);
   } else {
-    // softmax / epilogue warps: head x, row r of the query tile
+    // softmax / epilogue warps: head x, row r of each item's query tile
     const int x = (warp - 3) >> 2;
     const int qw = warp & 3;        // TMEM lane quadrant of this warp
     const int r = qw * 32 + lane;   // query row within the tile
-    const int t = t0 + r;
-    const int s_q = s0 + t;         // this row's cache slot
-    const int s_row0 = s0 + t0;     // slot of the tile's first row
     const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + C::S_COL + x * kKT;
     const uint32_t o_addr = tmem + lane_base + C::O_COL + x * DH;
     uint8_t* prow = sP + x * C::P_BYTES + r * 128;  // this row in P's two swizzle blocks
-    float m_used = -INFINITY, l_sum = 0.f;
-    bool ok = x < nq;
-    if (ok && !fresh) {
-      // keys come from the BF16 cache: convert this row of Q once, in place
-      // (element by element, so the swizzled placement is kept)
-      ok = mbar_wait(q_full, 0, abort_flag, a.err);
-      if (ok) {
+    int c = 0, vcount = 0;  // head x's S tiles and this CTA's V tiles before the item
+    bool ok = true;
+    for (int ni = 0, it = item_of(0); ok && it >= 0; it = item_of(++ni)) {
+      const AttnItem I = attn_item(it, a);
+      if (x >= I.nq) {
+        vcount += I.n_kv;
+        continue;
+      }
+      const int t = I.t0 + r;
+      const int s_q = I.s0 + t;         // this row's cache slot
+      const int s_row0 = I.s0 + I.t0;   // slot of the tile's first row
+      float m_used = -INFINITY, l_sum = 0.f;
+      for (int j = 0; ok && j < I.n_kv; ++j) {
+        const int cj = c + j;
+        if (!mbar_wait(&s_full[x], cj & 1, abort_flag, a.err)) { ok = false; break; }
+        tc_fence_after();
+        float s[kKT];
+        {
+          uint32_t raw[kKT];
+          tmem_ld128_wait(s_addr, raw);
 #pragma unroll
-        for (int blk = 0; blk < DH / 64; ++blk) {
-          uint4* row = reinterpret_cast<uint4*>(sQ + x * C::TILE_BYTES + blk * (kQT * 128) +
-                                                r * 128);
+          for (int i = 0; i < kKT; ++i) s[i] = __uint_as_float(raw[i]);
+        }
+        tc_fence_before();
+        mbar_arrive(&s_free[x]);  // S_x(j+1) may now be computed into the same columns
+        const int key0 = j * kKT;
+        if (key0 + kKT - 1 > s_row0) {
+          // a tile that reaches past the first row's slot: causal mask
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 u4 = row[c];
-            const uint32_t w[4] = {u4.x, u4.y, u4.z, u4.w};
-            uint32_t o[4];
+          for (int i = 0; i < kKT; ++i) s[i] = (key0 + i <= s_q) ? s[i] : -INFINITY;
+        }
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 f = unpack_f16x2(w[e]);
-              o[e] = pack_bf16x2(f.x, f.y);
+        for (int i = 0; i < kKT; i += 8) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) m4[q] = max3(m4[q], s[i + 2 * q], s[i + 2 * q + 1]);
+        }
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2;
+        float alpha = 1.f;
+        if (mx > m_used + kRescaleLog2) {
+          alpha = ex2(m_used - mx);  // 0 on the first tile (m_used = -inf)
+          l_sum *= alpha;
+          m_used = mx;
+        }
+        // P = 2^(s * scale - m), FP32 row sum, rounded to the operand type,
+        // stored in the 128-byte swizzle: 16-byte chunk q of row r sits at chunk
+        // q ^ (r & 7) of the row's 128-byte line.  Keys 0-63 are packed before
+        // the wait for the previous P.V (which still reads the buffer), keys
+        // 64-127 are stored as they are computed.
+        const float neg_m = -m_used;
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2(fmaf(s[2 * i], a.scale_log2, neg_m));
+          const float p1 = ex2(fmaf(s[2 * i + 1], a.scale_log2, neg_m));
+          l_sum += p0 + p1;
+          pk[i] = pack2(p0, p1, I.fresh);
+        }
+        if (j > 0) {
+          // O_x += P_x(j-1) V must be done: it reads the P buffer, and O is
+          // rescaled below (O_x += P_x(j) V waits for this thread).  At j = 0
+          // the previous item's epilogue already waited for its last P.V.
+          if (!mbar_wait(&o_done[x], (cj - 1) & 1, abort_flag, a.err)) { ok = false; break; }
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(prow + ((q ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e4 = 0; e4 < 4; ++e4) {
+            const int e = 64 + 8 * q + 2 * e4;
+            const float p0 = ex2(fmaf(s[e], a.scale_log2, neg_m));
+            const float p1 = ex2(fmaf(s[e + 1], a.scale_log2, neg_m));
+            l_sum += p0 + p1;
+            w[e4] = pack2(p0, p1, I.fresh);
+          }
+          *reinterpret_cast<uint4*>(prow + kQT * 128 + ((q ^ (r & 7)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int q = 0; q < DH / 32; ++q) {
+            uint32_t oo[32];
+            tmem_ld32_wait(o_addr + 32 * q, oo);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) oo[i] = __float_as_uint(__uint_as_float(oo[i]) * alpha);
+            tmem_st32(o_addr + 32 * q, oo);
+          }
+          tmem_st_wait();
+        }
+        if (key0 + kKT - 1 > I.kmax) {
+          // keys past the item's last visible slot may hold stale cache
+          // contents: zero their V rows so 0 * (non-finite) cannot reach O
+          // (both heads' threads write the same zeros; each head's P.V waits
+          // for its own)
+          if (!mbar_wait(v_full, (vcount + j) & 1, abort_flag, a.err)) { ok = false; break; }
+          if (key0 + r > I.kmax) {
+#pragma unroll
+            for (int q = 0; q < DH / 64; ++q) {
+              uint4* vr = reinterpret_cast<uint4*>(sV + q * kKT * 128 + r * 128);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) vr[e] = make_uint4(0, 0, 0, 0);
             }
-            row[c] = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
         fence_proxy_async_smem();
-        mbar_arrive(q_conv);
+        tc_fence_before();
+        mbar_arrive(&p_full[x]);
       }
-    }
-    for (int j = 0; ok && j < n_kv; ++j) {
-      if (!mbar_wait(&s_full[x], j & 1, abort_flag, a.err)) { ok = false; break; }
-      tc_fence_after();
-      float s[kKT];
-      {
-        uint32_t raw[kKT];
-        tmem_ld128_wait(s_addr, raw);
-#pragma unroll
-        for (int i = 0; i < kKT; ++i) s[i] = __uint_as_float(raw[i]);
-      }
-      tc_fence_before();
-      mbar_arrive(&s_free[x]);  // S_x(j+1) may now be computed into the same columns
-      const int key0 = j * kKT;
-      if (key0 + kKT - 1 > s_row0) {
-        // a tile that reaches past the first row's slot: causal mask
-#pragma unroll
-        for (int i = 0; i < kKT; ++i) s[i] = (key0 + i <= s_q) ? s[i] : -INFINITY;
-      }
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int i = 0; i < kKT; i += 8) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) m4[c] = max3(m4[c], s[i + 2 * c], s[i + 2 * c + 1]);
-      }
-      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2;
-      float alpha = 1.f;
-      if (mx > m_used + kRescaleLog2) {
-        alpha = ex2(m_used - mx);  // 0 on the first tile (m_used = -inf)
-        l_sum *= alpha;
-        m_used = mx;
-      }
-      // P = 2^(s * scale - m), FP32 row sum, rounded to the operand type, stored
-      // in the 128-byte swizzle: 16-byte chunk c of row r sits at chunk
-      // c ^ (r & 7) of the row's 128-byte line.  Keys 0-63 are packed before
-      // the wait for the previous P.V (which still reads the buffer), keys
-      // 64-127 are stored as they are computed.
-      const float neg_m = -m_used;
-      uint32_t pk[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float p0 = ex2(fmaf(s[2 * i], a.scale_log2, neg_m));
-        const float p1 = ex2(fmaf(s[2 * i + 1], a.scale_log2, neg_m));
-        l_sum += p0 + p1;
-        pk[i] = pack2(p0, p1, fresh);
-      }
-      if (j > 0) {
-        // O_x += P_x(j-1) V must be done: it reads the P buffer, and O is
-        // rescaled below (O_x += P_x(j) V waits for this thread)
-        if (!mbar_wait(&o_done[x], (j - 1) & 1, abort_flag, a.err)) { ok = false; break; }
-        tc_fence_after();
-      }
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int e = 64 + 8 * c + 2 * q;
-          const float p0 = ex2(fmaf(s[e], a.scale_log2, neg_m));
-          const float p1 = ex2(fmaf(s[e + 1], a.scale_log2, neg_m));
-          l_sum += p0 + p1;
-          w[q] = pack2(p0, p1, fresh);
-        }
-        *reinterpret_cast<uint4*>(prow + kQT * 128 + ((c ^ (r & 7)) << 4)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-        for (int c = 0; c < DH / 32; ++c) {
-          uint32_t oo[32];
-          tmem_ld32_wait(o_addr + 32 * c, oo);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) oo[i] = __float_as_uint(__uint_as_float(oo[i]) * alpha);
-          tmem_st32(o_addr + 32 * c, oo);
-        }
-        tmem_st_wait();
-      }
-      if (key0 + kKT - 1 > kmax) {
-        // keys past the CTA's last visible slot may hold stale cache contents:
-        // zero their V rows so 0 * (non-finite) cannot reach O (both heads'
-        // threads write the same zeros; each head's P.V waits for its own)
-        if (!mbar_wait(v_full, j & 1, abort_flag, a.err)) { ok = false; break; }
-        if (key0 + r > kmax) {
-#pragma unroll
-          for (int c = 0; c < DH / 64; ++c) {
-            uint4* vr = reinterpret_cast<uint4*>(sV + c * kKT * 128 + r * 128);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) vr[q] = make_uint4(0, 0, 0, 0);
-          }
-        }
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&p_full[x]);
-    }
-    if (ok && mbar_wait(&o_done[x], (n_kv - 1) & 1, abort_flag, a.err)) {
+      if (!ok) break;
+      // epilogue: O / l of this item, then O_x is free for the next item
+      if (!mbar_wait(&o_done[x], (c + I.n_kv - 1) & 1, abort_flag, a.err)) break;
       tc_fence_after();
       const float inv_l = 1.f / l_sum;
       const bool row_ok = t < a.T;
-      f16* dst = a.out + ((size_t)b * a.T + t) * (size_t)(a.Hq * DH) + (size_t)(hA + x) * DH;
+      f16* dst = a.out + ((size_t)I.b * a.T + t) * (size_t)(a.Hq * DH) + (size_t)(I.hA + x) * DH;
 #pragma unroll 1
-      for (int c = 0; c < DH / 32; ++c) {
+      for (int q = 0; q < DH / 32; ++q) {
         uint32_t oo[32];
-        tmem_ld32_wait(o_addr + 32 * c, oo);
+        tmem_ld32_wait(o_addr + 32 * q, oo);
         if (row_ok) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int e = 0; e < 4; ++e) {
             uint4 w;
-            w.x = pack_f16x2(__uint_as_float(oo[8 * q]) * inv_l, __uint_as_float(oo[8 * q + 1]) * inv_l);
-            w.y = pack_f16x2(__uint_as_float(oo[8 * q + 2]) * inv_l, __uint_as_float(oo[8 * q + 3]) * inv_l);
-            w.z = pack_f16x2(__uint_as_float(oo[8 * q + 4]) * inv_l, __uint_as_float(oo[8 * q + 5]) * inv_l);
-            w.w = pack_f16x2(__uint_as_float(oo[8 * q + 6]) * inv_l, __uint_as_float(oo[8 * q + 7]) * inv_l);
-            reinterpret_cast<uint4*>(dst + 32 * c)[q] = w;
+            w.x = pack_f16x2(__uint_as_float(oo[8 * e]) * inv_l, __uint_as_float(oo[8 * e + 1]) * inv_l);
+            w.y = pack_f16x2(__uint_as_float(oo[8 * e + 2]) * inv_l, __uint_as_float(oo[8 * e + 3]) * inv_l);
+            w.z = pack_f16x2(__uint_as_float(oo[8 * e + 4]) * inv_l, __uint_as_float(oo[8 * e + 5]) * inv_l);
+            w.w = pack_f16x2(__uint_as_float(oo[8 * e + 6]) * inv_l, __uint_as_float(oo[8 * e + 7]) * inv_l);
+            reinterpret_cast<uint4*>(dst + 32 * q)[e] = w;
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(&o_free[x]);
+      c += I.n_kv;
+      vcount += I.n_kv;
     }
   }
 
@@ -545,7 +624,9 @@ static qwen_status launch_dh(const CUtensorMap& q, const CUtensorMap& k, const C
   }
   const int n_qt = (a.T + kQT - 1) / kQT;
   const int npair = (a.Hq / a.Hkv + 1) / 2;
-  const int grid = n_qt * a.B * a.Hkv * npair;
+  const long long items = (long long)n_qt * a.B * a.Hkv * npair;
+  const int sms = device_sm_count();
+  const int grid = items < sms ? (int)items : sms;  // persistent: one CTA per SM
   launch_k(kern, dim3(grid), dim3(kAttnThreads), AttnCfg<DH>::SMEM_BYTES, st, q, k, v, k16, v16,
            a);
   count_launches();

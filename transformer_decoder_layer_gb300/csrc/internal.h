@@ -29,8 +29,8 @@ struct QkvParams {
   const float2* rope;      // [max_position][dh/2] (cos, sin)
   const int32_t* positions;  // [M]
   const int32_t* slot0;      // [B]: cache slot of the sequence's first new token
-  void* q_out;             // [B][Hq][T][dh], FP16 when q_f16 else BF16
-  int q_f16;
+  void* q_out;             // [B][Hq][T][dh], BF16, or with q_f16 FP16 for the
+  int q_f16;               // sequences with slot0[b] == 0 (BF16 for the others)
   __nv_bfloat16* k_cache;  // [B][Hkv][max_seq][dh]
   __nv_bfloat16* v_cache;
   __half* k16;             // optional FP16 copies of this call's K/V rows,

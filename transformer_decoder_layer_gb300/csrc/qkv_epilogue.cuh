@@ -79,8 +79,11 @@ __device__ __forceinline__ void qkv_head_finish(float (&v)[DH], int m, int head,
     }
   };
   if (kind == 0) {
+    // prefill: FP16 when the sequence starts at slot 0 (every key is this
+    // call's, read from FP16 copies), BF16 when earlier keys come from the
+    // BF16 cache, so the attention's two operands always share a type
     store(static_cast<uint16_t*>(p.q_out) + (((size_t)b * p.Hq + head) * p.T + t) * DH,
-          p.q_f16 != 0);
+          p.q_f16 != 0 && p.slot0[b] == 0);
     return;
   }
   const int slot = p.slot0[b] + t;
