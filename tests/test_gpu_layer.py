@@ -91,6 +91,25 @@ def test_qwen25_style_bias_prefill():
     assert_parity(k, kr, what="K cache")
 
 
+def test_prefill_attention_mixed_work_items():
+    """7 query heads per KV group (three two-head items and one one-head item per
+    group and query tile), two sequences of 2560 tokens of which the second
+    continues a filled cache (BF16 operands): 320 attention work items dealt
+    over 152 SMs in alternating directions, so CTAs process one-head and
+    two-head items, fresh and cached, one after another."""
+    shape = synth.LayerConfig(d=896, n_q_heads=14, n_kv_heads=2, head_dim=128, ffn=1792,
+                              qkv_bias=1)
+    T = 2560
+    rng = np.random.default_rng(7)
+    rows = np.unique(np.r_[0, 127, 128, 1279, 1280, T - 129, T - 128, T - 1,
+                           rng.integers(0, T, 24)])
+    y, ref, k, kr, v, vr = _prefill_case(shape, "mixed_items", 2, T, cache_start=[0, 300],
+                                         prefilled=[0, 300], rows=rows)
+    assert_parity(y, ref, what="Y")
+    assert_parity(k, kr, what="K cache")
+    assert_parity(v, vr, what="V cache")
+
+
 @pytest.mark.parametrize("T", [1024, 4096])
 def test_qwen3_8b_layer_prefill_sampled_rows(T):
     """Qwen3-8B-shaped layer at full size, sampled output rows."""
