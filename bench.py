@@ -12,8 +12,8 @@ gate/up + SiLU*up, down + residual.  Inputs are resident in HBM; weights
 The same line carries: the B sweep (1, 8, 32, 64); prefill of a Qwen3-8B-shaped
 layer (tokens/s, TFLOP/s, per-kernel tensor roofline); `roofline` for the
 dominant decode kernel from CUDA events recorded around it inside the timed
-region; `e2e` through the C ABI with pinned host buffers copied in and out every
-step; `cpu_baseline` (the FP64 oracle on the host cores, a bounded sample);
+region; `e2e` through the C ABI's host-buffer decode call (qwen_layer_decode_host:
+pinned host inputs copied in and the output copied out every step); `cpu_baseline` (the FP64 oracle on the host cores, a bounded sample);
 `clocks` sampled with nvidia-smi during the timed region; `gpu_launches`
 counted by the library.
 
@@ -210,19 +210,18 @@ class DecodeBench:
         return total_ms, kern_ms, n_launch
 
     def e2e(self, steps, warmup):
-        """Through the C ABI with pinned host buffers copied in/out every step."""
+        """Through the C ABI's host-buffer decode call: every step copies x,
+        positions and cache lengths in from pinned host memory and y back out
+        (qwen_layer_decode_host), steps enqueued back to back."""
         torch = self.torch
         xh = self.x_cpu.pin_memory()
         ph = torch.full((self.B,), CACHE_FILLED, dtype=torch.int32).pin_memory()
         ch = torch.full((self.B,), CACHE_FILLED, dtype=torch.int32).pin_memory()
         yh = torch.empty((self.B, self.shape.d), dtype=torch.bfloat16).pin_memory()
+        ws = self.layer.host_workspace(self.B)
 
         def one():
-            self.x.copy_(xh, non_blocking=True)
-            self.pos.copy_(ph, non_blocking=True)
-            self.clen.copy_(ch, non_blocking=True)
-            self.step()
-            yh.copy_(self.y, non_blocking=True)
+            self.layer.decode_host(xh, ph, ch, self.kc, self.vc, yh, workspace=ws)
 
         for _ in range(warmup):
             one()

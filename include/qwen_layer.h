@@ -184,6 +184,24 @@ QWEN_API qwen_status qwen_layer_decode_ex(qwen_layer_t layer, const void* x, con
                                           void* k_cache, void* v_cache, void* workspace,
                                           size_t workspace_bytes, void* stream);
 
+/* One decode step with the inputs and the output in HOST memory (the call a
+ * serving loop makes): x_host (BF16 [B, d]), positions_host and
+ * cache_len_host (int32 [B]) in, y_host (BF16 [B, d]) out.  When all four are
+ * pinned host memory mapped for the device, the step's kernels read the inputs
+ * and write the output through the host link directly (no copies between
+ * kernels); otherwise the inputs are copied to staging space inside the
+ * workspace, the step runs, and y is copied back, all enqueued on `stream`.
+ * Nothing synchronises: the caller synchronises the stream before reading
+ * y_host or changing the host inputs.  The workspace must hold
+ * qwen_layer_host_workspace_bytes(cfg, B).  Errors as qwen_layer_decode, plus
+ * QWEN_ERR_CUDA if a copy cannot be enqueued. */
+QWEN_API size_t qwen_layer_host_workspace_bytes(const qwen_layer_config* cfg, int32_t B);
+QWEN_API qwen_status qwen_layer_decode_host(qwen_layer_t layer, const void* x_host, void* y_host,
+                                            int32_t B, const int32_t* positions_host,
+                                            const int32_t* cache_len_host, void* k_cache,
+                                            void* v_cache, void* workspace,
+                                            size_t workspace_bytes, void* stream);
+
 /* MoE block alone on T tokens: Y = R + sum_j w_j Expert_{idx_j}(Z)
  * [+ sigmoid(Z W_sg) SharedExpert(Z)],  Z = RMSNorm_2(R).
  *   r        [T, d] BF16 residual-stream input; y [T, d] BF16 output.

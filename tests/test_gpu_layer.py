@@ -201,3 +201,30 @@ def test_prefill_then_decode_matches_longer_prefill():
     yd = g.decode(x[:, T - 1].contiguous(), np.array([T - 1]), [T - 1], kc, vc)
     assert_parity(f64(yd.float())[0], f64(yf.float())[0, -1], what="decode vs prefill row")
     assert torch.equal(kc[:, :, :T - 1], kf[:, :, :T - 1])
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["mapped", "pageable"])
+def test_decode_from_host_buffers_matches_device_call(pinned):
+    """qwen_layer_decode_host gives the same bits as the device-buffer call,
+    with pinned host buffers (the kernels read and write them directly) and
+    with pageable ones (staged copies)."""
+    shape = synth.TINY
+    B, L = 5, 300
+    w_cpu = synth.layer_weights(shape, "dhost")
+    x = synth.activations([B, shape.d], "dhost")
+    kc, vc = synth.kv_cache(B, shape.n_kv_heads, L + 1, shape.head_dim, L, "dhost")
+    g = GpuLayer(shape, w_cpu, max_tokens=B, max_batch=B, max_seq=L + 1, max_position=L + 1)
+    lens = np.array([L, 7, 150, L, 1], dtype=np.int32)
+    k1, v1 = kc.cuda(), vc.cuda()
+    y_dev = g.decode(x, lens, lens, k1, v1)
+    k2, v2 = kc.cuda(), vc.cuda()
+    xh = x.contiguous().clone()
+    lh = torch.from_numpy(lens).clone()
+    yh = torch.empty_like(xh)
+    if pinned:
+        xh, lh, yh = xh.pin_memory(), lh.pin_memory(), yh.pin_memory()
+    g.layer.decode_host(xh, lh, lh, k2, v2, yh)
+    torch.cuda.synchronize()
+    assert g.layer.poll_error() == 0
+    assert torch.equal(yh, y_dev.cpu())
+    assert torch.equal(k1, k2) and torch.equal(v1, v2)

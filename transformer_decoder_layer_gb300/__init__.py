@@ -69,6 +69,9 @@ _SIGS = {
                                              _VP, _VP, _SZ, _VP]),
     "qwen_layer_decode_ex": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _VP,
                                             _VP, _SZ, _VP]),
+    "qwen_layer_host_workspace_bytes": (_SZ, [ctypes.POINTER(_Config), _I32]),
+    "qwen_layer_decode_host": (ctypes.c_int, [_VP, _VP, _VP, _I32, _VP, _VP, _VP, _VP, _VP,
+                                              _SZ, _VP]),
     "qwen_moe_ffn": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I32, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "qwen_head_workspace_bytes": (_SZ, [_I32, _I32, _I32]),
     "qwen_head_last_token": (ctypes.c_int, [_VP, _I32, _I32, _I32, _VP, _VP, _I32, _F32, _VP,
@@ -319,6 +322,34 @@ class Layer:
                                           _ptr(k_cache), _ptr(v_cache), _ptr(ws), ws.numel(),
                                           _stream(stream)), "qwen_layer_decode")
         return out if out is not None else out32
+
+    def host_workspace(self, B, device="cuda"):
+        """Workspace for decode_host (the decode workspace plus host staging)."""
+        import torch
+        n = lib().qwen_layer_host_workspace_bytes(ctypes.byref(self.cfg.c), B)
+        return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+    def decode_host(self, x_host, positions_host, cache_len_host, k_cache, v_cache, y_host,
+                    workspace=None, stream=None):
+        """One decode step from host buffers: x_host [B, d] BF16, positions_host and
+        cache_len_host [B] int32 (CPU tensors, pinned for asynchronous copies);
+        the output lands in y_host [B, d] BF16 once the stream is synchronised."""
+        import torch
+        for n, t in (("x_host", x_host), ("positions_host", positions_host),
+                     ("cache_len_host", cache_len_host), ("y_host", y_host)):
+            if t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{n} must be a contiguous host tensor")
+        if x_host.dtype != torch.bfloat16 or y_host.dtype != torch.bfloat16:
+            raise ValueError("x_host and y_host must be bfloat16")
+        if positions_host.dtype != torch.int32 or cache_len_host.dtype != torch.int32:
+            raise ValueError("positions_host and cache_len_host must be int32")
+        B = x_host.shape[0]
+        ws = self.host_workspace(B) if workspace is None else workspace
+        _check(lib().qwen_layer_decode_host(self.handle, _ptr(x_host), _ptr(y_host), B,
+                                            _ptr(positions_host), _ptr(cache_len_host),
+                                            _ptr(k_cache), _ptr(v_cache), _ptr(ws), ws.numel(),
+                                            _stream(stream)), "qwen_layer_decode_host")
+        return y_host
 
     def moe_ffn(self, r, r_fp32=None, out=None, topk_idx=None, topk_w=None, logits=None,
                 workspace=None, stream=None):

@@ -429,6 +429,71 @@ qwen_status qwen_layer_decode(qwen_layer_t layer, const void* x, void* y, int32_
                               v_cache, workspace, workspace_bytes, stream);
 }
 
+// Device address of host memory the GPU can access (pinned and mapped), else
+// nullptr.
+static const void* host_device_view(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the query's error
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// Host staging for qwen_layer_decode_host, after the decode workspace: x, y
+// (BF16 [B][d]) and positions, cache lengths (int32 [B]).
+size_t qwen_layer_host_workspace_bytes(const qwen_layer_config* cfg, int32_t B) {
+  if (!cfg || !config_valid(*cfg) || B <= 0) return 0;
+  const size_t act = align256((size_t)B * cfg->d * 2), idx = align256((size_t)B * 4);
+  return align256(workspace_layout(*cfg, B, 1).total) + 2 * act + 2 * idx;
+}
+
+qwen_status qwen_layer_decode_host(qwen_layer_t layer, const void* x_host, void* y_host,
+                                   int32_t B, const int32_t* positions_host,
+                                   const int32_t* cache_len_host, void* k_cache, void* v_cache,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  if (!layer) return QWEN_ERR_INVALID_ARG;
+  const qwen_layer_config& c = layer->cfg;
+  if (B < 0) return QWEN_ERR_INVALID_ARG;
+  if (B == 0) return QWEN_OK;
+  if (!x_host || !y_host || !positions_host || !cache_len_host || !workspace)
+    return QWEN_ERR_INVALID_ARG;
+  if (B > c.max_batch || B > c.max_tokens) return QWEN_ERR_CAPACITY;
+  if (workspace_bytes < qwen_layer_host_workspace_bytes(&c, B)) return QWEN_ERR_CAPACITY;
+  // Host memory the GPU can address (pinned and mapped): the kernels read the
+  // inputs and write the output over the host link themselves, so no copy
+  // sits between the step's kernels.  Otherwise: staged copies.
+  const void* xv = host_device_view(x_host);
+  const void* pv = host_device_view(positions_host);
+  const void* lv = host_device_view(cache_len_host);
+  void* yv = const_cast<void*>(host_device_view(y_host));
+  if (xv && pv && lv && yv)
+    return qwen_layer_decode_ex(layer, xv, nullptr, yv, nullptr, B,
+                                static_cast<const int32_t*>(pv), static_cast<const int32_t*>(lv),
+                                k_cache, v_cache, workspace, workspace_bytes, stream);
+  const size_t act = (size_t)B * c.d * 2, idx = (size_t)B * 4;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  size_t o = align256(workspace_layout(c, B, 1).total);
+  void* xd = ws + o;
+  o += align256(act);
+  void* yd = ws + o;
+  o += align256(act);
+  int32_t* pd = reinterpret_cast<int32_t*>(ws + o);
+  o += align256(idx);
+  int32_t* ld = reinterpret_cast<int32_t*>(ws + o);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(xd, x_host, act, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(pd, positions_host, idx, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(ld, cache_len_host, idx, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return QWEN_ERR_CUDA;
+  const qwen_status s = qwen_layer_decode_ex(layer, xd, nullptr, yd, nullptr, B, pd, ld, k_cache,
+                                             v_cache, workspace, workspace_bytes, stream);
+  if (s != QWEN_OK) return s;
+  return cudaMemcpyAsync(y_host, yd, act, cudaMemcpyDeviceToHost, st) == cudaSuccess
+             ? QWEN_OK
+             : QWEN_ERR_CUDA;
+}
+
 qwen_status qwen_moe_ffn(qwen_layer_t layer, const void* r, const float* r_fp32, void* y,
                          int32_t T, int32_t* topk_idx, float* topk_w, float* logits,
                          void* workspace, size_t workspace_bytes, void* stream) {
