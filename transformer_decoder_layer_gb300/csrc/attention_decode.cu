@@ -11,14 +11,19 @@
 // swizzle) through a 4-stage ring; the tiny contraction runs on mma.sync
 // (m16n8k16, BF16 -> FP32) with the group's heads as the 16 rows.
 //
-// Work unit = (sequence b, KV head g, split sp): the sequence's 64-key blocks
-// are divided evenly among `splits` units.  A persistent CTA walks its units;
+// Work split (stream-K style): the (sequence, KV head) pairs' 64-key blocks are
+// laid end to end, each pair taking nbv = ceil(max_seq / 64) places, and CTA c
+// takes the contiguous range [c * per, (c + 1) * per): every CTA gets the same
+// number of blocks, its range covering the end of one pair and the start of
+// the next.  A work unit = the part of one pair inside one CTA's range (blocks
+// past the sequence's length are skipped); it writes its partial to slot
+// c - (first CTA of the pair).  A persistent CTA walks its units;
 // the producer warp streams each unit's query rows (bulk copy) and K/V blocks
 // (TMA) through rings of equal depth, so it can run ahead across unit
 // boundaries.  4 compute warps each take 16 keys of every block and keep their
 // own running max / sum / O; the warps merge through shared memory and the
 // unit's unnormalised partial (m, l, O) goes to a workspace.  A merge kernel
-// combines the splits of each head in a fixed order (deterministic).
+// combines the slots of each head in a fixed order (deterministic).
 #include <cmath>
 
 #include "common.cuh"
@@ -84,10 +89,11 @@ struct DecAttnCfg {
 struct DecAttnArgs {
   const bf16* q;  // [B][Hq][DH]
   const int32_t* cache_len;
-  int B, Hq, Hkv, max_seq, splits;
+  int B, Hq, Hkv, max_seq;
+  int nbv, per, slots;  // key blocks per pair, blocks per CTA, partial slots per pair
   float scale_log2;
-  float* part_o;   // [B*Hq][splits][DH]
-  float* part_ml;  // [B*Hq][splits][2]
+  float* part_o;   // [B*Hq][slots][DH]
+  float* part_ml;  // [B*Hq][slots][2]
   int* err;
 };
 
@@ -115,7 +121,25 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = a.Hq / a.Hkv;
-  const int units = a.B * a.Hkv * a.splits;
+  // this CTA's lu-th unit: pair, key range [k0, k1) (empty when the range lies
+  // past the sequence's length) and partial slot; false when there is none
+  const long long v_end = (long long)a.B * a.Hkv * a.nbv;
+  const long long v0 = (long long)blockIdx.x * a.per;
+  const long long v1 = v0 + a.per < v_end ? v0 + a.per : v_end;
+  auto unit_of = [&](int lu, int& pair, int& k0, int& k1, int& slot, int& n_keys) -> bool {
+    const long long p = v0 / a.nbv + lu;
+    if (p * a.nbv >= v1) return false;
+    pair = (int)p;
+    const long long lo = (v0 > p * a.nbv ? v0 : p * a.nbv) - p * a.nbv;
+    const long long hi = (v1 < (p + 1) * a.nbv ? v1 : (p + 1) * a.nbv) - p * a.nbv;
+    const int b = pair / a.Hkv;
+    // the new token sits in slot cache_len[b]: keys 0..cache_len[b] (clamped to the cache)
+    n_keys = min((b < DecAttnCfg<DH>::LEN_SLOTS ? s_len[b] : a.cache_len[b]) + 1, a.max_seq);
+    k0 = (int)lo * kKB;
+    k1 = min((int)hi * kKB, n_keys);
+    slot = (int)blockIdx.x - (int)((p * a.nbv) / a.per);
+    return true;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kDStages; ++s) {
@@ -148,14 +172,9 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
       const uint64_t pol = l2_evict_first();
       int stage = 0;
       uint32_t phase = 0;
-      int lu = 0;  // local unit counter
-      for (int u = blockIdx.x; u < units; u += gridDim.x, ++lu) {
-        const int pair = u / a.splits, sp = u - pair * a.splits;
+      int pair, k0, k1, slot, n_keys;
+      for (int lu = 0; unit_of(lu, pair, k0, k1, slot, n_keys); ++lu) {
         const int b = pair / a.Hkv, g = pair - b * a.Hkv;
-        const int n_keys = min((b < C::LEN_SLOTS ? s_len[b] : a.cache_len[b]) + 1, a.max_seq);
-        const int nb = (n_keys + kKB - 1) / kKB;
-        const int k0 = kKB * (int)((long long)sp * nb / a.splits);
-        const int k1 = min(kKB * (int)((long long)(sp + 1) * nb / a.splits), n_keys);
         const int row0 = pair * a.max_seq;  // (b * Hkv + g) * max_seq
         // the unit's G query rows (contiguous in q) into its slot of the Q ring
         const int qs = lu % kDStages;
@@ -197,16 +216,10 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
   int stage = 0;
   uint32_t phase = 0;
   const uint32_t smem_base = smem_u32(smem);
-  int lu = 0;
-  for (int u = blockIdx.x; u < units; u += gridDim.x, ++lu) {
-    const int pair = u / a.splits, sp = u - pair * a.splits;
+  int pair, k0, k1, slot, n_keys;
+  for (int lu = 0; unit_of(lu, pair, k0, k1, slot, n_keys); ++lu) {
     const int b = pair / a.Hkv, g = pair - b * a.Hkv;
-    // the new token sits in slot cache_len[b]: keys 0..cache_len[b] (clamped to the cache)
-    const int n_keys = min((b < C::LEN_SLOTS ? s_len[b] : a.cache_len[b]) + 1, a.max_seq);
     const int L = n_keys - 1;  // last visible key
-    const int nb = (n_keys + kKB - 1) / kKB;
-    const int k0 = kKB * (int)((long long)sp * nb / a.splits);
-    const int k1 = min(kKB * (int)((long long)(sp + 1) * nb / a.splits), n_keys);
     const int h0 = g * G;
     // Q fragments (rows = heads of the group, zero beyond G) from the slot the
     // producer filled.  The slot is released at the end of the unit: only then
@@ -389,7 +402,7 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
 #pragma unroll
       for (int w = 0; w < kCW; ++w) acc += wr[rI][w] * buf[w * C::FRAG_FLOATS + i * 32 + lane];
       if (row < G) {
-        const size_t ph = (size_t)(b * a.Hq + h0 + row) * a.splits + sp;
+        const size_t ph = (size_t)(b * a.Hq + h0 + row) * a.slots + slot;
         a.part_o[ph * DH + col] = acc;
       }
     }
@@ -398,7 +411,7 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
       for (int rI = 0; rI < 2; ++rI) {
         const int row = gid + 8 * rI;
         if (row < G) {
-          const size_t ph = (size_t)(b * a.Hq + h0 + row) * a.splits + sp;
+          const size_t ph = (size_t)(b * a.Hq + h0 + row) * a.slots + slot;
           a.part_ml[ph * 2] = Mr[rI];
           a.part_ml[ph * 2 + 1] = Lr[rI];
         }
@@ -407,19 +420,23 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
   }
 }
 
-// out[b][h*DH + d] = sum_s 2^(m_s - M) o_s[d] / sum_s 2^(m_s - M) l_s
+// out[b][h*DH + d] = sum_s 2^(m_s - M) o_s[d] / sum_s 2^(m_s - M) l_s over the
+// slots s that CTAs wrote for head h's (sequence, KV head) pair: the CTAs whose
+// block ranges meet the pair's [p * nbv, (p + 1) * nbv)
 template <int DH>
 __global__ void attn_decode_merge_kernel(const float* __restrict__ part_o,
-                                         const float* __restrict__ part_ml, int BH, int splits,
-                                         f16* __restrict__ out) {
+                                         const float* __restrict__ part_ml, int BH, int slots,
+                                         int G, int nbv, int per, f16* __restrict__ out) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ float merge_f[];  // [warps][splits]: the weight of each split
+  extern __shared__ float merge_f[];  // [warps][slots]: the weight of each slot
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= BH) return;
-  float* fs = merge_f + (threadIdx.x >> 5) * splits;
-  const float* ml = part_ml + (size_t)wid * splits * 2;
+  const long long pair = wid / G;  // (b * Hq + h) / G = b * Hkv + h / G
+  const int splits = (int)(((pair + 1) * nbv - 1) / per - (pair * nbv) / per) + 1;
+  float* fs = merge_f + (threadIdx.x >> 5) * slots;
+  const float* ml = part_ml + (size_t)wid * slots * 2;
   // the lanes share the splits for the global max and the row sum
   float mloc = -INFINITY;
   for (int s = lane; s < splits; s += 32) mloc = fmaxf(mloc, ml[2 * s]);
@@ -436,7 +453,7 @@ __global__ void attn_decode_merge_kernel(const float* __restrict__ part_o,
   float acc[DH / 32];
 #pragma unroll
   for (int i = 0; i < DH / 32; ++i) acc[i] = 0.f;
-  const float* po = part_o + (size_t)wid * splits * DH + lane;
+  const float* po = part_o + (size_t)wid * slots * DH + lane;
 #pragma unroll 4
   for (int s = 0; s < splits; ++s) {
     const float f = fs[s];
@@ -478,34 +495,30 @@ static bool tmap_cache(CUtensorMap* m, const void* base, uint64_t rows, int dh) 
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Splits per (sequence, KV head): at least enough units to give every SM one
-// (measured: B=32 with 128 (sequence, KV head) pairs ran 4 us faster with 2
-// splits on all 152 SMs than with 1 split on 128), then the smallest estimated
-// makespan ceil(units / CTAs) * (blocks per unit + per-unit overhead), with one
-// block-equivalent of overhead per unit (query fetch, warp merge, partials).
+// The stream-K split: pairs x nbv blocks over the SMs, `per` blocks per CTA;
+// a pair meets at most (nbv - 1) / per + 2 CTA ranges, its partial slots.
+struct AttnSplit {
+  int nbv, per, slots, grid;
+};
+
+static AttnSplit attn_split(int B, int Hkv, int max_seq) {
+  AttnSplit sp;
+  const long long sms = device_sm_count();
+  sp.nbv = (max_seq + kKB - 1) / kKB;
+  const long long total = (long long)B * Hkv * sp.nbv;
+  sp.per = (int)((total + sms - 1) / sms);
+  sp.grid = (int)((total + sp.per - 1) / sp.per);
+  sp.slots = (sp.nbv - 1) / sp.per + 2;
+  return sp;
+}
+
 void decode_attn_plan(const qwen_layer_config& c, int B, int* splits) {
-  const int sms = device_sm_count();
-  const long long pairs = (long long)B * c.n_kv_heads;
-  const int nb = (c.max_seq + kKB - 1) / kKB;
-  long long s_fill = (sms + pairs - 1) / pairs;
-  if (s_fill > nb) s_fill = nb;
-  if (s_fill > 256) s_fill = 256;
-  int best = (int)s_fill;
-  double best_t = 1e30;
-  for (int s = (int)s_fill; s <= nb && s <= 256; ++s) {
-    const double per_cta = std::ceil((double)(pairs * s) / sms);
-    const double t = per_cta * ((double)nb / s + 1.0);
-    if (t < best_t - 1e-9) {
-      best_t = t;
-      best = s;
-    }
-  }
-  *splits = best;
+  *splits = attn_split(B, c.n_kv_heads, c.max_seq).slots;
 }
 
 template <int DH>
 static qwen_status launch_attn_dec(const CUtensorMap& tk, const CUtensorMap& tv,
-                                   const DecAttnArgs& a, f16* out, cudaStream_t st) {
+                                   const DecAttnArgs& a, int grid, f16* out, cudaStream_t st) {
   auto kern = attn_decode_kernel<DH>;
   static bool attr = false;
   if (!attr) {
@@ -514,16 +527,14 @@ static qwen_status launch_attn_dec(const CUtensorMap& tk, const CUtensorMap& tv,
       return QWEN_ERR_CUDA;
     attr = true;
   }
-  const int units = a.B * a.Hkv * a.splits;
-  const int sms = device_sm_count();
-  const int grid = units < sms ? units : sms;
   launch_k(kern, dim3(grid), dim3(kDecAttnThreads), DecAttnCfg<DH>::SMEM_BYTES, st, tk, tv, a);
   count_launches();
   if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;
   const int BH = a.B * a.Hq;
   launch_k(attn_decode_merge_kernel<DH>, dim3((BH * 32 + 255) / 256), dim3(256),
-           (size_t)(256 / 32) * a.splits * sizeof(float), st,
-           (const float*)a.part_o, (const float*)a.part_ml, BH, a.splits, out);
+           (size_t)(256 / 32) * a.slots * sizeof(float), st,
+           (const float*)a.part_o, (const float*)a.part_ml, BH, a.slots, a.Hq / a.Hkv, a.nbv,
+           a.per, out);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
@@ -533,7 +544,9 @@ qwen_status attention_decode(const bf16* q, const bf16* kc, const bf16* vc,
                              int splits, float* part_o, float* part_ml, f16* out,
                              int* err, cudaStream_t st) {
   if (B == 0) return QWEN_OK;
-  if (Hq / Hkv > 16 || splits < 1) return QWEN_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16) return QWEN_ERR_UNSUPPORTED;
+  const AttnSplit sp = attn_split(B, Hkv, max_seq);
+  if (splits < sp.slots) return QWEN_ERR_CAPACITY;  // partial space sized for fewer slots
   CUtensorMap tk, tv;
   if (!tmap_cache(&tk, kc, (uint64_t)B * Hkv * max_seq, dh)) return QWEN_ERR_CUDA;
   if (!tmap_cache(&tv, vc, (uint64_t)B * Hkv * max_seq, dh)) return QWEN_ERR_CUDA;
@@ -544,13 +557,15 @@ qwen_status attention_decode(const bf16* q, const bf16* kc, const bf16* vc,
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.max_seq = max_seq;
-  a.splits = splits;
+  a.nbv = sp.nbv;
+  a.per = sp.per;
+  a.slots = sp.slots;
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)dh);
   a.part_o = part_o;
   a.part_ml = part_ml;
   a.err = err;
-  if (dh == 128) return launch_attn_dec<128>(tk, tv, a, out, st);
-  if (dh == 64) return launch_attn_dec<64>(tk, tv, a, out, st);
+  if (dh == 128) return launch_attn_dec<128>(tk, tv, a, sp.grid, out, st);
+  if (dh == 64) return launch_attn_dec<64>(tk, tv, a, sp.grid, out, st);
   return QWEN_ERR_UNSUPPORTED;
 }
 
