@@ -61,6 +61,8 @@ struct GemmEpilogue {
   // B is a packed layer weight in the blocked layout (128 x 64 tiles, each
   // group's rows padded to a multiple of 128); else row-major with row stride ldb.
   int b_blocked;
+  // Set by gemm_tc (dense mode): tiles from split_from on are 128 wide.
+  int split_tail, split_from;
 };
 
 int device_sm_count();
