@@ -38,6 +38,7 @@ def test_rmsnorm_matches_oracle(q, rows, d):
     (300, 520, 1000),     # ragged M, N and K tails
     (1024, 6144, 4096),   # many tiles, grouped raster
     (257, 768, 512),      # tiny-layer QKV width
+    (2000, 1800, 1000),   # 2-CTA pair tiles: ragged M, N and K; the last B half lies past N
 ])
 def test_linear_matches_oracle(q, M, N, K):
     x = synth.activations([M, K], "lin", f"x{M}_{K}")

@@ -107,6 +107,14 @@ def test_moe_ffn_shared_expert_without_renormalisation():
         assert_parity(y, no_shared, what="Qwen2-MoE Y without the shared expert")
 
 
+def test_moe_ffn_pair_tiles():
+    """T=2000 over 16 experts (about 500 routed rows each): the grouped expert
+    GEMMs take 256-row tiles on 2-CTA pairs, ragged at every group's end."""
+    y, ref, gi, gw, glog, logits, oidx, owts, gap = _run_moe_ffn(SMALL_MOE, "moe_pair", 2000)
+    _check_routing(gi, gw, glog, logits, oidx, owts, gap)
+    assert_parity(y, ref, what="MoE Y (pair tiles)")
+
+
 def test_moe_ffn_fp32_residual_input():
     y, ref, gi, gw, glog, logits, oidx, owts, gap = _run_moe_ffn(SMALL_MOE, "moe_s32", 77,
                                                                  fp32_input=True)

@@ -26,11 +26,16 @@ constexpr int kBK = 64;  // 64 bf16 = 128 bytes = one swizzle row
 constexpr int kGemmThreads = 192;
 constexpr int kGroupM = 16;  // raster: 16 m-blocks share a sweep over n
 
-template <int BN>
+// PAIR: a 2-CTA cluster computes a 256 x BN tile with cta_group::2 MMAs; each
+// CTA stages 128 rows of A and BN/2 rows of B per k-block, so a 256 x 256 x 64
+// step moves 32 KB into each SM per 512 MMA cycles instead of 48 KB (the
+// per-SM TMA ingress, about 57-76 bytes per cycle, bounds 1-SM 128 x 256 tiles).
+template <int BN, bool PAIR = false>
 struct GemmCfg {
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int STAGES = PAIR ? 6 : (BN == 256 ? 4 : 6);
+  static constexpr int TILE_M = PAIR ? 2 * kBM : kBM;  // output rows per tile
   static constexpr int A_BYTES = kBM * kBK * 2;
-  static constexpr int B_BYTES = BN * kBK * 2;
+  static constexpr int B_BYTES = (PAIR ? BN / 2 : BN) * kBK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;  // two accumulators
   static constexpr int SMEM_BYTES = 1024 /*align slack*/ + STAGES * STAGE_BYTES + 256 + 1024;
@@ -51,9 +56,9 @@ struct TileInfo {
 // twice as many SMs: tile split_from + 2 i + h is half h of tile split_from + i.
 __device__ __forceinline__ bool get_tile(int tile, int M, int N, int BN, int n_nblk,
                                          const GemmEpilogue& epi, const int* s_tile_prefix,
-                                         TileInfo& ti) {
+                                         TileInfo& ti, int bm = kBM) {
   if (epi.group_offsets == nullptr) {
-    const int n_mblk = (M + kBM - 1) / kBM;
+    const int n_mblk = (M + bm - 1) / bm;
     int half = -1;
     ti.bw = BN;
     if (epi.split_tail && tile >= epi.split_from) {
@@ -70,7 +75,7 @@ __device__ __forceinline__ bool get_tile(int tile, int M, int N, int BN, int n_n
     const int r = tile - g * per_group;
     const int mb = first_m + r % gm;
     const int nb = r / gm;
-    ti.m0 = mb * kBM;
+    ti.m0 = mb * bm;
     ti.n0 = nb * BN + (half > 0 ? 128 : 0);
     ti.row_end = M;
     ti.b_row0 = ti.n0;
@@ -89,7 +94,7 @@ __device__ __forceinline__ bool get_tile(int tile, int M, int N, int BN, int n_n
   }
   const int g = lo;
   const int row_begin = epi.group_offsets[g];
-  ti.m0 = row_begin + (mt - s_tile_prefix[g]) * kBM;
+  ti.m0 = row_begin + (mt - s_tile_prefix[g]) * bm;
   ti.row_end = epi.group_offsets[g + 1];
   ti.n0 = nb * BN;
   ti.b_row0 = g * N + ti.n0;
@@ -267,12 +272,12 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, bool row_
   }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmBh, int M, int N, int K, uint32_t idesc,
                    uint32_t idesc_half, GemmEpilogue epi, int* err) {
-  using C = GemmCfg<BN>;
+  using C = GemmCfg<BN, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -282,7 +287,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* empty = full + C::STAGES;
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_tile_prefix = reinterpret_cast<int*>(tmem_slot + 4);  // up to 256 groups
 
@@ -291,6 +297,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int lane = threadIdx.x & 31;
   const int n_nblk = (N + BN - 1) / BN;
   const int n_kblk = (K + kBK - 1) / kBK;
+  // pair mode: both CTAs of a cluster walk the same tiles; rank 0 issues the MMAs
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int n_units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     if (epi.group_offsets) pdl_wait();  // the group offsets come from the previous kernel
@@ -300,15 +310,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], PAIR ? 256 : 128);  // the epilogue threads of both CTAs
     }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     if (epi.group_offsets) {
       int acc = 0;
       for (int g = 0; g < epi.n_groups; ++g) {
         s_tile_prefix[g] = acc;
         const int rows = epi.group_offsets[g + 1] - epi.group_offsets[g];
-        acc += (rows + kBM - 1) / kBM;
+        acc += (rows + C::TILE_M - 1) / C::TILE_M;
       }
       s_tile_prefix[epi.n_groups] = acc;
     }
@@ -317,29 +328,54 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (epi.split_tail) tma_prefetch_desc(&tmBh);
+    if (epi.split_tail || PAIR) tma_prefetch_desc(&tmBh);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, C::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA signal
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   // B tile of k-block kb: row-major [N, K] (2-D map, rows from b_row0) or the
   // blocked layout of packed weights (4-D map, 128 x 64 tiles from b_tile);
-  // tmB carries a whole BN-row tile, tmBh the 128 rows of a split-tail tile
+  // tmB carries a whole BN-row tile, tmBh 128 rows (a split-tail tile, or this
+  // CTA's half of B in pair mode)
   auto load_b = [&](uint8_t* dst, uint64_t* bar, int kb, const TileInfo& t) {
-    const CUtensorMap* m = t.bw == BN ? &tmB : &tmBh;
-    if (epi.b_blocked)
-      tma_load_4d_w(dst, m, bar, 0, 0, kb, t.b_tile);
-    else
-      tma_load_2d_w(dst, m, bar, kb * kBK, t.b_row0);
+    if constexpr (PAIR) {
+      const uint32_t bar0 = cluster_addr(bar, 0);
+      if (epi.b_blocked)
+        tma_load_4d_pair_w(dst, &tmBh, bar0, 0, 0, kb, t.b_tile + rank);
+      else
+        tma_load_2d_pair_w(dst, &tmBh, bar0, kb * kBK, t.b_row0 + rank * (BN / 2));
+    } else {
+      const CUtensorMap* m = t.bw == BN ? &tmB : &tmBh;
+      if (epi.b_blocked)
+        tma_load_4d_w(dst, m, bar, 0, 0, kb, t.b_tile);
+      else
+        tma_load_2d_w(dst, m, bar, kb * kBK, t.b_row0);
+    }
   };
+  auto load_a = [&](uint8_t* dst, uint64_t* bar, int kb, const TileInfo& t) {
+    if constexpr (PAIR)
+      tma_load_2d_pair_w(dst, &tmA, cluster_addr(bar, 0), kb * kBK, t.m0 + rank * kBM);
+    else
+      tma_load_2d_w(dst, &tmA, bar, kb * kBK, t.m0);
+  };
+  // bytes the stage's barrier waits for (in pair mode: rank 0's barrier, both CTAs' tiles)
   auto stage_bytes = [&](const TileInfo& t) -> uint32_t {
-    return (uint32_t)(C::A_BYTES + t.bw * kBK * 2);
+    return PAIR ? (uint32_t)(2 * (C::A_BYTES + C::B_BYTES))
+                : (uint32_t)(C::A_BYTES + t.bw * kBK * 2);
   };
 
   // warps 0 and 1 run converged and issue from one elected lane (a lone lane
@@ -350,10 +386,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int pre = 0;
       TileInfo ti;
       if (epi.b_static && !epi.group_offsets &&
-          get_tile(blockIdx.x, M, N, BN, n_nblk, epi, s_tile_prefix, ti)) {
+          get_tile(unit, M, N, BN, n_nblk, epi, s_tile_prefix, ti, C::TILE_M)) {
         pre = min(C::STAGES, n_kblk);
         for (int i = 0; i < pre; ++i) {
-          mbar_arrive_expect_tx_w(&full[i], stage_bytes(ti));
+          if (rank == 0) mbar_arrive_expect_tx_w(&full[i], stage_bytes(ti));
           load_b(sB + i * C::B_BYTES, &full[i], i, ti);
         }
       }
@@ -361,25 +397,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int g = 0;
-      for (int tile = blockIdx.x; get_tile(tile, M, N, BN, n_nblk, epi, s_tile_prefix, ti);
-           tile += gridDim.x) {
+      for (int tile = unit; get_tile(tile, M, N, BN, n_nblk, epi, s_tile_prefix, ti, C::TILE_M);
+           tile += n_units) {
         for (int kb = 0; kb < n_kblk; ++kb, ++g) {
-          if (g < pre) {
-            tma_load_2d_w(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * kBK, ti.m0);
-          } else {
+          if (g >= pre) {
             if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, err)) goto producer_done;
-            mbar_arrive_expect_tx_w(&full[stage], stage_bytes(ti));
-            tma_load_2d_w(sA + stage * C::A_BYTES, &tmA, &full[stage], kb * kBK, ti.m0);
+            if (rank == 0) mbar_arrive_expect_tx_w(&full[stage], stage_bytes(ti));
             load_b(sB + stage * C::B_BYTES, &full[stage], kb, ti);
           }
+          load_a(sA + stage * C::A_BYTES, &full[stage], kb, ti);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      // drain: wait until the MMA warp has consumed every stage we filled, so
-      // no TMA write is still in flight when the CTA exits
+      // drain: wait until the MMAs have consumed every stage we filled, so no
+      // TMA write is still in flight when the CTA exits
       for (int s = 0; s < C::STAGES; ++s) {
         if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, err)) break;
         if (++stage == C::STAGES) {
@@ -390,13 +424,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     producer_done:;
     }
   } else if (warp == 1) {
-    {
+    if (rank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       TileInfo ti;
-      for (int tile = blockIdx.x; get_tile(tile, M, N, BN, n_nblk, epi, s_tile_prefix, ti);
-           tile += gridDim.x, ++local) {
+      for (int tile = unit; get_tile(tile, M, N, BN, n_nblk, epi, s_tile_prefix, ti, C::TILE_M);
+           tile += n_units, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!mbar_wait_w(&tempty[acc], acc_phase ^ 1u, abort_flag, err)) break;
@@ -415,16 +449,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int k = 0; k < kBK / 16; ++k) {
             const uint64_t ad = smem_desc_sw128(a0 + 32 * k, 16, 1024);
             const uint64_t bd = smem_desc_sw128(b0 + 32 * k, 16, 1024);
-            umma_f16_w(d_tmem, ad, bd, ti.bw == BN ? idesc : idesc_half, (kb | k) != 0);
+            if constexpr (PAIR)
+              umma_f16_pair_w(d_tmem, ad, bd, idesc, (kb | k) != 0);
+            else
+              umma_f16_w(d_tmem, ad, bd, ti.bw == BN ? idesc : idesc_half, (kb | k) != 0);
           }
-          umma_commit_w(&empty[stage]);
+          if constexpr (PAIR)
+            umma_commit_pair_w(&empty[stage], 0x3);
+          else
+            umma_commit_w(&empty[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit_w(&tfull[acc]);
+        if constexpr (PAIR)
+          umma_commit_pair_w(&tfull[acc], 0x3);
+        else
+          umma_commit_w(&tfull[acc]);
+      }
+      if constexpr (PAIR) {
+        // the MMAs read the other CTA's shared memory: all of them have to be
+        // complete before that CTA may leave (also on an early exit)
+        umma_commit_pair_w(mma_done, 0x1);
+        __syncwarp();
+        if (!mbar_wait_drain(mma_done, 0, err)) *abort_flag = 1;
       }
     }
   } else {
@@ -432,25 +482,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int local = 0;
     TileInfo ti;
-    for (int tile = blockIdx.x; get_tile(tile, M, N, BN, n_nblk, epi, s_tile_prefix, ti);
-         tile += gridDim.x, ++local) {
+    const uint32_t tempty0 = PAIR ? cluster_addr(&tempty[0], 0) : 0u;
+    const uint32_t tempty1 = PAIR ? cluster_addr(&tempty[1], 0) : 0u;
+    for (int tile = unit; get_tile(tile, M, N, BN, n_nblk, epi, s_tile_prefix, ti, C::TILE_M);
+         tile += n_units, ++local) {
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, err)) break;
       tc_fence_after();
-      const int row = ti.m0 + q * 32 + lane;
+      const int row = ti.m0 + rank * kBM + q * 32 + lane;
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
       epilogue_tile<BN, EPI>(taddr, row, row < ti.row_end, ti.n0, N, epi, err, ti.bw);
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      if constexpr (PAIR)
+        mbar_arrive_cluster(acc ? tempty1 : tempty0);
+      else
+        mbar_arrive(&tempty[acc]);
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync_all();  // neither CTA leaves while the pair's MMAs may read it
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
@@ -505,22 +566,88 @@ static bool make_tmap_blocked(CUtensorMap* map, const void* base, uint64_t row_t
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int EPI>
+// 2-CTA clusters of the pair kernel that fit on the device at once (every
+// epilogue variant has the same shared memory and thread count); 0 if the
+// query fails, which keeps every GEMM on 1-SM tiles.
+static int pair_clusters() {
+  static int n = -1;
+  if (n < 0) {
+    n = 0;
+    auto kern = gemm_tc_kernel<256, EPI_STORE, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             GemmCfg<256, true>::SMEM_BYTES) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (device_sm_count() / 2));
+      cfg.blockDim = dim3(kGemmThreads);
+      cfg.dynamicSmemBytes = GemmCfg<256, true>::SMEM_BYTES;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int c = 0;
+      if (cudaOccupancyMaxActiveClusters(&c, kern, &cfg) == cudaSuccess && c > 0) n = c;
+    }
+    cudaGetLastError();  // a failed query leaves no sticky error behind
+  }
+  return n;
+}
+
+template <int BN, int EPI, bool PAIR>
 static qwen_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tbh,
                              int M, int N, int K, uint32_t idesc, uint32_t idesc_half,
-                             const GemmEpilogue& epi, int* err, int grid, cudaStream_t st) {
-  auto kern = gemm_tc_kernel<BN, EPI>;
+                             const GemmEpilogue& epi, int* err, int units, cudaStream_t st) {
+  auto kern = gemm_tc_kernel<BN, EPI, PAIR>;
+  using C = GemmCfg<BN, PAIR>;
   static bool attr_done = false;  // per template instance
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (PAIR) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             GemmCfg<BN>::SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+        cudaSuccess)
       return QWEN_ERR_CUDA;
     attr_done = true;
   }
-  launch_k(kern, dim3(grid), dim3(kGemmThreads), GemmCfg<BN>::SMEM_BYTES, st, ta, tb, tbh, M, N,
-           K, idesc, idesc_half, epi, err);
+  // persistent grid: co-resident CTAs (pair mode: clusters)
+  const int max_units = PAIR ? pair_clusters() : device_sm_count();
+  if (pdl_enabled()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  const int grid_units = units < max_units ? units : max_units;
+  cfg.gridDim = dim3((PAIR ? 2 : 1) * grid_units);
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tbh, M, N, K, idesc, idesc_half, epi, err) !=
+      cudaSuccess)
+    return QWEN_ERR_CUDA;
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
+}
+
+template <int EPI>
+static qwen_status launch_epi(bool pair, const CUtensorMap& ta, const CUtensorMap& tb,
+                              const CUtensorMap& tbh, int M, int N, int K, uint32_t idesc,
+                              uint32_t idesc_half, const GemmEpilogue& epi, int* err, int units,
+                              cudaStream_t st) {
+  return pair ? launch_bn<256, EPI, true>(ta, tb, tbh, M, N, K, idesc, idesc_half, epi, err, units,
+                                          st)
+              : launch_bn<256, EPI, false>(ta, tb, tbh, M, N, K, idesc, idesc_half, epi, err,
+                                           units, st);
 }
 
 qwen_status gemm_tc(const void* A, int lda, const void* B, int ldb, int M, int N, int K,
@@ -546,13 +673,20 @@ qwen_status gemm_tc(const void* A, int lda, const void* B, int ldb, int M, int N
              !make_tmap_16(&tbh, B, b_rows, (uint64_t)K, (uint64_t)ldb, 128, op_f16)) {
     return QWEN_ERR_CUDA;
   }
-  const uint32_t idesc = idesc_f32acc(kBM, BN, op_f16);
-  const uint32_t idesc_half = idesc_f32acc(kBM, 128, op_f16);
   const int sms = device_sm_count();
-  int grid;
   epi.split_tail = 0;
   epi.split_from = 0;
+  // 1-SM tiles (128 x 256) or pair tiles (256 x 256 on a 2-CTA cluster).  A
+  // 1-SM tile is bound by its SM's TMA ingress and took about 1.1x the time of
+  // a pair tile in measurements (T=4096 gate/up and down projections); the
+  // choice compares the two wave counts on that basis.
+  bool pair = false;
+  int grid;
   if (epi.group_offsets) {
+    // expert groups: the row count per group is only known on the device; a
+    // 256-row tile wastes more of a group's ragged last tile, which measured as
+    // a loss at 256 routed rows per expert on average and a gain at 512
+    pair = M >= 384 * epi.n_groups && pair_clusters() > 0;
     grid = sms;  // the number of tiles is only known on the device
   } else {
     // Wave quantisation: with T tiles on S SMs the last wave holds T mod S
@@ -563,28 +697,42 @@ qwen_status gemm_tc(const void* A, int lda, const void* B, int ldb, int M, int N
     const int tiles = ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
     const int full_waves = tiles / sms, rem = tiles - full_waves * sms;
     int units = tiles;
+    double t_one = full_waves + (rem > 0 ? 1.0 : 0.0);
     if (rem > 0) {
-      const double t_whole = full_waves + 1.0;
       const double t_split = full_waves + ((2 * rem + sms - 1) / sms) * (2.0 / 3.0);
-      if (t_split < 0.96 * t_whole) {
+      if (t_split < 0.96 * t_one) {
         epi.split_tail = 1;
         epi.split_from = full_waves * sms;
         units = epi.split_from + 2 * rem;
+        t_one = t_split;
       }
     }
     grid = units < sms ? units : sms;
+    const int clusters = M >= 2 * kBM ? pair_clusters() : 0;
+    if (clusters > 0) {
+      const int ptiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + BN - 1) / BN);
+      const int pwaves = (ptiles + clusters - 1) / clusters;
+      if (pwaves < 1.1 * t_one) {
+        pair = true;
+        epi.split_tail = 0;
+        epi.split_from = 0;
+        grid = ptiles;
+      }
+    }
   }
+  const uint32_t idesc = idesc_f32acc(pair ? 2 * kBM : kBM, BN, op_f16);
+  const uint32_t idesc_half = idesc_f32acc(kBM, 128, op_f16);
   switch (epi.mode) {
     case EPI_STORE:
-      return launch_bn<BN, EPI_STORE>(ta, tb, tbh, M, N, K, idesc, idesc_half, epi, err, grid, st);
+      return launch_epi<EPI_STORE>(pair, ta, tb, tbh, M, N, K, idesc, idesc_half, epi, err, grid, st);
     case EPI_RESID:
-      return launch_bn<BN, EPI_RESID>(ta, tb, tbh, M, N, K, idesc, idesc_half, epi, err, grid, st);
+      return launch_epi<EPI_RESID>(pair, ta, tb, tbh, M, N, K, idesc, idesc_half, epi, err, grid, st);
     case EPI_SWIGLU:
-      return launch_bn<BN, EPI_SWIGLU>(ta, tb, tbh, M, N, K, idesc, idesc_half, epi, err, grid, st);
+      return launch_epi<EPI_SWIGLU>(pair, ta, tb, tbh, M, N, K, idesc, idesc_half, epi, err, grid, st);
     case EPI_QKV:
-      return launch_bn<BN, EPI_QKV>(ta, tb, tbh, M, N, K, idesc, idesc_half, epi, err, grid, st);
+      return launch_epi<EPI_QKV>(pair, ta, tb, tbh, M, N, K, idesc, idesc_half, epi, err, grid, st);
     case EPI_F32:
-      return launch_bn<BN, EPI_F32>(ta, tb, tbh, M, N, K, idesc, idesc_half, epi, err, grid, st);
+      return launch_epi<EPI_F32>(pair, ta, tb, tbh, M, N, K, idesc, idesc_half, epi, err, grid, st);
     default: return QWEN_ERR_INVALID_ARG;
   }
 }
