@@ -53,6 +53,22 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Two FP32 values as one 64-bit operand of the packed f32x2 instructions (lo
+// in the low word).
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+// Two exponent arguments s0 c + n, s1 c + n by one packed FP32 FMA.
+__device__ __forceinline__ void fma_pair(float s0, float s1, uint64_t c2, uint64_t n2, float& x0,
+                                         float& x1) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(f32x2(s0, s1)), "l"(c2), "l"(n2));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(d));
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -476,18 +492,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           m_used = mx;
         }
         // P = 2^(s * scale - m), FP32 row sum, rounded to the operand type,
-        // stored in the 128-byte swizzle: 16-byte chunk q of row r sits at chunk
-        // q ^ (r & 7) of the row's 128-byte line.  Keys 0-63 are packed before
-        // the wait for the previous P.V (which still reads the buffer), keys
-        // 64-127 are stored as they are computed.
+        // stored in the 128-byte swizzle: 16-byte chunk q of row r sits at
+        // chunk q ^ (r & 7) of the row's 128-byte line.  Keys 0-63 are packed
+        // before the wait for the previous P.V (which still reads the buffer),
+        // keys 64-127 are stored as they are computed.  Arguments and sums of
+        // two keys at a time go through the packed FP32 FMA and add.
         const float neg_m = -m_used;
+        const uint64_t c2 = f32x2(a.scale_log2, a.scale_log2), n2 = f32x2(neg_m, neg_m);
+        uint64_t l2 = f32x2(0.f, 0.f);
+        auto p8 = [&](int k0, uint32_t (&w)[4]) {
+#pragma unroll
+          for (int e4 = 0; e4 < 4; ++e4) {
+            float x0, x1;
+            fma_pair(s[k0 + 2 * e4], s[k0 + 2 * e4 + 1], c2, n2, x0, x1);
+            const float p0 = ex2(x0), p1 = ex2(x1);
+            asm("add.rn.f32x2 %0, %0, %1;" : "+l"(l2) : "l"(f32x2(p0, p1)));
+            w[e4] = pack2(p0, p1, I.fresh);
+          }
+        };
         uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = ex2(fmaf(s[2 * i], a.scale_log2, neg_m));
-          const float p1 = ex2(fmaf(s[2 * i + 1], a.scale_log2, neg_m));
-          l_sum += p0 + p1;
-          pk[i] = pack2(p0, p1, I.fresh);
+        for (int q = 0; q < 8; ++q) {
+          uint32_t w[4];
+          p8(8 * q, w);
+#pragma unroll
+          for (int e4 = 0; e4 < 4; ++e4) pk[4 * q + e4] = w[e4];
         }
         if (j > 0) {
           // O_x += P_x(j-1) V must be done: it reads the P buffer, and O is
@@ -503,16 +532,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           uint32_t w[4];
-#pragma unroll
-          for (int e4 = 0; e4 < 4; ++e4) {
-            const int e = 64 + 8 * q + 2 * e4;
-            const float p0 = ex2(fmaf(s[e], a.scale_log2, neg_m));
-            const float p1 = ex2(fmaf(s[e + 1], a.scale_log2, neg_m));
-            l_sum += p0 + p1;
-            w[e4] = pack2(p0, p1, I.fresh);
-          }
+          p8(64 + 8 * q, w);
           *reinterpret_cast<uint4*>(prow + kQT * 128 + ((q ^ (r & 7)) << 4)) =
               make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        {
+          float lo, hi;
+          asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(l2));
+          l_sum += lo + hi;
         }
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
