@@ -62,6 +62,22 @@ def test_linear_large_sampled_rows(q):
     assert_parity(y[rows].float().cpu().numpy(), ref, what="linear large")
 
 
+def test_linear_pair_split_tail_sampled_rows(q):
+    """4096 x 4096 x 1024: 256 pair tiles on the co-resident clusters leave a
+    partial last wave, which runs as 256 x 128 half tiles (each CTA of a pair
+    holding 64 rows of W).  Whole rows sampled across every m-block."""
+    M, N, K = 4096, 4096, 1024
+    x = synth.activations([M, K], "linsplit")
+    w = synth.normal_bf16([N, K], synth.seed_for("linsplit", "w"), 0.02)
+    y = q.linear(x.cuda(), w.cuda())
+    assert q.poll_error() == 0
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.r_[0, 255, 256, 1023, 1024, 3839, 3840, M - 1,
+                           [256 * m + rng.integers(0, 256) for m in range(M // 256)]])
+    ref = oracle.linear(synth.to_f64(x[rows]), synth.to_f64(w))
+    assert_parity(y[rows].float().cpu().numpy(), ref, what="linear pair split tail")
+
+
 def test_linear_is_deterministic(q):
     x = synth.activations([512, 1024], "det").cuda()
     w = synth.normal_bf16([768, 1024], 5, 0.02).cuda()

@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (epi.split_tail || PAIR) tma_prefetch_desc(&tmBh);
+    if (epi.split_tail || PAIR) tma_prefetch_desc(&tmBh);  // pair mode: tmB only for split tails
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -348,16 +348,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   // B tile of k-block kb: row-major [N, K] (2-D map, rows from b_row0) or the
-  // blocked layout of packed weights (4-D map, 128 x 64 tiles from b_tile);
-  // tmB carries a whole BN-row tile, tmBh 128 rows (a split-tail tile, or this
-  // CTA's half of B in pair mode)
+  // blocked layout of packed weights (4-D map, 128 x 64 tiles from b_tile).
+  // 1-SM tiles: tmB carries a whole BN-row tile, tmBh the 128 rows of a
+  // split-tail tile.  Pair tiles: each CTA loads its half of B, 128 rows by
+  // tmBh, or 64 rows by tmB for a 128-wide split-tail tile.
   auto load_b = [&](uint8_t* dst, uint64_t* bar, int kb, const TileInfo& t) {
     if constexpr (PAIR) {
       const uint32_t bar0 = cluster_addr(bar, 0);
-      if (epi.b_blocked)
-        tma_load_4d_pair_w(dst, &tmBh, bar0, 0, 0, kb, t.b_tile + rank);
-      else
-        tma_load_2d_pair_w(dst, &tmBh, bar0, kb * kBK, t.b_row0 + rank * (BN / 2));
+      if (t.bw == BN) {
+        if (epi.b_blocked)
+          tma_load_4d_pair_w(dst, &tmBh, bar0, 0, 0, kb, t.b_tile + rank);
+        else
+          tma_load_2d_pair_w(dst, &tmBh, bar0, kb * kBK, t.b_row0 + rank * (BN / 2));
+      } else {
+        if (epi.b_blocked)
+          tma_load_4d_pair_w(dst, &tmB, bar0, 0, rank * 64, kb, t.b_tile);
+        else
+          tma_load_2d_pair_w(dst, &tmB, bar0, kb * kBK, t.b_row0 + rank * 64);
+      }
     } else {
       const CUtensorMap* m = t.bw == BN ? &tmB : &tmBh;
       if (epi.b_blocked)
@@ -374,7 +382,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   };
   // bytes the stage's barrier waits for (in pair mode: rank 0's barrier, both CTAs' tiles)
   auto stage_bytes = [&](const TileInfo& t) -> uint32_t {
-    return PAIR ? (uint32_t)(2 * (C::A_BYTES + C::B_BYTES))
+    return PAIR ? (uint32_t)(2 * (C::A_BYTES + (t.bw / 2) * kBK * 2))
                 : (uint32_t)(C::A_BYTES + t.bw * kBK * 2);
   };
 
@@ -450,7 +458,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t ad = smem_desc_sw128(a0 + 32 * k, 16, 1024);
             const uint64_t bd = smem_desc_sw128(b0 + 32 * k, 16, 1024);
             if constexpr (PAIR)
-              umma_f16_pair_w(d_tmem, ad, bd, idesc, (kb | k) != 0);
+              umma_f16_pair_w(d_tmem, ad, bd, ti.bw == BN ? idesc : idesc_half, (kb | k) != 0);
             else
               umma_f16_w(d_tmem, ad, bd, ti.bw == BN ? idesc : idesc_half, (kb | k) != 0);
           }
@@ -552,13 +560,13 @@ static bool make_tmap_16(CUtensorMap* map, const void* base, uint64_t rows, uint
 // {64 elements, 128 rows, K/64 tiles, row tiles}; a box of `box_tiles`
 // consecutive row tiles lands in shared memory as box_tiles * 128 rows.
 static bool make_tmap_blocked(CUtensorMap* map, const void* base, uint64_t row_tiles, uint64_t K,
-                              uint32_t box_tiles, bool f16) {
+                              uint32_t box_tiles, bool f16, uint32_t box_rows = 128) {
   auto enc = get_encode_fn();
   if (!enc || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
   const uint64_t kt = K / kBK;
   cuuint64_t dims[4] = {(cuuint64_t)kBK, 128, kt, row_tiles};
   cuuint64_t strides[3] = {kBK * 2, 128 * kBK * 2, kt * 128 * kBK * 2};
-  cuuint32_t box[4] = {(cuuint32_t)kBK, 128, 1, box_tiles};
+  cuuint32_t box[4] = {(cuuint32_t)kBK, box_rows, 1, box_tiles};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return enc(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -658,21 +666,6 @@ qwen_status gemm_tc(const void* A, int lda, const void* B, int ldb, int M, int N
     return QWEN_ERR_UNSUPPORTED;
   constexpr int BN = 256;
   GemmEpilogue epi = epi_in;
-  const uint64_t b_rows = epi.group_offsets ? (uint64_t)N * epi.n_groups : (uint64_t)N;
-  CUtensorMap ta, tb, tbh;
-  if (!make_tmap_16(&ta, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, kBM, op_f16))
-    return QWEN_ERR_CUDA;
-  // B: boxes of a whole tile (BN rows) and of a split-tail half (128 rows)
-  if (epi.b_blocked) {
-    if (K % kBK) return QWEN_ERR_UNSUPPORTED;
-    const uint64_t tiles = (uint64_t)(epi.group_offsets ? epi.n_groups : 1) * ((N + 127) / 128);
-    if (!make_tmap_blocked(&tb, B, tiles, (uint64_t)K, BN / 128, op_f16) ||
-        !make_tmap_blocked(&tbh, B, tiles, (uint64_t)K, 1, op_f16))
-      return QWEN_ERR_CUDA;
-  } else if (!make_tmap_16(&tb, B, b_rows, (uint64_t)K, (uint64_t)ldb, BN, op_f16) ||
-             !make_tmap_16(&tbh, B, b_rows, (uint64_t)K, (uint64_t)ldb, 128, op_f16)) {
-    return QWEN_ERR_CUDA;
-  }
   const int sms = device_sm_count();
   epi.split_tail = 0;
   epi.split_from = 0;
@@ -680,6 +673,23 @@ qwen_status gemm_tc(const void* A, int lda, const void* B, int ldb, int M, int N
   // 1-SM tile is bound by its SM's TMA ingress and took about 1.1x the time of
   // a pair tile in measurements (T=4096 gate/up and down projections); the
   // choice compares the two wave counts on that basis.
+  //
+  // Wave quantisation: with T tiles on S units (SMs or clusters) the last wave
+  // holds T mod S tiles.  Cutting those in two 128-wide halves spreads them
+  // over twice as many units.  A 1-SM half tile takes about 2/3 of a full one
+  // (its B box is half, its A box the same); a pair half tile (each CTA: 128
+  // rows of A and 64 of B per k-block, 24 KB per 256 MMA cycles) about 0.78 at
+  // the ingress rate.  Split when that shortens the estimate by 4 % or more
+  // (below that, measured gains and losses were within noise).
+  auto tail_split = [](int tiles, int units, double half_cost, double& t) -> bool {
+    const int full_waves = tiles / units, rem = tiles - full_waves * units;
+    t = full_waves + (rem > 0 ? 1.0 : 0.0);
+    if (rem == 0) return false;
+    const double t_split = full_waves + ((2 * rem + units - 1) / units) * half_cost;
+    if (t_split >= 0.96 * t) return false;
+    t = t_split;
+    return true;
+  };
   bool pair = false;
   int grid;
   if (epi.group_offsets) {
@@ -689,39 +699,46 @@ qwen_status gemm_tc(const void* A, int lda, const void* B, int ldb, int M, int N
     pair = M >= 384 * epi.n_groups && pair_clusters() > 0;
     grid = sms;  // the number of tiles is only known on the device
   } else {
-    // Wave quantisation: with T tiles on S SMs the last wave holds T mod S
-    // tiles.  Cutting those in two 128-wide halves spreads them over twice as
-    // many SMs; a half tile takes about 2/3 of a full one (its B box is half,
-    // its A box the same), so split when that shortens the estimate by 4 % or
-    // more (below that, measured gains and losses were within noise).
     const int tiles = ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
-    const int full_waves = tiles / sms, rem = tiles - full_waves * sms;
-    int units = tiles;
-    double t_one = full_waves + (rem > 0 ? 1.0 : 0.0);
-    if (rem > 0) {
-      const double t_split = full_waves + ((2 * rem + sms - 1) / sms) * (2.0 / 3.0);
-      if (t_split < 0.96 * t_one) {
-        epi.split_tail = 1;
-        epi.split_from = full_waves * sms;
-        units = epi.split_from + 2 * rem;
-        t_one = t_split;
-      }
-    }
-    grid = units < sms ? units : sms;
+    double t_one;
+    const bool split_one = tail_split(tiles, sms, 2.0 / 3.0, t_one);
     const int clusters = M >= 2 * kBM ? pair_clusters() : 0;
-    if (clusters > 0) {
-      const int ptiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + BN - 1) / BN);
-      const int pwaves = (ptiles + clusters - 1) / clusters;
-      if (pwaves < 1.1 * t_one) {
-        pair = true;
-        epi.split_tail = 0;
-        epi.split_from = 0;
-        grid = ptiles;
-      }
+    const int ptiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + BN - 1) / BN);
+    double t_pair = 0.0;
+    const bool split_pair = clusters > 0 && tail_split(ptiles, clusters, 0.78, t_pair);
+    pair = clusters > 0 && t_pair < 1.1 * t_one;
+    const bool split = pair ? split_pair : split_one;
+    const int n = pair ? ptiles : tiles, units = pair ? clusters : sms;
+    grid = n;
+    if (split) {
+      const int full_waves = n / units;
+      epi.split_tail = 1;
+      epi.split_from = full_waves * units;
+      grid = epi.split_from + 2 * (n - epi.split_from);
     }
+    if (!pair && grid > sms) grid = sms;
+  }
+  const uint64_t b_rows = epi.group_offsets ? (uint64_t)N * epi.n_groups : (uint64_t)N;
+  CUtensorMap ta, tb, tbh;
+  if (!make_tmap_16(&ta, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, kBM, op_f16))
+    return QWEN_ERR_CUDA;
+  // B boxes.  1-SM tiles: tb a whole tile (BN rows), tbh a split-tail half
+  // (128 rows).  Pair tiles: tbh one CTA's half of a tile (128 rows), tb one
+  // CTA's half of a split-tail tile (64 rows).
+  const uint32_t tb_rows = pair ? 64 : BN;
+  if (epi.b_blocked) {
+    if (K % kBK) return QWEN_ERR_UNSUPPORTED;
+    const uint64_t tiles = (uint64_t)(epi.group_offsets ? epi.n_groups : 1) * ((N + 127) / 128);
+    const bool ok_tb = pair ? make_tmap_blocked(&tb, B, tiles, (uint64_t)K, 1, op_f16, 64)
+                            : make_tmap_blocked(&tb, B, tiles, (uint64_t)K, BN / 128, op_f16);
+    if (!ok_tb || !make_tmap_blocked(&tbh, B, tiles, (uint64_t)K, 1, op_f16))
+      return QWEN_ERR_CUDA;
+  } else if (!make_tmap_16(&tb, B, b_rows, (uint64_t)K, (uint64_t)ldb, tb_rows, op_f16) ||
+             !make_tmap_16(&tbh, B, b_rows, (uint64_t)K, (uint64_t)ldb, 128, op_f16)) {
+    return QWEN_ERR_CUDA;
   }
   const uint32_t idesc = idesc_f32acc(pair ? 2 * kBM : kBM, BN, op_f16);
-  const uint32_t idesc_half = idesc_f32acc(kBM, 128, op_f16);
+  const uint32_t idesc_half = idesc_f32acc(pair ? 2 * kBM : kBM, 128, op_f16);
   switch (epi.mode) {
     case EPI_STORE:
       return launch_epi<EPI_STORE>(pair, ta, tb, tbh, M, N, K, idesc, idesc_half, epi, err, grid, st);
