@@ -148,6 +148,7 @@ struct AttnArgs {
   const int32_t* slot0;  // [B] cache slot of the first new token
   f16* out;              // [B*T][Hq*DH], FP16 operand of the O projection
   float scale_log2;      // log2(e) / sqrt(dh)
+  int hpi;               // query heads per work item: 2, or 1 when 2 leave SMs idle
   int* err;
 };
 
@@ -155,7 +156,9 @@ struct AttnArgs {
 
 // One work item: sequence b, KV group g, query heads hA (and hA + 1 when
 // nq = 2), query rows [t0, t0 + 128).  Items are numbered heaviest first (the
-// last query tiles see the most keys).
+// last query tiles see the most keys).  With one head per item (a.hpi = 1)
+// there are twice as many items, each half the work per key tile: for short
+// sequences the longest item, not the total, sets the time.
 struct AttnItem {
   int b, g, hA, nq, t0, s0, kmax, n_kv, kv_row0;
   bool fresh;  // every key is this call's (slot0 == 0): FP16 operands
@@ -163,7 +166,7 @@ struct AttnItem {
 
 __device__ __forceinline__ AttnItem attn_item(int it, const AttnArgs& a) {
   const int gs = a.Hq / a.Hkv;
-  const int npair = (gs + 1) >> 1;
+  const int npair = (gs + a.hpi - 1) / a.hpi;
   const int n_qt = (a.T + kQT - 1) / kQT;
   const int per_qt = a.B * a.Hkv * npair;
   AttnItem I;
@@ -173,8 +176,8 @@ __device__ __forceinline__ AttnItem attn_item(int it, const AttnArgs& a) {
   u /= npair;
   I.g = u % a.Hkv;
   I.b = u / a.Hkv;
-  I.hA = I.g * gs + 2 * pr;
-  I.nq = (2 * pr + 1 < gs) ? 2 : 1;
+  I.hA = I.g * gs + a.hpi * pr;
+  I.nq = (a.hpi == 2 && 2 * pr + 1 < gs) ? 2 : 1;
   I.t0 = qt * kQT;
   I.s0 = a.slot0[I.b];
   I.fresh = I.s0 == 0;
@@ -233,7 +236,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gs = a.Hq / a.Hkv;
-  const int n_items = ((a.T + kQT - 1) / kQT) * a.B * a.Hkv * ((gs + 1) >> 1);
+  const int n_items = ((a.T + kQT - 1) / kQT) * a.B * a.Hkv * ((gs + a.hpi - 1) / a.hpi);
   // this CTA's ni-th item (-1: none left).  Snake order over the heaviest-first
   // item list: round r takes items [r G, (r+1) G), CTA k the k-th of them in
   // even rounds and the (G-1-k)-th in odd rounds, which balances the summed
@@ -650,7 +653,7 @@ static qwen_status launch_dh(const CUtensorMap& q, const CUtensorMap& k, const C
     attr = true;
   }
   const int n_qt = (a.T + kQT - 1) / kQT;
-  const int npair = (a.Hq / a.Hkv + 1) / 2;
+  const int npair = (a.Hq / a.Hkv + a.hpi - 1) / a.hpi;
   const long long items = (long long)n_qt * a.B * a.Hkv * npair;
   const int sms = device_sm_count();
   const int grid = items < sms ? (int)items : sms;  // persistent: one CTA per SM
@@ -676,6 +679,13 @@ qwen_status attention_prefill(const f16* q, const bf16* k_cache, const bf16* v_c
   a.B = B; a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.max_seq = max_seq;
   a.slot0 = slot0; a.out = out; a.err = err;
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)dh);
+  // two heads per item share each K/V tile (half the TMA traffic per MMA
+  // cycle); below 1.5 items per SM, one head per item shortens the longest
+  // item instead
+  {
+    const long long pairs = (long long)((T + kQT - 1) / kQT) * B * Hkv * ((Hq / Hkv + 1) / 2);
+    a.hpi = pairs * 2 < 3LL * device_sm_count() ? 1 : 2;
+  }
   if (dh == 128) return launch_dh<128>(tq, tk, tv, tk16, tv16, a, st);
   if (dh == 64) return launch_dh<64>(tq, tk, tv, tk16, tv16, a, st);
   return QWEN_ERR_UNSUPPORTED;
