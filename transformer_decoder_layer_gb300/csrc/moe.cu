@@ -66,9 +66,12 @@ __device__ __forceinline__ void topk_warp(float* lrow, const float* __restrict__
       v[i] = -INFINITY;
     }
   }
-  float sel[8];
-  int sel_i[8];
-  for (int j = 0; j < k; ++j) {
+  // fixed-bound loops with j < k guards keep these in registers
+  float sel[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  int sel_i[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j >= k) break;
     float bv = -INFINITY;
     int bi = 0x7fffffff;
 #pragma unroll
@@ -103,14 +106,18 @@ __device__ __forceinline__ void topk_warp(float* lrow, const float* __restrict__
   }
   if (lane == 0) {
     float s = 0.f, p[8];
-    for (int j = 0; j < k; ++j) {
-      p[j] = expf(sel[j] - sel[0]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      p[j] = j < k ? expf(sel[j] - sel[0]) : 0.f;
       s += p[j];
     }
     const float den = norm ? s : all;
-    for (int j = 0; j < k; ++j) {
-      idx_row[j] = sel_i[j];
-      w_row[j] = p[j] / den;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        idx_row[j] = sel_i[j];
+        w_row[j] = p[j] / den;
+      }
     }
     if (g_out) *g_out = 1.f / (1.f + expf(-lrow[E]));
   }
@@ -126,6 +133,51 @@ __global__ void topk_kernel(float* __restrict__ logits, int ldl, const float* __
   if (t >= T) return;
   topk_warp(logits + (size_t)t * ldl, bias, E, k, norm, idx + (size_t)t * k, w + (size_t)t * k,
             gscale ? gscale + t : nullptr);
+}
+
+// Run by one warp: exclusive scan of tot[0..E) (E <= 256, 8 experts per
+// lane).  base[e] becomes the scan value (plus its old value when `add`);
+// when `publish`, offsets[0..E] get the scan and act the compacted list of
+// non-empty experts in increasing order, act = [count, ids...].
+__device__ __forceinline__ void expert_scan_warp(const int32_t* tot, int E, int32_t* base,
+                                                 bool add, bool publish, int32_t* offsets,
+                                                 int32_t* act) {
+  const int lane = threadIdx.x & 31;
+  int c[8], sum = 0, nz = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int x = lane * 8 + j;
+    c[j] = x < E ? tot[x] : 0;
+    sum += c[j];
+    nz += c[j] > 0;
+  }
+  int incl = sum, nzi = nz;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    const int u = __shfl_up_sync(0xffffffffu, nzi, o);
+    if (lane >= o) {
+      incl += v;
+      nzi += u;
+    }
+  }
+  int off = incl - sum, na = nzi - nz;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int x = lane * 8 + j;
+    if (x < E) {
+      base[x] = (add ? base[x] : 0) + off;
+      if (publish) {
+        offsets[x] = off;
+        if (c[j]) act[1 + na++] = x;
+      }
+    }
+    off += c[j];
+  }
+  if (publish && lane == 31) {
+    offsets[E] = incl;
+    act[0] = nzi;
+  }
 }
 
 // Per-block expert counts: block g counts entries [g*1024, (g+1)*1024).
@@ -161,31 +213,22 @@ __global__ void __launch_bounds__(kPermBlock) perm_scatter_kernel(
   const int g = blockIdx.x, lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int all = 0, before = 0;
-    for (int b = 0; b < G; ++b) {
-      const int c = blk_counts[(size_t)b * E + e];
-      all += c;
-      before += b < g ? c : 0;
+    for (int b0 = 0; b0 < G; b0 += 8) {
+      int c[8];  // eight independent loads in flight
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[j] = b0 + j < G ? blk_counts[(size_t)(b0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        all += c[j];
+        before += b0 + j < g ? c[j] : 0;
+      }
     }
     tot[e] = all;
     base[e] = before;
   }
   for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int o = 0, na = 0;
-    for (int e = 0; e < E; ++e) {
-      if (g == 0) {
-        offsets[e] = o;
-        if (tot[e]) act[1 + na++] = e;
-      }
-      base[e] += o;
-      o += tot[e];
-    }
-    if (g == 0) {
-      offsets[E] = o;
-      act[0] = na;
-    }
-  }
+  if (wid == 0) expert_scan_warp(tot, E, base, true, g == 0, offsets, act);
   const int i = g * kPermBlock + threadIdx.x;
   const bool valid = i < n;
   const int e = valid ? min(max(idx[i], 0), E - 1) : -1;
@@ -246,43 +289,7 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
   const int rank_w = __popc(same & ((1u << lane) - 1u));
   if (valid && rank_w == 0) wcnt[wid * E + e] = __popc(same);
   __syncthreads();
-  if (wid == 0) {
-    // exclusive scan of tot over E <= 256 experts, 8 per lane, and the
-    // compacted list of non-empty experts in increasing order
-    int c[8], sum = 0, nz = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int x = lane * 8 + j;
-      c[j] = x < E ? tot[x] : 0;
-      sum += c[j];
-      nz += c[j] > 0;
-    }
-    int incl = sum, nzi = nz;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      const int u = __shfl_up_sync(0xffffffffu, nzi, o);
-      if (lane >= o) {
-        incl += v;
-        nzi += u;
-      }
-    }
-    int off = incl - sum, na = nzi - nz;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int x = lane * 8 + j;
-      if (x < E) {
-        offsets[x] = off;
-        base[x] = off;
-        if (c[j]) act[1 + na++] = x;
-      }
-      off += c[j];
-    }
-    if (lane == 31) {
-      offsets[E] = incl;
-      act[0] = nzi;
-    }
-  }
+  if (wid == 0) expert_scan_warp(tot, E, base, false, true, offsets, act);
   __syncthreads();
   if (valid) {
     int pos = base[e] + rank_w;
