@@ -715,18 +715,18 @@ def profile_run(args):
             layer.prefill(x, pos, start, kc, vc, out=y, workspace=ws)
     else:
         shape = synth.QWEN3_8B
-        T = args.tokens
+        T, Bp = args.tokens, args.prefill_batch
         w = {k: v.to(dev) for k, v in synth.layer_weights(shape, "bench_prefill").items()}
-        cfg = q.LayerConfig(shape, max_tokens=T, max_batch=1, max_seq=T, max_position=T)
+        cfg = q.LayerConfig(shape, max_tokens=Bp * T, max_batch=Bp, max_seq=T, max_position=T)
         layer = q.Layer(cfg, w)
-        x = synth.activations([1, T, shape.d], "bench_prefill", f"x1_{T}").to(dev)
-        kc = torch.zeros((1, shape.n_kv_heads, T, shape.head_dim), dtype=torch.bfloat16,
+        x = synth.activations([Bp, T, shape.d], "bench_prefill", f"x{Bp}_{T}").to(dev)
+        kc = torch.zeros((Bp, shape.n_kv_heads, T, shape.head_dim), dtype=torch.bfloat16,
                          device=dev)
         vc = torch.zeros_like(kc)
-        pos = torch.arange(T, dtype=torch.int32, device=dev)
-        start = torch.zeros(1, dtype=torch.int32, device=dev)
+        pos = torch.arange(T, dtype=torch.int32, device=dev).repeat(Bp)
+        start = torch.zeros(Bp, dtype=torch.int32, device=dev)
         y = torch.empty_like(x)
-        ws = layer.workspace(1, T)
+        ws = layer.workspace(Bp, T)
         for _ in range(args.steps):
             layer.prefill(x, pos, start, kc, vc, out=y, workspace=ws)
     torch.cuda.synchronize()
@@ -752,6 +752,8 @@ def main():
                     help="run --steps untimed eager steps of one workload and exit "
                          "(a short, deterministic launch sequence for a profiler capture)")
     ap.add_argument("--tokens", type=int, default=4096, help="prefill length for --profile")
+    ap.add_argument("--prefill-batch", type=int, default=1,
+                    help="sequences of --tokens each for --profile prefill")
     ap.add_argument("--moe-shape", choices=["qwen3", "qwen2"], default="qwen3",
                     help="MoE layer shape for --profile moe / moe_decode: Qwen3-30B-A3B or "
                          "Qwen2-57B-A14B (shared expert)")
