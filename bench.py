@@ -7,7 +7,7 @@ tokens (the new token is position/slot 4096), in microseconds per step per
 layer (lower is better).  A step is the whole layer: RMSNorm, fused QKV (+bias,
 RoPE, cache append), split-KV attention, O projection + residual, RMSNorm,
 gate/up + SiLU*up, down + residual.  Inputs are resident in HBM; weights
-(466 MB) plus the KV cache exceed the 126 MB L2, so no flush is needed.
+(466 MB) plus the KV cache exceed the 129 MB L2, so no flush is needed.
 
 The same line carries: the B sweep (1, 8, 32, 64); prefill of a Qwen3-8B-shaped
 layer (tokens/s, TFLOP/s, per-kernel tensor roofline); `roofline` for the
@@ -53,6 +53,21 @@ def load_peaks():
                 float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), "measured")
     except Exception:
         return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def job_us_per_step(rank_ms, steps, world):
+    """Whole-job time per decode step over `world` replicas: the slowest rank's
+    time for its `steps` steps (a MAX all-reduce when world > 1), divided by
+    the steps all ranks ran together."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dev = (torch.device("cuda", torch.cuda.current_device())
+               if dist.get_backend() == "nccl" else torch.device("cpu"))
+        t = torch.tensor([float(rank_ms)], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        rank_ms = float(t.item())
+    return rank_ms * 1e3 / (steps * world)
 
 
 # ------------------------------------------------------------------ clocks
@@ -822,12 +837,8 @@ def main():
     # the dominant kernel is timed in a second replay of the same K steps with
     # CUDA events around its stage in every step
     _, kern_ms, _ = bench.timed(args.steps, args.warmup, trace_stage="gate_up")
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
     # whole job: world * steps decode steps in the slowest rank's time
-    us_per_step = total_ms * 1e3 / (args.steps * world)
+    us_per_step = job_us_per_step(total_ms, args.steps, world)
     step_bytes = decode_bytes(shape, B)
 
     # roofline of the dominant kernel: the gate/up projection (weights dominate)
