@@ -66,7 +66,7 @@ __device__ __forceinline__ void qkv_head_finish(float (&v)[DH], int m, int head,
     }
   }
   const int b = m / p.T, t = m - (m / p.T) * p.T;
-  auto store = [&](void* dst, bool f16_out) {
+  auto store = [&](void* dst, bool f16_out, bool streaming = false) {
     uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
     for (int i = 0; i < DH / 8; ++i) {
@@ -75,7 +75,10 @@ __device__ __forceinline__ void qkv_head_finish(float (&v)[DH], int m, int head,
       o.y = pack2(v[8 * i + 2], v[8 * i + 3], f16_out);
       o.z = pack2(v[8 * i + 4], v[8 * i + 5], f16_out);
       o.w = pack2(v[8 * i + 6], v[8 * i + 7], f16_out);
-      d4[i] = o;
+      if (streaming)
+        __stcs(d4 + i, o);
+      else
+        d4[i] = o;
     }
   };
   if (kind == 0) {
@@ -92,9 +95,13 @@ __device__ __forceinline__ void qkv_head_finish(float (&v)[DH], int m, int head,
     return;
   }
   const int g = kind == 1 ? head - p.Hq : head - p.Hq - p.Hkv;
-  store((kind == 1 ? p.k_cache : p.v_cache) + (((size_t)b * p.Hkv + g) * p.max_seq + slot) * DH,
-        false);
   __half* fresh = kind == 1 ? p.k16 : p.v16;
+  // a sequence from slot 0 has its attention read the FP16 copies, so its
+  // cache rows are not read again in this call: streaming stores keep them
+  // from displacing Q and the copies in L2
+  const bool fresh_read = fresh != nullptr && p.slot0[b] == 0;
+  store((kind == 1 ? p.k_cache : p.v_cache) + (((size_t)b * p.Hkv + g) * p.max_seq + slot) * DH,
+        false, fresh_read);
   if (fresh) store(fresh + (((size_t)b * p.Hkv + g) * p.T + t) * DH, true);
 }
 
