@@ -8,11 +8,15 @@
 //
 // CTA layout (192 threads, one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer: A tile [128 x 64] and B tile [BN x 64] per stage
-//   warp 1      TMEM allocator + MMA issuer (one elected lane)
+//               (pair tiles: this CTA's [BN/2 x 64] half of B)
+//   warp 1      TMEM allocator + MMA issuer (one elected lane; pair tiles:
+//               only the even CTA of the cluster issues)
 //   warps 2..5  epilogue: tcgen05.ld of the 128 x BN FP32 accumulator, fused
 //               math, global stores.  Warp w reads TMEM lanes 32*(w%4)..+31.
 // Two accumulators in TMEM (2 x BN columns) let the epilogue of tile i overlap
-// the main loop of tile i+1.
+// the main loop of tile i+1.  Tile shapes: 1-SM tiles of 128 x BN, or pair
+// tiles of 256 x BN on a cluster of two CTAs (see GemmCfg); the host picks
+// the shape with the shorter estimated run (gemm_tc).
 #include "common.cuh"
 #include "internal.h"
 #include "qkv_epilogue.cuh"
