@@ -110,7 +110,50 @@ def test_prefill_attention_mixed_work_items():
     assert_parity(v, vr, what="V cache")
 
 
-@pytest.mark.parametrize("T", [1024, 4096])
+def test_single_token_prefill_over_mixed_cache_offsets():
+    """T=1 for three sequences whose chunks start at slots 0, 5 and 17: one
+    query row per attention item, fresh and cached items in one call."""
+    shape = synth.LayerConfig(d=512, n_q_heads=8, n_kv_heads=2, head_dim=64, ffn=1536,
+                              qk_norm=1)
+    y, ref, k, kr, v, vr = _prefill_case(shape, "t1_mixed", 3, 1, cache_start=[0, 5, 17],
+                                         max_seq=32, prefilled=[0, 5, 17])
+    assert_parity(y, ref, what="Y")
+    assert_parity(k, kr, what="K cache")
+    assert_parity(v, vr, what="V cache")
+
+
+def test_empty_calls_succeed_without_launches():
+    """Zero rows, zero tokens and zero sequences are valid calls: success, no
+    kernel launched, nothing written."""
+    import transformer_decoder_layer_gb300 as q
+    shape = synth.LayerConfig(d=512, n_q_heads=8, n_kv_heads=2, head_dim=64, ffn=256,
+                              qk_norm=1, n_experts=16, top_k=4)
+    g = GpuLayer(shape, synth.layer_weights(shape, "empty"), max_tokens=8, max_batch=2,
+                 max_seq=8, max_position=8)
+    bf, i32, dev = torch.bfloat16, torch.int32, "cuda"
+    kc = torch.zeros((2, 2, 8, 64), dtype=bf, device=dev)
+    vc = torch.zeros_like(kc)
+    torch.cuda.synchronize()
+    n0 = q.launch_count()
+    assert q.linear(torch.empty((0, 512), dtype=bf, device=dev),
+                    torch.zeros((256, 512), dtype=bf, device=dev)).shape == (0, 256)
+    assert q.rmsnorm(torch.empty((0, 512), dtype=bf, device=dev),
+                     torch.ones(512, dtype=bf, device=dev), 1e-6).shape == (0, 512)
+    yp = g.layer.prefill(torch.empty((2, 0, 512), dtype=bf, device=dev),
+                         torch.empty(0, dtype=i32, device=dev), torch.zeros(2, dtype=i32, device=dev),
+                         kc, vc)
+    assert yp.shape == (2, 0, 512)
+    yd = g.layer.decode(torch.empty((0, 512), dtype=bf, device=dev),
+                        torch.empty(0, dtype=i32, device=dev), torch.empty(0, dtype=i32, device=dev),
+                        kc, vc)
+    assert yd.shape == (0, 512)
+    assert g.layer.moe_ffn(torch.empty((0, 512), dtype=bf, device=dev)).shape == (0, 512)
+    assert q.launch_count() == n0
+    assert g.layer.poll_error() == 0 and q.poll_error() == 0
+    assert torch.count_nonzero(kc) == 0 and torch.count_nonzero(vc) == 0
+
+
+@pytest.mark.parametrize("T", [1024, 4096, 16384])
 def test_qwen3_8b_layer_prefill_sampled_rows(T):
     """Qwen3-8B-shaped layer at full size, sampled output rows."""
     rng = np.random.default_rng(T)

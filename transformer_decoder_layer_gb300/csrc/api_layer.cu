@@ -92,10 +92,11 @@ WorkspaceLayout workspace_layout(const qwen_layer_config& c, int B, int T) {
   };
   W.xh = take(M * d * 2);
   W.q = take(M * nq * 2);
-  if (T > 1) {  // FP16 copies of the call's K/V rows for the prefill attention
-    W.k16 = take(M * (size_t)c.n_kv_heads * dh * 2);
-    W.v16 = take(M * (size_t)c.n_kv_heads * dh * 2);
-  }
+  // FP16 copies of the call's K/V rows for the prefill attention.  Laid out for
+  // every T: a prefill of one token per sequence uses this (B, 1) layout too,
+  // and its copies must not share memory with each other or with X-hat.
+  W.k16 = take(M * (size_t)c.n_kv_heads * dh * 2);
+  W.v16 = take(M * (size_t)c.n_kv_heads * dh * 2);
   W.attn = take(M * nq * 2);
   W.r32 = take(M * d * 4);  // residual stream R kept in FP32
   // MoE: Z rows are [Z_hi | Z_lo] (2d FP16), the router's split-precision operand
