@@ -133,6 +133,24 @@ QWEN_API size_t qwen_layer_packed_bytes(const qwen_layer_config* cfg);
  * holds only transient values: it may be reused across calls on one stream. */
 QWEN_API size_t qwen_layer_workspace_bytes(const qwen_layer_config* cfg, int32_t B, int32_t T);
 
+/* One region of a layer workspace: a name, its byte offset and its size. */
+typedef struct qwen_workspace_region {
+  const char* name; /* static string owned by the library */
+  size_t offset;
+  size_t bytes;
+} qwen_workspace_region;
+
+/* The regions the library places in a workspace for (B, T) under `cfg`, in
+ * layout order.  Host only: no device is touched.  Writes up to
+ * `max_regions` entries to `out` (which may be NULL when max_regions is 0)
+ * and returns the number of regions, or -1 when cfg is invalid, B or T is not
+ * positive, or out is NULL with max_regions > 0.  Offsets are 256-byte
+ * aligned, regions do not overlap, and each ends at or before
+ * qwen_layer_workspace_bytes(cfg, B, T).  For inspection and tests; the
+ * kernels use exactly these offsets. */
+QWEN_API int32_t qwen_layer_workspace_regions(const qwen_layer_config* cfg, int32_t B, int32_t T,
+                                              qwen_workspace_region* out, int32_t max_regions);
+
 /* Validate cfg, pack the weights into `packed` (device, packed_bytes as
  * returned above, 256-byte aligned), build the RoPE table and return a handle.
  * Enqueues the packing on `stream` and synchronises it before returning.

@@ -53,11 +53,18 @@ class _Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in _WEIGHT_FIELDS]
 
 
+class _Region(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("offset", ctypes.c_size_t),
+                ("bytes", ctypes.c_size_t)]
+
+
 _VP, _I32, _SZ, _F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
 _SIGS = {
     "qwen_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "qwen_layer_packed_bytes": (_SZ, [ctypes.POINTER(_Config)]),
     "qwen_layer_workspace_bytes": (_SZ, [ctypes.POINTER(_Config), _I32, _I32]),
+    "qwen_layer_workspace_regions": (_I32, [ctypes.POINTER(_Config), _I32, _I32,
+                                            ctypes.POINTER(_Region), _I32]),
     "qwen_layer_create": (ctypes.c_int, [ctypes.POINTER(_Config), ctypes.POINTER(_Weights), _VP,
                                          _SZ, _VP, ctypes.POINTER(_VP)]),
     "qwen_layer_destroy": (None, [_VP]),
@@ -178,6 +185,17 @@ def poll_error(stream=None):
 
 def head_workspace_bytes(B, d, V):
     return lib().qwen_head_workspace_bytes(B, d, V)
+
+
+def workspace_regions(cfg, B, T):
+    """[(name, offset, bytes)] of the layer workspace for (B, T) under a
+    LayerConfig, in layout order (host only)."""
+    n = lib().qwen_layer_workspace_regions(ctypes.byref(cfg.c), B, T, None, 0)
+    if n < 0:
+        raise ValueError(f"invalid config or sizes (B={B}, T={T})")
+    arr = (_Region * max(n, 1))()
+    lib().qwen_layer_workspace_regions(ctypes.byref(cfg.c), B, T, arr, n)
+    return [(r.name.decode(), int(r.offset), int(r.bytes)) for r in arr[:n]]
 
 
 def head_last_token(y, gamma_final, w_lm, eps, logits=None, workspace=None, stream=None):

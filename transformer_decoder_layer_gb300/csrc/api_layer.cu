@@ -85,49 +85,50 @@ WorkspaceLayout workspace_layout(const qwen_layer_config& c, int B, int T) {
   const size_t M = (size_t)B * T, d = c.d, dh = c.head_dim, nq = (size_t)c.n_q_heads * dh,
                f = c.ffn;
   size_t o = 0;
-  auto take = [&](size_t bytes) {
+  auto take = [&](const char* name, size_t bytes) {
     const size_t at = o;
     o = align256(o + bytes);
+    if (W.n_reg < WorkspaceLayout::kMaxRegions) W.reg[W.n_reg++] = {name, at, bytes};
     return at;
   };
-  W.xh = take(M * d * 2);
-  W.q = take(M * nq * 2);
+  W.xh = take("xh", M * d * 2);
+  W.q = take("q", M * nq * 2);
   // FP16 copies of the call's K/V rows for the prefill attention.  Laid out for
   // every T: a prefill of one token per sequence uses this (B, 1) layout too,
   // and its copies must not share memory with each other or with X-hat.
-  W.k16 = take(M * (size_t)c.n_kv_heads * dh * 2);
-  W.v16 = take(M * (size_t)c.n_kv_heads * dh * 2);
-  W.attn = take(M * nq * 2);
-  W.r32 = take(M * d * 4);  // residual stream R kept in FP32
+  W.k16 = take("k16", M * (size_t)c.n_kv_heads * dh * 2);
+  W.v16 = take("v16", M * (size_t)c.n_kv_heads * dh * 2);
+  W.attn = take("attn", M * nq * 2);
+  W.r32 = take("r32", M * d * 4);  // residual stream R kept in FP32
   // MoE: Z rows are [Z_hi | Z_lo] (2d FP16), the router's split-precision operand
-  W.z = take(M * d * 2 * (c.n_experts ? 2 : 1));
+  W.z = take("z", M * d * 2 * (c.n_experts ? 2 : 1));
   if (c.n_experts == 0) {
-    W.h = take(M * f * 2);
+    W.h = take("h", M * f * 2);
   } else {
     const size_t e = c.n_experts, k = c.top_k, mk = M * k;
-    W.logits = take(M * (size_t)router_rows(c) * 4);
-    W.topk_idx = take(mk * 4);
-    W.topk_w = take(mk * 4);
-    W.blk_counts = take(moe_perm_blocks(mk) * e * 4);
-    W.offsets = take((e + 1) * 4);
-    W.act = take((e + 1) * 4);
-    W.perm = take(mk * 4);
-    W.inv = take(mk * 4);
-    W.zp = take(mk * d * 2);
-    W.hp = take(mk * f * 2);
-    W.yp = take(mk * d * 2);
+    W.logits = take("logits", M * (size_t)router_rows(c) * 4);
+    W.topk_idx = take("topk_idx", mk * 4);
+    W.topk_w = take("topk_w", mk * 4);
+    W.blk_counts = take("blk_counts", moe_perm_blocks(mk) * e * 4);
+    W.offsets = take("offsets", (e + 1) * 4);
+    W.act = take("act", (e + 1) * 4);
+    W.perm = take("perm", mk * 4);
+    W.inv = take("inv", mk * 4);
+    W.zp = take("zp", mk * d * 2);
+    W.hp = take("hp", mk * f * 2);
+    W.yp = take("yp", mk * d * 2);
     if (c.shared_ffn) {
-      W.hs = take(M * (size_t)c.shared_ffn * 2);
-      W.ys32 = take(M * d * 4);
-      W.gscale = take(M * 4);
+      W.hs = take("hs", M * (size_t)c.shared_ffn * 2);
+      W.ys32 = take("ys32", M * d * 4);
+      W.gscale = take("gscale", M * 4);
     }
   }
   if (T == 1) {
     int splits = 0;
     decode_attn_plan(c, B, &splits);
-    W.part = take(decode_part_bytes(c, B));
-    W.attn_o = take((size_t)B * c.n_q_heads * splits * dh * 4);
-    W.attn_ml = take((size_t)B * c.n_q_heads * splits * 2 * 4);
+    W.part = take("part", decode_part_bytes(c, B));
+    W.attn_o = take("attn_o", (size_t)B * c.n_q_heads * splits * dh * 4);
+    W.attn_ml = take("attn_ml", (size_t)B * c.n_q_heads * splits * 2 * 4);
   }
   W.total = o;
   return W;
@@ -215,6 +216,16 @@ size_t qwen_layer_packed_bytes(const qwen_layer_config* cfg) {
 size_t qwen_layer_workspace_bytes(const qwen_layer_config* cfg, int32_t B, int32_t T) {
   if (!cfg || !config_valid(*cfg) || B <= 0 || T <= 0) return 0;
   return workspace_layout(*cfg, B, T).total;
+}
+
+int32_t qwen_layer_workspace_regions(const qwen_layer_config* cfg, int32_t B, int32_t T,
+                                     qwen_workspace_region* out, int32_t max_regions) {
+  if (!cfg || !config_valid(*cfg) || B <= 0 || T <= 0 || max_regions < 0) return -1;
+  if (max_regions > 0 && !out) return -1;
+  const WorkspaceLayout W = workspace_layout(*cfg, B, T);
+  for (int i = 0; i < W.n_reg && i < max_regions; ++i)
+    out[i] = {W.reg[i].name, W.reg[i].off, W.reg[i].bytes};
+  return W.n_reg;
 }
 
 qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_weights* w,

@@ -23,6 +23,14 @@ struct WorkspaceLayout {
   // decode (T == 1)
   size_t part, attn_o, attn_ml;
   size_t total;
+  // the regions above in layout order, named (qwen_layer_workspace_regions)
+  struct Region {
+    const char* name;
+    size_t off, bytes;
+  };
+  static constexpr int kMaxRegions = 32;
+  Region reg[kMaxRegions];
+  int n_reg;
 };
 
 }  // namespace qwen
