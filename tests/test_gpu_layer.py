@@ -153,7 +153,7 @@ def test_empty_calls_succeed_without_launches():
     assert torch.count_nonzero(kc) == 0 and torch.count_nonzero(vc) == 0
 
 
-@pytest.mark.parametrize("T", [1024, 4096, 16384])
+@pytest.mark.parametrize("T", [1024, 4096])
 def test_qwen3_8b_layer_prefill_sampled_rows(T):
     """Qwen3-8B-shaped layer at full size, sampled output rows."""
     rng = np.random.default_rng(T)
