@@ -23,7 +23,6 @@ pinned by ``tests/test_oracle_*.py`` except where a module header says
 """
 
 from .layer import (  # noqa: F401
-    round_to_bf16,
     rmsnorm,
     linear,
     silu,

@@ -40,21 +40,6 @@ import numpy as np
 # Elementary steps
 # --------------------------------------------------------------------------
 
-def round_to_bf16(x):
-    """Round float64 values to the nearest bfloat16 (ties to even), returned as
-    float64.  Used only when a caller asks the oracle to model BF16 storage.
-
-    bfloat16 keeps the top 16 bits of an IEEE float32; the value is first
-    rounded to float32 (exact for every value this oracle stores), then the
-    low 16 bits are rounded to nearest even on the bit pattern.
-    """
-    f = np.asarray(x, dtype=np.float64).astype(np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    lsb = (u >> 16) & 1
-    u = ((u + 0x7FFF + lsb) >> 16) << 16
-    return u.astype(np.uint32).view(np.float32).astype(np.float64)
-
-
 def rmsnorm(x, gamma, eps):
     """RMSNorm over the last axis.
 
@@ -176,44 +161,45 @@ def gqa_attention(q, k, v, q_slots, k_slots, causal=True, return_probs=False):
 # Blocks
 # --------------------------------------------------------------------------
 
-def _qkv(xh, w, cfg):
-    """Q/K/V projections, optional bias, QK-norm, RoPE ([P3] §4-§6)."""
+def _qkv(xh, w, cfg, positions):
+    """Q/K/V projections, optional bias, QK-norm, then RoPE ([P3] §4-§6).
+
+    [P3] §5: with QK-norm each head vector of Q (and of K) is normalised on
+    its own, over its dh channels, with one length-dh gamma shared by all Q
+    heads (gamma_q) and one shared by all K heads (gamma_k); V is not
+    normalised.  [P3] §6 then rotates the normalised Q and K by position.
+    Returns q [T,Hq,dh], k [T,Hkv,dh] (both rotated) and v [T,Hkv,dh].
+    """
     t = xh.shape[0]
     hq, hkv, dh = cfg["n_q_heads"], cfg["n_kv_heads"], cfg["head_dim"]
+    theta = cfg["rope_theta"]
     bias = bool(cfg.get("qkv_bias", 0))
     q = linear(xh, w["w_q"], w["b_q"] if bias else None).reshape(t, hq, dh)
     k = linear(xh, w["w_k"], w["b_k"] if bias else None).reshape(t, hkv, dh)
     v = linear(xh, w["w_v"], w["b_v"] if bias else None).reshape(t, hkv, dh)
     if cfg.get("qk_norm", 0):
-        # [P3] §5: per-head RMSNorm over dh with one shared gamma for Q and one
-        # for K; V is not normalised.  Order: projection -> QK-norm -> RoPE.
         q = rmsnorm(q, w["gamma_q"], cfg["rms_eps"])
         k = rmsnorm(k, w["gamma_k"], cfg["rms_eps"])
+    q = apply_rope_rotate_half(q, positions, theta)
+    k = apply_rope_rotate_half(k, positions, theta)
     return q, k, v
 
 
 def attention_block(x, w, cfg, positions, k_cache, v_cache, slots,
-                    causal=True, rows=None, cache_bf16=False):
+                    causal=True, rows=None):
     """R = X + Attention(RMSNorm_1(X)) for one sequence ([P3] §2, §4-§9).
 
     x: [T, d]; positions, slots: [T] ints; k_cache, v_cache: [Hkv, S_max, dh]
     float64 arrays updated in place with the new post-QK-norm, post-RoPE K and
     V rows ([P1] §09.1; [P3] §12).  ``rows`` restricts the returned rows (the
     K/V of every row is still computed and written, since later rows read it).
-    ``cache_bf16`` models a cache held in BF16 storage: appended K/V rows are
-    rounded to BF16, so attention reads what such a cache holds.
     Returns R for the requested rows.
     """
     x = np.asarray(x, dtype=np.float64)
-    eps, theta = cfg["rms_eps"], cfg["rope_theta"]
     slots = np.asarray(slots)
     positions = np.asarray(positions)
-    xh = rmsnorm(x, w["gamma_attn"], eps)
-    q, k, v = _qkv(xh, w, cfg)
-    q = apply_rope_rotate_half(q, positions, theta)
-    k = apply_rope_rotate_half(k, positions, theta)
-    if cache_bf16:
-        k, v = round_to_bf16(k), round_to_bf16(v)
+    xh = rmsnorm(x, w["gamma_attn"], cfg["rms_eps"])
+    q, k, v = _qkv(xh, w, cfg, positions)
     k_cache[:, slots, :] = k.transpose(1, 0, 2)
     v_cache[:, slots, :] = v.transpose(1, 0, 2)
     if rows is None:
@@ -240,7 +226,7 @@ def mlp_block(r, w, cfg):
 
 
 def layer_forward(x, w, cfg, positions, k_cache, v_cache, slots,
-                  causal=True, rows=None, cache_bf16=False):
+                  causal=True, rows=None):
     """Dense layer forward for one sequence: attention block then MLP block.
 
     [P3] §2: R = X + Attention(RMSNorm_1(X)), Y = R + MLP(RMSNorm_2(R)); the
@@ -248,7 +234,7 @@ def layer_forward(x, w, cfg, positions, k_cache, v_cache, slots,
     same call with T = 1 in slot ``cache_len`` ([P1] §09.1).
     """
     r = attention_block(x, w, cfg, positions, k_cache, v_cache, slots,
-                        causal=causal, rows=rows, cache_bf16=cache_bf16)
+                        causal=causal, rows=rows)
     return mlp_block(r, w, cfg)
 
 

@@ -496,31 +496,3 @@ def test_head_last_token_identity_lm_head():
     y = np.array([[1.0, 0.0, -1.0, 0.5]])
     logits = O.head_last_token(y, np.ones(4), np.eye(4), 0.0)
     assert np.allclose(logits[0], np.array([1.0, 0.0, -1.0, 0.5]) / 0.75, atol=1e-15)
-
-
-def test_round_to_bf16_matches_the_format():
-    """BF16 keeps 8 significant bits: 1 + 2^-8 rounds to 1 (tie to even),
-    1 + 3*2^-8 rounds up to 1 + 2^-6... checked against torch's own BF16
-    conversion and a few hand values."""
-    import torch
-    vals = np.array([1.0, 1 + 2**-8, 1 + 3 * 2**-8, -2.5, 3.0e38, 1e-40, 0.1, 65504.0])
-    got = O.round_to_bf16(vals)
-    assert got[0] == 1.0 and got[1] == 1.0 and got[2] == 1 + 2**-6
-    ref = torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16).double().numpy()
-    assert np.array_equal(got, ref)
-
-
-def test_bf16_cache_mode_rounds_only_the_cache():
-    """cache_bf16 rounds the appended K/V; with T=1 the output is V's BF16
-    rounding passed through (same construction as the single-token test)."""
-    cfg = small_cfg(d=16, n_q_heads=4, n_kv_heads=2, head_dim=4)
-    w = rand_weights(cfg, 19)
-    w["w_o"] = np.eye(16)
-    w["w_down"] = np.zeros_like(w["w_down"])
-    x = np.random.default_rng(20).standard_normal((1, 16))
-    kc = np.zeros((2, 1, 4))
-    vc = np.zeros_like(kc)
-    y = O.layer_forward(x, w, cfg, [5], kc, vc, [0], cache_bf16=True)
-    assert np.array_equal(vc, O.round_to_bf16(vc))
-    v = vc[:, 0, :].reshape(-1)
-    assert np.allclose(y[0] - x[0], np.concatenate([v[0:4], v[0:4], v[4:8], v[4:8]]), atol=1e-13)
