@@ -253,8 +253,9 @@ QWEN_API qwen_status qwen_head_last_token(const void* y, int32_t B, int32_t T, i
  * B * d * 2 must be <= 2 MiB (e.g. B = 256 at d = 4096, B = 128 at d = 8192)
  * and B <= 256, else QWEN_ERR_CAPACITY.  The array's device address is looked
  * up on the first call made on each device (make that first call before any
- * stream capture).  All calls share the array: calls that overlap on the GPU
- * race on it.  Nothing is allocated or freed. */
+ * stream capture) and kept until the process exits, so the device must not be
+ * reset (cudaDeviceReset) between calls.  All calls share the array: calls
+ * that overlap on the GPU race on it.  Nothing is allocated or freed. */
 QWEN_API qwen_status qwen_head_last_token_noalloc(const void* y, int32_t B, int32_t T, int32_t d,
                                                   const void* gamma_final, const void* w_lm,
                                                   int32_t V, float eps, float* logits,

@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cstdio>
 #include <cstdlib>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -14,16 +15,27 @@ static std::atomic<unsigned long long> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 
 // Status word for entry points that have no layer handle (qwen_linear, ...).
-// A module-scope device variable: no allocation is needed to use it.
+// A module-scope device variable: no allocation is needed to use it.  Each
+// device has its own copy; host code looks its address up per device.
 static __device__ int g_lib_status;
 
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
 int* lib_status_ptr() {
-  static int* p = nullptr;
-  if (!p) {
+  static std::mutex mu;
+  static int* addr[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
     void* a = nullptr;
-    if (cudaGetSymbolAddress(&a, g_lib_status) == cudaSuccess) p = static_cast<int*>(a);
+    if (cudaGetSymbolAddress(&a, g_lib_status) == cudaSuccess) addr[dev] = static_cast<int*>(a);
   }
-  return p;
+  return addr[dev];
 }
 
 bool pdl_enabled() {
@@ -36,16 +48,16 @@ bool pdl_enabled() {
 }
 
 int device_sm_count() {
-  static int cached = 0;
-  if (!cached) {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-      cached = n;
-    else
-      cached = 1;
+  static std::atomic<int> cached[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (!n) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return 1;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached;
+  return n;
 }
 
 }  // namespace qwen

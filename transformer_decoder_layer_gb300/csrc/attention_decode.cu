@@ -520,13 +520,8 @@ template <int DH>
 static qwen_status launch_attn_dec(const CUtensorMap& tk, const CUtensorMap& tv,
                                    const DecAttnArgs& a, int grid, f16* out, cudaStream_t st) {
   auto kern = attn_decode_kernel<DH>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             DecAttnCfg<DH>::SMEM_BYTES) != cudaSuccess)
-      return QWEN_ERR_CUDA;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};  // one bit per device
+  if (!smem_attr_once(kern, DecAttnCfg<DH>::SMEM_BYTES, attr)) return QWEN_ERR_CUDA;
   launch_k(kern, dim3(grid), dim3(kDecAttnThreads), DecAttnCfg<DH>::SMEM_BYTES, st, tk, tv, a);
   count_launches();
   if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;

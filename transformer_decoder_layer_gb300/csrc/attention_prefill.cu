@@ -645,13 +645,8 @@ static qwen_status launch_dh(const CUtensorMap& q, const CUtensorMap& k, const C
                              const CUtensorMap& k16, const CUtensorMap& v16, const AttnArgs& a,
                              cudaStream_t st) {
   auto kern = attn_prefill_kernel<DH>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             AttnCfg<DH>::SMEM_BYTES) != cudaSuccess)
-      return QWEN_ERR_CUDA;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};  // one bit per device
+  if (!smem_attr_once(kern, AttnCfg<DH>::SMEM_BYTES, attr)) return QWEN_ERR_CUDA;
   const int n_qt = (a.T + kQT - 1) / kQT;
   const int npair = (a.Hq / a.Hkv + a.hpi - 1) / a.hpi;
   const long long items = (long long)n_qt * a.B * a.Hkv * npair;

@@ -644,13 +644,8 @@ static qwen_status launch_dec(const CUtensorMap& tw, const CUtensorMap& tx, int 
                               cudaStream_t st) {
   using C = DecCfg<BP, EPI>;
   auto kern = gemm_decode_kernel<BP, EPI>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES) != cudaSuccess)
-      return QWEN_ERR_CUDA;
-    attr = true;
-  }
+  static std::atomic<uint64_t> attr{0};  // one bit per device
+  if (!smem_attr_once(kern, C::SMEM_BYTES, attr)) return QWEN_ERR_CUDA;
   const int units = ((N + kDBM - 1) / kDBM) * splits * max_groups;
   const int sms = device_sm_count();
   const int grid = units < sms ? units : sms;

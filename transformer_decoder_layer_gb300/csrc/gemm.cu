@@ -1,6 +1,7 @@
-// Persistent tcgen05 GEMM for sm_103a: D[M,N] = A[M,K] * B[N,K]^T in BF16 with
-// FP32 accumulation in tensor memory, fed by TMA through an mbarrier ring, with
-// fused epilogues for the decoder layer's projections.
+// Persistent tcgen05 GEMM for sm_103a: D[M,N] = A[M,K] * B[N,K]^T with FP16
+// operands (the layer's packed weights and activations) or BF16 operands
+// (qwen_linear), FP32 accumulation in tensor memory, fed by TMA through an
+// mbarrier ring, with fused epilogues for the decoder layer's projections.
 //
 // Every projection of the layer is a "token rows x weight rows" product of this
 // shape ("Qwen2.5-7B 结构拆解" §03.2: [B,S,d] is flattened to [B*S,d] and each
@@ -582,28 +583,32 @@ static bool make_tmap_blocked(CUtensorMap* map, const void* base, uint64_t row_t
 // epilogue variant has the same shared memory and thread count); 0 if the
 // query fails, which keeps every GEMM on 1-SM tiles.
 static int pair_clusters() {
-  static int n = -1;
-  if (n < 0) {
-    n = 0;
-    auto kern = gemm_tc_kernel<256, EPI_STORE, true>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             GemmCfg<256, true>::SMEM_BYTES) == cudaSuccess) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(2 * (device_sm_count() / 2));
-      cfg.blockDim = dim3(kGemmThreads);
-      cfg.dynamicSmemBytes = GemmCfg<256, true>::SMEM_BYTES;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      int c = 0;
-      if (cudaOccupancyMaxActiveClusters(&c, kern, &cfg) == cudaSuccess && c > 0) n = c;
-    }
-    cudaGetLastError();  // a failed query leaves no sticky error behind
+  // per device: 0 = not queried yet, else the count plus one
+  static std::atomic<int> known[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0) return 0;
+  const int k = known[dev].load(std::memory_order_relaxed);
+  if (k) return k - 1;
+  int n = 0;
+  auto kern = gemm_tc_kernel<256, EPI_STORE, true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           GemmCfg<256, true>::SMEM_BYTES) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (device_sm_count() / 2));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = GemmCfg<256, true>::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int c = 0;
+    if (cudaOccupancyMaxActiveClusters(&c, kern, &cfg) == cudaSuccess && c > 0) n = c;
   }
+  cudaGetLastError();  // a failed query leaves no sticky error behind
+  known[dev].store(n + 1, std::memory_order_relaxed);
   return n;
 }
 
@@ -613,7 +618,7 @@ static qwen_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const
                              const GemmEpilogue& epi, int* err, int units, cudaStream_t st) {
   auto kern = gemm_tc_kernel<BN, EPI, PAIR>;
   using C = GemmCfg<BN, PAIR>;
-  static bool attr_done = false;  // per template instance
+  static std::atomic<uint64_t> attr_done{0};  // per template instance, one bit per device
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
@@ -627,12 +632,7 @@ static qwen_status launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const
     attr[na].val.clusterDim.z = 1;
     ++na;
   }
-  if (!attr_done) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-        cudaSuccess)
-      return QWEN_ERR_CUDA;
-    attr_done = true;
-  }
+  if (!smem_attr_once(kern, C::SMEM_BYTES, attr_done)) return QWEN_ERR_CUDA;
   // persistent grid: co-resident CTAs (pair mode: clusters)
   const int max_units = PAIR ? pair_clusters() : device_sm_count();
   if (pdl_enabled()) {

@@ -14,7 +14,11 @@
 // must not use the symbol's name as an address, so the device address is
 // looked up once per device with cudaGetSymbolAddress, on the first call made
 // with that device current (that first call should therefore come before any
-// stream capture).  All calls share the one array and it keeps the last call's
+// stream capture).  The looked-up address is kept for the life of the process:
+// a cudaDeviceReset between calls would reload the module and leave it stale,
+// so the caller must not reset the device while using this entry point.  The
+// GEMM's device status word (read by qwen_poll_error) is looked up per device
+// the same way.  All calls share the one array and it keeps the last call's
 // contents; every call overwrites the part it uses before reading it, so no
 // clearing is needed.  Calls that overlap on the GPU (different streams, or
 // different threads without ordering) race on the array.
@@ -33,11 +37,10 @@ static __device__ __align__(256) uint8_t g_head_scratch[kQwenHeadScratchBytes];
 // Device address of g_head_scratch for the current device (set up once per
 // device), or nullptr if the lookup fails.
 static void* head_scratch_address() {
-  constexpr int kMaxDevices = 64;
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
   if (!addr[dev]) {
     void* p = nullptr;
@@ -63,7 +66,8 @@ qwen_status qwen_head_last_token_noalloc(const void* y, int32_t B, int32_t T, in
   if (B > 256) return QWEN_ERR_CAPACITY;
   if ((size_t)B * (size_t)d * 2 > kQwenHeadScratchBytes) return QWEN_ERR_CAPACITY;
   void* scratch = head_scratch_address();
-  if (!scratch) return QWEN_ERR_CUDA;
+  int* status = lib_status_ptr();
+  if (!scratch || !status) return QWEN_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   bf16* xn = static_cast<bf16*>(scratch);
   const bf16* last = static_cast<const bf16*>(y) + (size_t)(T - 1) * d;
@@ -72,8 +76,7 @@ qwen_status qwen_head_last_token_noalloc(const void* y, int32_t B, int32_t T, in
   if (s) return s;
   // one K split: the decode GEMM writes its [B][V] FP32 result straight into
   // the logits, so no partial buffer is needed
-  return gemm_decode_splitk(w_lm, xn, d, B, V, d, 1, /*op_f16=*/false, logits, lib_status_ptr(),
-                            st);
+  return gemm_decode_splitk(w_lm, xn, d, B, V, d, 1, /*op_f16=*/false, logits, status, st);
 }
 
 }  // extern "C"

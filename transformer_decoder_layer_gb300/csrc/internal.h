@@ -1,6 +1,8 @@
 // Host-side launchers shared between the C ABI (api.cu) and the kernel files.
 #pragma once
 
+#include <atomic>
+
 #include <cstddef>
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -65,7 +67,27 @@ struct GemmEpilogue {
   int split_tail, split_from;
 };
 
+// Devices the library tells apart (per-device set-up below).
+constexpr int kMaxDevices = 64;
+// The current device, or -1 if it cannot be read or is kMaxDevices or above.
+int current_device();
+// SM count of the current device (cached per device; 1 if it cannot be read).
 int device_sm_count();
+
+// Raise a kernel's dynamic shared memory limit on the current device, once
+// per device: `done` holds one bit per device.  False on failure.
+template <typename Kern>
+bool smem_attr_once(Kern kern, int bytes, std::atomic<uint64_t>& done) {
+  const int dev = current_device();
+  if (dev < 0) return false;
+  const uint64_t bit = 1ull << dev;
+  if (done.load(std::memory_order_acquire) & bit) return true;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return false;
+  done.fetch_or(bit, std::memory_order_release);
+  return true;
+}
 
 // Whether kernels are launched with programmatic dependent launch (default on;
 // QWEN_PDL=0 in the environment turns it off).
@@ -91,7 +113,9 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
 }
 // Host-side count of kernel launches issued by the library (qwen_launch_count).
 void count_launches(int n = 1);
-int* lib_status_ptr();  // device status word used by handle-less entry points
+// Device status word used by handle-less entry points, on the current device
+// (its address is looked up once per device); nullptr if the lookup fails.
+int* lib_status_ptr();
 
 // The tensor-core GEMM.  A [M,K] (row stride lda elements), B [N,K] (ldb),
 // both BF16 or both FP16 (op_f16).  For grouped mode, B holds n_groups stacked
