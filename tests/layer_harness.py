@@ -57,3 +57,17 @@ class GpuLayer:
 
 def f64(t):
     return synth.to_f64(t.cpu() if hasattr(t, "cpu") else t)
+
+
+def workspace_region(layer_cfg, ws, B, T, name, dtype, shape):
+    """View of one named region of a layer workspace (the layout the C ABI
+    reports through qwen_layer_workspace_regions) as a tensor."""
+    import transformer_decoder_layer_gb300 as q
+    for n, off, nbytes in q.workspace_regions(layer_cfg, B, T):
+        if n == name:
+            view = ws[off:off + nbytes].view(dtype)
+            count = 1
+            for s in shape:
+                count *= s
+            return view[:count].reshape(shape)
+    raise KeyError(name)

@@ -8,7 +8,10 @@ the last position ("Qwen2.5-7B 结构拆解" §01, §03.8), through the C ABI.
   by element: prefill attention reads this call's K/V rows from FP16 copies
   (the BF16 cache rows are only read by later calls), so the BF16 storage
   rounding of the cache does not enter the prefill result;
-* prefill at T=1024: the last-token logits equal prefill(1023) + decode(1);
+* prefill at T=1024 (the full prefill workload): all 152064 last-token
+  logits against the FP64 oracle run through the 28 layers, element by
+  element at the stated tolerance;
+* also at T=1024: the last-token logits equal prefill(1023) + decode(1);
   both sides are GPU results with independent rounding, so the bound is twice
   the oracle bound.
 """
@@ -97,6 +100,30 @@ def test_stack_prefill_128_tokens(stack_setup):
                                  np.arange(T))
     ref = oracle.head_last_token(h[-1:], f64(gamma_f), f64(w_lm), cfg["rms_eps"])[0]
     assert_parity(logits.cpu().numpy()[0], ref, what="stack prefill logits")
+
+
+def test_stack_prefill_1024_last_token_logits(stack_setup):
+    """Qwen2.5-7B 结构拆解 §03.8: a prefill of 1024 tokens computes logits for
+    the last position only.  The oracle runs every layer over all 1024 rows
+    (later layers read every row's K/V) and only the last row through the
+    final layer's attention output and MLP."""
+    q, st, cpu_w, gamma_f, w_lm = stack_setup
+    T = 1024
+    x = synth.activations([1, T, SHAPE.d], "c5pf1024")
+    start = torch.zeros(1, dtype=torch.int32, device="cuda")
+    logits, _ = st.prefill(x.cuda(), torch.arange(T, dtype=torch.int32, device="cuda"), start)
+    assert st.poll_error() == 0
+    got = logits.cpu().numpy()[0]
+    cfg = SHAPE.as_dict()
+    h = f64(x)[0]
+    for l in range(L_LAYERS):
+        kk = np.zeros((SHAPE.n_kv_heads, T, SHAPE.head_dim))
+        vv = np.zeros_like(kk)
+        rows = [T - 1] if l == L_LAYERS - 1 else None
+        h = oracle.layer_forward(h, synth.weights_f64(cpu_w[l]), cfg, np.arange(T), kk, vv,
+                                 np.arange(T), rows=rows)
+    ref = oracle.head_last_token(h[-1:], f64(gamma_f), f64(w_lm), cfg["rms_eps"])[0]
+    assert_parity(got, ref, what="stack prefill T=1024 logits")
 
 
 def test_stack_prefill_1024_equals_prefill_then_decode(stack_setup):
