@@ -32,6 +32,13 @@
  *     error before anything is launched.  Device-side range problems (a cache
  *     slot >= max_seq, a position >= max_position, a bounded wait that ran
  *     out) set a sticky status word that qwen_layer_poll_error returns.
+ *   - The tensor-core operands inside a layer are FP16 (weights converted from
+ *     BF16 at create; normalised activations, attention output and the SwiGLU
+ *     product H rounded to FP16).  FP16 stops at 65504: a weight of larger
+ *     magnitude makes qwen_layer_create fail with QWEN_ERR_OVERFLOW, and an
+ *     activation that would round past it (or is NaN) is stored as +-65504
+ *     and sets QWEN_ERR_OVERFLOW in the status word.  Results are never
+ *     silently infinite.
  *   - Only head_dim 64 or 128, d % 64 == 0, ffn % 64 == 0 and Hq % Hkv == 0
  *     are supported on the GPU; anything else returns QWEN_ERR_UNSUPPORTED.
  *     There is no CPU fallback.
@@ -59,7 +66,10 @@ typedef enum {
   QWEN_ERR_CAPACITY = 3,    /* B, T or buffer larger than the handle allows   */
   QWEN_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed             */
   QWEN_ERR_TIMEOUT = 5,     /* device: a bounded wait ran out                */
-  QWEN_ERR_RANGE = 6        /* device: cache slot or position out of range   */
+  QWEN_ERR_RANGE = 6,       /* device: cache slot or position out of range   */
+  QWEN_ERR_OVERFLOW = 7     /* a value beyond the FP16 operand range: a weight
+                               at create, or (device) an activation written as
+                               an FP16 GEMM operand                           */
 } qwen_status;
 
 /* Layer shape and capacities.  Plain data, validated by qwen_layer_create. */
@@ -155,7 +165,9 @@ QWEN_API int32_t qwen_layer_workspace_regions(const qwen_layer_config* cfg, int3
  * returned above, 256-byte aligned), build the RoPE table and return a handle.
  * Enqueues the packing on `stream` and synchronises it before returning.
  * The handle (host memory, owned by the library) remembers `packed`, which
- * must outlive the handle. */
+ * must outlive the handle.  Returns QWEN_ERR_OVERFLOW, and no handle, when a
+ * projection, expert or router weight is too large for FP16 (it would round
+ * to infinity; |w| >= 65520). */
 QWEN_API qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_weights* w,
                               void* packed, size_t packed_bytes, void* stream,
                               qwen_layer_t* out);
@@ -306,7 +318,8 @@ QWEN_API qwen_status qwen_layer_set_trace(qwen_layer_t layer, void* const* event
 QWEN_API uint64_t qwen_launch_count(void);
 
 /* Synchronise `stream`, then read and clear the handle's device status word.
- * Returns QWEN_OK, QWEN_ERR_TIMEOUT or QWEN_ERR_RANGE (or QWEN_ERR_CUDA). */
+ * Returns QWEN_OK, QWEN_ERR_TIMEOUT, QWEN_ERR_RANGE or QWEN_ERR_OVERFLOW (or
+ * QWEN_ERR_CUDA); the first error recorded since the last poll wins. */
 QWEN_API qwen_status qwen_layer_poll_error(qwen_layer_t layer, void* stream);
 
 /* Synchronise `stream`, then read and clear the library-wide device status

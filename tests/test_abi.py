@@ -48,6 +48,8 @@ def test_binding_signatures_cover_header(built_lib):
     L = q.lib()
     assert L.qwen_status_string(0) == b"ok"
     assert L.qwen_status_string(6).startswith(b"cache slot")
+    assert b"FP16" in L.qwen_status_string(7)
+    assert q.STATUS[7] == "QWEN_ERR_OVERFLOW"
 
 
 def test_config_struct_layout_matches_c(built_lib):

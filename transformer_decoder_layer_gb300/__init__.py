@@ -22,6 +22,7 @@ __all__ = [
 STATUS = {
     0: "QWEN_OK", 1: "QWEN_ERR_INVALID_ARG", 2: "QWEN_ERR_UNSUPPORTED",
     3: "QWEN_ERR_CAPACITY", 4: "QWEN_ERR_CUDA", 5: "QWEN_ERR_TIMEOUT", 6: "QWEN_ERR_RANGE",
+    7: "QWEN_ERR_OVERFLOW",
 }
 
 

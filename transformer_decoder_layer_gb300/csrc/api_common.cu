@@ -75,6 +75,7 @@ const char* qwen_status_string(qwen_status s) {
     case QWEN_ERR_CUDA: return "CUDA error";
     case QWEN_ERR_TIMEOUT: return "device wait timed out";
     case QWEN_ERR_RANGE: return "cache slot or position out of range";
+    case QWEN_ERR_OVERFLOW: return "value beyond the FP16 operand range (|x| > 65504)";
   }
   return "unknown status";
 }

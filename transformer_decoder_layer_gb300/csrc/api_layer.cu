@@ -147,8 +147,9 @@ static bool copy_d2d(void* dst, const void* src, size_t bytes, cudaStream_t st) 
 
 // Copy BF16 weight rows into the packed FP16 buffer.  BF16 -> FP16 is exact
 // for magnitudes in [2^-14, 65504] (FP16 keeps more mantissa bits); smaller
-// magnitudes land on the FP16 subnormal grid (absolute error <= 2^-25) and
-// larger ones saturate.
+// magnitudes land on the FP16 subnormal grid (absolute error <= 2^-25).  A
+// weight that FP16 cannot hold (it would round to infinity) records
+// QWEN_ERR_OVERFLOW in *err and qwen_layer_create fails.
 //
 // Destination: the blocked layout, a [rows][dst_cols] matrix stored as 128 x 64
 // tiles of 16 KB, tile (row / 128, col / 64) at ((row/128) * dst_cols/64 +
@@ -162,10 +163,11 @@ static bool copy_d2d(void* dst, const void* src, size_t bytes, cudaStream_t st) 
 // group g starts at destination row roff + g * gpad.  Columns go to coff + c.
 __global__ void pack_blocked_f16_kernel(f16* __restrict__ dst, const bf16* __restrict__ src,
                                         size_t rows, int cols, int mode, size_t gsz, size_t gpad,
-                                        size_t roff, int dst_cols, int coff) {
+                                        size_t roff, int dst_cols, int coff, int* err) {
   const int cpr = cols / 8;  // 16-byte chunks per source row
   const size_t nch = rows * (size_t)cpr;
   const size_t kt = (size_t)dst_cols / 64;
+  bool bad = false;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nch;
        i += (size_t)gridDim.x * blockDim.x) {
     const size_t r = i / cpr;
@@ -181,15 +183,16 @@ __global__ void pack_blocked_f16_kernel(f16* __restrict__ dst, const bf16* __res
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float2 f = unpack_bf16x2(w[j]);
-      o[j] = pack_f16x2(fminf(fmaxf(f.x, -65504.f), 65504.f), fminf(fmaxf(f.y, -65504.f), 65504.f));
+      o[j] = pack_f16x2_chk(f.x, f.y, bad);
     }
     *reinterpret_cast<uint4*>(dst + off) = make_uint4(o[0], o[1], o[2], o[3]);
   }
+  record_overflow(err, bad);
 }
 
 // BF16 [rows][cols] -> blocked FP16 (see pack_blocked_f16_kernel); gsz = 0:
 // one group; dst_cols = 0: cols.
-static bool pack_blocked(f16* dst, const void* src, size_t rows, size_t cols, int mode,
+static bool pack_blocked(f16* dst, const void* src, size_t rows, size_t cols, int mode, int* err,
                          cudaStream_t st, size_t gsz = 0, size_t gpad = 0, size_t roff = 0,
                          size_t dst_cols = 0, size_t coff = 0) {
   if (rows == 0) return true;
@@ -197,7 +200,8 @@ static bool pack_blocked(f16* dst, const void* src, size_t rows, size_t cols, in
   const int blocks = (int)((nch + 255) / 256 < 65535 ? (nch + 255) / 256 : 65535);
   pack_blocked_f16_kernel<<<blocks, 256, 0, st>>>(dst, static_cast<const bf16*>(src), rows,
                                                   (int)cols, mode, gsz ? gsz : rows, gpad, roff,
-                                                  (int)(dst_cols ? dst_cols : cols), (int)coff);
+                                                  (int)(dst_cols ? dst_cols : cols), (int)coff,
+                                                  err);
   count_launches();
   return cudaGetLastError() == cudaSuccess;
 }
@@ -288,9 +292,9 @@ qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_wei
   }
   // zero the weight area first: the rows that pad matrices to 128 stay zero
   ok = ok && cudaMemsetAsync(P + L.w_qkv, 0, L.total - L.w_qkv, st) == cudaSuccess;
-  ok = ok && pack_blocked(h->w_qkv, w->w_q, nq, d, 0, st);
-  ok = ok && pack_blocked(h->w_qkv, w->w_k, nkv, d, 0, st, 0, 0, nq);
-  ok = ok && pack_blocked(h->w_qkv, w->w_v, nkv, d, 0, st, 0, 0, nq + nkv);
+  ok = ok && pack_blocked(h->w_qkv, w->w_q, nq, d, 0, h->status, st);
+  ok = ok && pack_blocked(h->w_qkv, w->w_k, nkv, d, 0, h->status, st, 0, 0, nq);
+  ok = ok && pack_blocked(h->w_qkv, w->w_v, nkv, d, 0, h->status, st, 0, 0, nq + nkv);
   if (c.qkv_bias && ok) {
     bf16_to_f32_kernel<<<(int)((nq + 255) / 256), 256, 0, st>>>(
         static_cast<const bf16*>(w->b_q), h->b_qkv, (int)nq);
@@ -301,24 +305,24 @@ qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_wei
     count_launches(3);
     ok = cudaGetLastError() == cudaSuccess;
   }
-  ok = ok && pack_blocked(h->w_o, w->w_o, d, nq, 0, st);
+  ok = ok && pack_blocked(h->w_o, w->w_o, d, nq, 0, h->status, st);
   const size_t n_exp = moe ? (size_t)c.n_experts : 1;
-  ok = ok && pack_blocked(h->w_gu, w->w_gate, n_exp * f, d, 1, st, f, 2 * f);
-  ok = ok && pack_blocked(h->w_gu, w->w_up, n_exp * f, d, 2, st, f, 2 * f);
-  ok = ok && pack_blocked(h->w_down, w->w_down, n_exp * d, f, 0, st, d, round128(d));
+  ok = ok && pack_blocked(h->w_gu, w->w_gate, n_exp * f, d, 1, h->status, st, f, 2 * f);
+  ok = ok && pack_blocked(h->w_gu, w->w_up, n_exp * f, d, 2, h->status, st, f, 2 * f);
+  ok = ok && pack_blocked(h->w_down, w->w_down, n_exp * d, f, 0, h->status, st, d, round128(d));
   if (moe) {
     // rows [W_r | W_r]; with a shared expert W_sg is row E (rows after it zero)
-    ok = ok && pack_blocked(h->w_router, w->w_router, n_exp, d, 0, st, 0, 0, 0, 2 * d, 0);
-    ok = ok && pack_blocked(h->w_router, w->w_router, n_exp, d, 0, st, 0, 0, 0, 2 * d, d);
+    ok = ok && pack_blocked(h->w_router, w->w_router, n_exp, d, 0, h->status, st, 0, 0, 0, 2 * d, 0);
+    ok = ok && pack_blocked(h->w_router, w->w_router, n_exp, d, 0, h->status, st, 0, 0, 0, 2 * d, d);
     if (c.router_bias) ok = ok && copy_d2d(h->b_router, w->b_router, n_exp * 4, st);
   }
   if (c.shared_ffn) {
     const size_t sf = c.shared_ffn;
-    ok = ok && pack_blocked(h->w_router, w->w_shared_expert_gate, 1, d, 0, st, 0, 0, n_exp, 2 * d, 0);
-    ok = ok && pack_blocked(h->w_router, w->w_shared_expert_gate, 1, d, 0, st, 0, 0, n_exp, 2 * d, d);
-    ok = ok && pack_blocked(h->w_sgu, w->w_shared_gate, sf, d, 1, st, sf, 2 * sf);
-    ok = ok && pack_blocked(h->w_sgu, w->w_shared_up, sf, d, 2, st, sf, 2 * sf);
-    ok = ok && pack_blocked(h->w_sdown, w->w_shared_down, d, sf, 0, st, d, round128(d));
+    ok = ok && pack_blocked(h->w_router, w->w_shared_expert_gate, 1, d, 0, h->status, st, 0, 0, n_exp, 2 * d, 0);
+    ok = ok && pack_blocked(h->w_router, w->w_shared_expert_gate, 1, d, 0, h->status, st, 0, 0, n_exp, 2 * d, d);
+    ok = ok && pack_blocked(h->w_sgu, w->w_shared_gate, sf, d, 1, h->status, st, sf, 2 * sf);
+    ok = ok && pack_blocked(h->w_sgu, w->w_shared_up, sf, d, 2, h->status, st, sf, 2 * sf);
+    ok = ok && pack_blocked(h->w_sdown, w->w_shared_down, d, sf, 0, h->status, st, d, round128(d));
   }
   // RoPE table: (cos, sin) of p * theta^(-2i/dh), angles and trig in FP64.
   // Qwen3 layer page, §6 (frequency equation).
@@ -336,9 +340,13 @@ qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_wei
                          st) == cudaSuccess;
     ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
   }
-  if (!ok) {
+  // a weight beyond the FP16 range was recorded by the packing kernels
+  int packed_status = 0;
+  ok = ok && cudaMemcpy(&packed_status, h->status, sizeof(int), cudaMemcpyDeviceToHost) ==
+                 cudaSuccess;
+  if (!ok || packed_status) {
     delete h;
-    return QWEN_ERR_CUDA;
+    return ok ? static_cast<qwen_status>(packed_status) : QWEN_ERR_CUDA;
   }
   *out = h;
   return QWEN_OK;
@@ -621,7 +629,7 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
 
   // RMSNorm_1 -> X-hat (FP16 operand)
   QWEN_STAGE_RUN(QWEN_STAGE_NORM1, rmsnorm_launch(x, L->gamma_attn, xh, true, nullptr, x32, B,
-                                                  d, c.rms_eps, st));
+                                                  d, c.rms_eps, st, 0, 0, nullptr, err));
   // Q/K/V, then bias, QK-norm, RoPE, Q store and K/V append at slot cache_len[b]
   const QkvParams qp = make_qkv_params(L, positions, cache_len, q, false, kc, vc, nullptr,
                                        nullptr, 1);
@@ -648,7 +656,8 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
     // O projection; its split reduction + residual is fused with RMSNorm_2
     QWEN_STAGE_RUN(QWEN_STAGE_O, decode_proj(L->w_o, attn, B, d, nq, part, err, st, S));
     QWEN_STAGE_RUN(QWEN_STAGE_O_FINISH,
-                   reduce_resid_norm(part, S, B, d, x, x32, r32, L->gamma_mlp, c.rms_eps, z, st));
+                   reduce_resid_norm(part, S, B, d, x, x32, r32, L->gamma_mlp, c.rms_eps, z, err,
+                                     st));
     // gate/up in one K split with SiLU*up in the epilogue -> H, then down
     QWEN_STAGE_RUN(QWEN_STAGE_GATE_UP,
                    gemm_decode_splitk(L->w_gu, z, d, B, 2 * f, d, 1, /*op_f16=*/true, nullptr,
@@ -662,8 +671,8 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
     // MoE: the split reduction + residual also writes [Z_hi | Z_lo] = RMSNorm_2(R)
     QWEN_STAGE_RUN(QWEN_STAGE_O, decode_proj(L->w_o, attn, B, d, nq, part, err, st, S));
     QWEN_STAGE_RUN(QWEN_STAGE_O_FINISH,
-                   reduce_resid_norm(part, S, B, d, x, x32, r32, L->gamma_mlp, c.rms_eps, z, st,
-                                     2 * (size_t)d, z + d));
+                   reduce_resid_norm(part, S, B, d, x, x32, r32, L->gamma_mlp, c.rms_eps, z, err,
+                                     st, 2 * (size_t)d, z + d));
   } else {
     GemmEpilogue e{};
     e.mode = EPI_RESID;
@@ -683,10 +692,10 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
   }
   // RMSNorm_2 -> Z, gate/up + SiLU*up -> H, down + residual -> Y
   QWEN_STAGE_RUN(QWEN_STAGE_NORM2, rmsnorm_launch(nullptr, L->gamma_mlp, z, true, nullptr, r32, B,
-                                                  d, c.rms_eps, st));
+                                                  d, c.rms_eps, st, 0, 0, nullptr, err));
   if (swap) {
     QWEN_STAGE_RUN(QWEN_STAGE_GATE_UP, decode_proj(L->w_gu, z, B, 2 * f, d, part, err, st, S));
-    QWEN_STAGE_RUN(QWEN_STAGE_GATE_UP_FINISH, reduce_swiglu(part, S, B, f, hbuf, st));
+    QWEN_STAGE_RUN(QWEN_STAGE_GATE_UP_FINISH, reduce_swiglu(part, S, B, f, hbuf, err, st));
     QWEN_STAGE_RUN(QWEN_STAGE_DOWN, decode_proj(L->w_down, hbuf, B, d, f, part, err, st, S));
     QWEN_STAGE_RUN(QWEN_STAGE_DOWN_FINISH,
                    reduce_resid(part, S, B, d, nullptr, r32, y, y32, st));
@@ -732,7 +741,7 @@ qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, const float* x32, bf16
 
   // RMSNorm_1 -> X-hat (FP16 operand)
   QWEN_STAGE_RUN(QWEN_STAGE_NORM1, rmsnorm_launch(x, L->gamma_attn, xh, true, nullptr, x32, M,
-                                                  d, c.rms_eps, st));
+                                                  d, c.rms_eps, st, 0, 0, nullptr, err));
   // fused QKV: bias, QK-norm, RoPE, Q store, K/V cache append
   GemmEpilogue e{};
   e.mode = EPI_QKV;
@@ -762,7 +771,7 @@ qwen_status layer_prefill(qwen_layer_s* L, const bf16* x, const float* x32, bf16
   }
   // RMSNorm_2, gate/up + SiLU*mul, down + residual
   QWEN_STAGE_RUN(QWEN_STAGE_NORM2, rmsnorm_launch(nullptr, L->gamma_mlp, z, true, nullptr, r32, M,
-                                                  d, c.rms_eps, st));
+                                                  d, c.rms_eps, st, 0, 0, nullptr, err));
   GemmEpilogue eg{};
   eg.mode = EPI_SWIGLU;
   eg.b_static = 1;

@@ -426,7 +426,8 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
 template <int DH>
 __global__ void attn_decode_merge_kernel(const float* __restrict__ part_o,
                                          const float* __restrict__ part_ml, int BH, int slots,
-                                         int G, int nbv, int per, f16* __restrict__ out) {
+                                         int G, int nbv, int per, f16* __restrict__ out,
+                                         int* err) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ float merge_f[];  // [warps][slots]: the weight of each slot
@@ -463,9 +464,11 @@ __global__ void attn_decode_merge_kernel(const float* __restrict__ part_o,
     }
   }
   const float inv = 1.f / lsum;
+  bool bad = false;  // C is the next GEMM's FP16 operand: V rows past 65504 reach it
 #pragma unroll
   for (int i = 0; i < DH / 32; ++i)
-    out[(size_t)wid * DH + lane + 32 * i] = __float2half_rn(acc[i] * inv);
+    out[(size_t)wid * DH + lane + 32 * i] = f16_chk(acc[i] * inv, bad);
+  record_overflow(err, bad);
 }
 
 // ------------------------------------------------------------------ host side
@@ -529,7 +532,7 @@ static qwen_status launch_attn_dec(const CUtensorMap& tk, const CUtensorMap& tv,
   launch_k(attn_decode_merge_kernel<DH>, dim3((BH * 32 + 255) / 256), dim3(256),
            (size_t)(256 / 32) * a.slots * sizeof(float), st,
            (const float*)a.part_o, (const float*)a.part_ml, BH, a.slots, a.Hq / a.Hkv, a.nbv,
-           a.per, out);
+           a.per, out, a.err);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }

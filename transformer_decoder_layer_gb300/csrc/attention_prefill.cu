@@ -581,6 +581,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const float inv_l = 1.f / l_sum;
       const bool row_ok = t < a.T;
       f16* dst = a.out + ((size_t)I.b * a.T + t) * (size_t)(a.Hq * DH) + (size_t)(I.hA + x) * DH;
+      bool bad = false;  // C is the next GEMM's FP16 operand: V rows past 65504 reach it
 #pragma unroll 1
       for (int q = 0; q < DH / 32; ++q) {
         uint32_t oo[32];
@@ -588,15 +589,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (row_ok) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(oo[8 * e + i]) * inv_l;
             uint4 w;
-            w.x = pack_f16x2(__uint_as_float(oo[8 * e]) * inv_l, __uint_as_float(oo[8 * e + 1]) * inv_l);
-            w.y = pack_f16x2(__uint_as_float(oo[8 * e + 2]) * inv_l, __uint_as_float(oo[8 * e + 3]) * inv_l);
-            w.z = pack_f16x2(__uint_as_float(oo[8 * e + 4]) * inv_l, __uint_as_float(oo[8 * e + 5]) * inv_l);
-            w.w = pack_f16x2(__uint_as_float(oo[8 * e + 6]) * inv_l, __uint_as_float(oo[8 * e + 7]) * inv_l);
+            w.x = pack_f16x2_chk(f[0], f[1], bad);
+            w.y = pack_f16x2_chk(f[2], f[3], bad);
+            w.z = pack_f16x2_chk(f[4], f[5], bad);
+            w.w = pack_f16x2_chk(f[6], f[7], bad);
             reinterpret_cast<uint4*>(dst + 32 * q)[e] = w;
           }
         }
       }
+      record_overflow(a.err, bad);
       tc_fence_before();
       mbar_arrive(&o_free[x]);
       c += I.n_kv;

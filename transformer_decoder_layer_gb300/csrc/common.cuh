@@ -517,6 +517,32 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool to_f16) {
   return to_f16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
 }
 
+// FP16 operands stop at 65504.  A value whose FP16 rounding would be infinite
+// (|v| >= 65520) or that is NaN has no FP16 encoding: the checked conversions
+// store it saturated to +-65504 and set `bad`; the kernel then records
+// QWEN_ERR_OVERFLOW once (record_overflow).
+__device__ __forceinline__ float f16_sat(float v, bool& bad) {
+  const bool ok = fabsf(v) < 65520.f;  // false for NaN
+  bad |= !ok;
+  return ok ? v : copysignf(65504.f, v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2_chk(float lo, float hi, bool& bad) {
+  return pack_f16x2(f16_sat(lo, bad), f16_sat(hi, bad));
+}
+
+__device__ __forceinline__ uint32_t pack2_chk(float lo, float hi, bool to_f16, bool& bad) {
+  return to_f16 ? pack_f16x2_chk(lo, hi, bad) : pack_bf16x2(lo, hi);
+}
+
+__device__ __forceinline__ f16 f16_chk(float v, bool& bad) {
+  return __float2half_rn(f16_sat(v, bad));
+}
+
+__device__ __forceinline__ void record_overflow(int* err, bool bad) {
+  if (bad) record_error(err, QWEN_ERR_OVERFLOW);
+}
+
 __device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
   __half2 v = *reinterpret_cast<__half2*>(&u);
   return __half22float2(v);

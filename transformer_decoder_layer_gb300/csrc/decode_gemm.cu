@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
                        const int32_t* gact, const int32_t* goff, const int32_t* tidx,
                        const int32_t* tinv, int tk, int* err) {
   using C = DecCfg<BP, EPI>;
+  bool f16_bad = false;  // an H value beyond the FP16 range (SwiGLU epilogue)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
               if (row >= 0 && f_tile + fr < fdim) {
                 const float gv = xch[(c + i) * 64 + fr];
                 hout[(size_t)row * fdim + f_tile + fr] =
-                    __float2half_rn(silu_f(gv) * __uint_as_float(r[i]));
+                    f16_chk(silu_f(gv) * __uint_as_float(r[i]), f16_bad);
               }
             }
           }
@@ -322,6 +323,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
       }
     }
   }
+  record_overflow(err, f16_bad);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -375,7 +377,7 @@ __global__ void reduce_resid_kernel(const float* __restrict__ part, int splits, 
 
 // h[b][j] = SiLU(gate_j) * up_j with gate row (j/64)*128 + j%64 and up row +64.
 __global__ void reduce_swiglu_kernel(const float* __restrict__ part, int splits, int B, int f,
-                                     f16* __restrict__ h) {
+                                     f16* __restrict__ h, int* err) {
   pdl_trigger();
   pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;  // over B * f, j fastest
@@ -387,7 +389,9 @@ __global__ void reduce_swiglu_kernel(const float* __restrict__ part, int splits,
   const float* src = part + (size_t)b * N + n_gate;
   float gu[2] = {0.f, 0.f};  // gate, up
   add_splits<2, 8>(src, plane, 64, splits, 2, gu);
-  h[i] = __float2half_rn(silu_f(gu[0]) * gu[1]);
+  bool bad = false;
+  h[i] = f16_chk(silu_f(gu[0]) * gu[1], bad);
+  record_overflow(err, bad);
 }
 
 // One warp per (b, head): lane e holds channels e, e+32, e+64, e+96 (dh = 128)
@@ -464,7 +468,7 @@ template <int PER>
 __global__ void __launch_bounds__(1024) reduce_resid_norm_kernel(
     const float* __restrict__ part, int splits, int B, int N, const bf16* __restrict__ resid,
     const float* __restrict__ resid32, float* __restrict__ out32, const bf16* __restrict__ gamma,
-    float eps, f16* __restrict__ z, size_t zs, f16* __restrict__ z_lo) {
+    float eps, f16* __restrict__ z, size_t zs, f16* __restrict__ z_lo, int* err) {
   pdl_trigger();
   pdl_wait();
   __shared__ float red[32];
@@ -498,16 +502,18 @@ __global__ void __launch_bounds__(1024) reduce_resid_norm_kernel(
   for (int w = 0; w < 32; ++w) tot += red[w];
   const float rstd = rsqrtf(tot / (float)N + eps);
   const size_t zrow = (size_t)b * zs;
+  bool bad = false;
 #pragma unroll
   for (int j = 0; j < PER; ++j) {
     const int n = threadIdx.x + 1024 * j;
     if (n < N) {
       const float o = __bfloat162float(gamma[n]) * (v[j] * rstd);
-      const f16 hi = __float2half_rn(o);
+      const f16 hi = f16_chk(o, bad);
       z[zrow + n] = hi;
-      if (z_lo) z_lo[zrow + n] = __float2half_rn(o - __half2float(hi));
+      if (z_lo) z_lo[zrow + n] = f16_chk(o - __half2float(hi), bad);
     }
   }
+  record_overflow(err, bad);
 }
 
 __global__ void reduce_f32_kernel(const float* __restrict__ part, int splits, int B, int N,
@@ -732,9 +738,10 @@ qwen_status reduce_resid(const float* part, int splits, int B, int N, const bf16
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
 
-qwen_status reduce_swiglu(const float* part, int splits, int B, int f, f16* h, cudaStream_t st) {
+qwen_status reduce_swiglu(const float* part, int splits, int B, int f, f16* h, int* err,
+                          cudaStream_t st) {
   launch_k(reduce_swiglu_kernel, dim3(blocks_for((long long)f * B, 256)), dim3(256), 0, st, part,
-           splits, B, f, h);
+           splits, B, f, h, err);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
@@ -754,15 +761,15 @@ qwen_status reduce_qkv(const float* part, int splits, int B, int Nqkv, const Qkv
 
 qwen_status reduce_resid_norm(const float* part, int splits, int B, int N, const bf16* resid,
                               const float* resid32, float* out32, const bf16* gamma, float eps,
-                              f16* z, cudaStream_t st, size_t z_stride, f16* z_lo) {
+                              f16* z, int* err, cudaStream_t st, size_t z_stride, f16* z_lo) {
   if (N > 1024 * 8) return QWEN_ERR_UNSUPPORTED;
   const size_t zs = z_stride ? z_stride : (size_t)N;
   if (N <= 1024 * 4)
     launch_k(reduce_resid_norm_kernel<4>, dim3(B), dim3(1024), 0, st, part, splits, B, N, resid,
-             resid32, out32, gamma, eps, z, zs, z_lo);
+             resid32, out32, gamma, eps, z, zs, z_lo, err);
   else
     launch_k(reduce_resid_norm_kernel<8>, dim3(B), dim3(1024), 0, st, part, splits, B, N, resid,
-             resid32, out32, gamma, eps, z, zs, z_lo);
+             resid32, out32, gamma, eps, z, zs, z_lo, err);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }

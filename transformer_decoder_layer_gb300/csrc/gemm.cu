@@ -144,6 +144,7 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, bool row_
     }
   } else if constexpr (EPI == EPI_SWIGLU) {
     // columns [128j, 128j+64) are gate rows, [128j+64, 128j+128) the matching up rows
+    bool bad = false;  // an H value beyond the FP16 range
 #pragma unroll 1
     for (int j = 0; j < bw; j += 128) {
 #pragma unroll 1
@@ -165,16 +166,18 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, bool row_
               o[e] = silu_f(gv) * __uint_as_float(u[8 * q + e]);
             }
             uint4 w;
-            w.x = pack2(o[0], o[1], epi.out_f16);
-            w.y = pack2(o[2], o[3], epi.out_f16);
-            w.z = pack2(o[4], o[5], epi.out_f16);
-            w.w = pack2(o[6], o[7], epi.out_f16);
+            w.x = pack2_chk(o[0], o[1], epi.out_f16, bad);
+            w.y = pack2_chk(o[2], o[3], epi.out_f16, bad);
+            w.z = pack2_chk(o[4], o[5], epi.out_f16, bad);
+            w.w = pack2_chk(o[6], o[7], epi.out_f16, bad);
             dst[q] = w;
           }
         }
       }
     }
+    record_overflow(err, bad);
   } else {
+    bool bad = false;  // an FP16 output beyond the format's range
 #pragma unroll 1
     for (int c = 0; c < bw; c += 32) {
       uint32_t r[32];
@@ -257,23 +260,24 @@ __device__ __forceinline__ void epilogue_tile(uint32_t taddr, int row, bool row_
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 w;
-            w.x = pack2(o[8 * q], o[8 * q + 1], epi.out_f16);
-            w.y = pack2(o[8 * q + 2], o[8 * q + 3], epi.out_f16);
-            w.z = pack2(o[8 * q + 4], o[8 * q + 5], epi.out_f16);
-            w.w = pack2(o[8 * q + 6], o[8 * q + 7], epi.out_f16);
+            w.x = pack2_chk(o[8 * q], o[8 * q + 1], epi.out_f16, bad);
+            w.y = pack2_chk(o[8 * q + 2], o[8 * q + 3], epi.out_f16, bad);
+            w.z = pack2_chk(o[8 * q + 4], o[8 * q + 5], epi.out_f16, bad);
+            w.w = pack2_chk(o[8 * q + 6], o[8 * q + 7], epi.out_f16, bad);
             reinterpret_cast<uint4*>(dst)[q] = w;
           }
         } else {
 #pragma unroll
           for (int i = 0; i < 32; i += 2)
             if (i < N - col) {
-              const uint32_t p = pack2(o[i], o[i + 1], epi.out_f16);
+              const uint32_t p = pack2_chk(o[i], o[i + 1], epi.out_f16, bad);
               dst[i] = static_cast<uint16_t>(p & 0xFFFFu);
               if (i + 1 < N - col) dst[i + 1] = static_cast<uint16_t>(p >> 16);
             }
         }
       }
     }
+    record_overflow(err, bad);
   }
 }
 

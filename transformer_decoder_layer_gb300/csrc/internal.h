@@ -139,10 +139,12 @@ qwen_status attention_prefill(const __half* q, const __nv_bfloat16* k_cache,
 // elements apart (0 = d), read from x32 (FP32) when given, else x (BF16);
 // y is BF16, or FP16 when y_f16, rows `y_stride` apart (0 = d).  With y_lo
 // (FP16 y only) the rounding residual y - fp16(y) is written there as FP16, rows
-// `y_stride` apart: y + y_lo carries the FP32 value to about 2^-22.
+// `y_stride` apart: y + y_lo carries the FP32 value to about 2^-22.  An FP16
+// value beyond the format's range is stored saturated and QWEN_ERR_OVERFLOW is
+// recorded in *err (when err is not NULL).
 qwen_status rmsnorm_launch(const __nv_bfloat16* x, const __nv_bfloat16* gamma, void* y,
                            bool y_f16, float* y32, const float* x32, int rows, int d, float eps,
                            cudaStream_t st, size_t x_stride = 0, size_t y_stride = 0,
-                           __half* y_lo = nullptr);
+                           __half* y_lo = nullptr, int* err = nullptr);
 
 }  // namespace qwen

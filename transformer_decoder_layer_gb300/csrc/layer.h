@@ -148,11 +148,13 @@ qwen_status reduce_resid(const float* part, int splits, int B, int N, const __nv
 // R = sum of splits + residual (FP32, out32), then Z = RMSNorm(R) (FP16, rows
 // z_stride apart, 0 = N).  With z_lo the FP16 rounding residual of Z is written
 // there as well (same row stride): the [Z_hi | Z_lo] operand of the router.
+// Z values beyond the FP16 range are stored saturated and recorded in *err as
+// QWEN_ERR_OVERFLOW (as are H values in reduce_swiglu).
 qwen_status reduce_resid_norm(const float* part, int splits, int B, int N,
                               const __nv_bfloat16* resid, const float* resid32, float* out32,
-                              const __nv_bfloat16* gamma, float eps, __half* z, cudaStream_t st,
-                              size_t z_stride = 0, __half* z_lo = nullptr);
-qwen_status reduce_swiglu(const float* part, int splits, int B, int f, __half* h,
+                              const __nv_bfloat16* gamma, float eps, __half* z, int* err,
+                              cudaStream_t st, size_t z_stride = 0, __half* z_lo = nullptr);
+qwen_status reduce_swiglu(const float* part, int splits, int B, int f, __half* h, int* err,
                           cudaStream_t st);
 qwen_status reduce_qkv(const float* part, int splits, int B, int Nqkv, const QkvParams& p,
                        int* err, cudaStream_t st);

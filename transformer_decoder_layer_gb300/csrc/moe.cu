@@ -489,7 +489,7 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
 
   // 1. RMSNorm_2 -> [Z_hi | Z_lo] (FP16 parts of the FP32 result)
   if (!z_ready && (s = rmsnorm_launch(r, L->gamma_mlp, z, true, nullptr, r32, T, d, c.rms_eps,
-                                      st, 0, 2 * (size_t)d, z + d)))
+                                      st, 0, 2 * (size_t)d, z + d, err)))
     return s;
   // 2. router logits (and the shared gate's, column E): one tensor-core GEMM
   // over K = 2d against [W_r | W_r]

@@ -66,15 +66,16 @@ __device__ __forceinline__ void qkv_head_finish(float (&v)[DH], int m, int head,
     }
   }
   const int b = m / p.T, t = m - (m / p.T) * p.T;
+  bool bad = false;  // an FP16 value (prefill Q, K/V copies) beyond the format's range
   auto store = [&](void* dst, bool f16_out, bool streaming = false) {
     uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
     for (int i = 0; i < DH / 8; ++i) {
       uint4 o;
-      o.x = pack2(v[8 * i], v[8 * i + 1], f16_out);
-      o.y = pack2(v[8 * i + 2], v[8 * i + 3], f16_out);
-      o.z = pack2(v[8 * i + 4], v[8 * i + 5], f16_out);
-      o.w = pack2(v[8 * i + 6], v[8 * i + 7], f16_out);
+      o.x = pack2_chk(v[8 * i], v[8 * i + 1], f16_out, bad);
+      o.y = pack2_chk(v[8 * i + 2], v[8 * i + 3], f16_out, bad);
+      o.z = pack2_chk(v[8 * i + 4], v[8 * i + 5], f16_out, bad);
+      o.w = pack2_chk(v[8 * i + 6], v[8 * i + 7], f16_out, bad);
       if (streaming)
         __stcs(d4 + i, o);
       else
@@ -87,6 +88,7 @@ __device__ __forceinline__ void qkv_head_finish(float (&v)[DH], int m, int head,
     // BF16 cache, so the attention's two operands always share a type
     store(static_cast<uint16_t*>(p.q_out) + (((size_t)b * p.Hq + head) * p.T + t) * DH,
           p.q_f16 != 0 && p.slot0[b] == 0);
+    record_overflow(err, bad);
     return;
   }
   const int slot = p.slot0[b] + t;
@@ -103,6 +105,7 @@ __device__ __forceinline__ void qkv_head_finish(float (&v)[DH], int m, int head,
   store((kind == 1 ? p.k_cache : p.v_cache) + (((size_t)b * p.Hkv + g) * p.max_seq + slot) * DH,
         false, fresh_read);
   if (fresh) store(fresh + (((size_t)b * p.Hkv + g) * p.T + t) * DH, true);
+  record_overflow(err, bad);
 }
 
 }  // namespace qwen

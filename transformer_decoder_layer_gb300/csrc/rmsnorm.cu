@@ -15,7 +15,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
                                                       void* __restrict__ y, bool y_f16,
                                                       float* __restrict__ y32, int rows, int d,
                                                       float eps, size_t xs, size_t ys,
-                                                      __half* __restrict__ y_lo) {
+                                                      __half* __restrict__ y_lo, int* err) {
   pdl_trigger();
   pdl_wait();
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
   const uint4* gr = reinterpret_cast<const uint4*>(gamma);
   uint4* yr = reinterpret_cast<uint4*>(static_cast<uint16_t*>(y) + (size_t)row * ys);
   uint4* lr = y_lo ? reinterpret_cast<uint4*>(y_lo + (size_t)row * ys) : nullptr;
+  bool bad = false;
 #pragma unroll
   for (int i = 0; i < MAXC; ++i) {
     const int c = lane + 32 * i;
@@ -75,10 +76,10 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
         o[2 * j + 1] = g.y * (v[i][2 * j + 1] * rstd);
       }
       uint4 out;
-      out.x = pack2(o[0], o[1], y_f16);
-      out.y = pack2(o[2], o[3], y_f16);
-      out.z = pack2(o[4], o[5], y_f16);
-      out.w = pack2(o[6], o[7], y_f16);
+      out.x = pack2_chk(o[0], o[1], y_f16, bad);
+      out.y = pack2_chk(o[2], o[3], y_f16, bad);
+      out.z = pack2_chk(o[4], o[5], y_f16, bad);
+      out.w = pack2_chk(o[6], o[7], y_f16, bad);
       yr[c] = out;
       if (lr) {
         // residual of the FP16 rounding, itself rounded to FP16
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float2 h = unpack_f16x2(hw[j]);
-          lo[j] = pack_f16x2(o[2 * j] - h.x, o[2 * j + 1] - h.y);
+          lo[j] = pack_f16x2_chk(o[2 * j] - h.x, o[2 * j + 1] - h.y, bad);
         }
         lr[c] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
@@ -98,6 +99,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
       }
     }
   }
+  record_overflow(err, bad);
 }
 
 // Few rows (decode batches): one CTA per row, one 8-element chunk per thread,
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
 __global__ void __launch_bounds__(1024) rmsnorm_row_kernel(
     const bf16* __restrict__ x, const float* __restrict__ x32, const bf16* __restrict__ gamma,
     void* __restrict__ y, bool y_f16, float* __restrict__ y32, int d, float eps, size_t xs,
-    size_t ys, __half* __restrict__ y_lo) {
+    size_t ys, __half* __restrict__ y_lo, int* err) {
   pdl_trigger();
   pdl_wait();
   __shared__ float red[32];
@@ -151,11 +153,12 @@ __global__ void __launch_bounds__(1024) rmsnorm_row_kernel(
     o[2 * j] = g.x * (v[2 * j] * rstd);
     o[2 * j + 1] = g.y * (v[2 * j + 1] * rstd);
   }
+  bool bad = false;
   uint4 out;
-  out.x = pack2(o[0], o[1], y_f16);
-  out.y = pack2(o[2], o[3], y_f16);
-  out.z = pack2(o[4], o[5], y_f16);
-  out.w = pack2(o[6], o[7], y_f16);
+  out.x = pack2_chk(o[0], o[1], y_f16, bad);
+  out.y = pack2_chk(o[2], o[3], y_f16, bad);
+  out.z = pack2_chk(o[4], o[5], y_f16, bad);
+  out.w = pack2_chk(o[6], o[7], y_f16, bad);
   reinterpret_cast<uint4*>(static_cast<uint16_t*>(y) + (size_t)row * ys)[c] = out;
   if (y_lo) {
     const uint32_t hw[4] = {out.x, out.y, out.z, out.w};
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(1024) rmsnorm_row_kernel(
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float2 h = unpack_f16x2(hw[j]);
-      lo[j] = pack_f16x2(o[2 * j] - h.x, o[2 * j + 1] - h.y);
+      lo[j] = pack_f16x2_chk(o[2 * j] - h.x, o[2 * j + 1] - h.y, bad);
     }
     reinterpret_cast<uint4*>(y_lo + (size_t)row * ys)[c] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
@@ -172,11 +175,12 @@ __global__ void __launch_bounds__(1024) rmsnorm_row_kernel(
     y4[2 * c] = make_float4(o[0], o[1], o[2], o[3]);
     y4[2 * c + 1] = make_float4(o[4], o[5], o[6], o[7]);
   }
+  record_overflow(err, bad);
 }
 
 qwen_status rmsnorm_launch(const bf16* x, const bf16* gamma, void* y, bool y_f16, float* y32,
                            const float* x32, int rows, int d, float eps, cudaStream_t st,
-                           size_t x_stride, size_t y_stride, __half* y_lo) {
+                           size_t x_stride, size_t y_stride, __half* y_lo, int* err) {
   if (rows == 0) return QWEN_OK;
   if (d <= 0 || (d & 7) || d > 8192) return QWEN_ERR_UNSUPPORTED;
   const size_t xs = x_stride ? x_stride : (size_t)d;
@@ -185,7 +189,7 @@ qwen_status rmsnorm_launch(const bf16* x, const bf16* gamma, void* y, bool y_f16
   if (rows <= 2 * device_sm_count()) {
     const int threads = ((d >> 3) + 31) & ~31;  // <= 1024 for d <= 8192
     launch_k(rmsnorm_row_kernel, dim3(rows), dim3(threads), 0, st, x, x32, gamma, y, y_f16, y32, d,
-             eps, xs, ys, y_lo);
+             eps, xs, ys, y_lo, err);
     count_launches();
     return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
   }
@@ -193,13 +197,13 @@ qwen_status rmsnorm_launch(const bf16* x, const bf16* gamma, void* y, bool y_f16
   const int blocks = (rows * 32 + threads - 1) / threads;
   if (d <= 2048)
     launch_k(rmsnorm_kernel<8>, dim3(blocks), dim3(threads), 0, st, x, x32, gamma, y, y_f16, y32,
-             rows, d, eps, xs, ys, y_lo);
+             rows, d, eps, xs, ys, y_lo, err);
   else if (d <= 4096)
     launch_k(rmsnorm_kernel<16>, dim3(blocks), dim3(threads), 0, st, x, x32, gamma, y, y_f16, y32,
-             rows, d, eps, xs, ys, y_lo);
+             rows, d, eps, xs, ys, y_lo, err);
   else
     launch_k(rmsnorm_kernel<32>, dim3(blocks), dim3(threads), 0, st, x, x32, gamma, y, y_f16, y32,
-             rows, d, eps, xs, ys, y_lo);
+             rows, d, eps, xs, ys, y_lo, err);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
