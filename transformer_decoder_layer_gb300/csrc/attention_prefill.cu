@@ -8,11 +8,15 @@
 // repeat) and tiles above the diagonal are skipped.  §12 of the Qwen3 page: the
 // [T,T] probability matrix is never written to memory.
 //
-// One CTA = one sequence b, one KV group g, two query heads of that group (A
-// and B; B absent for the last head of an odd-sized group) and one tile of 128
-// query rows.  Both heads read every staged K/V tile: a single SM's TMA
-// delivers about 64 bytes per cycle, and one head alone would need a 64 KB K/V
-// tile per 1024 cycles of MMA work; two heads halve that.
+// Persistent: one CTA per SM walks a list of work items.  A work item = one
+// sequence b, one KV group g, two query heads of that group (A and B; B absent
+// for the last head of an odd-sized group, or in every item when one head per
+// item is chosen for short sequences) and one tile of 128 query rows.  Both
+// heads read every staged K/V tile: a single SM's TMA delivers about 64 bytes
+// per cycle, and one head alone would need a 64 KB K/V tile per 1024 cycles of
+// MMA work; two heads halve that.  Items are numbered heaviest first and dealt
+// to the CTAs in a snake order; the K/V ring and the S/P/O hand-offs carry
+// over from one item to the next.
 //   warp 0      TMA: Q_A, Q_B once, then K (2 stages) and V (1 stage) tiles of
 //               128 keys, in the order K(j+1), V(j)
 //   warps 1, 2  MMA issuers of head A and head B (TMEM allocation by warp 1):
