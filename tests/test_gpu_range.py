@@ -134,3 +134,27 @@ def test_create_refuses_weights_beyond_fp16(value, ok):
         with pytest.raises(q.QwenError) as e:
             GpuLayer(SHAPE, w, max_tokens=8, max_batch=1, max_seq=8, max_position=8)
         assert e.value.code == QWEN_ERR_OVERFLOW
+
+
+def test_chunked_prefill_over_large_cached_values_reports_overflow():
+    """Prefill of a chunk onto a filled cache reads the cached BF16 K/V: cached
+    V rows of 1e5 give attention outputs past 65504 in the prefill attention
+    kernel's read-out.  The first sequence has an ordinary cache and must
+    still match the oracle."""
+    B, T, L = 2, 64, 100
+    w = synth.layer_weights(SHAPE, "range_pfkv")
+    x = synth.activations([B, T, SHAPE.d], "range_pfkv")
+    kc, vc = synth.kv_cache(B, SHAPE.n_kv_heads, L + T, SHAPE.head_dim, [L, L], "range_pfkv")
+    vc[1, :, :L] = 1.0e5
+    g = GpuLayer(SHAPE, w, max_tokens=B * T, max_batch=B, max_seq=L + T, max_position=L + T)
+    kd, vd = kc.cuda(), vc.cuda()
+    pos = torch.arange(L, L + T, dtype=torch.int32, device="cuda").repeat(B)
+    start = torch.full((B,), L, dtype=torch.int32, device="cuda")
+    y = g.layer.prefill(x.cuda(), pos, start, kd, vd,
+                        out=torch.empty((B, T, SHAPE.d), dtype=torch.bfloat16, device="cuda"))
+    assert g.layer.poll_error() == QWEN_ERR_OVERFLOW
+    assert torch.isfinite(y.float()).all()
+    kk, vv = f64(kc[0]), f64(vc[0])
+    ref = oracle.layer_forward(f64(x)[0], synth.weights_f64(w), SHAPE.as_dict(),
+                               np.arange(L, L + T), kk, vv, np.arange(L, L + T))
+    assert_parity(f64(y.float())[0], ref, what="the sequence with an ordinary cache")

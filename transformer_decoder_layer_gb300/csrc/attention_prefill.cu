@@ -73,6 +73,13 @@ __device__ __forceinline__ void fma_pair(float s0, float s1, uint64_t c2, uint64
   asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(d));
 }
 
+// Two products x0 c, x1 c by one packed FP32 multiply.
+__device__ __forceinline__ void mul_pair(float x0, float x1, uint64_t c2, float& y0, float& y1) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(f32x2(x0, x1)), "l"(c2));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(y0), "=f"(y1) : "l"(d));
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -211,9 +218,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV,
                         const __grid_constant__ CUtensorMap tmK16,
-                        const __grid_constant__ CUtensorMap tmV16, AttnArgs a) {
+                        const __grid_constant__ CUtensorMap tmV16,
+                        const __grid_constant__ CUtensorMap tmO, AttnArgs a) {
   pdl_trigger();
-  pdl_wait();
   using C = AttnCfg<DH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -235,7 +242,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t* o_done = bars + 15;   // [2] per head: O_x += P_x V complete
   uint64_t* o_free = bars + 17;   // [2] per head: the item's O_x has been read out
   uint64_t* mma_idle = bars + 19; // [2] per head
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
+  uint64_t* staged = bars + 21;   // [2] per head: the item's output rows are in P_x
+  uint64_t* st_read = bars + 23;  // [2] per head: the output store has read P_x
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 25);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -271,6 +280,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&o_done[x], 1);
       mbar_init(&o_free[x], 128);
       mbar_init(&mma_idle[x], 1);
+      mbar_init(&staged[x], 128);
+      mbar_init(&st_read[x], 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -283,6 +294,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // barrier and TMEM set-up overlap the previous kernel's tail; everything
+  // below reads what it wrote (Q, the K/V rows, the slot offsets)
+  pdl_wait();
 
   if (warp == 0) {
     // TMA producer, converged; one elected lane issues.  Per item: Q once the
@@ -456,6 +470,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint8_t* prow = sP + x * C::P_BYTES + r * 128;  // this row in P's two swizzle blocks
     int c = 0, vcount = 0;  // head x's S tiles and this CTA's V tiles before the item
     bool ok = true;
+    int n_out = 0;  // output tiles of head x staged so far
+    const bool issuer = qw == 3 && lane == 0;  // issues head x's output stores
     for (int ni = 0, it = item_of(0); ok && it >= 0; it = item_of(++ni)) {
       const AttnItem I = attn_item(it, a);
       if (x >= I.nq) {
@@ -531,6 +547,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           // the previous item's epilogue already waited for its last P.V.
           if (!mbar_wait(&o_done[x], (cj - 1) & 1, abort_flag, a.err)) { ok = false; break; }
           tc_fence_after();
+        } else if (n_out > 0) {
+          // the previous item's output store reads P_x: wait until it has
+          if (issuer) {
+            bulk_wait_group_read0();
+            mbar_arrive(&st_read[x]);
+          }
+          if (!mbar_wait(&st_read[x], (n_out - 1) & 1, abort_flag, a.err)) { ok = false; break; }
         }
 #pragma unroll
         for (int q = 0; q < 8; ++q)
@@ -579,40 +602,68 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_arrive(&p_full[x]);
       }
       if (!ok) break;
-      // epilogue: O / l of this item, then O_x is free for the next item
+      // epilogue: O / l of this item, then O_x is free for the next item.
+      // The last P.V has completed, so P_x's buffer is free: the rows are
+      // written there in P's 128-byte-swizzled layout, which is the layout a
+      // TMA store of two 64-column boxes reads, and one thread of the head
+      // stores the tile asynchronously (rows past the sequence's end are
+      // clipped by the tensor map's T extent).
       if (!mbar_wait(&o_done[x], (c + I.n_kv - 1) & 1, abort_flag, a.err)) break;
       tc_fence_after();
       const float inv_l = 1.f / l_sum;
-      const bool row_ok = t < a.T;
-      f16* dst = a.out + ((size_t)I.b * a.T + t) * (size_t)(a.Hq * DH) + (size_t)(I.hA + x) * DH;
+      const uint64_t inv2 = f32x2(inv_l, inv_l);
       bool bad = false;  // C is the next GEMM's FP16 operand: V rows past 65504 reach it
 #pragma unroll 1
-      for (int q = 0; q < DH / 32; ++q) {
-        uint32_t oo[32];
-        tmem_ld32_wait(o_addr + 32 * q, oo);
-        if (row_ok) {
+      for (int h = 0; h < DH / 64; ++h) {  // 64 columns = one swizzle block of the row
+        uint32_t oo[64];
+        tmem_ld32(o_addr + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(oo));
+        tmem_ld32(o_addr + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(oo + 32));
+        tmem_ld_wait();
+        float f[64];
+        float mx = 0.f;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float f[8];
+        for (int i = 0; i < 64; i += 2) {
+          mul_pair(__uint_as_float(oo[i]), __uint_as_float(oo[i + 1]), inv2, f[i], f[i + 1]);
+          mx = max3(mx, fabsf(f[i]), fabsf(f[i + 1]));
+        }
+        // the common case converts plainly; a row that FP16 cannot hold
+        // (|o| >= 65520, or NaN) takes the saturating conversion
+        const bool sat = !(mx < 65520.f);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(oo[8 * e + i]) * inv_l;
-            uint4 w;
-            w.x = pack_f16x2_chk(f[0], f[1], bad);
-            w.y = pack_f16x2_chk(f[2], f[3], bad);
-            w.z = pack_f16x2_chk(f[4], f[5], bad);
-            w.w = pack_f16x2_chk(f[6], f[7], bad);
-            reinterpret_cast<uint4*>(dst + 32 * q)[e] = w;
+        for (int q = 0; q < 8; ++q) {
+          uint32_t w[4];
+          if (sat) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[e] = pack_f16x2_chk(f[8 * q + 2 * e], f[8 * q + 2 * e + 1], bad);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[e] = pack_f16x2(f[8 * q + 2 * e], f[8 * q + 2 * e + 1]);
           }
+          *reinterpret_cast<uint4*>(prow + h * (kQT * 128) + ((q ^ (r & 7)) << 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      record_overflow(a.err, bad);
       tc_fence_before();
-      mbar_arrive(&o_free[x]);
+      mbar_arrive(&o_free[x]);  // O_x has been read: the next item's P.V may overwrite it
+      record_overflow(a.err, bad);
+      fence_proxy_async_smem();  // the staged rows are visible to the TMA store
+      mbar_arrive(&staged[x]);
+      if (issuer) {
+        if (!mbar_wait(&staged[x], n_out & 1, abort_flag, a.err)) break;
+#pragma unroll
+        for (int h = 0; h < DH / 64; ++h)
+          tma_store_3d(&tmO, sP + x * C::P_BYTES + h * (kQT * 128), (I.hA + x) * DH + 64 * h, I.t0,
+                       I.b);
+        bulk_commit_group();
+      }
+      ++n_out;
       c += I.n_kv;
       vcount += I.n_kv;
     }
   }
 
+  // the output stores this CTA issued are complete before its shared memory goes
+  if (warp >= 3 && (warp & 3) == 3 && lane == 0) bulk_wait_group0();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -649,10 +700,25 @@ static bool tmap_rows_dh(CUtensorMap* m, const void* base, uint64_t rows, int dh
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The attention output [B][T][Hq * dh] FP16 as a 3-D map with boxes of 64
+// columns x 128 rows of one sequence, so a tile's rows past T are clipped
+// instead of landing in the next sequence.
+static bool tmap_out(CUtensorMap* m, const void* base, int B, int T, int width) {
+  auto enc = encode_fn();
+  if (!enc || (reinterpret_cast<uintptr_t>(base) & 15) || ((width * 2) & 15)) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)T * width * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int DH>
 static qwen_status launch_dh(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                             const CUtensorMap& k16, const CUtensorMap& v16, const AttnArgs& a,
-                             cudaStream_t st) {
+                             const CUtensorMap& k16, const CUtensorMap& v16, const CUtensorMap& o,
+                             const AttnArgs& a, cudaStream_t st) {
   auto kern = attn_prefill_kernel<DH>;
   static std::atomic<uint64_t> attr{0};  // one bit per device
   if (!smem_attr_once(kern, AttnCfg<DH>::SMEM_BYTES, attr)) return QWEN_ERR_CUDA;
@@ -662,7 +728,7 @@ static qwen_status launch_dh(const CUtensorMap& q, const CUtensorMap& k, const C
   const int sms = device_sm_count();
   const int grid = items < sms ? (int)items : sms;  // persistent: one CTA per SM
   launch_k(kern, dim3(grid), dim3(kAttnThreads), AttnCfg<DH>::SMEM_BYTES, st, q, k, v, k16, v16,
-           a);
+           o, a);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
@@ -679,6 +745,8 @@ qwen_status attention_prefill(const f16* q, const bf16* k_cache, const bf16* v_c
   if (!tmap_rows_dh(&tv, v_cache, (uint64_t)B * Hkv * max_seq, dh, false)) return QWEN_ERR_CUDA;
   if (!tmap_rows_dh(&tk16, k16, (uint64_t)B * Hkv * T, dh, true)) return QWEN_ERR_CUDA;
   if (!tmap_rows_dh(&tv16, v16, (uint64_t)B * Hkv * T, dh, true)) return QWEN_ERR_CUDA;
+  CUtensorMap to;
+  if (!tmap_out(&to, out, B, T, Hq * dh)) return QWEN_ERR_CUDA;
   AttnArgs a;
   a.B = B; a.T = T; a.Hq = Hq; a.Hkv = Hkv; a.max_seq = max_seq;
   a.slot0 = slot0; a.out = out; a.err = err;
@@ -690,8 +758,8 @@ qwen_status attention_prefill(const f16* q, const bf16* k_cache, const bf16* v_c
     const long long pairs = (long long)((T + kQT - 1) / kQT) * B * Hkv * ((Hq / Hkv + 1) / 2);
     a.hpi = pairs * 2 < 3LL * device_sm_count() ? 1 : 2;
   }
-  if (dh == 128) return launch_dh<128>(tq, tk, tv, tk16, tv16, a, st);
-  if (dh == 64) return launch_dh<64>(tq, tk, tv, tk16, tv16, a, st);
+  if (dh == 128) return launch_dh<128>(tq, tk, tv, tk16, tv16, to, a, st);
+  if (dh == 64) return launch_dh<64>(tq, tk, tv, tk16, tv16, to, a, st);
   return QWEN_ERR_UNSUPPORTED;
 }
 

@@ -287,6 +287,29 @@ __device__ __forceinline__ void tma_load_2d_w(void* dst, const CUtensorMap* map,
       : "memory");
 }
 
+// 3-D tiled store from shared memory (bulk-group completion), one thread.
+// The shared-memory source must be made visible to the async proxy first
+// (fence_proxy_async_smem by every writing thread, then a barrier).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0,
+                                             int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The stores committed so far have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// The stores committed so far are complete (their writes performed).
+__device__ __forceinline__ void bulk_wait_group0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // 4-D tiled load (the blocked weight layout: coordinates {0, 0, k-tile,
 // row-tile}), issued by one elected lane of a converged warp.
 __device__ __forceinline__ void tma_load_4d_w(void* dst, const CUtensorMap* map, uint64_t* bar,
