@@ -576,7 +576,11 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t u) {
   return __bfloat1622float2(v);
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+// SiLU(z) = z / (1 + e^-z).  The division uses the approximate reciprocal
+// (relative error about 2^-21, far below the FP16/BF16 rounding of every
+// result it feeds); for z < -87 the denominator overflows and the result is
+// 0, SiLU's limit.
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

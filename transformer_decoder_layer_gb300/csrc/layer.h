@@ -105,6 +105,17 @@ constexpr int kMoeDecodeMaxRows = 64;
 // Bytes of FP32 partials the decode GEMM of the layer needs for batch B.
 size_t decode_part_bytes(const qwen_layer_config& c, int B);
 
+// Expert GEMMs with the weights on the MMA's M side (moe_gemm.cu): W a packed
+// blocked stack [E][Nw][K], X the routed rows [rows][K] grouped by expert
+// (rows [offsets[e], offsets[e+1]) for expert e, offsets on the device).
+// swiglu: W interleaves gate and up rows in 64-row blocks and out = H [rows]
+// [Nw / 2] = SiLU(gate) * up; else out = X W_e^T [rows][Nw].  FP16 out, row
+// stride ldo.  Supported when Nw % 256 == 0, K % 64 == 0 and E <= 256.
+bool gemm_expert_supported(int E, int Nw, int K);
+qwen_status gemm_expert(const __half* W, int E, int Nw, int K, const __half* X, int rows, int ldx,
+                        const int32_t* offsets, __half* out, int ldo, bool swiglu, int* err,
+                        cudaStream_t st);
+
 // CTAs of the MoE permutation for `entries` (token, slot) pairs (1024 each).
 int moe_perm_blocks(size_t entries);
 // Attention split-KV plan: number of splits per (sequence, KV head) for batch B.

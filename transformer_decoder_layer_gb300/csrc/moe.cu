@@ -589,24 +589,32 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
     if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;
     return copy_routing(idx, wts, logits, topk_idx_out, topk_w_out, logits_out, T, E, R, k, st);
   }
-  GemmEpilogue eg{};
-  eg.mode = EPI_SWIGLU;
-  eg.out = hp;
-  eg.out_f16 = 1;
-  eg.ldo = mf;
-  eg.group_offsets = offsets;
-  eg.n_groups = E;
-  eg.b_blocked = 1;
-  if ((s = gemm_tc(zp, d, L->w_gu, d, n, 2 * mf, d, true, eg, err, st))) return s;
-  GemmEpilogue ed{};
-  ed.mode = EPI_STORE;
-  ed.out = yp;
-  ed.out_f16 = 1;
-  ed.ldo = d;
-  ed.group_offsets = offsets;
-  ed.n_groups = E;
-  ed.b_blocked = 1;
-  if ((s = gemm_tc(hp, mf, L->w_down, mf, n, d, mf, true, ed, err, st))) return s;
+  if (gemm_expert_supported(E, 2 * mf, d) && gemm_expert_supported(E, d, mf)) {
+    // weights on the M side, routed rows in chunks of up to 256 (moe_gemm.cu)
+    if ((s = gemm_expert(L->w_gu, E, 2 * mf, d, zp, n, d, offsets, hp, mf, true, err, st)))
+      return s;
+    if ((s = gemm_expert(L->w_down, E, d, mf, hp, n, mf, offsets, yp, d, false, err, st)))
+      return s;
+  } else {
+    GemmEpilogue eg{};
+    eg.mode = EPI_SWIGLU;
+    eg.out = hp;
+    eg.out_f16 = 1;
+    eg.ldo = mf;
+    eg.group_offsets = offsets;
+    eg.n_groups = E;
+    eg.b_blocked = 1;
+    if ((s = gemm_tc(zp, d, L->w_gu, d, n, 2 * mf, d, true, eg, err, st))) return s;
+    GemmEpilogue ed{};
+    ed.mode = EPI_STORE;
+    ed.out = yp;
+    ed.out_f16 = 1;
+    ed.ldo = d;
+    ed.group_offsets = offsets;
+    ed.n_groups = E;
+    ed.b_blocked = 1;
+    if ((s = gemm_tc(hp, mf, L->w_down, mf, n, d, mf, true, ed, err, st))) return s;
+  }
   // 7. weighted combine (+ gated shared expert) + residual
   launch_k(combine_kernel<false>, dim3(nblk((long long)T * (d / 8), 256)), dim3(256), 0, st,
            (const f16*)yp, (const float*)nullptr, 1, (size_t)0, (const int32_t*)inv,
