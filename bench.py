@@ -252,7 +252,8 @@ class DecodeBench:
         return a.elapsed_time(b), h2d, d2h
 
 
-def prefill_bench(q, torch, shape, B, T, steps, warmup, peak_tflops, tag="bench_prefill"):
+def prefill_bench(q, torch, shape, B, T, steps, warmup, peak_tflops, tag="bench_prefill",
+                  hbm_gbs=6659.3):
     import synth
     dev = torch.device("cuda")
     w = {k: v.to(dev) for k, v in synth.layer_weights(shape, tag).items()}
@@ -279,7 +280,7 @@ def prefill_bench(q, torch, shape, B, T, steps, warmup, peak_tflops, tag="bench_
         torch.cuda.synchronize()
         tot.append(t0.elapsed_time(t1))
     # the stages, from trace events around each
-    stages = ["qkv", "attn", "o", "gate_up", "down"]
+    stages = ["norm1", "qkv", "attn", "o", "norm2", "gate_up", "down"]
     per = {s: [] for s in stages}
     traced = []
     for _ in range(steps):
@@ -308,9 +309,17 @@ def prefill_bench(q, torch, shape, B, T, steps, warmup, peak_tflops, tag="bench_
     attn_exec = 2 * B * hq * dh * T * (T + 1)
     flops = {"qkv": 2 * M * d * (hq * dh + 2 * shape.n_kv_heads * dh), "attn": attn_exec,
              "o": 2 * M * hq * dh * d, "gate_up": 2 * M * d * 2 * f, "down": 2 * M * f * d}
+    # the norms are HBM-bound: RMSNorm_1 reads X (BF16) and writes X-hat (FP16),
+    # RMSNorm_2 reads R (FP32) and writes Z (FP16)
+    norm_bytes = {"norm1": M * d * (2 + 2), "norm2": M * d * (4 + 2)}
     kern = {}
     for s in stages:
         t = statistics.median(per[s])
+        if s in norm_bytes:
+            gbs = norm_bytes[s] / (t * 1e-3) / 1e9
+            kern[s] = {"ms": round(t, 4), "GB_per_s": round(gbs, 1),
+                       "frac_hbm": round(gbs / hbm_gbs, 3)}
+            continue
         tf = flops[s] / (t * 1e-3) / 1e12
         kern[s] = {"ms": round(t, 4), "tflops": round(tf, 1), "frac": round(tf / peak_tflops, 3)}
     del layer
@@ -890,7 +899,7 @@ def main():
     if rank == 0 and not args.no_prefill:
         pf = []
         for (pb, pt) in ((1, 4096), (1, 1024), (8, 1024), (1, 16384)):
-            pf.append(prefill_bench(q, torch, synth.QWEN3_8B, pb, pt, 5, 3, bf16_tf))
+            pf.append(prefill_bench(q, torch, synth.QWEN3_8B, pb, pt, 5, 3, bf16_tf, hbm_gbs=hbm_gbs))
         line["prefill"] = pf
     if rank == 0 and not args.no_prefill:
         line["moe_prefill"] = moe_prefill_bench(q, torch, bf16_tf)

@@ -1,14 +1,37 @@
-// RMSNorm over the feature axis, one warp per row, 128-bit loads/stores.
+// RMSNorm over the feature axis, 128-bit loads/stores.
 //
 // Qwen3 layer page ("推理系统 03"), §3: y_j = gamma_j x_j / sqrt(mean_k x_k^2 + eps),
-// with the mean square accumulated in FP32.  The whole row stays in registers
-// between the reduction and the scaling, so each element is read once.
+// with the mean square accumulated in FP32.
 #include "common.cuh"
 #include "internal.h"
 
 namespace qwen {
 
-template <int MAXC>
+// 8 elements of chunk c of a row (BF16 or FP32 input) as FP32.
+__device__ __forceinline__ void rms_load8(const bf16* __restrict__ xr, const float* __restrict__ xr32,
+                                          int c, float (&v)[8]) {
+  if (xr32) {
+    const float4 a = reinterpret_cast<const float4*>(xr32)[2 * c];
+    const float4 b = reinterpret_cast<const float4*>(xr32)[2 * c + 1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 u = reinterpret_cast<const uint4*>(xr)[c];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = unpack_bf16x2(w[j]);
+      v[2 * j] = f.x;
+      v[2 * j + 1] = f.y;
+    }
+  }
+}
+
+// One warp per row, two passes: the sum of squares over the row (loads of
+// several 512-byte row segments in flight per warp), then the row again (now
+// in L1 or L2), scaled and stored.  Keeping the whole row in registers
+// instead (128 values per lane at d = 4096) left room for 8 warps per SM and
+// reached a quarter to half of the HBM bandwidth.
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x,
                                                       const float* __restrict__ x32,
                                                       const bf16* __restrict__ gamma,
@@ -22,39 +45,15 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   const int nch = d >> 3;  // 8-element chunks
-  float v[MAXC][8];
+  const bf16* xr = x32 ? nullptr : x + (size_t)row * xs;
+  const float* xr32 = x32 ? x32 + (size_t)row * xs : nullptr;
   float ss = 0.f;
-  if (x32) {
-    const float4* xr = reinterpret_cast<const float4*>(x32 + (size_t)row * xs);
+#pragma unroll 8
+  for (int c = lane; c < nch; c += 32) {
+    float v[8];
+    rms_load8(xr, xr32, c, v);
 #pragma unroll
-    for (int i = 0; i < MAXC; ++i) {
-      const int c = lane + 32 * i;
-      if (c < nch) {
-        const float4 a = xr[2 * c], b = xr[2 * c + 1];
-        v[i][0] = a.x; v[i][1] = a.y; v[i][2] = a.z; v[i][3] = a.w;
-        v[i][4] = b.x; v[i][5] = b.y; v[i][6] = b.z; v[i][7] = b.w;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) ss = fmaf(v[i][j], v[i][j], ss);
-      }
-    }
-  } else {
-    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)row * xs);
-#pragma unroll
-    for (int i = 0; i < MAXC; ++i) {
-      const int c = lane + 32 * i;
-      if (c < nch) {
-        const uint4 u = xr[c];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f = unpack_bf16x2(w[j]);
-          v[i][2 * j] = f.x;
-          v[i][2 * j + 1] = f.y;
-          ss = fmaf(f.x, f.x, ss);
-          ss = fmaf(f.y, f.y, ss);
-        }
-      }
-    }
+    for (int j = 0; j < 8; ++j) ss = fmaf(v[j], v[j], ss);
   }
   ss = warp_sum(ss);
   const float rstd = rsqrtf(ss / (float)d + eps);
@@ -62,41 +61,40 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
   uint4* yr = reinterpret_cast<uint4*>(static_cast<uint16_t*>(y) + (size_t)row * ys);
   uint4* lr = y_lo ? reinterpret_cast<uint4*>(y_lo + (size_t)row * ys) : nullptr;
   bool bad = false;
+#pragma unroll 4
+  for (int c = lane; c < nch; c += 32) {
+    float v[8];
+    rms_load8(xr, xr32, c, v);
+    const uint4 gu = gr[c];
+    const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w};
+    float o[8];
 #pragma unroll
-  for (int i = 0; i < MAXC; ++i) {
-    const int c = lane + 32 * i;
-    if (c < nch) {
-      const uint4 gu = gr[c];
-      const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w};
-      float o[8];
+    for (int j = 0; j < 4; ++j) {
+      const float2 g = unpack_bf16x2(gw[j]);
+      o[2 * j] = g.x * (v[2 * j] * rstd);
+      o[2 * j + 1] = g.y * (v[2 * j + 1] * rstd);
+    }
+    uint4 out;
+    out.x = pack2_chk(o[0], o[1], y_f16, bad);
+    out.y = pack2_chk(o[2], o[3], y_f16, bad);
+    out.z = pack2_chk(o[4], o[5], y_f16, bad);
+    out.w = pack2_chk(o[6], o[7], y_f16, bad);
+    yr[c] = out;
+    if (lr) {
+      // residual of the FP16 rounding, itself rounded to FP16
+      const uint32_t hw[4] = {out.x, out.y, out.z, out.w};
+      uint32_t lo[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float2 g = unpack_bf16x2(gw[j]);
-        o[2 * j] = g.x * (v[i][2 * j] * rstd);
-        o[2 * j + 1] = g.y * (v[i][2 * j + 1] * rstd);
+        const float2 h = unpack_f16x2(hw[j]);
+        lo[j] = pack_f16x2_chk(o[2 * j] - h.x, o[2 * j + 1] - h.y, bad);
       }
-      uint4 out;
-      out.x = pack2_chk(o[0], o[1], y_f16, bad);
-      out.y = pack2_chk(o[2], o[3], y_f16, bad);
-      out.z = pack2_chk(o[4], o[5], y_f16, bad);
-      out.w = pack2_chk(o[6], o[7], y_f16, bad);
-      yr[c] = out;
-      if (lr) {
-        // residual of the FP16 rounding, itself rounded to FP16
-        const uint32_t hw[4] = {out.x, out.y, out.z, out.w};
-        uint32_t lo[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 h = unpack_f16x2(hw[j]);
-          lo[j] = pack_f16x2_chk(o[2 * j] - h.x, o[2 * j + 1] - h.y, bad);
-        }
-        lr[c] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
-      if (y32) {
-        float4* y4 = reinterpret_cast<float4*>(y32 + (size_t)row * d);
-        y4[2 * c] = make_float4(o[0], o[1], o[2], o[3]);
-        y4[2 * c + 1] = make_float4(o[4], o[5], o[6], o[7]);
-      }
+      lr[c] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    if (y32) {
+      float4* y4 = reinterpret_cast<float4*>(y32 + (size_t)row * d);
+      y4[2 * c] = make_float4(o[0], o[1], o[2], o[3]);
+      y4[2 * c + 1] = make_float4(o[4], o[5], o[6], o[7]);
     }
   }
   record_overflow(err, bad);
@@ -195,15 +193,8 @@ qwen_status rmsnorm_launch(const bf16* x, const bf16* gamma, void* y, bool y_f16
   }
   const int threads = 256;
   const int blocks = (rows * 32 + threads - 1) / threads;
-  if (d <= 2048)
-    launch_k(rmsnorm_kernel<8>, dim3(blocks), dim3(threads), 0, st, x, x32, gamma, y, y_f16, y32,
-             rows, d, eps, xs, ys, y_lo, err);
-  else if (d <= 4096)
-    launch_k(rmsnorm_kernel<16>, dim3(blocks), dim3(threads), 0, st, x, x32, gamma, y, y_f16, y32,
-             rows, d, eps, xs, ys, y_lo, err);
-  else
-    launch_k(rmsnorm_kernel<32>, dim3(blocks), dim3(threads), 0, st, x, x32, gamma, y, y_f16, y32,
-             rows, d, eps, xs, ys, y_lo, err);
+  launch_k(rmsnorm_kernel, dim3(blocks), dim3(threads), 0, st, x, x32, gamma, y, y_f16, y32, rows,
+           d, eps, xs, ys, y_lo, err);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
