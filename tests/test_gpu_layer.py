@@ -213,6 +213,30 @@ def test_decode_batch_64_dh128_g8():
     assert_parity(y, ref, what="Y")
 
 
+def test_prefill_reproducible_bit_for_bit():
+    """T=512 of a d=1024 layer (GEMMs of fewer tiles than SMs, split-tail
+    tiles, split attention work items): the result matches the oracle and is
+    the same, bit for bit, on every run."""
+    shape = QWEN3_SMALL
+    T = 512
+    w_cpu = synth.layer_weights(shape, "repro")
+    x = synth.activations([1, T, shape.d], "repro")
+    g = GpuLayer(shape, w_cpu, T, 1, T, T)
+    pos = np.arange(T)[None]
+    outs = []
+    for _ in range(3):
+        kc, vc = (torch.zeros((1, shape.n_kv_heads, T, shape.head_dim), dtype=torch.bfloat16,
+                              device="cuda") for _ in range(2))
+        outs.append((g.prefill(x, pos, [0], kc, vc), kc, vc))
+    for y, kc, vc in outs[1:]:
+        assert torch.equal(y, outs[0][0])
+        assert torch.equal(kc, outs[0][1]) and torch.equal(vc, outs[0][2])
+    z = np.zeros((1, shape.n_kv_heads, T, shape.head_dim))
+    ref, k_ref, _ = oracle_prefill(shape, synth.weights_f64(w_cpu), f64(x), pos, [0], z, z)
+    assert_parity(f64(outs[0][0].float()), ref, what="Y")
+    assert_parity(f64(outs[0][1].float()), k_ref, what="K cache")
+
+
 def test_causality_bit_exact_on_gpu():
     """Changing the last position leaves earlier rows bit-identical (推理系统 03 §14)."""
     shape = QWEN3_SMALL

@@ -24,6 +24,7 @@
 // own running max / sum / O; the warps merge through shared memory and the
 // unit's unnormalised partial (m, l, O) goes to a workspace.  A merge kernel
 // combines the slots of each head in a fixed order (deterministic).
+#include <algorithm>
 #include <cmath>
 
 #include "common.cuh"
@@ -422,42 +423,71 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
 
 // out[b][h*DH + d] = sum_s 2^(m_s - M) o_s[d] / sum_s 2^(m_s - M) l_s over the
 // slots s that CTAs wrote for head h's (sequence, KV head) pair: the CTAs whose
-// block ranges meet the pair's [p * nbv, (p + 1) * nbv).  One CTA per (b, h),
-// one thread per dh element: every thread reads the slots' (m, l) pairs (the
-// same addresses: broadcast) for M, then sums its element over the slots with
-// many partial-output loads in flight (a warp per head, 4 slots at a time,
-// took 12 us at B=1 with 34 slots per head).
+// block ranges meet the pair's [p * nbv, (p + 1) * nbv).  One CTA per (b, h)
+// of SG groups of DH threads: thread (j, t) takes slots j, j + SG, ... of
+// element t, up to 8 slots' loads in flight at once, and merges them in slot
+// order with a running maximum (sums rescaled by 2^(old max - new max) when it
+// grows); the groups' results are then merged in order j = 0, 1, .. through
+// shared memory.  A slot whose key range was empty has m = -inf and adds
+// nothing.
+__device__ __forceinline__ void merge_in(float m, float l, float o, float& M, float& L, float& A) {
+  if (m == -INFINITY) return;
+  if (m > M) {
+    const float f = ex2f(M - m);  // 0 while M is -inf
+    L = fmaf(L, f, l);
+    A = fmaf(A, f, o);
+    M = m;
+  } else {
+    const float f = ex2f(m - M);
+    L = fmaf(f, l, L);
+    A = fmaf(f, o, A);
+  }
+}
+
 template <int DH>
-__global__ void __launch_bounds__(DH) attn_decode_merge_kernel(
+__global__ void __launch_bounds__(1024) attn_decode_merge_kernel(
     const float* __restrict__ part_o, const float* __restrict__ part_ml, int BH, int slots,
     int G, int nbv, int per, f16* __restrict__ out, int* err) {
   pdl_trigger();
   pdl_wait();
+  __shared__ float sm_m[1024 / DH], sm_l[1024 / DH];
+  __shared__ float sm_a[1024];
   const int wid = blockIdx.x;  // b * Hq + h
-  const int t = threadIdx.x;   // dh element
+  const int t = threadIdx.x % DH, j = threadIdx.x / DH;
+  const int SG = blockDim.x / DH;
   if (wid >= BH) return;
   const long long pair = wid / G;  // (b * Hq + h) / G = b * Hkv + h / G
   const int splits = (int)(((pair + 1) * nbv - 1) / per - (pair * nbv) / per) + 1;
   const float* ml = part_ml + (size_t)wid * slots * 2;
-  // both passes unrolled and branch-free, so their loads are issued together
-  // rather than one L2 round trip after another
-  float M = -INFINITY;
-#pragma unroll 16
-  for (int s = 0; s < splits; ++s) M = fmaxf(M, ml[2 * s]);
   const float* po = part_o + (size_t)wid * slots * DH + t;
-  float acc = 0.f, lsum = 0.f;
-#pragma unroll 16
-  for (int s = 0; s < splits; ++s) {
-    // an empty split (m = -inf) left its slot unwritten: its values are
-    // loaded (the slot is inside the buffer) but weighted out by the selects
-    const float m = ml[2 * s], l = ml[2 * s + 1], o = po[(size_t)s * DH];
-    const bool used = m != -INFINITY;
-    const float f = used ? ex2f(m - M) : 0.f;
-    lsum = fmaf(f, used ? l : 0.f, lsum);
-    acc = fmaf(f, used ? o : 0.f, acc);
+  float M = -INFINITY, L = 0.f, A = 0.f;
+  for (int s0 = j; s0 < splits; s0 += 8 * SG) {
+    float m[8], l[8], o[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int sl = s0 + c * SG;
+      const bool in = sl < splits;
+      m[c] = in ? ml[2 * sl] : -INFINITY;
+      l[c] = in ? ml[2 * sl + 1] : 0.f;
+      o[c] = in ? po[(size_t)sl * DH] : 0.f;
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) merge_in(m[c], l[c], o[c], M, L, A);
+  }
+  if (SG > 1) {
+    if (t == 0) {
+      sm_m[j] = M;
+      sm_l[j] = L;
+    }
+    sm_a[threadIdx.x] = A;
+    __syncthreads();
+    if (j != 0) return;
+    M = -INFINITY;
+    L = A = 0.f;
+    for (int q = 0; q < SG; ++q) merge_in(sm_m[q], sm_l[q], sm_a[q * DH + t], M, L, A);
   }
   bool bad = false;  // C is the next GEMM's FP16 operand: V rows past 65504 reach it
-  out[(size_t)wid * DH + t] = f16_chk(acc / lsum, bad);
+  out[(size_t)wid * DH + t] = f16_chk(A / L, bad);
   record_overflow(err, bad);
 }
 
@@ -519,7 +549,9 @@ static qwen_status launch_attn_dec(const CUtensorMap& tk, const CUtensorMap& tv,
   count_launches();
   if (cudaGetLastError() != cudaSuccess) return QWEN_ERR_CUDA;
   const int BH = a.B * a.Hq;
-  launch_k(attn_decode_merge_kernel<DH>, dim3(BH), dim3(DH), 0, st, (const float*)a.part_o,
+  // slot groups: about 4 slots per thread, at most 1024 threads
+  const int sg = std::max(1, std::min(1024 / DH, (a.slots + 3) / 4));
+  launch_k(attn_decode_merge_kernel<DH>, dim3(BH), dim3(DH * sg), 0, st, (const float*)a.part_o,
            (const float*)a.part_ml, BH, a.slots, a.Hq / a.Hkv, a.nbv, a.per, out, a.err);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;

@@ -470,11 +470,19 @@ __global__ void __launch_bounds__(1024) reduce_resid_norm_kernel(
     const float* __restrict__ resid32, float* __restrict__ out32, const bf16* __restrict__ gamma,
     float eps, f16* __restrict__ z, size_t zs, f16* __restrict__ z_lo, int* err) {
   pdl_trigger();
-  pdl_wait();
   __shared__ float red[32];
   const int b = blockIdx.x;
   const size_t plane = (size_t)B * N;
   const size_t row = (size_t)b * N;
+  // gamma is a weight (no kernel writes it): read before the wait, so the
+  // scaling after the row reduction needs no further load
+  float gm[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int n = threadIdx.x + 1024 * j;
+    gm[j] = n < N ? __bfloat162float(gamma[n]) : 0.f;
+  }
+  pdl_wait();
   float v[PER];
 #pragma unroll
   for (int j = 0; j < PER; ++j) {
@@ -507,7 +515,7 @@ __global__ void __launch_bounds__(1024) reduce_resid_norm_kernel(
   for (int j = 0; j < PER; ++j) {
     const int n = threadIdx.x + 1024 * j;
     if (n < N) {
-      const float o = __bfloat162float(gamma[n]) * (v[j] * rstd);
+      const float o = gm[j] * (v[j] * rstd);
       const f16 hi = f16_chk(o, bad);
       z[zrow + n] = hi;
       if (z_lo) z_lo[zrow + n] = f16_chk(o - __half2float(hi), bad);

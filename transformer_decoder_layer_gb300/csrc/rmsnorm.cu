@@ -107,12 +107,14 @@ __global__ void __launch_bounds__(1024) rmsnorm_row_kernel(
     void* __restrict__ y, bool y_f16, float* __restrict__ y32, int d, float eps, size_t xs,
     size_t ys, __half* __restrict__ y_lo, int* err) {
   pdl_trigger();
-  pdl_wait();
   __shared__ float red[32];
   const int row = blockIdx.x;
   const int c = threadIdx.x;  // chunk
   const int nch = d >> 3;
   const int lane = c & 31, wid = c >> 5;
+  // gamma is a weight (no kernel writes it): read before the wait
+  const uint4 gu = c < nch ? reinterpret_cast<const uint4*>(gamma)[c] : make_uint4(0, 0, 0, 0);
+  pdl_wait();
   float v[8];
   float ss = 0.f;
   if (c < nch) {
@@ -142,7 +144,6 @@ __global__ void __launch_bounds__(1024) rmsnorm_row_kernel(
   for (int w = 0; w < nw; ++w) tot += red[w];
   if (c >= nch) return;
   const float rstd = rsqrtf(tot / (float)d + eps);
-  const uint4 gu = reinterpret_cast<const uint4*>(gamma)[c];
   const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w};
   float o[8];
 #pragma unroll
