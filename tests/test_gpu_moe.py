@@ -275,14 +275,17 @@ def test_moe_layer_prefill_shared_expert():
 
 
 @pytest.mark.parametrize("shape,tag,B", [(SMALL_MOE, "moed", 8), (SMALL_QWEN2_MOE, "q2moed", 8),
-                                         (SMALL_MOE, "moed1", 1), (SMALL_MOE, "moed64", 64),
+                                         (SMALL_MOE, "moed1", 1), (SMALL_QWEN2_MOE, "q2moed2", 2),
+                                         (SMALL_MOE, "moed64", 64),
                                          (SMALL_QWEN2_MOE, "q2moed65", 65)],
-                         ids=["qwen3", "qwen2_shared", "qwen3_b1", "qwen3_b64", "qwen2_b65"])
+                         ids=["qwen3", "qwen2_shared", "qwen3_b1", "qwen2_b2", "qwen3_b64",
+                              "qwen2_b65"])
 def test_moe_layer_decode(shape, tag, B):
     """MoE layer decode against 100 cached slots.  Up to 64 tokens the experts
     run as the grouped swap-AB decode GEMM (B=64 is its largest padding); 65
     tokens take the 128-row grouped GEMM.  The Qwen2-MoE cases run the shared
-    expert through the split-K GEMMs."""
+    expert through the split-K GEMMs.  One or two tokens are routed by the
+    CTA-wide expert ranks, more by the per-token warp top-k."""
     L = 100
     w_cpu = synth.layer_weights(shape, tag)
     x = synth.activations([B, shape.d], tag)

@@ -42,6 +42,7 @@ namespace {
 
 constexpr int kPermBlock = 1024;  // permutation entries per CTA
 constexpr int kRouteMaxSplits = 8;  // router K splits when the routing is one CTA
+constexpr int kRankMaxT = 2;        // tokens up to which the routing ranks experts CTA-wide
 
 // One warp: top-k of the logits row `lrow` (columns [0, E) are Z W_r^T on entry
 // and Z W_r^T + b_r on exit) and its gate weights: norm != 0, a softmax over
@@ -50,7 +51,7 @@ constexpr int kRouteMaxSplits = 8;  // router K splits when the routing is one C
 // of the shared gate's logit lrow[E].
 __device__ __forceinline__ void topk_warp(float* lrow, const float* __restrict__ bias, int E,
                                           int k, int norm, int32_t* idx_row, float* w_row,
-                                          float* g_out) {
+                                          float* g_out, int32_t* sel_out = nullptr) {
   const int lane = threadIdx.x & 31;
   const int per = (E + 31) / 32;  // <= 8
   float v[8];
@@ -117,6 +118,7 @@ __device__ __forceinline__ void topk_warp(float* lrow, const float* __restrict__
       if (j < k) {
         idx_row[j] = sel_i[j];
         w_row[j] = p[j] / den;
+        if (sel_out) sel_out[j] = sel_i[j];
       }
     }
     if (g_out) *g_out = 1.f / (1.f + expf(-lrow[E]));
@@ -246,11 +248,21 @@ __global__ void __launch_bounds__(kPermBlock) perm_scatter_kernel(
 
 // Decode-sized routing in one CTA of 1024 threads (T * k <= 1024, T <= 64,
 // S <= kRouteMaxSplits):
-//   logits[t] = sum over the S router split partials part[s][t][0..R) (in
-//   split order; one thread per logit), then the top-k of every token (one
-//   warp per token), then the stable counting sort by expert (offsets, list of
-//   non-empty experts, perm, inv) as the separate kernels below do.  No Z rows
-//   are gathered: the expert gate/up GEMM reads the token rows directly.
+//   1. logits[t] = sum over the S router split partials part[s][t][0..R) (in
+//      split order; one thread per logit);
+//   2-3. the top-k and gate weights of every token.  Up to kRankMaxT tokens,
+//      spread over the whole CTA: b_r is added (the biased logits written
+//      back, as topk_warp does) with a copy in shared memory (NaN as -inf);
+//      (t, e) is selected in slot j when j experts of token t precede it, a
+//      larger logit or an equal one of lower index ahead (the order of
+//      topk_warp's k rounds of warp arg-max); then one warp per token forms
+//      the weights with topk_warp's arithmetic.  More tokens: topk_warp, one
+//      warp per token (its k rounds beat T * E rank counts there);
+//   4. the stable counting sort by expert: counts, then thread e takes the
+//      sum of the counts below e (its first sorted position) and its place in
+//      the list of non-empty experts, then perm / inv as perm_scatter_kernel.
+// No Z rows are gathered: the expert gate/up GEMM reads the token rows
+// directly.  Shared memory: route_small_smem(T, E) bytes.
 __global__ void __launch_bounds__(1024) route_small_kernel(
     const float* __restrict__ part, int S, int T, int R, const float* __restrict__ bias, int E,
     int k, int norm, float* __restrict__ logits, int32_t* __restrict__ idx,
@@ -259,13 +271,17 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
   pdl_trigger();
   pdl_wait();
   extern __shared__ int32_t sm[];
-  int32_t* tot = sm;              // [E] entries per expert
-  int32_t* base = tot + E;        // [E] first sorted position of each expert
-  int32_t* wcnt = base + E;       // [32][E] entries of e per warp
+  int32_t* tot = sm;                                    // [E] entries per expert
+  int32_t* base = tot + E;                              // [E] first sorted position
+  int32_t* wcnt = base + E;                             // [32][E] entries of e per warp
+  int32_t* si = wcnt + 32 * E;                          // [T][8] selected experts
+  float* sv = reinterpret_cast<float*>(si + 8 * T);     // [T][8] their logits
+  float* xs = sv + 8 * T;                               // [T][E] biased logits, NaN -> -inf
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int n = T * k;
   const size_t plane = (size_t)T * R;
-  // split sums: all S loads of a logit are issued before the in-order adds
+  const bool by_rank = T <= kRankMaxT;
+  // 1. split sums (all S loads of a logit issued before the in-order adds)
   for (int i = threadIdx.x; i < T * R; i += blockDim.x) {
     float p[kRouteMaxSplits];
 #pragma unroll
@@ -273,23 +289,96 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
     float a = 0.f;
 #pragma unroll
     for (int sp = 0; sp < kRouteMaxSplits; ++sp) a += p[sp];
+    const int t = i / R, e = i - t * R;
+    if (by_rank && e < E) {
+      a += bias ? bias[e] : 0.f;
+      xs[t * E + e] = a == a ? a : -INFINITY;  // a NaN logit is never preferred
+    }
     logits[i] = a;
   }
   for (int e = threadIdx.x; e < E; e += blockDim.x) tot[e] = 0;
   for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
-  for (int t = wid; t < T; t += 32)
-    topk_warp(logits + (size_t)t * R, bias, E, k, norm, idx + (size_t)t * k, w + (size_t)t * k,
-              gscale ? gscale + t : nullptr);
-  __syncthreads();  // idx rows written by lane 0 of each warp are visible
+  if (!by_rank) {
+    for (int t = wid; t < T; t += 32)
+      topk_warp(logits + (size_t)t * R, bias, E, k, norm, idx + (size_t)t * k,
+                w + (size_t)t * k, gscale ? gscale + t : nullptr, si + t * 8);
+  }
+  // 2. ranks (a warp's lanes read the same logit of one token: broadcast)
+  for (int i = threadIdx.x; by_rank && i < T * E; i += blockDim.x) {
+    const int t = i / E, e = i - t * E;
+    const float* row = xs + t * E;
+    const float x = row[e];
+    int r = 0;
+#pragma unroll 8
+    for (int f = 0; f < E; ++f) {
+      const float y = row[f];
+      r += (y > x) | ((y == x) & (f < e));
+    }
+    if (r < k) {
+      si[t * 8 + r] = e;
+      sv[t * 8 + r] = x;
+    }
+  }
+  __syncthreads();
+  // 3. gate weights: norm != 0, a softmax over the k selected logits; norm == 0,
+  // the selected entries of the softmax over all E logits; the shared gate's
+  // sigmoid from logit column E
+  for (int t = wid; by_rank && t < T; t += 32) {
+    const float top = sv[t * 8];
+    float all = 0.f;
+    if (!norm) {
+#pragma unroll
+      for (int i2 = 0; i2 < 8; ++i2) {
+        const int e = lane + 32 * i2;
+        const float x = e < E ? xs[t * E + e] : -INFINITY;
+        all += x == -INFINITY ? 0.f : expf(x - top);
+      }
+      all = warp_sum(all);
+    }
+    if (lane == 0) {
+      float s = 0.f, p[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        p[j] = j < k ? expf(sv[t * 8 + j] - top) : 0.f;
+        s += p[j];
+      }
+      const float den = norm ? s : all;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j < k) {
+          idx[(size_t)t * k + j] = si[t * 8 + j];
+          w[(size_t)t * k + j] = p[j] / den;
+        }
+      }
+      if (gscale) gscale[t] = 1.f / (1.f + expf(-logits[(size_t)t * R + E]));
+    }
+  }
+  // 4. counting sort of the entries t * k + j by expert, stable in entry order
   const bool valid = threadIdx.x < n;
-  const int e = valid ? min(max(idx[threadIdx.x], 0), E - 1) : -1;
+  const int e = valid ? si[(threadIdx.x / k) * 8 + threadIdx.x % k] : -1;
   if (valid) atomicAdd(&tot[e], 1);
   const unsigned same = __match_any_sync(0xffffffffu, e);
   const int rank_w = __popc(same & ((1u << lane) - 1u));
   if (valid && rank_w == 0) wcnt[wid * E + e] = __popc(same);
   __syncthreads();
-  if (wid == 0) expert_scan_warp(tot, E, base, false, true, offsets, act);
+  if (threadIdx.x < E) {
+    const int x = threadIdx.x;
+    int off = 0, na = 0;
+    for (int f = 0; f < x; ++f) {
+      const int c = tot[f];
+      off += c;
+      na += c > 0;
+    }
+    base[x] = off;
+    offsets[x] = off;
+    const int c = tot[x];
+    if (c > 0) act[1 + na] = x;
+    if (x == E - 1) {
+      offsets[E] = off + c;
+      act[0] = na + (c > 0);
+    }
+  }
   __syncthreads();
   if (valid) {
     int pos = base[e] + rank_w;
@@ -297,6 +386,11 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
     perm[pos] = threadIdx.x;
     inv[threadIdx.x] = pos;
   }
+}
+
+// Shared memory of route_small_kernel.
+inline size_t route_small_smem(int T, int E) {
+  return ((size_t)34 * E + 16 * (size_t)T + (size_t)T * E) * 4;
 }
 
 // zp[pos] = z[perm[pos] / k]  (16-bit rows of d elements; z rows `zs` apart),
@@ -503,7 +597,12 @@ qwen_status moe_forward(qwen_layer_s* L, const bf16* r, const float* r32, bf16* 
     if (grouped_dec) {
       // 3 + 5 in one CTA: split sum, top-k, counting sort (it reads the
       // router partials, so it runs before the shared expert reuses them)
-      launch_k(route_small_kernel, dim3(1), dim3(1024), 34 * E * sizeof(int32_t), st,
+      static std::atomic<uint64_t> attr{0};  // one bit per device
+      const size_t smem = route_small_smem(T, E);
+      // the limit is raised once per device, for the largest use
+      if (!smem_attr_once(route_small_kernel, (int)route_small_smem(kMoeDecodeMaxRows, 256), attr))
+        return QWEN_ERR_CUDA;
+      launch_k(route_small_kernel, dim3(1), dim3(1024), smem, st,
                (const float*)part, S, T, R, (const float*)L->b_router, E, k, c.norm_topk_prob,
                logits, idx, wts, gsc, offsets, act, perm, inv);
       count_launches();
