@@ -213,6 +213,52 @@ def test_decode_batch_64_dh128_g8():
     assert_parity(y, ref, what="Y")
 
 
+@pytest.mark.parametrize("B", [256, 300], ids=["swap_max", "row_tiled"])
+def test_decode_large_batches(B):
+    """B=256 is the largest batch of the swap-AB decode GEMMs (tokens on the
+    MMA's N = 256); B=300 takes the prefill-shaped GEMMs with their fused QKV,
+    residual and SwiGLU epilogues.  Ragged cache lengths; every sequence is
+    checked against the oracle, with its appended K/V row."""
+    lens = [int(v) for v in np.random.default_rng(B).integers(0, 90, B)]
+    y, ref, k, kr, v, vr, cl = _decode_case(synth.TINY, f"dec_big{B}", B, lens, 96)
+    assert_parity(y, ref, what="Y")
+    for b in range(0, B, 37):
+        assert_parity(k[b, :, cl[b]], kr[b, :, cl[b]], what=f"K row b={b}")
+        assert_parity(v[b, :, cl[b]], vr[b, :, cl[b]], what=f"V row b={b}")
+
+
+@pytest.mark.parametrize("bad", ["slot", "position"])
+def test_decode_reports_out_of_range(bad):
+    """A cache slot at max_seq or a position at max_position is reported as
+    QWEN_ERR_RANGE in the status word (nothing is written outside the cache);
+    the other sequences of the step are unaffected."""
+    shape = synth.TINY
+    B, S = 4, 64
+    w_cpu = synth.layer_weights(shape, "dec_oor")
+    x = synth.activations([B, shape.d], "dec_oor")
+    kc, vc = synth.kv_cache(B, shape.n_kv_heads, S, shape.head_dim, 20, "dec_oor")
+    g = GpuLayer(shape, w_cpu, max_tokens=B, max_batch=B, max_seq=S, max_position=S)
+    lens = [20, 20, 20, 20]
+    pos = [20, 20, 20, 20]
+    if bad == "slot":
+        lens[2] = S  # no slot for the new row
+    else:
+        pos[2] = S   # beyond the RoPE table
+    kd, vd = kc.cuda(), vc.cuda()
+    t = torch
+    y = g.layer.decode(x.cuda(), t.as_tensor(pos, dtype=t.int32).cuda(),
+                       t.as_tensor(lens, dtype=t.int32).cuda(), kd, vd)
+    range_code = next(c for c, n in g.q.STATUS.items() if n == "QWEN_ERR_RANGE")
+    assert g.layer.poll_error() == range_code
+    assert g.layer.poll_error() == 0  # polling clears the word
+    # the well-formed sequences match the oracle
+    ok = [0, 1, 3]
+    ref, _, _ = oracle_prefill(shape, synth.weights_f64(w_cpu), f64(x)[ok][:, None, :],
+                               np.array(pos)[ok][:, None], [lens[i] for i in ok],
+                               f64(kc)[ok], f64(vc)[ok])
+    assert_parity(f64(y.float())[ok], ref[:, 0], what="Y of the other sequences")
+
+
 def test_prefill_reproducible_bit_for_bit():
     """T=512 of a d=1024 layer (GEMMs of fewer tiles than SMs, split-tail
     tiles, split attention work items): the result matches the oracle and is
