@@ -602,10 +602,10 @@ static inline void mark(const qwen_layer_s* L, int stage, int end, cudaStream_t 
 // One projection of a decode step: swap-AB split-K on the tensor cores; the
 // reduction that follows applies the step's epilogue.
 static qwen_status decode_proj(const f16* Wt, const f16* X, int B, int N, int K, float* part,
-                               int* err, cudaStream_t st, int& splits) {
+                               int* err, cudaStream_t st, int& splits, bool late_release = false) {
   splits = decode_splits(N, K, B);
   return gemm_decode_splitk(Wt, X, K, B, N, K, splits, /*op_f16=*/true, part, err, st,
-                            /*w_packed=*/true);
+                            /*w_packed=*/true, nullptr, late_release);
 }
 
 qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16* y, float* y32,
@@ -634,7 +634,12 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
   const QkvParams qp = make_qkv_params(L, positions, cache_len, q, false, kc, vc, nullptr,
                                        nullptr, 1);
   if (swap) {
-    QWEN_STAGE_RUN(QWEN_STAGE_QKV, decode_proj(L->w_qkv, xh, B, nqkv, d, part, err, st, S));
+    // the QKV GEMM releases the kernels after it only once its threads have
+    // waited for RMSNorm_1, i.e. once everything enqueued before the step has
+    // completed: the attention then streams cache rows of earlier steps before
+    // its own wait
+    QWEN_STAGE_RUN(QWEN_STAGE_QKV, decode_proj(L->w_qkv, xh, B, nqkv, d, part, err, st, S,
+                                               /*late_release=*/true));
     QWEN_STAGE_RUN(QWEN_STAGE_QKV_FINISH, reduce_qkv(part, S, B, nqkv, qp, err, st));
   } else {
     GemmEpilogue e{};
@@ -650,7 +655,8 @@ qwen_status layer_decode(qwen_layer_s* L, const bf16* x, const float* x32, bf16*
   QWEN_STAGE_RUN(QWEN_STAGE_ATTN,
                  attention_decode(q, kc, vc, cache_len, B, Hq, Hkv, dh, c.max_seq, splits,
                                   reinterpret_cast<float*>(ws + W.attn_o),
-                                  reinterpret_cast<float*>(ws + W.attn_ml), attn, err, st));
+                                  reinterpret_cast<float*>(ws + W.attn_ml), attn, err, st,
+                                  /*early=*/swap));
   // O projection + residual -> R (FP32)
   if (swap && !c.n_experts) {
     // O projection; its split reduction + residual is fused with RMSNorm_2

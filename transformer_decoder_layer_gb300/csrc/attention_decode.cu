@@ -96,6 +96,12 @@ struct DecAttnArgs {
   float* part_o;   // [B*Hq][slots][DH]
   float* part_ml;  // [B*Hq][slots][2]
   int* err;
+  // A kernel of this step before the previous one released the kernels after
+  // it only once its threads had passed their dependency wait, so everything
+  // enqueued before the step has completed when this kernel starts: the
+  // producer may load cache blocks that lie wholly below the new token's slot
+  // (written by earlier steps) before waiting for the kernel before this one.
+  int early;
 };
 
 }  // namespace
@@ -105,7 +111,9 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
     attn_decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        DecAttnArgs a) {
   pdl_trigger();
-  pdl_wait();
+  // early: the set-up reads only cache_len (written before the step) and the
+  // producer waits after its first loads; otherwise everyone waits here
+  if (!a.early) pdl_wait();
   using C = DecAttnCfg<DH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -171,9 +179,32 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
       }
       __syncwarp();
       const uint64_t pol = l2_evict_first();
+      auto load_block = [&](int stage, int row) {
+        uint8_t* st = smem + stage * C::STAGE_BYTES;
+        mbar_arrive_expect_tx_w(&full[stage], C::STAGE_BYTES);
+#pragma unroll
+        for (int c = 0; c < DH / 64; ++c) {
+          // the cache is read once per step: evicted first
+          tma_load_2d_hint_w(st + c * C::BOX_BYTES, &tmK, &full[stage], c * 64, row, pol);
+          tma_load_2d_hint_w(st + C::KV_BYTES + c * C::BOX_BYTES, &tmV, &full[stage], c * 64, row,
+                             pol);
+        }
+      };
       int stage = 0;
       uint32_t phase = 0;
       int pair, k0, k1, slot, n_keys;
+      // first unit: the blocks wholly below the new token's slot (written by
+      // earlier steps) into the empty ring, before the wait
+      int pre = 0;
+      if (a.early) {
+        if (unit_of(0, pair, k0, k1, slot, n_keys)) {
+          const int b = pair / a.Hkv;
+          const int cl = b < C::LEN_SLOTS ? s_len[b] : a.cache_len[b];
+          for (int blk = k0; blk < k1 && pre < kDStages && blk + kKB <= cl; blk += kKB, ++pre)
+            load_block(pre, pair * a.max_seq + blk);
+        }
+        pdl_wait();
+      }
       for (int lu = 0; unit_of(lu, pair, k0, k1, slot, n_keys); ++lu) {
         const int b = pair / a.Hkv, g = pair - b * a.Hkv;
         const int row0 = pair * a.max_seq;  // (b * Hkv + g) * max_seq
@@ -183,16 +214,10 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
         mbar_arrive_expect_tx_w(&q_full[qs], (uint32_t)(G * DH * 2));
         bulk_load_w(sQ + qs * 16 * DH, a.q + ((size_t)b * a.Hq + (size_t)g * G) * DH,
                   (uint32_t)(G * DH * 2), &q_full[qs]);
-        for (int blk = k0; blk < k1; blk += kKB) {
-          if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, a.err)) goto prod_done;
-          uint8_t* st = smem + stage * C::STAGE_BYTES;
-          mbar_arrive_expect_tx_w(&full[stage], C::STAGE_BYTES);
-#pragma unroll
-          for (int c = 0; c < DH / 64; ++c) {
-            // the cache is read once per step: evicted first
-            tma_load_2d_hint_w(st + c * C::BOX_BYTES, &tmK, &full[stage], c * 64, row0 + blk, pol);
-            tma_load_2d_hint_w(st + C::KV_BYTES + c * C::BOX_BYTES, &tmV, &full[stage], c * 64,
-                             row0 + blk, pol);
+        for (int blk = k0, i = 0; blk < k1; blk += kKB, ++i) {
+          if (lu > 0 || i >= pre) {  // else loaded before the wait
+            if (!mbar_wait_w(&empty[stage], phase ^ 1u, abort_flag, a.err)) goto prod_done;
+            load_block(stage, row0 + blk);
           }
           if (++stage == kDStages) {
             stage = 0;
@@ -213,6 +238,7 @@ __global__ void __launch_bounds__(kDecAttnThreads, 1)
   }
 
   // ---------------- compute warps
+  if (a.early) pdl_wait();  // the query rows come from the kernel before
   const int gid = lane >> 2, tq = lane & 3;
   int stage = 0;
   uint32_t phase = 0;
@@ -560,7 +586,7 @@ static qwen_status launch_attn_dec(const CUtensorMap& tk, const CUtensorMap& tv,
 qwen_status attention_decode(const bf16* q, const bf16* kc, const bf16* vc,
                              const int32_t* cache_len, int B, int Hq, int Hkv, int dh, int max_seq,
                              int splits, float* part_o, float* part_ml, f16* out,
-                             int* err, cudaStream_t st) {
+                             int* err, cudaStream_t st, bool early) {
   if (B == 0) return QWEN_OK;
   if (Hq / Hkv > 16) return QWEN_ERR_UNSUPPORTED;
   const AttnSplit sp = attn_split(B, Hkv, max_seq);
@@ -582,6 +608,7 @@ qwen_status attention_decode(const bf16* q, const bf16* kc, const bf16* vc,
   a.part_o = part_o;
   a.part_ml = part_ml;
   a.err = err;
+  a.early = early ? 1 : 0;
   if (dh == 128) return launch_attn_dec<128>(tk, tv, a, sp.grid, out, st);
   if (dh == 64) return launch_attn_dec<64>(tk, tv, a, sp.grid, out, st);
   return QWEN_ERR_UNSUPPORTED;

@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
                        int B, int N, int K, int splits, uint32_t idesc, int w_packed,
                        float* __restrict__ part, f16* __restrict__ hout,
                        const int32_t* gact, const int32_t* goff, const int32_t* tidx,
-                       const int32_t* tinv, int tk, int* err) {
+                       const int32_t* tinv, int tk, int late, int* err) {
   using C = DecCfg<BP, EPI>;
   bool f16_bad = false;  // an H value beyond the FP16 range (SwiGLU epilogue)
   extern __shared__ uint8_t smem_raw[];
@@ -83,7 +83,10 @@ __global__ void __launch_bounds__(kDThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  pdl_trigger();
+  // late: each thread releases the next kernel only after its own dependency
+  // wait (warp 1 waits for that alone), so the kernels after this one start
+  // once the kernel before it, and everything before that, has completed
+  if (!late) pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = (N + kDBM - 1) / kDBM;
   const int n_kblk = (K + kDBK - 1) / kDBK;
@@ -169,6 +172,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
         }
       }
       pdl_wait();
+      if (late) pdl_trigger();
       if (grouped) units = gact[0] * per_group;
       int stage = 0;
       uint32_t phase = 0;
@@ -202,10 +206,9 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
   } else if (warp == 1) {
     {
-      if (grouped) {
-        pdl_wait();
-        units = gact[0] * per_group;
-      }
+      if (grouped || late) pdl_wait();
+      if (late) pdl_trigger();
+      if (grouped) units = gact[0] * per_group;
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -241,6 +244,7 @@ __global__ void __launch_bounds__(kDThreads, 1)
     }
   } else {
     pdl_wait();  // the partials may still be read by the previous kernel
+    if (late) pdl_trigger();
     if (grouped) units = gact[0] * per_group;
     const int q = warp & 3;
     int local = 0;
@@ -654,7 +658,7 @@ template <int BP, int EPI>
 static qwen_status launch_dec(const CUtensorMap& tw, const CUtensorMap& tx, int B, int N, int K,
                               int splits, bool op_f16, bool w_packed, float* part, f16* hout,
                               const int32_t* gact, const int32_t* goff, const int32_t* tidx,
-                              const int32_t* tinv, int tk, int max_groups, int* err,
+                              const int32_t* tinv, int tk, int max_groups, bool late, int* err,
                               cudaStream_t st) {
   using C = DecCfg<BP, EPI>;
   auto kern = gemm_decode_kernel<BP, EPI>;
@@ -665,7 +669,7 @@ static qwen_status launch_dec(const CUtensorMap& tw, const CUtensorMap& tx, int 
   const int grid = units < sms ? units : sms;
   launch_k(kern, dim3(grid), dim3(kDThreads), C::SMEM_BYTES, st, tw, tx, B, N, K, splits,
            idesc_f32acc(kDBM, BP, op_f16), w_packed ? 1 : 0, part, hout, gact, goff, tidx, tinv,
-           tk, err);
+           tk, late ? 1 : 0, err);
   count_launches();
   return cudaGetLastError() == cudaSuccess ? QWEN_OK : QWEN_ERR_CUDA;
 }
@@ -678,7 +682,8 @@ static qwen_status decode_gemm_launch(const void* W, int groups, const void* X, 
                                       bool w_packed, float* part, f16* hout,
                                       const int32_t* gact, const int32_t* goff,
                                       const int32_t* tidx, const int32_t* tinv, int tk,
-                                      int max_groups, int* err, cudaStream_t st) {
+                                      int max_groups, int* err, cudaStream_t st,
+                                      bool late = false) {
   if (B <= 0 || max_m <= 0 || max_m > 256) return QWEN_ERR_UNSUPPORTED;
   if ((K & 7) || splits < 1 || max_groups < 1) return QWEN_ERR_UNSUPPORTED;
   const int bp = pad_batch(max_m);
@@ -693,11 +698,11 @@ static qwen_status decode_gemm_launch(const void* W, int groups, const void* X, 
 #define QWEN_DEC_CASE(BPV)                                                                        \
   case BPV:                                                                                       \
     return hout ? launch_dec<BPV, DEC_SWIGLU>(tw, tx, B, N, K, 1, op_f16, w_packed, nullptr,      \
-                                              hout, gact, goff, tidx, tinv, tk, max_groups, err,  \
-                                              st)                                                 \
+                                              hout, gact, goff, tidx, tinv, tk, max_groups, late, \
+                                              err, st)                                            \
                 : launch_dec<BPV, DEC_PARTIAL>(tw, tx, B, N, K, splits, op_f16, w_packed, part,   \
                                                nullptr, gact, goff, nullptr, nullptr, 0,          \
-                                               max_groups, err, st);
+                                               max_groups, late, err, st);
   switch (bp) {
     QWEN_DEC_CASE(16)
     QWEN_DEC_CASE(32)
@@ -711,9 +716,9 @@ static qwen_status decode_gemm_launch(const void* W, int groups, const void* X, 
 
 qwen_status gemm_decode_splitk(const void* W, const void* X, int ldx, int B, int N, int K,
                                int splits, bool op_f16, float* part, int* err, cudaStream_t st,
-                               bool w_packed, f16* swiglu_out) {
+                               bool w_packed, f16* swiglu_out, bool late_release) {
   return decode_gemm_launch(W, 1, X, ldx, B, B, N, K, splits, op_f16, w_packed, part, swiglu_out,
-                            nullptr, nullptr, nullptr, nullptr, 0, 1, err, st);
+                            nullptr, nullptr, nullptr, nullptr, 0, 1, err, st, late_release);
 }
 
 qwen_status gemm_decode_grouped(const void* W, int E, const void* X, int rows, int max_m, int N,

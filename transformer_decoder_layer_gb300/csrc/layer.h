@@ -129,9 +129,13 @@ void decode_attn_plan(const qwen_layer_config& c, int B, int* splits);
 // W is row-major [N, K] (the caller's lm_head).
 // swiglu_out: W is an interleaved gate/up weight (64-row blocks); run with one
 // split and write H[b][f] = SiLU(gate) * up (FP16) instead of partials.
+// late_release: the kernel lets the kernels after it launch only once its
+// threads have passed their dependency wait (not at its start): everything
+// enqueued before the kernel before it has then completed.
 qwen_status gemm_decode_splitk(const void* W, const void* X, int ldx, int B, int N, int K,
                                int splits, bool op_f16, float* part, int* err, cudaStream_t st,
-                               bool w_packed = false, __half* swiglu_out = nullptr);
+                               bool w_packed = false, __half* swiglu_out = nullptr,
+                               bool late_release = false);
 
 // Grouped (mixture-of-experts) decode GEMM.  W: E stacked FP16 [N, K] weights;
 // X: `rows` FP16 rows of K, grouped by expert: rows [offsets[e], offsets[e+1])
@@ -174,9 +178,13 @@ qwen_status reduce_f32(const float* part, int splits, int B, int N, float* out, 
 
 // Split-KV decode attention and its merge: q [B][Hq][dh]; query b sits in cache
 // slot cache_len[b] and attends slots 0..cache_len[b].  out [B][Hq*dh].
+// early: an earlier kernel of the step released its dependents only after its
+// own dependency wait, so all work enqueued before the step has completed and
+// the attention may load cache rows below slot cache_len[b] without waiting.
 qwen_status attention_decode(const __nv_bfloat16* q, const __nv_bfloat16* kc,
                              const __nv_bfloat16* vc, const int32_t* cache_len, int B, int Hq,
                              int Hkv, int dh, int max_seq, int splits, float* part_o,
-                             float* part_ml, __half* out, int* err, cudaStream_t st);
+                             float* part_ml, __half* out, int* err, cudaStream_t st,
+                             bool early = false);
 
 }  // namespace qwen
