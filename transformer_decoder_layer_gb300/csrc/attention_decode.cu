@@ -20,7 +20,9 @@
 // c - (first CTA of the pair).  A persistent CTA walks its units;
 // the producer warp streams each unit's query rows (bulk copy) and K/V blocks
 // (TMA) through rings of equal depth, so it can run ahead across unit
-// boundaries.  4 compute warps each take 16 keys of every block and keep their
+// boundaries.  In the decode step the first unit's blocks that lie wholly below
+// the new token's slot are requested before the dependency wait (see
+// DecAttnArgs::early).  4 compute warps each take 16 keys of every block and keep their
 // own running max / sum / O; the warps merge through shared memory and the
 // unit's unnormalised partial (m, l, O) goes to a workspace.  A merge kernel
 // combines the slots of each head in a fixed order (deterministic).
