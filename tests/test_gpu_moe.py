@@ -309,3 +309,41 @@ def test_moe_layer_decode(shape, tag, B):
                                           np.array([L]))[0]
     assert_parity(r_gpu, r_ref, what="decode R")
     _teacher_forced_check(shape, w64, r_gpu, gi, gw, yg, what="decode Y on the GPU's R")
+
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_moe_layer_decode_qwen3_30b_a3b(a3b_weights, B):
+    """Full Qwen3-30B-A3B-shaped MoE layer decode against 4096 cached slots
+    (the bench's MoE decode workload): R of every sequence against the oracle,
+    then the MoE block teacher-forced on the GPU's R (top-k bit-exact where the
+    oracle's gap exceeds 1e-3, Y on every sequence), and the appended K/V rows."""
+    shape = synth.QWEN3_30B_A3B
+    L = 4096
+    x = synth.activations([B, shape.d], f"a3bd{B}")
+    kc, vc = synth.kv_cache(B, shape.n_kv_heads, L + 1, shape.head_dim, L, f"a3bd{B}")
+    g = GpuLayer(shape, a3b_weights, max_tokens=B, max_batch=B, max_seq=L + 1,
+                 max_position=L + 1)
+    kd, vd = kc.cuda(), vc.cuda()
+    ws = g.layer.workspace(B, 1)
+    lens = torch.full((B,), L, dtype=torch.int32, device="cuda")
+    y = g.layer.decode(x.cuda(), lens, lens.clone(), kd, vd,
+                       out=torch.empty((B, shape.d), dtype=torch.bfloat16, device="cuda"),
+                       workspace=ws)
+    assert g.layer.poll_error() == 0
+    r_gpu, gi, gw = _layer_routing(g, ws, B, 1, shape)
+    w64 = {n: (_PerExpertF64(t) if n in ("w_gate", "w_up", "w_down") else synth.to_f64(t))
+           for n, t in a3b_weights.items()}
+    cfg = shape.as_dict()
+    r_ref = np.empty_like(r_gpu)
+    k_ref = np.empty((B, shape.n_kv_heads, shape.head_dim))
+    v_ref = np.empty_like(k_ref)
+    for b in range(B):
+        kk, vv = f64(kc)[b].copy(), f64(vc)[b].copy()
+        r_ref[b] = oracle.attention_block(f64(x)[b][None], w64, cfg, np.array([L]), kk, vv,
+                                          np.array([L]))[0]
+        k_ref[b], v_ref[b] = kk[:, L], vv[:, L]
+    assert_parity(r_gpu, r_ref, what="decode R")
+    assert_parity(f64(kd.float())[:, :, L], k_ref, what="appended K")
+    assert_parity(f64(vd.float())[:, :, L], v_ref, what="appended V")
+    _teacher_forced_check(shape, w64, r_gpu, gi, gw, f64(y.float()),
+                          what="decode Y on the GPU's R")
