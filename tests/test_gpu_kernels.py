@@ -19,8 +19,11 @@ def q():
     return q
 
 
-@pytest.mark.parametrize("rows,d", [(1, 512), (7, 3584), (300, 4096), (33, 8192), (64, 2048)])
+@pytest.mark.parametrize("rows,d", [(1, 512), (7, 3584), (300, 4096), (33, 8192), (64, 2048),
+                                    (1024, 4096), (3000, 3584)])
 def test_rmsnorm_matches_oracle(q, rows, d):
+    """Up to 8 rows per SM one CTA per row (1024 rows included), above that a
+    warp per row (3000 rows)."""
     x = synth.activations([rows, d], "rms", f"x{rows}_{d}")
     g = synth.normal_bf16([d], synth.seed_for("rms", f"g{d}"), 0.1, 1.0)
     y32 = torch.empty((rows, d), dtype=torch.float32, device="cuda")

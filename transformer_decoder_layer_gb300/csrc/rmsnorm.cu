@@ -100,8 +100,9 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const bf16* __restrict__ x
   record_overflow(err, bad);
 }
 
-// Few rows (decode batches): one CTA per row, one 8-element chunk per thread,
-// so the row is read, reduced and written in one round trip each.
+// Up to a few rows per SM (decode batches, short prefills): one CTA per row,
+// one 8-element chunk per thread, so the row is read, reduced and written in
+// one round trip each.
 __global__ void __launch_bounds__(1024) rmsnorm_row_kernel(
     const bf16* __restrict__ x, const float* __restrict__ x32, const bf16* __restrict__ gamma,
     void* __restrict__ y, bool y_f16, float* __restrict__ y32, int d, float eps, size_t xs,
@@ -185,7 +186,11 @@ qwen_status rmsnorm_launch(const bf16* x, const bf16* gamma, void* y, bool y_f16
   const size_t xs = x_stride ? x_stride : (size_t)d;
   const size_t ys = y_stride ? y_stride : (size_t)d;
   if (y_lo && !y_f16) return QWEN_ERR_INVALID_ARG;
-  if (rows <= 2 * device_sm_count()) {
+  // one CTA per row up to 8 rows per SM: at 1024 rows (T = 1024 prefill) the
+  // warp-per-row kernel, with two passes over each row and 8 warps per SM, is
+  // bound by the latency of its dependent loads (12.5 -> ~6 us in the layer's
+  // timeline); at 4096 rows and above both kernels measure the same
+  if (rows <= 8 * device_sm_count()) {
     const int threads = ((d >> 3) + 31) & ~31;  // <= 1024 for d <= 8192
     launch_k(rmsnorm_row_kernel, dim3(rows), dim3(threads), 0, st, x, x32, gamma, y, y_f16, y32, d,
              eps, xs, ys, y_lo, err);
