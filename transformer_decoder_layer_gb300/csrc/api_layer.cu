@@ -52,6 +52,7 @@ PackedLayout packed_layout(const qwen_layer_config& c) {
   };
   L.status = take(256);
   L.rope = take((size_t)c.max_position * (dh / 2) * sizeof(float2));
+  L.rope_t = take((size_t)c.max_position * (dh / 2) * sizeof(float2));
   L.gamma_attn = take(d * 2);
   L.gamma_mlp = take(d * 2);
   L.gamma_q = take(dh * 2);
@@ -269,6 +270,7 @@ qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_wei
   h->L = L;
   h->status = reinterpret_cast<int*>(P + L.status);
   h->rope = reinterpret_cast<float2*>(P + L.rope);
+  h->rope_t = reinterpret_cast<float2*>(P + L.rope_t);
   h->gamma_attn = reinterpret_cast<bf16*>(P + L.gamma_attn);
   h->gamma_mlp = reinterpret_cast<bf16*>(P + L.gamma_mlp);
   h->gamma_q = c.qk_norm ? reinterpret_cast<bf16*>(P + L.gamma_q) : nullptr;
@@ -325,19 +327,27 @@ qwen_status qwen_layer_create(const qwen_layer_config* cfg, const qwen_layer_wei
     ok = ok && pack_blocked(h->w_sdown, w->w_shared_down, d, sf, 0, h->status, st, d, round128(d));
   }
   // RoPE table: (cos, sin) of p * theta^(-2i/dh), angles and trig in FP64.
-  // Qwen3 layer page, §6 (frequency equation).
+  // Qwen3 layer page, §6 (frequency equation).  Position-major for the decode
+  // reduction (a warp reads one position's row), frequency-major for the
+  // prefill epilogue (its lanes hold consecutive positions, so each load of
+  // one frequency is contiguous across the warp).
   if (ok) {
     const int half = c.head_dim / 2;
-    std::vector<float2> tab((size_t)c.max_position * half);
+    const size_t P_ = (size_t)c.max_position;
+    std::vector<float2> tab(P_ * half), tab_t(P_ * half);
     for (int i = 0; i < half; ++i) {
       const double omega = std::pow(c.rope_theta, -2.0 * i / (double)c.head_dim);
       for (int p = 0; p < c.max_position; ++p) {
         const double ang = (double)p * omega;
-        tab[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+        const float2 cs = make_float2((float)std::cos(ang), (float)std::sin(ang));
+        tab[(size_t)p * half + i] = cs;
+        tab_t[(size_t)i * P_ + p] = cs;
       }
     }
     ok = cudaMemcpyAsync(h->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice,
                          st) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(h->rope_t, tab_t.data(), tab_t.size() * sizeof(float2),
+                               cudaMemcpyHostToDevice, st) == cudaSuccess;
     ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
   }
   // a weight beyond the FP16 range was recorded by the packing kernels
@@ -808,6 +818,7 @@ QkvParams make_qkv_params(const qwen_layer_s* L, const int32_t* positions, const
   p.gamma_q = L->gamma_q;
   p.gamma_k = L->gamma_k;
   p.rope = L->rope;
+  p.rope_t = L->rope_t;
   p.positions = positions;
   p.slot0 = slot0;
   p.q_out = q;

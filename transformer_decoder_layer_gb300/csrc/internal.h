@@ -29,6 +29,7 @@ struct QkvParams {
   const __nv_bfloat16* gamma_q;   // [dh] or nullptr (no QK-norm)
   const __nv_bfloat16* gamma_k;   // [dh]
   const float2* rope;      // [max_position][dh/2] (cos, sin)
+  const float2* rope_t;    // the same, frequency-major [dh/2][max_position]
   const int32_t* positions;  // [M]
   const int32_t* slot0;      // [B]: cache slot of the sequence's first new token
   void* q_out;             // [B][Hq][T][dh], BF16, or with q_f16 FP16 for the

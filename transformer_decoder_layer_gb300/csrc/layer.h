@@ -10,7 +10,7 @@
 namespace qwen {
 
 struct PackedLayout {
-  size_t status, rope, gamma_attn, gamma_mlp, gamma_q, gamma_k, w_qkv, b_qkv, w_o, w_gu, w_down,
+  size_t status, rope, rope_t, gamma_attn, gamma_mlp, gamma_q, gamma_k, w_qkv, b_qkv, w_o, w_gu, w_down,
       w_router, b_router, w_sgu, w_sdown, total;
 };
 
@@ -40,7 +40,8 @@ struct qwen_layer_s {
   uint8_t* packed;
   qwen::PackedLayout L;
   int* status;
-  float2* rope;
+  float2* rope;    // [max_position][dh/2] (cos, sin)
+  float2* rope_t;  // the same table frequency-major, [dh/2][max_position]
   __nv_bfloat16 *gamma_attn, *gamma_mlp, *gamma_q, *gamma_k;
   // projection weights are held as FP16 (converted exactly from BF16 at create)
   __half* w_qkv;

@@ -53,16 +53,15 @@ __device__ __forceinline__ void qkv_head_finish(float (&v)[DH], int m, int head,
       record_error(err, QWEN_ERR_RANGE);
       return;
     }
-    const float4* tab = reinterpret_cast<const float4*>(p.rope + (size_t)pos * (DH / 2));
+    // frequency-major table: the lanes of a warp hold consecutive tokens, so
+    // each frequency's (cos, sin) loads are contiguous across the warp
+    const float2* tab = p.rope_t + pos;
 #pragma unroll
-    for (int i = 0; i < DH / 4; ++i) {
-      const float4 cs = __ldg(tab + i);  // (cos, sin) of pairs 2i and 2i+1
-      const float a0 = v[2 * i], b0 = v[2 * i + DH / 2];
-      const float a1 = v[2 * i + 1], b1 = v[2 * i + 1 + DH / 2];
-      v[2 * i] = a0 * cs.x - b0 * cs.y;
-      v[2 * i + DH / 2] = b0 * cs.x + a0 * cs.y;
-      v[2 * i + 1] = a1 * cs.z - b1 * cs.w;
-      v[2 * i + 1 + DH / 2] = b1 * cs.z + a1 * cs.w;
+    for (int i = 0; i < DH / 2; ++i) {
+      const float2 cs = __ldg(tab + (size_t)i * p.max_position);  // pair (i, i + dh/2)
+      const float a = v[i], b = v[i + DH / 2];
+      v[i] = a * cs.x - b * cs.y;
+      v[i + DH / 2] = b * cs.x + a * cs.y;
     }
   }
   const int b = m / p.T, t = m - (m / p.T) * p.T;
