@@ -18,6 +18,11 @@ template <int DH>
 __device__ __forceinline__ void qkv_head_finish(float (&v)[DH], int m, int head,
                                                 const QkvParams& p, int* err) {
   const int kind = head < p.Hq ? 0 : (head < p.Hq + p.Hkv ? 1 : 2);  // q, k, v
+  // the token's position and its sequence's first slot, loaded first: their
+  // latency then overlaps the bias and QK-norm arithmetic
+  const int b = m / p.T, t = m - (m / p.T) * p.T;
+  const int pos = kind < 2 ? p.positions[m] : 0;
+  const int s0 = p.slot0[b];
   if (p.bias) {
     const float4* bb = reinterpret_cast<const float4*>(p.bias + (size_t)head * DH);
 #pragma unroll
@@ -48,7 +53,6 @@ __device__ __forceinline__ void qkv_head_finish(float (&v)[DH], int m, int head,
         }
       }
     }
-    const int pos = p.positions[m];
     if (pos < 0 || pos >= p.max_position) {
       record_error(err, QWEN_ERR_RANGE);
       return;
@@ -64,7 +68,6 @@ __device__ __forceinline__ void qkv_head_finish(float (&v)[DH], int m, int head,
       v[i + DH / 2] = b * cs.x + a * cs.y;
     }
   }
-  const int b = m / p.T, t = m - (m / p.T) * p.T;
   bool bad = false;  // an FP16 value (prefill Q, K/V copies) beyond the format's range
   auto store = [&](void* dst, bool f16_out, bool streaming = false) {
     uint4* d4 = reinterpret_cast<uint4*>(dst);
@@ -86,11 +89,11 @@ __device__ __forceinline__ void qkv_head_finish(float (&v)[DH], int m, int head,
     // call's, read from FP16 copies), BF16 when earlier keys come from the
     // BF16 cache, so the attention's two operands always share a type
     store(static_cast<uint16_t*>(p.q_out) + (((size_t)b * p.Hq + head) * p.T + t) * DH,
-          p.q_f16 != 0 && p.slot0[b] == 0);
+          p.q_f16 != 0 && s0 == 0);
     record_overflow(err, bad);
     return;
   }
-  const int slot = p.slot0[b] + t;
+  const int slot = s0 + t;
   if (slot < 0 || slot >= p.max_seq) {
     record_error(err, QWEN_ERR_RANGE);
     return;
@@ -100,7 +103,7 @@ __device__ __forceinline__ void qkv_head_finish(float (&v)[DH], int m, int head,
   // a sequence from slot 0 has its attention read the FP16 copies, so its
   // cache rows are not read again in this call: streaming stores keep them
   // from displacing Q and the copies in L2
-  const bool fresh_read = fresh != nullptr && p.slot0[b] == 0;
+  const bool fresh_read = fresh != nullptr && s0 == 0;
   store((kind == 1 ? p.k_cache : p.v_cache) + (((size_t)b * p.Hkv + g) * p.max_seq + slot) * DH,
         false, fresh_read);
   if (fresh) store(fresh + (((size_t)b * p.Hkv + g) * p.T + t) * DH, true);
