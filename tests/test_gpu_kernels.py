@@ -20,10 +20,12 @@ def q():
 
 
 @pytest.mark.parametrize("rows,d", [(1, 512), (7, 3584), (300, 4096), (33, 8192), (64, 2048),
-                                    (1024, 4096), (3000, 3584)])
+                                    (1024, 4096), (3000, 3584), (2500, 2048), (4096, 4096),
+                                    (1500, 5120)])
 def test_rmsnorm_matches_oracle(q, rows, d):
-    """Up to 8 rows per SM one CTA per row (1024 rows included), above that a
-    warp per row (3000 rows)."""
+    """Up to 8 rows per SM one CTA per row (1024 rows included); above that a
+    warp per row (3000, 2500, 4096 and 1500 rows; d = 3584 and 5120 leave
+    lanes with fewer chunks than others)."""
     x = synth.activations([rows, d], "rms", f"x{rows}_{d}")
     g = synth.normal_bf16([d], synth.seed_for("rms", f"g{d}"), 0.1, 1.0)
     y32 = torch.empty((rows, d), dtype=torch.float32, device="cuda")
