@@ -41,7 +41,7 @@ CACHE_FILLED = 4096
 # DRAM bytes (read + write) of one gate/up decode launch at B=32, from the ncu
 # capture summarised in profiles/gemm_decode_gateup_qwen25_7b_b32.md; to be
 # replaced whenever that kernel changes
-GATE_UP_TRAFFIC_B32 = 271875584 + 2985472
+GATE_UP_TRAFFIC_B32 = 271870976 + 2988288
 
 
 def load_peaks():
